@@ -1,0 +1,467 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+None of these tests compares the oracle with itself or retypes its formulas: each
+checks a closed form, an invariant the pages state, an exact-arithmetic restatement
+of a different formulation, a brute-force search, or a hand-worked fixture under
+tests/golden/.
+"""
+import itertools
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from oracle import gptq_oracle as orc
+from synth import ActSpec, bf16_bits_to_f32, make_activations, make_weight
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _layer(m, d, n, seed, kind="heavy_tail", outliers=None):
+    W = bf16_bits_to_f32(make_weight(m, d, seed)).astype(np.float64)
+    X = bf16_bits_to_f32(make_activations(ActSpec(kind, n, d, seed=seed, outlier_count=outliers)))
+    return W, X.astype(np.float64)
+
+
+@pytest.fixture(scope="module")
+def toy():
+    """The 256 x 256 toy layer (512 Gaussian correlated tokens, 4 outlier channels x20)."""
+    W = bf16_bits_to_f32(make_weight(256, 256, 0)).astype(np.float64)
+    X = bf16_bits_to_f32(make_activations(
+        ActSpec("gauss_cov", 512, 256, seed=0, outlier_count=4, outlier_scale=20.0))).astype(np.float64)
+    return W, X, orc.hessian([X])
+
+
+# ----------------------------------------------------------------------------------
+# quantizer
+# ----------------------------------------------------------------------------------
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
+def test_quantizer_is_nearest_level(bits):
+    """clamp(round(w/s + z)) must be the nearest of all 2^b grid levels (exhaustive)."""
+    rng = np.random.default_rng(bits)
+    wg = rng.normal(0, 0.02, size=(64, 32))
+    s, z = orc.quant_params(wg, bits)
+    w = rng.normal(0, 0.03, size=(64, 200))          # includes values outside [min, max]
+    q = orc.quantize(w, s[:, None], z[:, None], bits)
+    levels = np.arange(2 ** bits)
+    vals = (levels[None, None, :] - z[:, None, None]) * s[:, None, None]
+    best = np.argmin(np.abs(w[:, :, None] - vals), axis=2)
+    assert np.array_equal(q.astype(np.int64), best)
+    assert q.min() >= 0 and q.max() <= 2 ** bits - 1
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
+def test_quant_params_span_the_group(bits):
+    """Level 0 and level 2^b-1 land within s/2 of the group's min and max; zero is an
+    integer in range; inside [min, max] dequantized values are within s/2."""
+    rng = np.random.default_rng(10 + bits)
+    wg = rng.normal(0, 0.02, size=(128, 128))
+    s, z = orc.quant_params(wg, bits)
+    qmax = 2 ** bits - 1
+    assert np.all(z == np.round(z)) and z.min() >= 0 and z.max() <= qmax
+    inner = (z > 0) & (z < qmax)
+    assert inner.any()
+    assert np.all(np.abs(-z * s - wg.min(1))[inner] <= s[inner] / 2 + 1e-15)
+    assert np.all(np.abs((qmax - z) * s - wg.max(1))[inner] <= s[inner] / 2 + 1e-15)
+    q = orc.quantize(wg, s[:, None], z[:, None], bits)
+    wq = orc.dequantize(q, s[:, None], z[:, None])
+    assert np.all(np.abs(wq - wg)[inner] <= (s[:, None] / 2 + 1e-15)[inner])
+
+
+def test_degenerate_group_clamps():
+    """max == min: scale is clamped to 1e-8 and the codes clamp into range."""
+    wg = np.full((3, 8), 0.25)
+    s, z = orc.quant_params(wg, 4)
+    assert np.all(s == 1e-8)
+    assert np.all(z == 0)
+    q = orc.quantize(wg, s[:, None], z[:, None], 4)
+    assert np.all(q == 15)
+
+
+# ----------------------------------------------------------------------------------
+# damping, act-order, Cholesky chain (golden fixtures and closed forms)
+# ----------------------------------------------------------------------------------
+def test_damping_golden():
+    g = _golden("damping_actorder.json")
+    for case in g["damping"]:
+        H = np.array(case["H"], dtype=np.float64)
+        Hd, lam = orc.damp(H, case["percdamp"])
+        assert lam == pytest.approx(case["lambda"], rel=1e-15)
+        assert np.allclose(np.diag(Hd), case["diag_damped"], rtol=1e-15)
+        off = ~np.eye(len(H), dtype=bool)
+        assert np.array_equal(Hd[off], H[off])
+
+
+def test_damping_rejects_nonpositive():
+    with pytest.raises(ValueError):
+        orc.damp(np.zeros((3, 3)), 0.01)
+
+
+def test_act_order_golden():
+    for case in _golden("damping_actorder.json")["act_order"]:
+        H = np.diag(np.array(case["diag"], dtype=np.float64))
+        assert orc.act_order_perm(H).tolist() == case["perm"]
+
+
+def test_hinv1_golden_2x2():
+    for case in _golden("hinv1_2x2.json")["cases"]:
+        U = orc.hinv1(np.array(case["H_d"], dtype=np.float64))
+        assert np.allclose(U, case["U"], rtol=1e-14, atol=1e-15)
+
+
+def test_hinv1_diagonal_closed_form():
+    h = np.array([1.0, 4.0, 0.25, 9.0, 2.0])
+    U = orc.hinv1(np.diag(h))
+    assert np.allclose(U, np.diag(1 / np.sqrt(h)), rtol=1e-15, atol=0)
+
+
+def test_hinv1_properties(toy):
+    """U upper with positive diagonal and U^T U H_d = I (residual ~ kappa * eps)."""
+    _, _, H = toy
+    Hd, _ = orc.damp(H, 0.01)
+    U = orc.hinv1(Hd)
+    assert np.allclose(np.tril(U, -1), 0)
+    assert np.all(np.diag(U) > 0)
+    kappa = np.linalg.cond(Hd)
+    assert np.abs(U.T @ U @ Hd - np.eye(len(Hd))).max() < 50 * kappa * np.finfo(float).eps
+
+
+def test_hinv1_reverse_identity(toy):
+    """Hinv1 = J chol_lower(J H_d J)^-1 J (J the reversal): the same factor by a
+    different route (uniqueness of the Cholesky factor with positive diagonal)."""
+    _, _, H = toy
+    Hd, _ = orc.damp(H, 0.01)
+    J = np.eye(len(Hd))[::-1]
+    L = np.linalg.cholesky(J @ Hd @ J)
+    U2 = J @ np.linalg.inv(L) @ J
+    U = orc.hinv1(Hd)
+    assert np.abs(U - U2).max() <= 1e-10 * np.abs(U).max()
+
+
+# ----------------------------------------------------------------------------------
+# Hessian
+# ----------------------------------------------------------------------------------
+def test_hessian_is_the_objectives_quadratic_form():
+    """||dW X^T||_F^2 == 1/2 tr(dW H dW^T) for H = 2 X^T X: pins the factor 2 and the
+    orientation (objective and Hessian of 'GPTQ: fixing errors as you go')."""
+    rng = np.random.default_rng(3)
+    X = rng.normal(size=(300, 40))
+    dW = rng.normal(size=(7, 40))
+    H = orc.hessian([X])
+    direct = np.sum((dW @ X.T) ** 2)
+    assert orc.loss_quadratic_form(dW, H) == pytest.approx(direct, rel=1e-12)
+
+
+def test_hessian_streaming_and_integers():
+    """Accumulating over batches equals one pass; integer data gives exact integers."""
+    rng = np.random.default_rng(4)
+    X = rng.integers(-8, 9, size=(1000, 24)).astype(np.float64)
+    H1 = orc.hessian([X])
+    H2 = orc.hessian([X[:333], X[333:700], X[700:]])
+    assert np.array_equal(H1, H2)
+    assert np.array_equal(H1, np.round(H1))
+    # one token: 2 x x^T has rank one and diagonal 2 x_i^2
+    x = X[:1]
+    H = orc.hessian([x])
+    assert np.linalg.matrix_rank(H) == 1
+    assert np.array_equal(np.diag(H), 2 * x[0] ** 2)
+    # sampled entries agree with the full product
+    rows, cols = np.array([0, 3, 23]), np.array([5, 3, 0])
+    assert np.array_equal(orc.hessian_entries(X, rows, cols), H1[rows, cols])
+
+
+# ----------------------------------------------------------------------------------
+# exact-rational OBQ in fixed order ("GPTQ: fixing errors as you go", The OBQ update)
+# ----------------------------------------------------------------------------------
+def _frac_inverse(A):
+    n = len(A)
+    M = [list(row) + [Fraction(int(i == j)) for j in range(n)] for i, row in enumerate(A)]
+    for c in range(n):
+        p = next(r for r in range(c, n) if M[r][c] != 0)
+        M[c], M[p] = M[p], M[c]
+        piv = M[c][c]
+        M[c] = [v / piv for v in M[c]]
+        for r in range(n):
+            if r != c and M[r][c] != 0:
+                f = M[r][c]
+                M[r] = [a - f * b for a, b in zip(M[r], M[c])]
+    return [row[n:] for row in M]
+
+
+def _frac_quant(wg, bits):
+    qmax = 2 ** bits - 1
+    mn, mx = min(wg), max(wg)
+    s = (mx - mn) / qmax
+    if s < Fraction(1e-8):
+        s = Fraction(1e-8)
+    z = min(max(round(-mn / s), 0), qmax)
+    return s, Fraction(z)
+
+
+def _obq_fixed_order(w0, Hd, bits, g):
+    """One row: quantize columns 0..d-1 in order; after each, update the free weights
+    by delta_F = -(w_q - quant(w_q)) / [H_F^-1]_qq * (H_F^-1)_{:,q} and remove q from
+    H_F^-1 by one step of Gaussian elimination. Exact rationals throughout."""
+    d = len(w0)
+    Hi = _frac_inverse(Hd)
+    w = list(w0)
+    free = list(range(d))
+    codes, losses, scales = [], [], []
+    qmax = 2 ** bits - 1
+    for q in range(d):
+        if q % g == 0:
+            s, z = _frac_quant(w[q:q + g], bits)
+            scales.append((s, z))
+        c = min(max(round(w[q] / s + z), 0), qmax)
+        wq = (c - z) * s
+        r = w[q] - wq
+        hqq = Hi[q][q]
+        codes.append(c)
+        losses.append(r * r / (2 * hqq))
+        for k in free:
+            w[k] -= r / hqq * Hi[k][q]
+        free.remove(q)
+        col = [Hi[a][q] for a in range(d)]
+        rowq = list(Hi[q])
+        for a in free:
+            for b in free:
+                Hi[a][b] -= col[a] * rowq[b] / hqq
+    return codes, losses, scales
+
+
+@pytest.mark.parametrize("bits,g,bs", [(2, 3, 1), (2, 3, 3), (3, 2, 4), (3, -1, 2), (4, 6, 6), (2, 2, 6)])
+def test_oracle_equals_exact_obq(bits, g, bs):
+    """The Cholesky-row form (Hinv1 rows, blocked) equals the explicit OBQ downdate form
+    in exact arithmetic: identical codes, scales and per-element losses."""
+    rng = np.random.default_rng(100 + bits * 10 + bs)
+    m, d = 3, 6
+    X = rng.integers(-3, 4, size=(5, d)).astype(np.float64)   # rank-deficient: damping needed
+    W = rng.integers(-200, 201, size=(m, d)) / 1024.0
+    H = orc.hessian([X])
+    Hd, _ = orc.damp(H, 0.01)
+    U = orc.hinv1(Hd)
+    res = orc.gptq_columns(W, U, bits, g, bs)
+    gg = d if g == -1 else g
+    Hd_f = [[Fraction(v) for v in row] for row in Hd]
+    for r in range(m):
+        codes, losses, scales = _obq_fixed_order([Fraction(v) for v in W[r]], Hd_f, bits, gg)
+        assert res["codes"][r].tolist() == codes
+        np.testing.assert_allclose(res["losses"][r], [float(x) for x in losses], rtol=1e-9, atol=1e-18)
+        np.testing.assert_allclose(res["scales"][r], [float(s) for s, _ in scales], rtol=1e-12)
+        np.testing.assert_array_equal(res["zeros"][r], [float(z) for _, z in scales])
+
+
+# ----------------------------------------------------------------------------------
+# blocking, special cases and brute force
+# ----------------------------------------------------------------------------------
+def test_blocksize_does_not_change_codes(toy):
+    """'GPTQ, Line by Line': the blocksize does not change the result (fp64 codes identical
+    for blocksize 1, 32, 128 and d; P3's unblocked listing is blocksize 1)."""
+    W, _, H = toy
+    Hd, _ = orc.damp(H, 0.01)
+    U = orc.hinv1(Hd)
+    ref = orc.gptq_columns(W, U, 4, 128, 1)
+    for bs in (32, 128, 256):
+        res = orc.gptq_columns(W, U, 4, 128, bs)
+        assert np.array_equal(res["codes"], ref["codes"])
+        assert np.array_equal(res["zeros"], ref["zeros"])
+        np.testing.assert_allclose(res["scales"], ref["scales"], rtol=1e-12)
+        np.testing.assert_allclose(res["losses"], ref["losses"], rtol=1e-8, atol=1e-20)
+
+
+def test_blocksize_invariance_per_channel_act_order():
+    """Same invariance for 3-bit per-channel act-order (blocksize 32 vs 128 vs 1)."""
+    W, X = _layer(48, 256, 1024, seed=7)
+    H = orc.hessian([X])
+    a = orc.gptq_layer(W, H, 3, -1, 32, act_order=True)
+    b = orc.gptq_layer(W, H, 3, -1, 128, act_order=True)
+    c = orc.gptq_layer(W, H, 3, -1, 1, act_order=True)
+    assert np.array_equal(a["codes"], b["codes"]) and np.array_equal(a["codes"], c["codes"])
+
+
+def test_diagonal_hessian_is_rtn():
+    """With a diagonal H every off-diagonal Hinv1 entry is zero, so no compensation
+    happens and GPTQ reduces to round-to-nearest, bit for bit."""
+    rng = np.random.default_rng(5)
+    W = rng.normal(0, 0.02, size=(32, 256))
+    H = np.diag(rng.uniform(0.5, 3.0, size=256))
+    for g, bs in ((128, 128), (64, 128), (-1, 32)):
+        res = orc.gptq_layer(W, H, 4, g, bs)
+        ref = orc.rtn(W, 4, g)
+        assert np.array_equal(res["codes"], ref["codes"])
+        assert np.array_equal(res["W_hat"], ref["W_hat"])
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_single_column_is_exhaustive_optimum(bits):
+    """d = 1: GPTQ = RTN = the best of all 2^b codes for the quadratic loss."""
+    rng = np.random.default_rng(bits)
+    W = rng.normal(0, 0.02, size=(20, 1))
+    H = np.array([[2.5]])
+    res = orc.gptq_layer(W, H, bits, -1, 1)
+    # with one column the group has min == max: the clamp gives scale 1e-8 -> code clamps;
+    # use the scale/zero GPTQ chose and search all codes
+    s, z = res["scales"][:, 0], res["zeros"][:, 0]
+    levels = (np.arange(2 ** bits)[None, :] - z[:, None]) * s[:, None]
+    loss = 0.5 * (W - levels) ** 2 * (H[0, 0] + res["lambda"])
+    assert np.array_equal(res["codes"][:, 0], np.argmin(loss, axis=1))
+    assert np.array_equal(res["codes"], orc.rtn(W, bits, -1)["codes"])
+
+
+def _ls_free_optimum(w0, Hd, fixed_idx, fixed_val):
+    """argmin over the free coordinates of 1/2 (w - w0) Hd (w - w0)^T with w fixed on
+    fixed_idx: w_F = w0_F - Hd_FF^-1 Hd_FX (v - w0_X)."""
+    d = len(w0)
+    Fi = [k for k in range(d) if k not in set(fixed_idx)]
+    w = w0.copy()
+    if fixed_idx:
+        dv = np.asarray(fixed_val) - w0[fixed_idx]
+        w[Fi] = w0[Fi] - np.linalg.solve(Hd[np.ix_(Fi, Fi)], Hd[np.ix_(Fi, fixed_idx)] @ dv)
+        w[fixed_idx] = fixed_val
+    return w
+
+
+def test_each_step_is_the_obq_choice():
+    """At every step the code GPTQ takes is the best of all 2^b candidates when the
+    columns to its right are re-optimized by least squares (the OBQ step), and GPTQ's
+    group statistics are taken from those least-squares-optimal weights."""
+    rng = np.random.default_rng(11)
+    m, d, bits, g = 4, 6, 2, 3
+    X = rng.normal(size=(40, d)) @ rng.normal(size=(d, d))
+    W = rng.normal(0, 0.02, size=(m, d))
+    H = orc.hessian([X])
+    res = orc.gptq_layer(W, H, bits, g, 3)
+    Hd = res["H_d"]
+    for r in range(m):
+        for j in range(d):
+            prev = list(range(j))
+            vals = list(res["W_hat"][r, :j])
+            wopt = _ls_free_optimum(W[r], Hd, prev, vals)
+            s, z = res["scales"][r, j // g], res["zeros"][r, j // g]
+            if j % g == 0:
+                grp = wopt[j:j + g]
+                assert s == pytest.approx((grp.max() - grp.min()) / (2 ** bits - 1), rel=1e-9)
+            best, best_loss = None, np.inf
+            for c in range(2 ** bits):
+                w = _ls_free_optimum(W[r], Hd, prev + [j], vals + [(c - z) * s])
+                loss = orc.loss_quadratic_form((w - W[r])[None, :], Hd)
+                if loss < best_loss - 1e-18:
+                    best, best_loss = c, loss
+            assert res["codes"][r, j] == best
+
+
+def test_exhaustive_search_lower_bounds_gptq():
+    """GPTQ is greedy: the best of all (2^b)^d code vectors (same scales and zeros) never
+    loses to it, and the loss identity makes both comparable."""
+    rng = np.random.default_rng(12)
+    d, bits = 5, 2
+    X = rng.normal(size=(30, d)) @ rng.normal(size=(d, d))
+    W = rng.normal(0, 0.02, size=(3, d))
+    H = orc.hessian([X])
+    res = orc.gptq_layer(W, H, bits, -1, d)
+    Hd = res["H_d"]
+    for r in range(3):
+        s, z = res["scales"][r, 0], res["zeros"][r, 0]
+        best = min(orc.loss_quadratic_form(((np.array(c) - z) * s - W[r])[None, :], Hd)
+                   for c in itertools.product(range(2 ** bits), repeat=d))
+        gptq = orc.loss_quadratic_form((res["W_hat"][r] - W[r])[None, :], Hd)
+        assert best <= gptq * (1 + 1e-12)
+        assert res["losses"][r].sum() == pytest.approx(gptq, rel=1e-10)
+
+
+def test_loss_identity(toy):
+    """Sum of Losses1 = 1/2 tr(dW H_d dW^T) = ||dW X^T||^2 + lambda/2 ||dW||^2."""
+    W, X, H = toy
+    res = orc.gptq_layer(W, H, 4, 128, 128)
+    dW = W - res["W_hat"]
+    total = res["losses"].sum()
+    assert total == pytest.approx(orc.loss_quadratic_form(dW, res["H_d"]), rel=1e-10)
+    direct = np.sum((dW @ X.T) ** 2) + 0.5 * res["lambda"] * np.sum(dW ** 2)
+    assert total == pytest.approx(direct, rel=1e-9)
+
+
+def test_hessian_scale_by_four(toy):
+    """H -> 4H: lambda x4, Hinv1 x1/2, errors x2, updates unchanged: identical codes,
+    scales and zeros; losses x4 exactly (powers of two)."""
+    W, _, H = toy
+    a = orc.gptq_layer(W, H, 4, 128, 128)
+    b = orc.gptq_layer(W, 4 * H, 4, 128, 128)
+    assert np.array_equal(a["codes"], b["codes"])
+    assert np.array_equal(a["scales"], b["scales"]) and np.array_equal(a["zeros"], b["zeros"])
+    np.testing.assert_allclose(b["losses"], 4 * a["losses"], rtol=1e-12, atol=0)
+
+
+def test_act_order_is_permutation_equivariant():
+    """act-order output = the natural-order loop on permuted W and H, scattered back."""
+    W, X = _layer(40, 128, 600, seed=8)
+    H = orc.hessian([X])
+    res = orc.gptq_layer(W, H, 3, -1, 32, act_order=True)
+    p = res["perm"]
+    assert np.all(np.diff(np.diag(H)[p]) <= 0)
+    Hd, _ = orc.damp(H, 0.01)
+    U = orc.hinv1(Hd[np.ix_(p, p)])
+    nat = orc.gptq_columns(W[:, p], U, 3, -1, 32)
+    assert np.array_equal(res["codes"][:, p], nat["codes"])
+    assert np.array_equal(res["losses"][:, p], nat["losses"])
+
+
+def test_rows_are_independent(toy):
+    W, _, H = toy
+    full = orc.gptq_layer(W, H, 4, 128, 128)
+    top = orc.gptq_layer(W[:100], H, 4, 128, 128)
+    bot = orc.gptq_layer(W[100:], H, 4, 128, 128)
+    assert np.array_equal(full["codes"], np.vstack([top["codes"], bot["codes"]]))
+    assert np.array_equal(full["scales"], np.vstack([top["scales"], bot["scales"]]))
+
+
+def test_gptq_beats_rtn_on_correlated_inputs(toy):
+    """'GPTQ: fixing errors as you go': the compensation lowers the output error."""
+    W, _, H = toy
+    res = orc.gptq_layer(W, H, 4, 128, 128)
+    e_gptq = orc.relative_output_error(W, res["W_hat"], H)
+    e_rtn = orc.relative_output_error(W, orc.rtn(W, 4, 128)["W_hat"], H)
+    assert e_gptq < 0.8 * e_rtn
+
+
+def test_codes_in_range_all_bits(toy):
+    W, _, H = toy
+    for bits, g in ((2, 64), (3, -1), (4, 128), (8, 128)):
+        res = orc.gptq_layer(W, H, bits, g, 128)
+        assert res["codes"].min() >= 0 and res["codes"].max() <= 2 ** bits - 1
+        assert np.all(res["zeros"] == np.round(res["zeros"]))
+
+
+def test_rejects_bad_grouping():
+    W = np.zeros((2, 192))
+    U = np.eye(192)
+    with pytest.raises(ValueError):
+        orc.gptq_columns(W, U, 4, 96, 128)     # neither divides the other
+    with pytest.raises(ValueError):
+        orc.gptq_columns(W, U, 4, 128, 128)    # 192 % 128 != 0
+
+
+# ----------------------------------------------------------------------------------
+# packing
+# ----------------------------------------------------------------------------------
+def test_pack_golden():
+    for case in _golden("pack_codes.json")["cases"]:
+        codes = np.array([case["codes"]])
+        words = orc.pack_codes(codes, case["bits"])
+        assert [f"0x{w:08x}" for w in words[0]] == case["words"]
+        assert np.array_equal(orc.unpack_codes(words, case["bits"], codes.shape[1]), codes)
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
+def test_pack_roundtrip(bits):
+    rng = np.random.default_rng(bits)
+    codes = rng.integers(0, 2 ** bits, size=(5, 263))
+    words = orc.pack_codes(codes, bits)
+    assert words.shape == (5, (263 * bits + 31) // 32)
+    assert np.array_equal(orc.unpack_codes(words, bits, 263), codes)
