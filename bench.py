@@ -1,0 +1,401 @@
+"""Benchmark of the GPTQ per-layer path on GB300.
+
+One step = the whole path for one layer: the Hessian over all calibration tokens
+(one bf16 SYRK), damping + Hinv1, and the blocked column loop with packed codes.
+Default workload: the Llama-style 4096 x 4096 projection, 4-bit, group 128, with
+262144 calibration tokens (128 sequences x 2048), synthetic seeded data.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gptq|reference]
+
+Prints one JSON line (rank 0). With N > 1 (torchrun) every rank quantizes its own
+replica of the layer (the path needs no exchange between GPUs); value is the total
+over ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GPTQ ms/layer + Mweights/s, 4096² 4-bit g128; SYRK TFLOP/s; % roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ----------------------------------------------------------------------------------
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["gptq", "reference"], default="gptq")
+    ap.add_argument("--workload", default="llama_4096_g128")
+    ap.add_argument("--layer", type=int, default=0, help="layer index within the workload")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--threads", type=int, default=None, help="host threads for input generation")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(k):
+            return int(os.environ[k])
+    return host_cores()
+
+
+# ----------------------------------------------------------------------------------
+# the oracle as it stands, on a bounded sample of the layer
+def oracle_sample(wl, layer, X_bits_sample, W_bits_rows, n_total, rows_total):
+    """Time the CPU oracle on a bounded sample and scale each stage to the full layer.
+
+    SYRK: the oracle Hessian over the sampled tokens, scaled by n_total / n_sample.
+    Factor: the full d x d damping + Cholesky chain (no sampling).
+    Column loop: the oracle loop over the sampled rows (rows are independent),
+    scaled by rows_total / rows_sample.
+    """
+    from oracle import gptq_oracle as orc
+    from synth import bf16_bits_to_f32
+
+    t0 = time.perf_counter()
+    Hs = orc.hessian([bf16_bits_to_f32(X_bits_sample)])
+    t1 = time.perf_counter()
+    Hd, _ = orc.damp(Hs, wl.percdamp)
+    perm = orc.act_order_perm(Hs) if wl.act_order else np.arange(Hs.shape[0])
+    U = orc.hinv1(Hd[np.ix_(perm, perm)])
+    t2 = time.perf_counter()
+    W = bf16_bits_to_f32(W_bits_rows).astype(np.float64)[:, perm]
+    orc.gptq_columns(W, U, wl.bits, wl.group_size, wl.blocksize)
+    t3 = time.perf_counter()
+    n_s, r_s = X_bits_sample.shape[0], W_bits_rows.shape[0]
+    syrk = (t1 - t0) * n_total / n_s
+    factor = t2 - t1
+    loop = (t3 - t2) * rows_total / r_s
+    return {"syrk_s": syrk, "factor_s": factor, "loop_s": loop, "total_s": syrk + factor + loop,
+            "sample_wall_s": t3 - t0, "tokens": n_s, "rows": r_s}
+
+
+# ----------------------------------------------------------------------------------
+class Clocks:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, enabled: bool):
+        self.proc = None
+        self.index = index
+        if enabled:
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", f"--id={index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                     "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except OSError:
+                self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def kernel_traffic(kernel_file: str, key: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source is unchanged."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(key)
+        with open(os.path.join(ROOT, "post_weight_quantization_gb300", "csrc", kernel_file), "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()[:16]
+        if rec and rec.get("source_sha256_16") == h:
+            return rec.get("dram_bytes_per_launch")
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+# ----------------------------------------------------------------------------------
+def run_reference(args):
+    """The oracle as it stands on the host cores, each step a bounded sample."""
+    import torch.distributed as dist  # noqa: F401  (only to honour torchrun env; rank 0 works)
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from synth import ActSpec, gen_activations_into, workload
+    from synth.workloads import CHUNK
+    wl = workload(args.workload)
+    layer = wl.layers[args.layer]
+    spec = wl.acts[layer.hessian]
+    n_sample = min(spec.n, 2 * CHUNK)
+    Xs = np.empty((n_sample, spec.d), dtype=np.uint16)
+    gen_activations_into(spec, Xs, args.threads, (0, n_sample))
+    Wfull = wl.weight(layer, threads=args.threads)
+    rows = min(layer.m, 32)
+    times = []
+    for i in range(args.warmup + args.steps):
+        r = oracle_sample(wl, layer, Xs, Wfull[:rows], spec.n, layer.m)
+        if i >= args.warmup:
+            times.append(r)
+    t = statistics.mean(x["total_s"] for x in times)
+    weights = layer.m * layer.d
+    value = weights / t / 1e6
+    sample = (f"per step: oracle Hessian over {n_sample} of {spec.n} tokens (scaled x{spec.n / n_sample:g}), "
+              f"full d={layer.d} factor chain, column loop over {rows} of {layer.m} rows (scaled)")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "Mweights/s",
+            "n_gpus": 0, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)",
+            "config": {"workload": args.workload, "layer": layer.name, "m": layer.m, "d": layer.d,
+                       "tokens": spec.n, "bits": wl.bits, "group_size": wl.group_size, "blocksize": wl.blocksize,
+                       "act_order": wl.act_order},
+            "cpu_baseline": {"value": round(value, 6), "unit": "Mweights/s", "cores": blas_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "Mweights/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "stages_s": {k: round(statistics.mean(x[k] for x in times), 4) for k in ("syrk_s", "factor_s", "loop_s")}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------------
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from post_weight_quantization_gb300 import gptq as g
+    from synth import gen_activations_into, workload
+    from synth.workloads import CHUNK
+
+    wl = workload(args.workload)
+    layer = wl.layers[args.layer]
+    spec = wl.acts[layer.hessian]
+    m, d, n = layer.m, layer.d, spec.n
+
+    # ---- inputs: pinned host buffers (also the end-to-end source), then HBM copies
+    t_gen = time.perf_counter()
+    X_host = torch.empty((n, d), dtype=torch.int16, pin_memory=True)
+    gen_activations_into(spec, X_host.numpy().view(np.uint16), args.threads)
+    W_bits = wl.weight(layer, threads=args.threads)
+    W_host = torch.from_numpy(W_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    t_gen = time.perf_counter() - t_gen
+    X = X_host.to(dev)
+    W = W_host.to(dev)
+    H = torch.empty((d, d), dtype=torch.float32, device=dev)
+    U = torch.empty((d, d), dtype=torch.float32, device=dev)
+    perm = torch.empty(d, dtype=torch.int32, device=dev) if wl.act_order else None
+    ws_f = torch.empty(g.gptq_workspace_size(g.GPTQ_WS_FACTOR, 0, d), dtype=torch.uint8, device=dev)
+    ws_q = torch.empty(g.gptq_workspace_size(g.GPTQ_WS_QUANTIZE, m, d, wl.bits, wl.group_size, wl.blocksize),
+                       dtype=torch.uint8, device=dev)
+    G = 1 if wl.group_size == -1 else d // wl.group_size
+    out = g.QuantizedLayer(torch.empty((m, (d * wl.bits + 31) // 32), dtype=torch.int32, device=dev),
+                           torch.empty((m, G), dtype=torch.float32, device=dev),
+                           torch.empty((m, G), dtype=torch.float32, device=dev),
+                           torch.empty(d, dtype=torch.float32, device=dev), wl.bits, wl.group_size, d)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev):
+        ev[0].record(stream)
+        g.gptq_hessian_accumulate(X, H, alpha=2.0, zero_first=True, stream=stream)
+        ev[1].record(stream)
+        g.gptq_factor(H, percdamp=wl.percdamp, act_order=wl.act_order, Hinv1=U, perm_out=perm, ws=ws_f,
+                      sync=False, stream=stream)
+        ev[2].record(stream)
+        g.gptq_quantize_layer(W, U, perm, bits=wl.bits, group_size=wl.group_size, blocksize=wl.blocksize, out=out,
+                              ws=ws_q, stream=stream)
+        ev[3].record(stream)
+
+    def mk():
+        return [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(mk())
+    torch.cuda.synchronize()
+    g.gptq_device_check()
+    g.gptq_factor_status(ws_f) if hasattr(g, "gptq_factor_status") else None
+
+    # ---- timed region
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = Clocks(local, not args.no_clocks and rank == 0)
+    launches0 = g.gptq_launch_count()
+    events = []
+    t_wall = time.perf_counter()
+    for _ in range(args.steps):
+        flush.zero_()                       # L2 flush between steps, outside the step's events
+        ev = mk()
+        step(ev)
+        events.append(ev)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    launches = g.gptq_launch_count() - launches0
+    clk = clocks.stop()
+    g.gptq_device_check()
+
+    st_ms = {"syrk": [], "factor": [], "quantize": []}
+    for ev in events:
+        st_ms["syrk"].append(ev[0].elapsed_time(ev[1]))
+        st_ms["factor"].append(ev[1].elapsed_time(ev[2]))
+        st_ms["quantize"].append(ev[2].elapsed_time(ev[3]))
+    step_ms = [a + b + c for a, b, c in zip(st_ms["syrk"], st_ms["factor"], st_ms["quantize"])]
+    t_local = sum(step_ms) / 1e3
+    t_max = t_local
+    if world > 1:
+        tt = torch.tensor([t_local], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_max = float(tt.item())
+    weights = m * d
+    value = world * args.steps * weights / t_max / 1e6
+    ms_per_step = t_max / args.steps * 1e3
+    syrk_ms = statistics.mean(st_ms["syrk"])
+    syrk_flops = float(n) * d * (d + 1)
+    peaks, peak_src = load_peaks()
+    syrk_tflops = syrk_flops / (syrk_ms * 1e-3) / 1e12
+    roofline = {"kernel": "syrk_kernel (Hessian, tcgen05 bf16)", "bound": "tensor",
+                "achieved": round(syrk_tflops, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(syrk_tflops / peaks["bf16_tflops"], 4),
+                "frac_of_sustained": round(syrk_tflops / peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]), 4),
+                "peak_source": f"{peak_src} (bf16 burst)",
+                "traffic": kernel_traffic("syrk_tc.cu", f"syrk_{args.workload}"),
+                "algorithmic_flops_per_launch": syrk_flops}
+
+    # ---- end to end through the public host-buffer API
+    e2e = None
+    if not args.no_e2e:
+        pipe = g.HostPipeline(m, d, bits=wl.bits, group_size=wl.group_size, blocksize=wl.blocksize,
+                              percdamp=wl.percdamp, act_order=wl.act_order, device=dev)
+        for _ in range(max(1, args.warmup)):
+            pipe.run(W_host, X_host)
+        torch.cuda.synchronize()
+        e_ms = []
+        for _ in range(args.steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            pipe.run(W_host, X_host)
+            b.record(stream)
+            b.synchronize()
+            e_ms.append(a.elapsed_time(b))
+        te = sum(e_ms) / 1e3
+        if world > 1:
+            tt = torch.tensor([te], dtype=torch.float64, device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            te = float(tt.item())
+        g.gptq_device_check()
+        e2e = {"value": round(world * args.steps * weights / te / 1e6, 4), "unit": "Mweights/s",
+               "ms_per_step": round(te / args.steps * 1e3, 4),
+               "h2d_bytes_per_step": pipe.bytes_h2d(n), "d2h_bytes_per_step": pipe.bytes_d2h()}
+
+    # ---- CPU oracle baseline (rank 0, N = 1 only), bounded sample
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n_s = min(n, 2 * CHUNK)
+        rows = min(m, 32)
+        r = oracle_sample(wl, layer, X_host.numpy().view(np.uint16)[:n_s], W_bits[:rows], n, m)
+        cpu = {"value": round(weights / r["total_s"] / 1e6, 6), "unit": "Mweights/s", "cores": blas_threads(),
+               "kind": "oracle",
+               "sample": (f"oracle Hessian over {n_s} of {n} tokens (scaled x{n / n_s:g}), full d={d} factor chain, "
+                          f"column loop over {rows} of {m} rows (scaled x{m / rows:g}); "
+                          f"sample wall {r['sample_wall_s']:.1f} s"),
+               "stages_s": {k: round(r[k], 3) for k in ("syrk_s", "factor_s", "loop_s")}}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 4), "unit": "Mweights/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16+f32",
+                "data": "synthetic (seeded generators; no dataset or trained weights available)",
+                "config": {"workload": args.workload, "layer": layer.name, "m": m, "d": d, "tokens": n,
+                           "bits": wl.bits, "group_size": wl.group_size, "blocksize": wl.blocksize,
+                           "percdamp": wl.percdamp, "act_order": wl.act_order,
+                           "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                           "l2": "inputs larger than L2 (X is %.2f GB per step) and a 256 MB L2 flush between "
+                                 "steps, outside the step's events" % (n * d * 2 / 1e9)},
+                "stages_ms": {k: round(statistics.mean(v), 4) for k, v in st_ms.items()},
+                "quantize_only_ms": round(statistics.mean(st_ms["factor"]) + statistics.mean(st_ms["quantize"]), 4),
+                "syrk_tflops": round(syrk_tflops, 2),
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+                "clocks": clk, "wall_s_timed_region": round(t_wall, 4), "input_generation_s": round(t_gen, 2)}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

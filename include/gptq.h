@@ -1,0 +1,226 @@
+/*
+ * gptq.h -- C ABI of the GB300 (sm_103a) GPTQ per-layer quantization library.
+ *
+ * GPTQ quantizes a linear layer's weight W (m x d, out x in) column by column and,
+ * after each column, moves the columns not yet quantized so that the layer output
+ * on calibration inputs X stays close to the original ("GPTQ: fixing errors as you
+ * go", sections "The algorithm, in words" and "going deeper / Objective").
+ * The library runs the three stages of that method on one GPU:
+ *
+ *   1. gptq_hessian_accumulate  H += alpha * X^T X over token batches
+ *   2. gptq_factor              damping, optional act-order, Hinv1 = upper
+ *                               Cholesky factor of H_d^-1
+ *   3. gptq_quantize_layer      blocked column loop: quantize, error feedback,
+ *                               lazy block updates, packed b-bit codes
+ *
+ * Conventions shared by every call:
+ *   - Pointers to matrices are DEVICE pointers owned by the caller. The library
+ *     allocates no memory: scratch comes from a caller-provided device workspace
+ *     whose size gptq_workspace_size() returns.
+ *   - Matrices are row-major with an explicit leading dimension in elements.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL means the legacy default
+ *     stream) and runs asynchronously, except where a call documents a
+ *     synchronization.
+ *   - Every call returns a gptq_status. Argument errors are detected on the host
+ *     and returned before anything is launched; no call aborts, traps or throws.
+ *     gptq_last_error() gives a one-line description of the last failure on the
+ *     calling thread.
+ *   - Floating-point arithmetic is IEEE fp32 (bf16 inputs to the Hessian product).
+ */
+#ifndef GPTQ_GB300_H
+#define GPTQ_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GPTQ_OK = 0,
+  GPTQ_ERR_INVALID_ARG = 1,   /* bad pointer, size, alignment or setting       */
+  GPTQ_ERR_NOT_PD = 2,        /* Cholesky met a non-positive pivot (info = index) */
+  GPTQ_ERR_NONFINITE = 3,     /* NaN or Inf met in H or W                      */
+  GPTQ_ERR_UNSUPPORTED = 4,   /* valid request this build does not implement   */
+  GPTQ_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed          */
+  GPTQ_ERR_TIMEOUT = 6        /* a bounded on-device wait gave up              */
+} gptq_status;
+
+/* A cudaStream_t, passed as an opaque pointer so this header needs no CUDA header. */
+typedef void* gptq_stream_t;
+
+/* Static text for a status code ("GPTQ_OK", ...). Never NULL. */
+const char* gptq_status_string(int status);
+
+/* One-line description of the last failure on the calling thread ("" if none). */
+const char* gptq_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int gptq_version(void);
+
+/* Number of CUDA kernels this library has launched in the process so far. */
+uint64_t gptq_launch_count(void);
+
+/*
+ * Synchronizes `stream`, then reads and clears the library's device error word,
+ * which kernels raise when a bounded on-device wait gives up (GPTQ_ERR_TIMEOUT) or
+ * when they meet a NaN or an Inf they cannot report otherwise (GPTQ_ERR_NONFINITE).
+ * The word is shared by all calls on the current device.
+ */
+gptq_status gptq_device_check(gptq_stream_t stream);
+
+/*
+ * Stage 1 -- Hessian accumulation.
+ *
+ * Defined by "The GPTQ Algorithm" (procedure step 2, H = 2 X X^T), "GPTQ: fixing
+ * errors as you go" (Objective: the squared error is a quadratic with Hessian
+ * H = 2 X X^T, the same for every row) and "GPTQ-style round-to-nearest with Hessian
+ * weighting" (section "Computing the Hessian": the layer's inputs reshaped to
+ * tokens x features, H += x^T x per calibration batch).
+ *
+ * Computes, for i <= j,   H[i][j] = (zero_first ? 0 : H[i][j]) + alpha * sum_t X[t][i] * X[t][j]
+ *
+ *   X      device, bf16 bits (uint16), n x d row-major (token-major), leading
+ *          dimension ldx >= d. The base must be 16-byte aligned and ldx a multiple
+ *          of 8 (rows start on 16-byte boundaries).
+ *   n      tokens in this batch (n >= 0; n == 0 only applies zero_first).
+ *   d      channels, 8 <= d <= 65536, d a multiple of 8.
+ *   H      device fp32, d x d row-major, leading dimension ldh >= d with ldh a
+ *          multiple of 4 and the base 16-byte aligned. Only the
+ *          upper triangle including the diagonal (i <= j) is written; the strictly
+ *          lower triangle is never touched.
+ *   alpha  scale of the product; 2 gives the pages' H = 2 X^T X. The caller keeps
+ *          any token count (the codes do not depend on a positive scale of H).
+ *   zero_first  non-zero: the upper triangle is overwritten instead of accumulated.
+ *
+ * Accumulation across calls in the same stream is exact in the sense of fp32
+ * addition; the order of partial sums inside one call is not fixed, so results can
+ * differ in the last bits from run to run.
+ */
+gptq_status gptq_hessian_accumulate(const uint16_t* X, int64_t n, int64_t d, int64_t ldx,
+                                    float* H, int64_t ldh, float alpha, int zero_first,
+                                    gptq_stream_t stream);
+
+/* Workspace kinds for gptq_workspace_size(). */
+enum { GPTQ_WS_FACTOR = 0, GPTQ_WS_QUANTIZE = 1 };
+
+/*
+ * Bytes of device workspace a call needs (0 for an invalid request). `which` is
+ * GPTQ_WS_FACTOR (uses d only) or GPTQ_WS_QUANTIZE (uses m, d, bits, group_size,
+ * blocksize). The workspace must be 256-byte aligned; its contents on entry do not
+ * matter.
+ */
+size_t gptq_workspace_size(int which, int64_t m, int64_t d, int bits, int group_size,
+                           int blocksize);
+
+/*
+ * Stage 2 -- damping, act-order and the inverse-Hessian factor.
+ *
+ * Defined by "GPTQ, Line by Line", questions "What does percdamp (dampening) do in
+ * GPTQ?" (lambda = percdamp * mean of diag H added to every diagonal entry) and "Why
+ * does GPTQ use Cholesky factorizations instead of inverting the Hessian directly?"
+ * (Hinv1 = upper Cholesky factor of H^-1, whose row j gives the update direction
+ * and whose diagonal gives the error denominator); act-order by "The GPTQ
+ * Algorithm" (ActOrder) and "GPTQ: fixing errors as you go" (act-order / desc_act:
+ * columns in order of decreasing H_qq).
+ *
+ *   H          device fp32, d x d, leading dimension d; only the upper triangle
+ *              (i <= j) is read. Not modified.
+ *   percdamp   damping fraction (the pages' default 0.01); must be >= 0.
+ *   act_order  non-zero: perm_out receives the column order (stable sort of
+ *              diag(H) descending, ties to the lower index) and Hinv1 is the
+ *              factor of the permuted matrix H_d[perm][:, perm].
+ *   perm_out   device int32[d]; required when act_order, ignored otherwise (may be
+ *              NULL).
+ *   Hinv1      device fp32, d x d, leading dimension d. Receives U with
+ *              H_d^-1 = U^T U, U upper triangular with a positive diagonal; the
+ *              strictly lower triangle is set to zero.
+ *   ws         device workspace of gptq_workspace_size(GPTQ_WS_FACTOR, 0, d, ...)
+ *              bytes.
+ *   info       host pointer or NULL. When non-NULL the call synchronizes `stream`
+ *              once and reports the outcome: *info = -1 on success, otherwise the
+ *              column (0-based, in processing order, i.e. after act-order) whose
+ *              pivot was not positive; the factorization runs from the last
+ *              column to the first, so this is the highest such column. The
+ *              return value is then GPTQ_ERR_NOT_PD, or
+ *              GPTQ_ERR_NONFINITE when diag(H) holds a NaN or an Inf (*info = 0).
+ *              When NULL nothing is synchronized and the outcome can be read later
+ *              with gptq_factor_status().
+ *
+ * The returned Hinv1 equals the pages' three-step chain (Cholesky of H_d, inverse
+ * by a Cholesky solve, upper Cholesky of the inverse) in exact arithmetic; the
+ * library reaches it by one Cholesky factorization and one triangular inverse of
+ * the index-reversed matrix: with J the reversal and J H_d J = L L^T (lower L),
+ * Hinv1 = J L^-1 J.
+ */
+gptq_status gptq_factor(const float* H, int64_t d, float percdamp, int act_order,
+                        int32_t* perm_out, float* Hinv1, void* ws, size_t ws_bytes,
+                        int64_t* info, gptq_stream_t stream);
+
+/*
+ * Outcome of the last gptq_factor() that used this workspace: synchronizes
+ * `stream`, sets *info as gptq_factor does and returns the same status.
+ */
+gptq_status gptq_factor_status(const void* ws, int64_t* info, gptq_stream_t stream);
+
+/*
+ * Stage 3 -- the blocked GPTQ column loop.
+ *
+ * Defined by "GPTQ, Line by Line", question "Why does GPTQ process the weight matrix
+ * in blocks of 128 columns?" (inside a block each quantized column updates the
+ * block's remaining columns by a rank-one product; after the block the block's
+ * errors Err1 are applied to the columns right of it by one product
+ * Err1 @ Hinv1[block, rest]) and by the listing of "GPTQ-style round-to-nearest with
+ * Hessian weighting" (per-group min/max scale and zero, quantize, dequantize, error
+ * divided by Hinv1[j][j], compensation along Hinv1[j][j+1:]).
+ *
+ *   W          device, m x d row-major, leading dimension ldw >= d; fp32
+ *              (w_dtype 0) or bf16 bits (w_dtype 1). Not modified.
+ *   Hinv1      device fp32 d x d (leading dimension d), the factor from
+ *              gptq_factor for the same column order; only the upper triangle is
+ *              read.
+ *   perm       device int32[d] column order from gptq_factor(act_order), or NULL
+ *              for the natural order. Outputs are always in the ORIGINAL column
+ *              order.
+ *   bits       2, 3, 4 or 8.
+ *   group_size columns sharing one (scale, zero) per row; -1 means one per row
+ *              (statistics from W before any update). Otherwise d % group_size == 0
+ *              and group_size % blocksize == 0 or blocksize % group_size == 0, so
+ *              that a group's statistics are read after all earlier compensation.
+ *              With perm != NULL only -1 is supported (GPTQ_ERR_UNSUPPORTED).
+ *   blocksize  lazy-update block width in [1, 256]; this build runs 32, 64 and 128
+ *              (the pages use 128) and returns GPTQ_ERR_UNSUPPORTED for others. It
+ *              does not change the result in exact arithmetic. Group sizes must be
+ *              multiples of 32 in this build (GPTQ_ERR_UNSUPPORTED otherwise).
+ *   qweight    device uint32, m x ceil(d*bits/32): per row a little-endian
+ *              bitstream, code of column j in bits [j*bits, j*bits + bits).
+ *   scales, zeros  device fp32, m x G row-major, G = d / group_size (1 when -1);
+ *              w_hat = (code - zero) * scale; zeros hold integers in [0, 2^bits-1].
+ *   col_losses device fp32[d]: for every column, the sum over rows of Err1^2 / 2,
+ *              the increase of 1/2 (w - w_hat) H_d (w - w_hat)^T caused by fixing that
+ *              column; their total is 1/2 tr(dW H_d dW^T).
+ *   ws         device workspace of gptq_workspace_size(GPTQ_WS_QUANTIZE, ...) bytes.
+ *   info       host pointer or NULL. When non-NULL the call synchronizes `stream`
+ *              and returns GPTQ_ERR_NONFINITE (with *info = 1) if W held a NaN or an
+ *              Inf; *info = 0 otherwise. When NULL nothing is synchronized.
+ */
+gptq_status gptq_quantize_layer(const void* W, int w_dtype, int64_t m, int64_t d, int64_t ldw,
+                                const float* Hinv1, const int32_t* perm, int bits,
+                                int group_size, int blocksize, uint32_t* qweight,
+                                float* scales, float* zeros, float* col_losses, void* ws,
+                                size_t ws_bytes, int64_t* info, gptq_stream_t stream);
+
+/*
+ * Helper for checks: unpack codes written by gptq_quantize_layer into one byte per
+ * code. qweight as above (m x ceil(d*bits/32) words, device); codes device uint8
+ * m x d row-major.
+ */
+gptq_status gptq_unpack_codes(const uint32_t* qweight, int64_t m, int64_t d, int bits,
+                              uint8_t* codes, gptq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GPTQ_GB300_H */

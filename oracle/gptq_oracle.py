@@ -129,7 +129,7 @@ def hinv1(Hd: np.ndarray, dtype=np.float64) -> np.ndarray:
     L = np.linalg.cholesky(Hd)
     Hinv = scipy.linalg.cho_solve((L, True), np.eye(Hd.shape[0], dtype=dtype))
     Hinv = (Hinv + Hinv.T) * dtype(0.5)   # cho_solve returns it up to rounding symmetry
-    return np.linalg.cholesky(Hinv).T.astype(dtype, copy=False)
+    return np.ascontiguousarray(np.linalg.cholesky(Hinv).T, dtype=dtype)
 
 
 # ----------------------------------------------------------------------------------

@@ -1,0 +1,333 @@
+// Stage 1: Hessian accumulation H += alpha * X^T X on the 5th-generation tensor cores.
+//
+// The Hessian of the layer-wise squared error is H = 2 X X^T with X channels x tokens
+// ("GPTQ: fixing errors as you go", Objective; "The GPTQ Algorithm", procedure step 2);
+// calibration batches add their X^T X into one running H ("GPTQ-style round-to-nearest
+// with Hessian weighting", section "Computing the Hessian"). Here X is token-major
+// (n x d, bf16) and only the upper triangle of the symmetric H is produced.
+//
+// Design (sm_103a):
+//   * H is cut into 128 x 256 tiles; only tiles that hold some (i, j) with j >= i are
+//     computed. The token axis is cut into S parts; a work unit is (tile, part).
+//   * A persistent grid of one CTA per SM takes units round-robin in part-major
+//     order, so all CTAs sweep the same token range at the same time and each X slab
+//     is fetched from HBM about once and re-served to the other tiles from L2.
+//   * Warp 0 (one thread) streams X tiles with TMA (128-byte swizzle) into a 4-stage
+//     shared-memory ring; warp 1 (one thread) issues tcgen05.mma kind::f16
+//     (bf16 x bf16 -> fp32, M = 128, N = 256, K = 16), both operands MN-major since
+//     X^T's rows are X's columns; the accumulator lives in tensor memory, two
+//     buffers of 256 columns so the epilogue of one unit overlaps the next unit's
+//     products. Warps 2-5 read the accumulator with tcgen05.ld, scale by alpha and
+//     add into H with vector fp32 reductions (units of the same tile from different
+//     token parts meet there).
+//   * Every wait is bounded; on a timeout the CTA raises the library's device error
+//     word, drains its own copies and products, frees tensor memory and returns.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "common.cuh"
+
+namespace gptq {
+namespace syrk {
+
+constexpr int BM = 128;                       // rows of an H tile (channels i)
+constexpr int BN = 256;                       // columns of an H tile (channels j)
+constexpr int BK = 64;                        // tokens per pipeline stage
+constexpr int STAGES = 4;
+constexpr int BOX = 64;                       // TMA box: 64 channels (128 bytes) x BK tokens
+constexpr int BOX_BYTES = BOX * BK * 2;       // 8 KB
+constexpr int A_BYTES = BM * BK * 2;          // 16 KB
+constexpr int B_BYTES = BN * BK * 2;          // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+constexpr uint32_t IDESC = umma_idesc(/*bf16*/ 1, /*A MN-major*/ true, /*B MN-major*/ true, BM, BN);
+// Within one stage a 16-token MMA step advances 16 rows of 128 bytes.
+constexpr uint32_t KSTEP_BYTES = 16 * 128;
+// MN-major, 128-byte swizzle: 8-row groups along K are 1024 bytes apart (SBO); the
+// next 64 channels (next TMA box) are BOX_BYTES apart (LBO).
+constexpr uint32_t SBO = 1024;
+constexpr uint32_t LBO = BOX_BYTES;
+
+struct Geometry {
+  int d, nr, nc, tiles, parts;
+  long long kiters;
+};
+
+// number of upper-triangle tiles in row-tiles [0, r)
+__device__ __forceinline__ long long tiles_before_row(int r, int nc) {
+  long long a = r / 2;
+  long long s = (r & 1) ? a * a : a * (a - 1);   // sum_{r' < r} floor(r' / 2)
+  return (long long)r * nc - s;
+}
+
+__device__ __forceinline__ void decode_tile(long long t, int nr, int nc, int& r, int& c) {
+  int lo = 0, hi = nr - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (tiles_before_row(mid, nc) <= t) lo = mid; else hi = mid - 1;
+  }
+  r = lo;
+  c = (lo / 2) + (int)(t - tiles_before_row(lo, nc));
+}
+
+struct Unit {
+  int r, c;
+  long long k0, k1;
+};
+
+__device__ __forceinline__ Unit decode_unit(long long u, const Geometry& g) {
+  Unit w;
+  long long part = u / g.tiles;
+  long long t = u - part * g.tiles;
+  decode_tile(t, g.nr, g.nc, w.r, w.c);
+  w.k0 = part * g.kiters / g.parts;
+  w.k1 = (part + 1) * g.kiters / g.parts;
+  return w;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+syrk_kernel(const __grid_constant__ CUtensorMap tmap, float* __restrict__ H, long long ldh, Geometry g,
+            float alpha, int* __restrict__ err_word) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tmem_full = empty + STAGES;
+  uint64_t* tmem_empty = tmem_full + 2;
+  uint64_t* drain = tmem_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tmem_full[b], 1);
+      mbar_init(&tmem_empty[b], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmap);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const long long num_units = (long long)g.tiles * g.parts;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer ----------------
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t armed = 0;            // stages that were ever armed
+    uint32_t last_phase[STAGES];
+    bool ok = true;
+    for (long long u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
+      Unit w = decode_unit(u, g);
+      for (long long k = w.k0; k < w.k1; ++k) {
+        if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
+        uint8_t* sA = smem + stage * STAGE_BYTES;
+        uint8_t* sB = sA + A_BYTES;
+        mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+        const int tok = (int)(k * BK);
+#pragma unroll
+        for (int h = 0; h < BM / BOX; ++h) tma_load_2d(sA + h * BOX_BYTES, &tmap, &full[stage], w.r * BM + h * BOX, tok);
+#pragma unroll
+        for (int h = 0; h < BN / BOX; ++h) tma_load_2d(sB + h * BOX_BYTES, &tmap, &full[stage], w.c * BN + h * BOX, tok);
+        armed |= 1u << stage;
+        last_phase[stage] = phase;
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (!ok) { *abort_flag = 1; report_device_error(err_word, DEVERR_TIMEOUT); }
+    // every armed load lands whatever the consumer did; wait for them before exit
+    for (int s = 0; s < STAGES; ++s)
+      if (armed & (1u << s)) mbar_wait_bounded(&full[s], last_phase[s], nullptr);
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer ----------------
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t it = 0;
+    bool ok = true, issued = false;
+    const uint32_t sbase = smem_u32(smem);
+    for (long long u = blockIdx.x; ok && u < num_units; u += gridDim.x, ++it) {
+      Unit w = decode_unit(u, g);
+      const uint32_t buf = it & 1u;
+      if (!mbar_wait_bounded(&tmem_empty[buf], ((it >> 1) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + buf * BN;
+      for (long long k = w.k0; k < w.k1; ++k) {
+        if (!mbar_wait_bounded(&full[stage], phase, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t a0 = sbase + stage * STAGE_BYTES;
+        const uint32_t b0 = a0 + A_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint64_t da = umma_sdesc_sw128(a0 + kk * KSTEP_BYTES, LBO, SBO);
+          const uint64_t db = umma_sdesc_sw128(b0 + kk * KSTEP_BYTES, LBO, SBO);
+          umma_f16(d_tmem, da, db, IDESC, (k > w.k0 || kk > 0) ? 1u : 0u);
+        }
+        issued = true;
+        umma_commit(&empty[stage]);
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+      umma_commit(&tmem_full[buf]);
+    }
+    if (!ok) { *abort_flag = 1; report_device_error(err_word, DEVERR_TIMEOUT); }
+    if (issued) {
+      umma_commit(drain);
+      mbar_wait_bounded(drain, 0, nullptr);
+    }
+  } else if (warp >= 2) {
+    // ---------------- epilogue: TMEM -> alpha * acc -> red.add into H ----------------
+    const int q = warp & 3;                  // TMEM lane quadrant this warp may access
+    const int row = q * 32 + lane;
+    uint32_t it = 0;
+    for (long long u = blockIdx.x; u < num_units; u += gridDim.x, ++it) {
+      Unit w = decode_unit(u, g);
+      const uint32_t buf = it & 1u;
+      if (!mbar_wait_bounded(&tmem_full[buf], (it >> 1) & 1u, abort_flag)) {
+        *abort_flag = 1;
+        report_device_error(err_word, DEVERR_TIMEOUT);
+        break;
+      }
+      tc_fence_after();
+      const int i = w.r * BM + row;
+      const int i_warp = w.r * BM + q * 32;
+      float* hrow = H + (long long)i * ldh;
+#pragma unroll 1
+      for (int cc = 0; cc < BN / 32; ++cc) {
+        const int j0 = w.c * BN + cc * 32;
+        if (j0 + 31 < i_warp || j0 >= g.d) continue;   // warp-uniform: nothing on or above the diagonal
+        float v[32];
+        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN + cc * 32, v);
+        if (i < g.d) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int j = j0 + 4 * e;
+            if (j >= i && j + 3 < g.d) {
+              atomicAdd(reinterpret_cast<float4*>(hrow + j),
+                        make_float4(alpha * v[4 * e], alpha * v[4 * e + 1], alpha * v[4 * e + 2], alpha * v[4 * e + 3]));
+            } else {
+#pragma unroll
+              for (int x = 0; x < 4; ++x)
+                if (j + x >= i && j + x < g.d) atomicAdd(hrow + j + x, alpha * v[4 * e + x]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tmem_empty[buf]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// zero the upper triangle (i <= j) of H
+__global__ void zero_upper_kernel(float* __restrict__ H, long long ldh, int d) {
+  const int i = blockIdx.y;
+  for (int j = i + blockIdx.x * blockDim.x + threadIdx.x; j < d; j += gridDim.x * blockDim.x)
+    H[(long long)i * ldh + j] = 0.0f;
+}
+
+}  // namespace syrk
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+int choose_parts(long long tiles, long long kiters, int grid) {
+  // minimise the estimated makespan ceil(units / grid) * (kiters / parts + fill)
+  int best = 1;
+  double best_cost = 1e300;
+  const int max_parts = (int)std::min<long long>(64, std::max<long long>(1, kiters / 8));
+  for (int s = 1; s <= max_parts; ++s) {
+    const long long units = tiles * s;
+    const double rounds = std::ceil((double)units / grid);
+    const double cost = rounds * ((double)kiters / s + 4.0);
+    if (cost < best_cost * 0.999) { best_cost = cost; best = s; }
+  }
+  return best;
+}
+}  // namespace
+
+gptq_status syrk_accumulate(const uint16_t* X, long long n, long long d, long long ldx, float* H, long long ldh,
+                            float alpha, int zero_first, cudaStream_t stream) {
+  using namespace syrk;
+  if (zero_first) {
+    dim3 grid((unsigned)std::max<long long>(1, std::min<long long>((d + 255) / 256, 64)), (unsigned)d);
+    zero_upper_kernel<<<grid, 256, 0, stream>>>(H, ldh, (int)d);
+    count_launch();
+    if (gptq_status st = check_launch("zero_upper_kernel")) return st;
+  }
+  if (n == 0) return GPTQ_OK;
+
+  PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_fn();
+  if (!encode) return set_error(GPTQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  CUtensorMap tmap;
+  cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)n};
+  cuuint64_t strides[1] = {(cuuint64_t)ldx * 2};
+  cuuint32_t box[2] = {BOX, BK};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult cr = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(X), dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return set_error(GPTQ_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)cr);
+
+  Geometry g;
+  g.d = (int)d;
+  g.nr = (int)((d + BM - 1) / BM);
+  g.nc = (int)((d + BN - 1) / BN);
+  long long tiles = 0;
+  for (int r = 0; r < g.nr; ++r) tiles += g.nc - (r * BM) / BN;
+  g.tiles = (int)tiles;
+  g.kiters = (n + BK - 1) / BK;
+  const int sms = sm_count();
+  g.parts = choose_parts(tiles, g.kiters, sms);
+  const long long units = tiles * g.parts;
+  const int grid = (int)std::min<long long>(units, sms);
+
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(syrk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
+      return set_error(GPTQ_ERR_CUDA, "cudaFuncSetAttribute(syrk_kernel) failed");
+    attr_set = true;
+  }
+  syrk_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(tmap, H, ldh, g, alpha, device_error_word());
+  count_launch();
+  return check_launch("syrk_kernel");
+}
+
+}  // namespace gptq

@@ -1,0 +1,327 @@
+"""Python binding of the GPTQ C ABI (include/gptq.h).
+
+Argument marshalling only: every step of the path runs in the CUDA library
+``libgptq.so``. PyTorch provides device memory and the current stream. The
+functions keep the C names; they take torch tensors, check dtype/device/shape,
+allocate outputs and workspaces with torch when the caller passes none, and raise
+``GPTQError`` on a non-OK status.
+
+If the library has not been built, importing this module fails with an ImportError
+that says how to build it; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgptq.so")
+
+GPTQ_OK = 0
+GPTQ_ERR_INVALID_ARG = 1
+GPTQ_ERR_NOT_PD = 2
+GPTQ_ERR_NONFINITE = 3
+GPTQ_ERR_UNSUPPORTED = 4
+GPTQ_ERR_CUDA = 5
+GPTQ_ERR_TIMEOUT = 6
+GPTQ_WS_FACTOR = 0
+GPTQ_WS_QUANTIZE = 1
+
+_c_int, _c_i64, _c_size, _c_float, _vp = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float, ctypes.c_void_p
+
+# name -> (restype, argtypes); mirrors include/gptq.h
+SIGNATURES = {
+    "gptq_status_string": (ctypes.c_char_p, [_c_int]),
+    "gptq_last_error": (ctypes.c_char_p, []),
+    "gptq_version": (_c_int, []),
+    "gptq_launch_count": (ctypes.c_uint64, []),
+    "gptq_device_check": (_c_int, [_vp]),
+    "gptq_hessian_accumulate": (_c_int, [_vp, _c_i64, _c_i64, _c_i64, _vp, _c_i64, _c_float, _c_int, _vp]),
+    "gptq_workspace_size": (_c_size, [_c_int, _c_i64, _c_i64, _c_int, _c_int, _c_int]),
+    "gptq_factor": (_c_int, [_vp, _c_i64, _c_float, _c_int, _vp, _vp, _vp, _c_size, ctypes.POINTER(_c_i64), _vp]),
+    "gptq_factor_status": (_c_int, [_vp, ctypes.POINTER(_c_i64), _vp]),
+    "gptq_quantize_layer": (_c_int, [_vp, _c_int, _c_i64, _c_i64, _c_i64, _vp, _vp, _c_int, _c_int, _c_int, _vp, _vp,
+                                     _vp, _vp, _vp, _c_size, ctypes.POINTER(_c_i64), _vp]),
+    "gptq_unpack_codes": (_c_int, [_vp, _c_i64, _c_i64, _c_int, _vp, _vp]),
+}
+
+
+class GPTQError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        super().__init__(message)
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with "
+                          "`python -m post_weight_quantization_gb300.build` (nvcc, sm_103a)")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+def library() -> ctypes.CDLL:
+    return _lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != GPTQ_OK:
+        name = _lib.gptq_status_string(status).decode()
+        detail = _lib.gptq_last_error().decode()
+        raise GPTQError(status, f"{what}: {name}: {detail}")
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _need_cuda(t: torch.Tensor, name: str, dtypes) -> None:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} must have dtype in {dtypes}, got {t.dtype}")
+
+
+# ----------------------------------------------------------------------------------
+def gptq_status_string(status: int) -> str:
+    return _lib.gptq_status_string(status).decode()
+
+
+def gptq_last_error() -> str:
+    return _lib.gptq_last_error().decode()
+
+
+def gptq_version() -> int:
+    return _lib.gptq_version()
+
+
+def gptq_launch_count() -> int:
+    return int(_lib.gptq_launch_count())
+
+
+def gptq_device_check(stream=None) -> None:
+    _check(_lib.gptq_device_check(_stream(stream)), "gptq_device_check")
+
+
+def gptq_workspace_size(which: int, m: int, d: int, bits: int = 4, group_size: int = 128,
+                        blocksize: int = 128) -> int:
+    return int(_lib.gptq_workspace_size(which, m, d, bits, group_size, blocksize))
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor:
+    # torch's allocator returns 512-byte aligned blocks, above the 256 bytes the ABI needs
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def gptq_hessian_accumulate(X: torch.Tensor, H: torch.Tensor, alpha: float = 2.0, zero_first: bool = False,
+                            stream=None) -> torch.Tensor:
+    """H[i, j] (i <= j) = (0 if zero_first else H[i, j]) + alpha * sum_t X[t, i] X[t, j].
+
+    X: (n, d) bf16 (or its uint16 bits) on the GPU, row stride a multiple of 8.
+    H: (d, d) float32 on the GPU; only the upper triangle is written.
+    """
+    _need_cuda(X, "X", (torch.bfloat16, torch.uint16, torch.int16))
+    _need_cuda(H, "H", (torch.float32,))
+    if X.dim() != 2 or H.dim() != 2 or X.stride(1) != 1 or H.stride(1) != 1:
+        raise ValueError("X and H must be 2-D with unit column stride")
+    n, d = X.shape
+    if H.shape[0] != d or H.shape[1] != d:
+        raise ValueError("H must be d x d")
+    _check(_lib.gptq_hessian_accumulate(_ptr(X), n, d, X.stride(0), _ptr(H), H.stride(0), float(alpha),
+                                        int(bool(zero_first)), _stream(stream)), "gptq_hessian_accumulate")
+    return H
+
+
+def gptq_factor(H: torch.Tensor, percdamp: float = 0.01, act_order: bool = False,
+                Hinv1: Optional[torch.Tensor] = None, perm_out: Optional[torch.Tensor] = None,
+                ws: Optional[torch.Tensor] = None, sync: bool = True, stream=None):
+    """Damp H, optionally compute the act-order permutation, and return (Hinv1, perm, info).
+
+    With sync=True the call waits for the GPU and raises GPTQError on a failed
+    factorization (info holds the failing column); otherwise info is None.
+    """
+    _need_cuda(H, "H", (torch.float32,))
+    d = H.shape[0]
+    if H.dim() != 2 or H.shape[1] != d or not H.is_contiguous():
+        raise ValueError("H must be a contiguous d x d tensor")
+    dev = H.device
+    if Hinv1 is None:
+        Hinv1 = torch.empty((d, d), dtype=torch.float32, device=dev)
+    if act_order and perm_out is None:
+        perm_out = torch.empty(d, dtype=torch.int32, device=dev)
+    if ws is None:
+        ws = _workspace(gptq_workspace_size(GPTQ_WS_FACTOR, 0, d), dev)
+    info = _c_i64(-1)
+    st = _lib.gptq_factor(_ptr(H), d, float(percdamp), int(bool(act_order)), _ptr(perm_out) if act_order else None,
+                          _ptr(Hinv1), _ptr(ws), ws.numel(), ctypes.byref(info) if sync else None, _stream(stream))
+    _check(st, "gptq_factor")
+    return Hinv1, (perm_out if act_order else None), (int(info.value) if sync else None)
+
+
+@dataclass
+class QuantizedLayer:
+    qweight: torch.Tensor      # (m, ceil(d * bits / 32)) int32 words (uint32 bit patterns)
+    scales: torch.Tensor       # (m, G) float32
+    zeros: torch.Tensor        # (m, G) float32
+    col_losses: torch.Tensor   # (d,) float32
+    bits: int
+    group_size: int
+    d: int
+
+
+def gptq_quantize_layer(W: torch.Tensor, Hinv1: torch.Tensor, perm: Optional[torch.Tensor] = None, bits: int = 4,
+                        group_size: int = 128, blocksize: int = 128, out: Optional[QuantizedLayer] = None,
+                        ws: Optional[torch.Tensor] = None, sync: bool = False, stream=None) -> QuantizedLayer:
+    """Run the blocked GPTQ column loop on W (m x d, fp32 or bf16) with Hinv1 from gptq_factor."""
+    _need_cuda(W, "W", (torch.float32, torch.bfloat16))
+    _need_cuda(Hinv1, "Hinv1", (torch.float32,))
+    if W.dim() != 2 or W.stride(1) != 1:
+        raise ValueError("W must be 2-D with unit column stride")
+    m, d = W.shape
+    if Hinv1.shape != (d, d) or not Hinv1.is_contiguous():
+        raise ValueError("Hinv1 must be a contiguous d x d tensor")
+    if perm is not None:
+        _need_cuda(perm, "perm", (torch.int32,))
+    dev = W.device
+    G = 1 if group_size == -1 else (d // group_size if group_size > 0 else 1)
+    if out is None:
+        out = QuantizedLayer(
+            qweight=torch.empty((m, (d * bits + 31) // 32), dtype=torch.int32, device=dev),
+            scales=torch.empty((m, G), dtype=torch.float32, device=dev),
+            zeros=torch.empty((m, G), dtype=torch.float32, device=dev),
+            col_losses=torch.empty(d, dtype=torch.float32, device=dev),
+            bits=bits, group_size=group_size, d=d)
+    if ws is None:
+        ws = _workspace(gptq_workspace_size(GPTQ_WS_QUANTIZE, m, d, bits, group_size, blocksize), dev)
+    info = _c_i64(0)
+    st = _lib.gptq_quantize_layer(_ptr(W), 0 if W.dtype == torch.float32 else 1, m, d, W.stride(0), _ptr(Hinv1),
+                                  _ptr(perm), bits, group_size, blocksize, _ptr(out.qweight), _ptr(out.scales),
+                                  _ptr(out.zeros), _ptr(out.col_losses), _ptr(ws), ws.numel(),
+                                  ctypes.byref(info) if sync else None, _stream(stream))
+    _check(st, "gptq_quantize_layer")
+    return out
+
+
+def gptq_unpack_codes(qweight: torch.Tensor, m: int, d: int, bits: int, stream=None) -> torch.Tensor:
+    _need_cuda(qweight, "qweight", (torch.int32,))
+    codes = torch.empty((m, d), dtype=torch.uint8, device=qweight.device)
+    _check(_lib.gptq_unpack_codes(_ptr(qweight), m, d, bits, _ptr(codes), _stream(stream)), "gptq_unpack_codes")
+    return codes
+
+
+# ----------------------------------------------------------------------------------
+def quantize_layer(W: torch.Tensor, X_batches, bits: int = 4, group_size: int = 128, blocksize: int = 128,
+                   percdamp: float = 0.01, act_order: bool = False, alpha: float = 2.0, stream=None):
+    """The whole per-layer path: H from calibration batches, Hinv1, then the column loop.
+
+    Returns (QuantizedLayer, H, Hinv1, perm).
+    """
+    d = W.shape[1]
+    H = torch.empty((d, d), dtype=torch.float32, device=W.device)
+    first = True
+    for X in X_batches:
+        gptq_hessian_accumulate(X, H, alpha=alpha, zero_first=first, stream=stream)
+        first = False
+    if first:
+        raise ValueError("no calibration batch")
+    Hinv1, perm, _ = gptq_factor(H, percdamp=percdamp, act_order=act_order, stream=stream)
+    q = gptq_quantize_layer(W, Hinv1, perm, bits=bits, group_size=group_size, blocksize=blocksize, stream=stream)
+    return q, H, Hinv1, perm
+
+
+class HostPipeline:
+    """End-to-end quantization of one layer from host (pinned) buffers.
+
+    The calibration tokens are copied to the GPU in chunks on a copy stream while the
+    Hessian accumulates the previous chunk on the compute stream (two device chunk
+    buffers, ping-pong), then W is copied, the factor and the column loop run, and
+    the packed codes, scales, zeros and per-column losses are copied back. Device
+    buffers are allocated once per shape and reused across calls.
+    """
+
+    def __init__(self, m: int, d: int, bits: int = 4, group_size: int = 128, blocksize: int = 128,
+                 percdamp: float = 0.01, act_order: bool = False, chunk_tokens: int = 16384,
+                 w_dtype=torch.bfloat16, device="cuda"):
+        self.m, self.d, self.bits, self.group_size, self.blocksize = m, d, bits, group_size, blocksize
+        self.percdamp, self.act_order, self.chunk = percdamp, act_order, chunk_tokens
+        dev = torch.device(device)
+        self.xbuf = [torch.empty((chunk_tokens, d), dtype=torch.int16, device=dev) for _ in range(2)]
+        self.W = torch.empty((m, d), dtype=w_dtype, device=dev)
+        self.H = torch.empty((d, d), dtype=torch.float32, device=dev)
+        self.Hinv1 = torch.empty((d, d), dtype=torch.float32, device=dev)
+        self.perm = torch.empty(d, dtype=torch.int32, device=dev) if act_order else None
+        self.ws_f = _workspace(gptq_workspace_size(GPTQ_WS_FACTOR, 0, d), dev)
+        self.ws_q = _workspace(gptq_workspace_size(GPTQ_WS_QUANTIZE, m, d, bits, group_size, blocksize), dev)
+        G = 1 if group_size == -1 else d // group_size
+        self.out = QuantizedLayer(
+            qweight=torch.empty((m, (d * bits + 31) // 32), dtype=torch.int32, device=dev),
+            scales=torch.empty((m, G), dtype=torch.float32, device=dev),
+            zeros=torch.empty((m, G), dtype=torch.float32, device=dev),
+            col_losses=torch.empty(d, dtype=torch.float32, device=dev),
+            bits=bits, group_size=group_size, d=d)
+        self.host_out = QuantizedLayer(
+            qweight=torch.empty(self.out.qweight.shape, dtype=torch.int32, pin_memory=True),
+            scales=torch.empty(self.out.scales.shape, dtype=torch.float32, pin_memory=True),
+            zeros=torch.empty(self.out.zeros.shape, dtype=torch.float32, pin_memory=True),
+            col_losses=torch.empty(d, dtype=torch.float32, pin_memory=True),
+            bits=bits, group_size=group_size, d=d)
+        self.copy_stream = torch.cuda.Stream(device=dev)
+        self.copied = [torch.cuda.Event() for _ in range(2)]
+        self.consumed = [torch.cuda.Event() for _ in range(2)]
+
+    def bytes_h2d(self, n_tokens: int) -> int:
+        return n_tokens * self.d * 2 + self.W.numel() * self.W.element_size()
+
+    def bytes_d2h(self) -> int:
+        o = self.out
+        return sum(t.numel() * t.element_size() for t in (o.qweight, o.scales, o.zeros, o.col_losses))
+
+    def run(self, W_host: torch.Tensor, X_host: torch.Tensor, stream=None) -> QuantizedLayer:
+        """W_host (m x d, pinned, dtype of the pipeline), X_host (n x d bf16 bits as int16,
+        pinned). Returns host tensors; synchronize the stream before reading them."""
+        comp = torch.cuda.current_stream() if stream is None else stream
+        n = X_host.shape[0]
+        first = True
+        for c, t0 in enumerate(range(0, n, self.chunk)):
+            t1 = min(n, t0 + self.chunk)
+            b = c & 1
+            buf = self.xbuf[b][: t1 - t0]
+            with torch.cuda.stream(self.copy_stream):
+                if c >= 2:
+                    self.copy_stream.wait_event(self.consumed[b])
+                buf.copy_(X_host[t0:t1], non_blocking=True)
+                self.copied[b].record(self.copy_stream)
+            comp.wait_event(self.copied[b])
+            gptq_hessian_accumulate(buf, self.H, alpha=2.0, zero_first=first, stream=comp)
+            self.consumed[b].record(comp)
+            first = False
+        with torch.cuda.stream(comp):
+            self.W.copy_(W_host, non_blocking=True)
+        gptq_factor(self.H, percdamp=self.percdamp, act_order=self.act_order, Hinv1=self.Hinv1, perm_out=self.perm,
+                    ws=self.ws_f, sync=False, stream=comp)
+        gptq_quantize_layer(self.W, self.Hinv1, self.perm, bits=self.bits, group_size=self.group_size,
+                            blocksize=self.blocksize, out=self.out, ws=self.ws_q, stream=comp)
+        with torch.cuda.stream(comp):
+            for src, dst in ((self.out.qweight, self.host_out.qweight), (self.out.scales, self.host_out.scales),
+                             (self.out.zeros, self.host_out.zeros), (self.out.col_losses, self.host_out.col_losses)):
+                dst.copy_(src, non_blocking=True)
+        return self.host_out

@@ -1,0 +1,128 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports every
+function include/gptq.h declares, and rejects bad arguments before launching."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gptq.h")
+
+
+@pytest.fixture(scope="module")
+def g():
+    from post_weight_quantization_gb300 import build as b
+    if not os.path.exists(b.LIB_PATH):
+        b.build()
+    from post_weight_quantization_gb300 import gptq
+    return gptq
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(gptq_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ("gptq_hessian_accumulate", "gptq_factor", "gptq_quantize_layer", "gptq_workspace_size",
+                     "gptq_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(g):
+    lib = g.library()
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+        assert name in g.SIGNATURES, f"binding lacks {name}"
+
+
+def test_status_strings(g):
+    assert g.gptq_status_string(0) == "GPTQ_OK"
+    assert g.gptq_status_string(2) == "GPTQ_ERR_NOT_PD"
+    assert g.gptq_status_string(6) == "GPTQ_ERR_TIMEOUT"
+    assert g.gptq_status_string(99) == "GPTQ_ERR_UNKNOWN"
+    assert g.gptq_version() >= 100
+
+
+def test_workspace_sizes(g):
+    f1 = g.gptq_workspace_size(g.GPTQ_WS_FACTOR, 0, 1024)
+    f2 = g.gptq_workspace_size(g.GPTQ_WS_FACTOR, 0, 2048)
+    assert f1 >= 1024 * 1024 * 4 and f2 > f1 and f1 % 256 == 0
+    q = g.gptq_workspace_size(g.GPTQ_WS_QUANTIZE, 4096, 4096, 4, 128, 128)
+    assert q >= 4096 * 4096 * 4
+    assert g.gptq_workspace_size(g.GPTQ_WS_QUANTIZE, 4096, 4096, 4, 128, 100) == 0
+    assert g.gptq_workspace_size(7, 1, 1, 4, 128, 128) == 0
+    assert g.gptq_workspace_size(g.GPTQ_WS_FACTOR, 0, 0) == 0
+
+
+# fake, aligned, never dereferenced device addresses: validation must fail first
+P = 0x10000000
+
+
+def _err(g, status):
+    return g.gptq_status_string(status)
+
+
+def test_hessian_argument_checks(g):
+    lib = g.library()
+    before = g.gptq_launch_count()
+    assert lib.gptq_hessian_accumulate(P, 10, 64, 64, None, 64, 2.0, 1, None) == g.GPTQ_ERR_INVALID_ARG
+    assert lib.gptq_hessian_accumulate(None, 10, 64, 64, P, 64, 2.0, 1, None) == g.GPTQ_ERR_INVALID_ARG
+    assert lib.gptq_hessian_accumulate(P, 10, 60, 64, P, 64, 2.0, 1, None) == g.GPTQ_ERR_INVALID_ARG   # d % 8
+    assert lib.gptq_hessian_accumulate(P, 10, 64, 60, P, 64, 2.0, 1, None) == g.GPTQ_ERR_INVALID_ARG   # ldx < d
+    assert lib.gptq_hessian_accumulate(P + 2, 10, 64, 64, P, 64, 2.0, 1, None) == g.GPTQ_ERR_INVALID_ARG
+    assert lib.gptq_hessian_accumulate(P, 10, 64, 64, P, 66, 2.0, 1, None) == g.GPTQ_ERR_INVALID_ARG   # ldh % 4
+    assert lib.gptq_hessian_accumulate(P, -1, 64, 64, P, 64, 2.0, 1, None) == g.GPTQ_ERR_INVALID_ARG
+    assert lib.gptq_hessian_accumulate(P, 10, 64, 64, P, 64, float("nan"), 1, None) == g.GPTQ_ERR_INVALID_ARG
+    assert "X" in g.gptq_last_error() or "alpha" in g.gptq_last_error() or g.gptq_last_error()
+    # n == 0 without zero_first is a no-op that launches nothing
+    assert lib.gptq_hessian_accumulate(None, 0, 64, 64, P, 64, 2.0, 0, None) == g.GPTQ_OK
+    assert g.gptq_launch_count() == before
+
+
+def test_factor_argument_checks(g):
+    lib = g.library()
+    before = g.gptq_launch_count()
+    ws = g.gptq_workspace_size(g.GPTQ_WS_FACTOR, 0, 64)
+    info = ctypes.c_int64(0)
+    call = lambda H, d, pd, ao, perm, U, w, wb: lib.gptq_factor(H, d, pd, ao, perm, U, w, wb, ctypes.byref(info), None)
+    assert call(None, 64, 0.01, 0, None, P, P, ws) == g.GPTQ_ERR_INVALID_ARG
+    assert call(P, 0, 0.01, 0, None, P, P, ws) == g.GPTQ_ERR_INVALID_ARG
+    assert call(P, 64, -0.5, 0, None, P, P, ws) == g.GPTQ_ERR_INVALID_ARG
+    assert call(P, 64, float("nan"), 0, None, P, P, ws) == g.GPTQ_ERR_INVALID_ARG
+    assert call(P, 64, 0.01, 1, None, P, P, ws) == g.GPTQ_ERR_INVALID_ARG           # act-order without perm
+    assert call(P, 64, 0.01, 0, None, P, P, ws - 1) == g.GPTQ_ERR_INVALID_ARG       # workspace too small
+    assert call(P, 64, 0.01, 0, None, P, P + 64, ws) == g.GPTQ_ERR_INVALID_ARG      # workspace misaligned
+    assert g.gptq_launch_count() == before
+
+
+def test_quantize_argument_checks(g):
+    lib = g.library()
+    before = g.gptq_launch_count()
+    m, d = 64, 256
+    ws = g.gptq_workspace_size(g.GPTQ_WS_QUANTIZE, m, d, 4, 128, 128)
+
+    def call(bits=4, gs=128, bs=128, perm=None, wsb=ws, W=P, dt=0, ldw=d, dd=d):
+        return lib.gptq_quantize_layer(W, dt, m, dd, ldw, P, perm, bits, gs, bs, P, P, P, P, P, wsb, None, None)
+
+    assert call(bits=5) == g.GPTQ_ERR_INVALID_ARG
+    assert call(gs=96) == g.GPTQ_ERR_INVALID_ARG            # d % g != 0
+    assert call(gs=64, bs=96) == g.GPTQ_ERR_INVALID_ARG     # neither divides the other... 96 % 64 and 64 % 96
+    assert call(bs=0) == g.GPTQ_ERR_INVALID_ARG
+    assert call(W=None) == g.GPTQ_ERR_INVALID_ARG
+    assert call(dt=2) == g.GPTQ_ERR_INVALID_ARG
+    assert call(ldw=d - 1) == g.GPTQ_ERR_INVALID_ARG
+    assert call(wsb=ws - 1) == g.GPTQ_ERR_INVALID_ARG
+    assert call(bs=16, gs=128) == g.GPTQ_ERR_UNSUPPORTED    # valid, not built
+    assert call(gs=16, bs=32) == g.GPTQ_ERR_UNSUPPORTED
+    assert call(perm=P, gs=128) == g.GPTQ_ERR_UNSUPPORTED   # act-order with groups
+    assert g.gptq_launch_count() == before
+
+
+def test_unpack_argument_checks(g):
+    lib = g.library()
+    assert lib.gptq_unpack_codes(None, 4, 4, 4, P, None) == g.GPTQ_ERR_INVALID_ARG
+    assert lib.gptq_unpack_codes(P, 4, 4, 5, P, None) == g.GPTQ_ERR_INVALID_ARG

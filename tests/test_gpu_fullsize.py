@@ -1,0 +1,188 @@
+"""Full-size parity of the Llama-style 4096 x 4096 projection (262144 calibration
+tokens, heavy-tailed correlated activations with 1% outlier channels), in the launch
+configuration the benchmark times: one Hessian call over all tokens, one factor
+call, one column-loop call over all 4096 rows.
+
+The oracle cannot redo the whole layer in seconds, so it checks samples it can
+compute one by one (Hessian entries from the token columns, rows of the column loop
+with the same Hinv1: rows are independent), the whole Hinv1 (one fp64 LAPACK chain)
+and properties that hold at any size (the loss identity, code range, permutation).
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import gptq_oracle as orc
+from synth import bf16_bits_to_f32, gen_activations_into, workload
+
+pytestmark = pytest.mark.gpu
+
+CODE_TOL = 0.005
+SCALE_RTOL = 1e-4
+ERR_RTOL = 0.02
+
+
+@pytest.fixture(scope="module")
+def g():
+    from post_weight_quantization_gb300 import build as b
+    b.build()
+    from post_weight_quantization_gb300 import gptq
+    return gptq
+
+
+@pytest.fixture(scope="module")
+def layer_inputs():
+    wl = workload("llama_4096_g128")
+    layer = wl.layers[0]
+    spec = wl.acts[layer.hessian]
+    X = np.empty((spec.n, spec.d), dtype=np.uint16)
+    gen_activations_into(spec, X)
+    W = wl.weight(layer)
+    return W, X
+
+
+@pytest.fixture(scope="module")
+def gpu_hessian(g, layer_inputs):
+    W, X = layer_inputs
+    Xd = torch.from_numpy(X.view(np.int16)).cuda()
+    H = torch.empty((X.shape[1], X.shape[1]), dtype=torch.float32, device="cuda")
+    g.gptq_hessian_accumulate(Xd, H, alpha=2.0, zero_first=True)
+    torch.cuda.synchronize()
+    g.gptq_device_check()
+    del Xd
+    Hn = H.cpu().numpy().astype(np.float64)
+    Hfull = np.triu(Hn) + np.triu(Hn, 1).T
+    return H, Hfull
+
+
+def test_hessian_sampled_entries(layer_inputs, gpu_hessian):
+    W, X = layer_inputs
+    _, Hfull = gpu_hessian
+    rng = np.random.default_rng(0)
+    ch = np.sort(rng.choice(X.shape[1], size=40, replace=False))
+    Xs = bf16_bits_to_f32(X[:, ch]).astype(np.float64)         # one pass over the tokens
+    iu = np.triu_indices(len(ch))
+    ref = 2.0 * (Xs.T @ Xs)
+    got = Hfull[np.ix_(ch, ch)]
+    A = np.abs(Xs)
+    bound = 2 * 2.0 * X.shape[0] * 2.0 ** -24 * (A.T @ A)
+    # the worst-case bound of recursive fp32 summation, whatever the rounding of the
+    # tensor core's accumulator
+    assert np.all(np.abs(got - ref)[iu] <= bound[iu])
+
+
+@pytest.fixture(scope="module")
+def exact_hessian(layer_inputs):
+    """The oracle's Hessian of all 262144 tokens in float64 (chunked)."""
+    _, X = layer_inputs
+    H = None
+    for t0 in range(0, X.shape[0], 16384):
+        H = orc.hessian_accumulate(H, bf16_bits_to_f32(X[t0:t0 + 16384]))
+    return H
+
+
+@pytest.mark.parametrize("bits,gs,act_order", [(4, 128, False), (3, -1, True)])
+def test_end_to_end_full_size(g, layer_inputs, gpu_hessian, exact_hessian, bits, gs, act_order):
+    """The whole GPU path (its own Hessian and factor) against the oracle run on the exact
+    float64 Hessian, on sampled rows."""
+    W_bits, _ = layer_inputs
+    H, Hfull = gpu_hessian
+    H64 = exact_hessian
+    m, d = W_bits.shape
+    U, perm, _ = g.gptq_factor(H, percdamp=0.01, act_order=act_order)
+    Wd = torch.from_numpy(W_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    q = g.gptq_quantize_layer(Wd, U, perm, bits=bits, group_size=gs, blocksize=128, sync=True)
+    torch.cuda.synchronize()
+    g.gptq_device_check()
+    p = np.arange(d) if perm is None else perm.cpu().numpy().astype(np.int64)
+    if act_order:
+        po = orc.act_order_perm(H64)
+        hx = np.diag(H64)
+        # near-ties of diag(H) may order differently; every swap must be within fp32 noise
+        assert np.all(np.abs(hx[p] - hx[po]) <= 1e-3 * hx[po])
+    Hd, _ = orc.damp(H64, 0.01)
+    Uo = orc.hinv1(Hd[np.ix_(p, p)])
+    rows = np.sort(np.random.default_rng(2).choice(m, size=64, replace=False))
+    W = bf16_bits_to_f32(W_bits)
+    Wp = W[rows][:, p]
+    res64 = orc.gptq_columns(Wp.astype(np.float64), Uo, bits, gs, 128)
+    res32 = orc.gptq_columns(np.ascontiguousarray(Wp), Uo.astype(np.float32), bits, gs, 128, dtype=np.float32)
+    codes = g.gptq_unpack_codes(q.qweight, m, d, bits).cpu().numpy().astype(np.int64)[rows][:, p]
+    scales = q.scales.cpu().numpy()[rows].astype(np.float64)
+    zeros = q.zeros.cpu().numpy()[rows].astype(np.float64)
+    mism32 = np.mean(codes != res32["codes"])
+    assert mism32 <= CODE_TOL, mism32
+    assert np.max(np.abs(scales[:, 0] - res64["scales"][:, 0]) / res64["scales"][:, 0]) <= SCALE_RTOL
+    gsz = d if gs == -1 else gs
+    gi = np.arange(d) // gsz
+    What_p = (codes - zeros[:, gi]) * scales[:, gi]
+    Hp = H64[np.ix_(p, p)]
+    e_gpu = orc.relative_output_error(Wp.astype(np.float64), What_p, Hp)
+    for res in (res64, res32):
+        e_orc = orc.relative_output_error(Wp.astype(np.float64), res["W_hat"].astype(np.float64), Hp)
+        assert abs(e_gpu - e_orc) <= ERR_RTOL * e_orc, (e_gpu, e_orc)
+
+
+@pytest.mark.parametrize("bits,gs,act_order", [(4, 128, False), (3, -1, True)])
+def test_layer_full_size(g, layer_inputs, gpu_hessian, bits, gs, act_order):
+    W_bits, _ = layer_inputs
+    H, Hfull = gpu_hessian
+    m, d = W_bits.shape
+    U, perm, info = g.gptq_factor(H, percdamp=0.01, act_order=act_order)
+    assert info == -1
+    Wd = torch.from_numpy(W_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    q = g.gptq_quantize_layer(Wd, U, perm, bits=bits, group_size=gs, blocksize=128, sync=True)
+    torch.cuda.synchronize()
+    g.gptq_device_check()
+
+    # ---- Hinv1 against the fp64 three-step chain on the same (GPU) Hessian
+    p = np.arange(d) if perm is None else perm.cpu().numpy().astype(np.int64)
+    assert np.array_equal(np.sort(p), np.arange(d))
+    if act_order:
+        assert np.all(np.diff(np.diag(Hfull)[p]) <= 0)
+    Hd, lam = orc.damp(Hfull, 0.01)
+    Uo = orc.hinv1(Hd[np.ix_(p, p)])
+    Ug = U.cpu().numpy()
+    assert np.all(np.tril(Ug, -1) == 0) and np.all(np.diag(Ug) > 0)
+    kappa_bound = np.trace(Hd) / lam          # lambda_max <= trace, lambda_min >= lambda
+    rel = np.linalg.norm(Ug - Uo) / np.linalg.norm(Uo)
+    assert rel < 50 * kappa_bound * 2.0 ** -24, rel
+
+    # ---- sampled rows of the column loop with the same Hinv1 (rows are independent)
+    rows = np.sort(np.random.default_rng(1).choice(m, size=64, replace=False))
+    W = bf16_bits_to_f32(W_bits)
+    Wp = W[rows][:, p]
+    res64 = orc.gptq_columns(Wp.astype(np.float64), Ug.astype(np.float64), bits, gs, 128)
+    res32 = orc.gptq_columns(np.ascontiguousarray(Wp), Ug, bits, gs, 128, dtype=np.float32)
+    codes_all = g.gptq_unpack_codes(q.qweight, m, d, bits).cpu().numpy().astype(np.int64)
+    codes = codes_all[rows][:, p]
+    scales = q.scales.cpu().numpy()[rows].astype(np.float64)
+    zeros = q.zeros.cpu().numpy()[rows].astype(np.float64)
+    mism32 = np.mean(codes != res32["codes"])
+    assert mism32 <= CODE_TOL, mism32
+    gsz = d if gs == -1 else gs
+    s32, z32 = orc.quant_params(np.ascontiguousarray(Wp[:, :gsz]), bits)
+    assert np.array_equal(zeros[:, 0].astype(np.float32), z32)
+    assert np.array_equal(scales[:, 0].astype(np.float32), s32)
+    assert np.max(np.abs(scales[:, 0] - res64["scales"][:, 0]) / res64["scales"][:, 0]) <= SCALE_RTOL
+    gi = np.arange(d) // gsz
+    What_p = (codes - zeros[:, gi]) * scales[:, gi]
+    Hp = Hfull[np.ix_(p, p)]
+    e_gpu = orc.relative_output_error(Wp.astype(np.float64), What_p, Hp)
+    for res in (res64, res32):
+        e_orc = orc.relative_output_error(Wp.astype(np.float64), res["W_hat"].astype(np.float64), Hp)
+        assert abs(e_gpu - e_orc) <= ERR_RTOL * e_orc, (e_gpu, e_orc)
+
+    # ---- properties at full size
+    assert codes_all.min() >= 0 and codes_all.max() <= 2 ** bits - 1
+    Gn = 1 if gs == -1 else d // gs
+    sc = q.scales.double()
+    ze = q.zeros.double()
+    gcols = torch.arange(d, device="cuda") // gsz
+    What = (torch.from_numpy(codes_all).cuda().double() - ze[:, gcols]) * sc[:, gcols]
+    dW = Wd.double() - What
+    Hdg = torch.from_numpy(Hd).cuda()
+    quad = 0.5 * float(((dW @ Hdg) * dW).sum())
+    total = float(q.col_losses.double().sum())
+    assert abs(total - quad) <= 1e-2 * quad, (total, quad)     # loss identity (sum of Losses1)
+    assert Gn == q.scales.shape[1]

@@ -1,0 +1,332 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the same
+seeded inputs, stage by stage and end to end.
+
+Tolerances (GPTQ's code choices are chaotic: one flipped code shifts the rest of its
+row, so codes are compared as a mismatch fraction):
+  * Hessian: exact for integer-valued bf16 inputs; otherwise within the fp32
+    summation bound 2 * n * 2^-24 * sum_t |x_ti| |x_tj|.
+  * Hinv1: relative Frobenius error below 50 * kappa(H_d) * 2^-24.
+  * Column loop on one block: codes, scales and zeros identical to the oracle's
+    float32 arithmetic (the kernel rounds each step the same way).
+  * Several blocks and end to end: at most 0.5% of codes differ from the oracle
+    run in float32 (integer decisions are compared in the precision the listing
+    quantizes in: bf16 rows with max == -min put -min/scale exactly on a .5 tie that
+    float32 and float64 round apart), first-group scales and zeros identical to the
+    float32 decision and within 1e-4 of the float64 oracle's scales, and the layer's
+    relative output error within 2% of both oracle runs'.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import gptq_oracle as orc
+from synth import ActSpec, bf16_bits_to_f32, make_activations, make_weight
+
+pytestmark = pytest.mark.gpu
+
+CODE_TOL = 0.005
+SCALE_RTOL = 1e-4
+ERR_RTOL = 0.02
+
+
+@pytest.fixture(scope="module")
+def g():
+    from post_weight_quantization_gb300 import build as b
+    b.build()
+    from post_weight_quantization_gb300 import gptq
+    return gptq
+
+
+def dev_bits(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+
+
+def gpu_hessian(g, X_bits, alpha=2.0):
+    d = X_bits.shape[1]
+    H = torch.empty((d, d), dtype=torch.float32, device="cuda")
+    g.gptq_hessian_accumulate(dev_bits(X_bits), H, alpha=alpha, zero_first=True)
+    return H
+
+
+def upper_of(Hg: torch.Tensor) -> np.ndarray:
+    H = Hg.cpu().numpy().astype(np.float64)
+    return np.triu(H) + np.triu(H, 1).T
+
+
+def gpu_codes(g, q, m, d, bits):
+    return g.gptq_unpack_codes(q.qweight, m, d, bits).cpu().numpy().astype(np.int64)
+
+
+def first_group_params(W32, bits, gs, perm=None):
+    """(scale, zero) of every row's first group from the original weights, in float32:
+    the decision the listing takes in float32 before any compensation."""
+    Wp = W32 if perm is None else W32[:, perm]
+    g = Wp.shape[1] if gs == -1 else gs
+    return orc.quant_params(np.ascontiguousarray(Wp[:, :g], dtype=np.float32), bits)
+
+
+def check_layer(W64, res64, res32, codes, scales, zeros, H0, bits, gs, perm=None):
+    """Tolerance checks of a GPU result against the oracle on the same W and H.
+
+    Integer decisions (codes, zeros) are compared with the oracle run in float32, the
+    precision the pages' listing quantizes in; scales with the float64 oracle
+    (1e-4 relative, first group of each row); the output error with both.
+    """
+    s32, z32 = first_group_params(W64.astype(np.float32), bits, gs, perm)
+    assert np.array_equal(zeros[:, 0].astype(np.float32), z32), "first-group zeros differ"
+    assert np.array_equal(scales[:, 0].astype(np.float32), s32), "first-group scales differ"
+    srel = np.max(np.abs(scales[:, 0] - res64["scales"][:, 0]) / res64["scales"][:, 0])
+    assert srel <= SCALE_RTOL, srel
+    mism32 = np.mean(codes != res32["codes"])
+    assert mism32 <= CODE_TOL, mism32
+    gi = np.arange(W64.shape[1]) // (W64.shape[1] if gs == -1 else gs)
+    What = (codes - zeros[:, gi]) * scales[:, gi]
+    e_gpu = orc.relative_output_error(W64, What, H0)
+    for res in (res64, res32):
+        e_orc = orc.relative_output_error(W64, res["W_hat"].astype(np.float64), H0)
+        assert abs(e_gpu - e_orc) <= ERR_RTOL * e_orc, (e_gpu, e_orc)
+    assert codes.min() >= 0 and codes.max() <= 2 ** bits - 1
+    return {"mismatch_fp32": mism32, "mismatch_fp64": float(np.mean(codes != res64["codes"])), "scale_rel": srel,
+            "err_gpu": e_gpu}
+
+
+# ----------------------------------------------------------------------------------
+# Stage 1: Hessian
+# ----------------------------------------------------------------------------------
+@pytest.mark.parametrize("n,d,ldx", [(512, 256, 256), (1000, 264, 264), (4096, 512, 520), (130, 8, 8),
+                                     (64, 1032, 1032), (2304, 640, 640)])
+def test_syrk_exact_on_integers(g, n, d, ldx):
+    rng = np.random.default_rng(n + d)
+    Xi = rng.integers(-8, 9, size=(n, d)).astype(np.float32)
+    Xb = np.zeros((n, ldx), dtype=np.uint16)
+    Xb[:, :d] = (Xi.view(np.uint32) >> 16).astype(np.uint16)   # small integers are exact in bf16
+    Xdev = dev_bits(Xb)[:, :d]
+    H = torch.full((d, d), 7.0, dtype=torch.float32, device="cuda")
+    g.gptq_hessian_accumulate(Xdev, H, alpha=2.0, zero_first=True)
+    Hc = H.cpu().numpy()
+    ref = orc.hessian([Xi.astype(np.float64)])
+    iu = np.triu_indices(d)
+    assert np.array_equal(Hc[iu], ref[iu].astype(np.float32))
+    il = np.tril_indices(d, -1)
+    assert np.all(Hc[il] == 7.0), "the strictly lower triangle must stay untouched"
+    g.gptq_device_check()
+
+
+def test_syrk_accumulates_across_batches(g):
+    rng = np.random.default_rng(1)
+    Xi = rng.integers(-8, 9, size=(3000, 384)).astype(np.float32)
+    Xb = (Xi.view(np.uint32) >> 16).astype(np.uint16)
+    H = torch.empty((384, 384), dtype=torch.float32, device="cuda")
+    g.gptq_hessian_accumulate(dev_bits(Xb[:1000]), H, alpha=2.0, zero_first=True)
+    g.gptq_hessian_accumulate(dev_bits(Xb[1000:2100]), H, alpha=2.0, zero_first=False)
+    g.gptq_hessian_accumulate(dev_bits(Xb[2100:]), H, alpha=2.0, zero_first=False)
+    ref = orc.hessian([Xi[:1000], Xi[1000:2100], Xi[2100:]])
+    iu = np.triu_indices(384)
+    assert np.array_equal(H.cpu().numpy()[iu], ref[iu])
+
+
+def test_syrk_float_error_bound(g):
+    spec = ActSpec("heavy_tail", 8192, 512, seed=5)
+    Xb = make_activations(spec)
+    X = bf16_bits_to_f32(Xb).astype(np.float64)
+    Hg = upper_of(gpu_hessian(g, Xb))
+    ref = orc.hessian([X])
+    A = np.abs(X)
+    bound = 2 * 2.0 * X.shape[0] * 2.0 ** -24 * (A.T @ A) + 1e-30
+    assert np.all(np.abs(Hg - ref) <= bound)
+    # and far tighter on average
+    assert np.abs(Hg - ref).sum() / np.abs(ref).sum() < 1e-5
+
+
+# ----------------------------------------------------------------------------------
+# Stage 2: factor
+# ----------------------------------------------------------------------------------
+def _spd(d, n, seed):
+    Xb = make_activations(ActSpec("heavy_tail", n, d, seed=seed))
+    X = bf16_bits_to_f32(Xb).astype(np.float64)
+    return orc.hessian([X])
+
+
+@pytest.mark.parametrize("d,n", [(256, 1024), (1000, 4096), (1024, 600), (100, 64)])
+def test_factor_matches_three_step_chain(g, d, n):
+    H = _spd(d, n, seed=d)
+    Hg = torch.from_numpy(H.astype(np.float32)).cuda()
+    U, _, info = g.gptq_factor(Hg, percdamp=0.01)
+    assert info == -1
+    Ug = U.cpu().numpy().astype(np.float64)
+    Hd, _ = orc.damp(H.astype(np.float32).astype(np.float64), 0.01)
+    Uo = orc.hinv1(Hd)
+    kappa = np.linalg.cond(Hd)
+    assert np.all(np.tril(Ug, -1) == 0)
+    assert np.all(np.diag(Ug) > 0)
+    rel = np.linalg.norm(Ug - Uo) / np.linalg.norm(Uo)
+    assert rel < 50 * kappa * 2.0 ** -24, (rel, kappa)
+
+
+def test_factor_diagonal_closed_form(g):
+    h = np.linspace(0.5, 4.0, 300)
+    Hg = torch.from_numpy(np.diag(h).astype(np.float32)).cuda()
+    U, _, _ = g.gptq_factor(Hg, percdamp=0.01)
+    lam = 0.01 * np.mean(h.astype(np.float32))
+    ref = 1.0 / np.sqrt(h.astype(np.float32) + np.float32(lam))
+    Ug = U.cpu().numpy()
+    np.testing.assert_allclose(np.diag(Ug), ref, rtol=4e-7)
+    assert np.count_nonzero(Ug - np.diag(np.diag(Ug))) == 0
+
+
+def test_factor_act_order_permutation(g):
+    H = _spd(384, 2048, seed=9)
+    H[5, 5] = H[17, 17] = H[200, 200] = H[100, 100]      # ties: lower index first
+    Hg = torch.from_numpy(H.astype(np.float32)).cuda()
+    U, perm, info = g.gptq_factor(Hg, percdamp=0.01, act_order=True)
+    po = orc.act_order_perm(H.astype(np.float32).astype(np.float64))
+    assert np.array_equal(perm.cpu().numpy(), po)
+    Hd, _ = orc.damp(H.astype(np.float32).astype(np.float64), 0.01)
+    Uo = orc.hinv1(Hd[np.ix_(po, po)])
+    rel = np.linalg.norm(U.cpu().numpy() - Uo) / np.linalg.norm(Uo)
+    assert rel < 50 * np.linalg.cond(Hd) * 2.0 ** -24
+
+
+def test_factor_reports_non_pd(g):
+    H = _spd(128, 512, seed=3)
+    H[40, :] = 0.0
+    H[:, 40] = 0.0
+    Hg = torch.from_numpy(H.astype(np.float32)).cuda()
+    with pytest.raises(g.GPTQError) as ei:
+        g.gptq_factor(Hg, percdamp=0.0)
+    assert ei.value.status == g.GPTQ_ERR_NOT_PD
+    Hn = H.copy()
+    Hn[7, 7] = -1.0
+    with pytest.raises(g.GPTQError) as ei:
+        g.gptq_factor(torch.from_numpy(Hn.astype(np.float32)).cuda(), percdamp=0.0)
+    assert ei.value.status == g.GPTQ_ERR_NOT_PD
+    Hn[7, 7] = np.nan
+    with pytest.raises(g.GPTQError) as ei:
+        g.gptq_factor(torch.from_numpy(Hn.astype(np.float32)).cuda(), percdamp=0.01)
+    assert ei.value.status == g.GPTQ_ERR_NONFINITE
+    # damping rescues the singular case (the pages' reason for it)
+    _, _, info = g.gptq_factor(Hg, percdamp=0.01)
+    assert info == -1
+    g.gptq_device_check()
+
+
+# ----------------------------------------------------------------------------------
+# Stage 3: the column loop with the same Hinv1 on both sides
+# ----------------------------------------------------------------------------------
+def _layer(m, d, n, seed):
+    W = bf16_bits_to_f32(make_weight(m, d, seed))
+    Xb = make_activations(ActSpec("heavy_tail", n, d, seed=seed))
+    return W, Xb
+
+
+@pytest.mark.parametrize("bits,gs", [(4, 128), (3, -1), (2, 64), (8, 32), (4, 32)])
+def test_one_block_identical_to_float32_oracle(g, bits, gs):
+    m, d = 96, 128
+    W, Xb = _layer(m, d, 2048, seed=bits * 7 + abs(gs))
+    H = orc.hessian([bf16_bits_to_f32(Xb)])
+    Hd, _ = orc.damp(H, 0.01)
+    U32 = orc.hinv1(Hd).astype(np.float32)
+    res = orc.gptq_columns(W.astype(np.float32), U32, bits, gs, 128, dtype=np.float32)
+    q = g.gptq_quantize_layer(torch.from_numpy(W).cuda(), torch.from_numpy(U32).cuda(), bits=bits,
+                              group_size=gs, blocksize=128, sync=True)
+    codes = gpu_codes(g, q, m, d, bits)
+    assert np.array_equal(codes, res["codes"])
+    assert np.array_equal(q.scales.cpu().numpy(), res["scales"])
+    assert np.array_equal(q.zeros.cpu().numpy(), res["zeros"])
+    np.testing.assert_allclose(q.col_losses.cpu().numpy(), res["losses"].sum(0), rtol=1e-5, atol=1e-30)
+
+
+@pytest.mark.parametrize("bits,gs,bs", [(4, 128, 128), (4, 128, 32), (2, 64, 128), (4, 256, 128), (3, -1, 64)])
+def test_column_loop_matches_oracle(g, bits, gs, bs):
+    m, d = 544, 1024
+    W, Xb = _layer(m, d, 8192, seed=bits + bs + abs(gs))
+    H = orc.hessian([bf16_bits_to_f32(Xb)])
+    Hd, _ = orc.damp(H, 0.01)
+    U32 = orc.hinv1(Hd).astype(np.float32)
+    W64 = W.astype(np.float64)
+    res64 = orc.gptq_columns(W64, U32.astype(np.float64), bits, gs, bs)
+    res32 = orc.gptq_columns(W, U32, bits, gs, bs, dtype=np.float32)
+    q = g.gptq_quantize_layer(torch.from_numpy(W).cuda(), torch.from_numpy(U32).cuda(), bits=bits,
+                              group_size=gs, blocksize=bs, sync=True)
+    codes = gpu_codes(g, q, m, d, bits)
+    check_layer(W64, res64, res32, codes, q.scales.cpu().numpy().astype(np.float64),
+                q.zeros.cpu().numpy().astype(np.float64), H, bits, gs)
+    np.testing.assert_allclose(q.col_losses.cpu().numpy().sum(), res64["losses"].sum(), rtol=0.01)
+
+
+def test_packing_layout_matches_oracle(g):
+    m, d, bits = 40, 384, 3
+    W, Xb = _layer(m, d, 2048, seed=77)
+    H = orc.hessian([bf16_bits_to_f32(Xb)])
+    Hd, _ = orc.damp(H, 0.01)
+    U32 = orc.hinv1(Hd).astype(np.float32)
+    q = g.gptq_quantize_layer(torch.from_numpy(W).cuda(), torch.from_numpy(U32).cuda(), bits=bits,
+                              group_size=128, blocksize=128)
+    words = q.qweight.cpu().numpy().view(np.uint32)
+    codes = gpu_codes(g, q, m, d, bits)
+    assert np.array_equal(orc.pack_codes(codes, bits), words)
+    assert np.array_equal(orc.unpack_codes(words, bits, d), codes)
+
+
+def test_nonfinite_weight_is_reported(g):
+    W = np.zeros((32, 128), dtype=np.float32)
+    W[3, 7] = np.nan
+    U = torch.eye(128, dtype=torch.float32, device="cuda")
+    with pytest.raises(g.GPTQError) as ei:
+        g.gptq_quantize_layer(torch.from_numpy(W).cuda(), U, bits=4, group_size=128, sync=True)
+    assert ei.value.status == g.GPTQ_ERR_NONFINITE
+
+
+# ----------------------------------------------------------------------------------
+# End to end: SYRK -> factor -> column loop, against the oracle from the same bytes
+# ----------------------------------------------------------------------------------
+def _end_to_end(g, W_bits, X_bits, bits, gs, bs, act_order):
+    m, d = W_bits.shape
+    W = bf16_bits_to_f32(W_bits)
+    Wd = dev_bits(W_bits).view(torch.bfloat16)
+    q, Hg, U, perm = g.quantize_layer(Wd, [dev_bits(X_bits)], bits=bits, group_size=gs, blocksize=bs,
+                                      act_order=act_order)
+    torch.cuda.synchronize()
+    g.gptq_device_check()
+    H = orc.hessian([bf16_bits_to_f32(X_bits)])
+    res64 = orc.gptq_layer(W.astype(np.float64), H, bits, gs, bs, 0.01, act_order)
+    res32 = orc.gptq_layer(W, H.astype(np.float32), bits, gs, bs, 0.01, act_order, dtype=np.float32)
+    p = None
+    if act_order:
+        p = perm.cpu().numpy().astype(np.int64)
+        assert np.array_equal(np.sort(p), np.arange(d))
+        hg = np.diag(Hg.cpu().numpy())[p]
+        assert np.all(np.diff(hg) <= 0), "the permutation must sort the GPU's diag(H) descending"
+        if not np.array_equal(p, res64["perm"]):
+            # near-ties of diag(H) within fp32 rounding may order differently; both orders
+            # are valid, so the oracle follows the GPU's order for the comparison
+            hx = np.diag(H)
+            assert np.all(np.abs(hx[p] - hx[res64["perm"]]) <= 1e-6 * hx.max())
+    codes = gpu_codes(g, q, m, d, bits)
+    return check_layer(W.astype(np.float64), res64, res32, codes, q.scales.cpu().numpy().astype(np.float64),
+                       q.zeros.cpu().numpy().astype(np.float64), H, bits, gs, p)
+
+
+def test_end_to_end_toy_256(g):
+    """The 256 x 256 toy layer: 512 Gaussian correlated tokens, 4 outlier channels x20, 4-bit g128."""
+    W_bits = make_weight(256, 256, 0)
+    X_bits = make_activations(ActSpec("gauss_cov", 512, 256, seed=0, outlier_count=4, outlier_scale=20.0))
+    _end_to_end(g, W_bits, X_bits, 4, 128, 128, False)
+
+
+@pytest.mark.parametrize("m,d,n,bits,gs,ao", [(520, 1024, 16384, 4, 128, False), (640, 768, 8192, 3, -1, True),
+                                              (384, 512, 4096, 2, 64, False), (1000, 1536, 4096, 4, 128, False)])
+def test_end_to_end_mid(g, m, d, n, bits, gs, ao):
+    W_bits = make_weight(m, d, 31)
+    X_bits = make_activations(ActSpec("heavy_tail", n, d, seed=31))
+    _end_to_end(g, W_bits, X_bits, bits, gs, 128, ao)
+
+
+def test_launch_counter_moves(g):
+    before = g.gptq_launch_count()
+    H = torch.empty((64, 64), dtype=torch.float32, device="cuda")
+    X = torch.zeros((128, 64), dtype=torch.bfloat16, device="cuda")
+    g.gptq_hessian_accumulate(X, H, zero_first=True)
+    torch.cuda.synchronize()
+    assert g.gptq_launch_count() > before
+    assert float(torch.triu(H).abs().max()) == 0.0
