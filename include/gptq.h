@@ -165,6 +165,29 @@ gptq_status gptq_factor(const float* H, int64_t d, float percdamp, int act_order
 gptq_status gptq_factor_status(const void* ws, int64_t* info, gptq_stream_t stream);
 
 /*
+ * gptq_factor without a caller workspace, for callers that cannot allocate device
+ * memory: code inside a runtime that owns the GPU's memory budget through its own
+ * pool, or a pipeline that cannot take cudaMalloc's implicit device synchronization.
+ * The pages have no counterpart of this call; it exists only for such callers.
+ *
+ * Same arguments, results and status codes as gptq_factor, minus ws / ws_bytes. The
+ * scratch is a device array inside the library sized for d <= 2048 (16 MiB + 256
+ * bytes), held on every GPU that loads the library until the process exits;
+ * d > 2048 returns GPTQ_ERR_INVALID_ARG before anything is launched. The call
+ * allocates nothing.
+ *
+ * The first call on a device (with that device current) looks up the array's device
+ * address and caches it; make that first call before any stream capture. All calls
+ * on a device share the one array and it keeps the last call's contents (nothing in
+ * it needs to start at zero): calls whose work overlaps on the GPU -- on different
+ * streams, or from different threads -- race on it and must be serialized by the
+ * caller.
+ */
+gptq_status gptq_factor_static(const float* H, int64_t d, float percdamp, int act_order,
+                               int32_t* perm_out, float* Hinv1, int64_t* info,
+                               gptq_stream_t stream);
+
+/*
  * Stage 3 -- the blocked GPTQ column loop.
  *
  * Defined by "GPTQ, Line by Line", question "Why does GPTQ process the weight matrix

@@ -44,6 +44,7 @@ SIGNATURES = {
     "gptq_workspace_size": (_c_size, [_c_int, _c_i64, _c_i64, _c_int, _c_int, _c_int]),
     "gptq_factor": (_c_int, [_vp, _c_i64, _c_float, _c_int, _vp, _vp, _vp, _c_size, ctypes.POINTER(_c_i64), _vp]),
     "gptq_factor_status": (_c_int, [_vp, ctypes.POINTER(_c_i64), _vp]),
+    "gptq_factor_static": (_c_int, [_vp, _c_i64, _c_float, _c_int, _vp, _vp, ctypes.POINTER(_c_i64), _vp]),
     "gptq_quantize_layer": (_c_int, [_vp, _c_int, _c_i64, _c_i64, _c_i64, _vp, _vp, _c_int, _c_int, _c_int, _vp, _vp,
                                      _vp, _vp, _vp, _c_size, ctypes.POINTER(_c_i64), _vp]),
     "gptq_unpack_codes": (_c_int, [_vp, _c_i64, _c_i64, _c_int, _vp, _vp]),
@@ -174,6 +175,25 @@ def gptq_factor(H: torch.Tensor, percdamp: float = 0.01, act_order: bool = False
     st = _lib.gptq_factor(_ptr(H), d, float(percdamp), int(bool(act_order)), _ptr(perm_out) if act_order else None,
                           _ptr(Hinv1), _ptr(ws), ws.numel(), ctypes.byref(info) if sync else None, _stream(stream))
     _check(st, "gptq_factor")
+    return Hinv1, (perm_out if act_order else None), (int(info.value) if sync else None)
+
+
+def gptq_factor_static(H: torch.Tensor, Hinv1: torch.Tensor, percdamp: float = 0.01, act_order: bool = False,
+                       perm_out: Optional[torch.Tensor] = None, sync: bool = True, stream=None):
+    """gptq_factor with the library's own device scratch (d <= 2048) instead of a workspace,
+    for callers that cannot allocate device memory. Outputs must be passed in."""
+    _need_cuda(H, "H", (torch.float32,))
+    _need_cuda(Hinv1, "Hinv1", (torch.float32,))
+    d = H.shape[0]
+    if not H.is_contiguous() or not Hinv1.is_contiguous() or Hinv1.shape != H.shape:
+        raise ValueError("H and Hinv1 must be contiguous d x d tensors")
+    if act_order:
+        _need_cuda(perm_out, "perm_out", (torch.int32,))
+    info = _c_i64(-1)
+    st = _lib.gptq_factor_static(_ptr(H), d, float(percdamp), int(bool(act_order)),
+                                 _ptr(perm_out) if act_order else None, _ptr(Hinv1),
+                                 ctypes.byref(info) if sync else None, _stream(stream))
+    _check(st, "gptq_factor_static")
     return Hinv1, (perm_out if act_order else None), (int(info.value) if sync else None)
 
 
