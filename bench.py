@@ -14,6 +14,7 @@ over ranks divided by the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -45,6 +46,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--threads", type=int, default=None, help="host threads for input generation")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="calibration tokens (default: the workload's); smaller cases are for profiling")
     return ap.parse_args()
 
 
@@ -234,6 +237,8 @@ def run_gpu(args):
     wl = workload(args.workload)
     layer = wl.layers[args.layer]
     spec = wl.acts[layer.hessian]
+    if args.tokens:
+        spec = dataclasses.replace(spec, n=int(args.tokens))
     m, d, n = layer.m, layer.d, spec.n
 
     # ---- inputs: pinned host buffers (also the end-to-end source), then HBM copies
@@ -369,6 +374,10 @@ def run_gpu(args):
                "stages_s": {k: round(r[k], 3) for k in ("syrk_s", "factor_s", "loop_s")}}
 
     if rank == 0:
+        if args.tokens:
+            line_note = {"note": f"profiling case: {n} tokens instead of the workload's {wl.acts[layer.hessian].n}"}
+        else:
+            line_note = {}
         line = {"metric": METRIC, "value": round(value, 4), "unit": "Mweights/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16+f32",
@@ -383,7 +392,8 @@ def run_gpu(args):
                 "quantize_only_ms": round(statistics.mean(st_ms["factor"]) + statistics.mean(st_ms["quantize"]), 4),
                 "syrk_tflops": round(syrk_tflops, 2),
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-                "clocks": clk, "wall_s_timed_region": round(t_wall, 4), "input_generation_s": round(t_gen, 2)}
+                "clocks": clk, "wall_s_timed_region": round(t_wall, 4), "input_generation_s": round(t_gen, 2),
+                **line_note}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

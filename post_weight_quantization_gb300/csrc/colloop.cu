@@ -13,9 +13,10 @@
 //
 // Kernels:
 //   prep_kernel        fp32 working copy of W in processing order; NaN/Inf check
-//   colblock_kernel<BS> one thread per row; the row's BS weights stay in registers,
-//                      the Hinv1 diagonal block sits in shared memory (every thread
-//                      reads the same entry: broadcast); codes are packed into the
+//   colblock_kernel<BS> one thread per row, the block as 32-column sub-blocks whose
+//                      weights stay in registers (the block's later columns wait in
+//                      shared memory); the Hinv1 diagonal block sits in shared memory
+//                      (every thread reads the same entry: broadcast); codes are packed into the
 //                      output bitstream as they are produced; Err1 is written
 //                      column-major (coalesced) for the lazy update; per-column loss
 //                      partial sums come from warp-shuffle reductions
@@ -97,7 +98,8 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // State of one row (one thread) while a block is processed.
 struct RowState {
-  const float* wrow;      // the row of the working copy
+  const float* wrow;      // the row of the working copy (global)
+  float* wsm;             // the row's block columns in shared memory (stride 1)
   float s, z, inv_s;      // current group's scale, zero and RN(1 / scale)
   uint64_t acc;           // code bits not yet stored
   int nacc, widx;         // bits held in acc; next output word
@@ -106,7 +108,7 @@ struct RowState {
 struct BlockArgs {
   const float* Us;        // Hinv1 diagonal block (shared memory), row-major BS x BS
   const float* inv_u;     // RN(1 / Hinv1[j][j]) of the block (shared memory)
-  int m, d, i1, ncols, g, G, wpr, lde, bits, r, lane;
+  int m, d, i1, ncols, g, G, wpr, lde, bits, r, lane, bs;
   bool active, natural;
   float qmax, inv_qmax;
   uint32_t* qweight;
@@ -114,19 +116,32 @@ struct BlockArgs {
   float *scales, *zeros, *errT, *part;
 };
 
-// Column T of the block; T is a compile-time constant so that w[] stays in registers.
-template <int BS, int T>
-__device__ __forceinline__ void column_step(float (&w)[BS], RowState& st, const BlockArgs& a) {
-  if (T >= a.ncols) return;
-  const int j = a.i1 + T;
-  if constexpr (T % 32 == 0) {
+constexpr int SUB = 32;   // columns per register-resident sub-block
+
+// Column T of sub-block c0 (block-local column c0 + T). T is a compile-time constant so
+// that w[] and e[] stay in registers; the sub-block's other columns live in w[].
+template <int T>
+__device__ __forceinline__ void column_step(float (&w)[SUB], float (&e)[SUB], RowState& st, const BlockArgs& a,
+                                            int c0) {
+  const int t = c0 + T;
+  if (t >= a.ncols) return;
+  const int j = a.i1 + t;
+  if constexpr (T == 0) {
     if ((j % a.g) == 0) {
-      // group statistics over the current weights of columns [j, j + g)
+      // group statistics over the current weights of columns [j, j + g): this
+      // sub-block (registers), the block's later columns (shared memory, already
+      // updated by the earlier sub-blocks) and, for groups wider than the block, the
+      // working copy (already updated by the lazy updates)
       float mn = INFINITY, mx = -INFINITY;
 #pragma unroll
-      for (int u = T; u < BS; ++u)
-        if (u < a.ncols && u - T < a.g) { mn = fminf(mn, w[u]); mx = fmaxf(mx, w[u]); }
-      for (int c = a.i1 + a.ncols; c < j + a.g && c < a.d; ++c) {   // a group spanning several blocks
+      for (int u = 0; u < SUB; ++u)
+        if (c0 + u < a.ncols && u < a.g) { mn = fminf(mn, w[u]); mx = fmaxf(mx, w[u]); }
+      for (int u = c0 + SUB; u < a.ncols && u - c0 < a.g; ++u) {
+        const float v = st.wsm[u];
+        mn = fminf(mn, v);
+        mx = fmaxf(mx, v);
+      }
+      for (int c = a.i1 + a.ncols; c < j + a.g && c < a.d; ++c) {
         const float v = st.wrow[c];
         mn = fminf(mn, v);
         mx = fmaxf(mx, v);
@@ -143,9 +158,10 @@ __device__ __forceinline__ void column_step(float (&w)[BS], RowState& st, const 
   const float x = w[T];
   const float q = fminf(fmaxf(rintf(__fadd_rn(div_mk(x, st.s, st.inv_s), st.z)), 0.0f), a.qmax);
   const float wq = __fmul_rn(__fsub_rn(q, st.z), st.s);
-  const float e = a.active ? div_mk(__fsub_rn(x, wq), a.Us[T * BS + T], a.inv_u[T]) : 0.0f;
-  a.errT[(long long)T * a.lde + a.r] = e;
-  const float lsum = warp_sum(__fmul_rn(__fmul_rn(e, e), 0.5f));
+  const float err = a.active ? div_mk(__fsub_rn(x, wq), a.Us[t * a.bs + t], a.inv_u[t]) : 0.0f;
+  e[T] = err;
+  a.errT[(long long)t * a.lde + a.r] = err;
+  const float lsum = warp_sum(__fmul_rn(__fmul_rn(err, err), 0.5f));
   if (a.lane == 0) a.part[(long long)blockIdx.x * a.d + j] = lsum;
   const uint32_t qi = (uint32_t)q;
   if (a.natural) {
@@ -160,36 +176,50 @@ __device__ __forceinline__ void column_step(float (&w)[BS], RowState& st, const 
   } else if (a.active) {
     a.codes8[(long long)a.r * a.d + j] = (uint8_t)qi;
   }
-  // rank-one update of the block's remaining columns (same rounding as w - e * u)
-  const float4* urow = reinterpret_cast<const float4*>(a.Us + T * BS);
+  // rank-one update of the sub-block's remaining columns (same rounding as w - e * u)
+  const float4* urow = reinterpret_cast<const float4*>(a.Us + t * a.bs + c0);
 #pragma unroll
-  for (int u4 = (T + 1) / 4; u4 < BS / 4; ++u4) {
+  for (int u4 = (T + 1) / 4; u4 < SUB / 4; ++u4) {
     const float4 uv = urow[u4];
-    if (4 * u4 + 0 > T) w[4 * u4 + 0] = __fsub_rn(w[4 * u4 + 0], __fmul_rn(e, uv.x));
-    if (4 * u4 + 1 > T) w[4 * u4 + 1] = __fsub_rn(w[4 * u4 + 1], __fmul_rn(e, uv.y));
-    if (4 * u4 + 2 > T) w[4 * u4 + 2] = __fsub_rn(w[4 * u4 + 2], __fmul_rn(e, uv.z));
-    if (4 * u4 + 3 > T) w[4 * u4 + 3] = __fsub_rn(w[4 * u4 + 3], __fmul_rn(e, uv.w));
+    if (4 * u4 + 0 > T) w[4 * u4 + 0] = __fsub_rn(w[4 * u4 + 0], __fmul_rn(err, uv.x));
+    if (4 * u4 + 1 > T) w[4 * u4 + 1] = __fsub_rn(w[4 * u4 + 1], __fmul_rn(err, uv.y));
+    if (4 * u4 + 2 > T) w[4 * u4 + 2] = __fsub_rn(w[4 * u4 + 2], __fmul_rn(err, uv.z));
+    if (4 * u4 + 3 > T) w[4 * u4 + 3] = __fsub_rn(w[4 * u4 + 3], __fmul_rn(err, uv.w));
   }
 }
 
-template <int BS, int... Ts>
-__device__ __forceinline__ void all_columns(std::integer_sequence<int, Ts...>, float (&w)[BS], RowState& st,
-                                            const BlockArgs& a) {
-  (column_step<BS, Ts>(w, st, a), ...);
+template <int... Ts>
+__device__ __forceinline__ void sub_block_steps(std::integer_sequence<int, Ts...>, float (&w)[SUB], float (&e)[SUB],
+                                                RowState& st, const BlockArgs& a, int c0) {
+  (column_step<Ts>(w, e, st, a, c0), ...);
 }
 
+// One row per thread. The block's BS columns are processed as BS / 32 sub-blocks: a
+// sub-block's 32 weights sit in registers and take their rank-one updates there; when
+// the sub-block is done its 32 errors are applied to the block's later columns, kept
+// in shared memory, in the same per-column order (so the rounding matches updating
+// every column after every step).
 template <int BS>
 __global__ void __launch_bounds__(ROWS_PER_CTA)
 colblock_kernel(const float* __restrict__ Wf, int m, int d, const float* __restrict__ U, int i1, int bits, int g,
                 uint32_t* __restrict__ qweight, int wpr, uint8_t* __restrict__ codes8, float* __restrict__ scales,
                 float* __restrict__ zeros, int G, float* __restrict__ errT, int lde, float* __restrict__ part) {
-  extern __shared__ __align__(16) float Us[];   // BS x BS, row t holds Hinv1[i1 + t][i1 + u]; then BS reciprocals
+  extern __shared__ __align__(16) float Us[];   // BS x BS Hinv1 block, BS reciprocals, 32 x (BS + 1) rows
   float* inv_u = Us + BS * BS;
+  float* Wsm = inv_u + BS;
+  constexpr int WLD = BS + 1;                    // padded row stride: lanes hit distinct banks
   const int lane = threadIdx.x;
   const int ncols = min(BS, d - i1);
   for (int idx = lane; idx < BS * BS; idx += ROWS_PER_CTA) {
     const int t = idx / BS, u = idx % BS;
     Us[idx] = (t < ncols && u < ncols && u >= t) ? U[(long long)(i1 + t) * d + i1 + u] : 0.0f;
+  }
+  // the CTA's 32 rows of the block, one coalesced row at a time
+  const int r0 = blockIdx.x * ROWS_PER_CTA;
+  for (int rr = 0; rr < ROWS_PER_CTA; ++rr) {
+    const bool ok = r0 + rr < m;
+    for (int c = lane; c < BS; c += ROWS_PER_CTA)
+      Wsm[rr * WLD + c] = (ok && c < ncols) ? Wf[(long long)(r0 + rr) * d + i1 + c] : 0.0f;
   }
   __syncwarp();
   for (int t = lane; t < BS; t += ROWS_PER_CTA) inv_u[t] = (t < ncols) ? __frcp_rn(Us[t * BS + t]) : 0.0f;
@@ -207,7 +237,8 @@ colblock_kernel(const float* __restrict__ Wf, int m, int d, const float* __restr
   a.wpr = wpr;
   a.lde = lde;
   a.bits = bits;
-  a.r = blockIdx.x * ROWS_PER_CTA + lane;
+  a.bs = BS;
+  a.r = r0 + lane;
   a.lane = lane;
   a.active = a.r < m;
   a.natural = (codes8 == nullptr);
@@ -222,6 +253,7 @@ colblock_kernel(const float* __restrict__ Wf, int m, int d, const float* __restr
 
   RowState st;
   st.wrow = Wf + (long long)(a.active ? a.r : 0) * d;
+  st.wsm = Wsm + lane * WLD;
   st.s = 1.0f;
   st.z = 0.0f;
   if ((i1 % g) != 0 && a.active) {   // the block continues a group that began in an earlier block
@@ -233,11 +265,23 @@ colblock_kernel(const float* __restrict__ Wf, int m, int d, const float* __restr
   st.nacc = 0;
   st.widx = (int)(((long long)i1 * bits) >> 5);
 
-  float w[BS];
+#pragma unroll 1
+  for (int c0 = 0; c0 < ncols; c0 += SUB) {
+    float w[SUB], e[SUB];
 #pragma unroll
-  for (int t = 0; t < BS; ++t) w[t] = (a.active && t < ncols) ? st.wrow[i1 + t] : 0.0f;
-
-  all_columns<BS>(std::make_integer_sequence<int, BS>{}, w, st, a);
+    for (int u = 0; u < SUB; ++u) w[u] = st.wsm[c0 + u];
+    sub_block_steps(std::make_integer_sequence<int, SUB>{}, w, e, st, a, c0);
+    // the sub-block's errors move the block's later columns, column by column
+    const int nsub = min(SUB, ncols - c0);
+#pragma unroll 1
+    for (int c = c0 + SUB; c < ncols; ++c) {
+      float x = st.wsm[c];
+#pragma unroll
+      for (int u = 0; u < SUB; ++u)
+        if (u < nsub) x = __fsub_rn(x, __fmul_rn(e[u], Us[(c0 + u) * BS + c]));
+      st.wsm[c] = x;
+    }
+  }
 
   if (a.natural && st.nacc > 0 && a.active) qweight[(long long)a.r * wpr + st.widx] = (uint32_t)st.acc;
 }
@@ -351,7 +395,7 @@ template <int BS>
 gptq_status run_blocks(float* Wf, int m, int d, const float* U, int bits, int g, uint32_t* qweight, int wpr,
                        uint8_t* codes8, float* scales, float* zeros, int G, float* errT, int lde, float* part,
                        cudaStream_t s) {
-  const size_t smem = (size_t)(BS * BS + BS) * sizeof(float);
+  const size_t smem = (size_t)(BS * BS + BS + ROWS_PER_CTA * (BS + 1)) * sizeof(float);
   static bool attr = false;
   if (!attr) {
     if (cudaFuncSetAttribute(colblock_kernel<BS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)

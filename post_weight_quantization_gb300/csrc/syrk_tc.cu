@@ -16,10 +16,13 @@
 //     shared-memory ring; warp 1 (one thread) issues tcgen05.mma kind::f16
 //     (bf16 x bf16 -> fp32, M = 128, N = 256, K = 16), both operands MN-major since
 //     X^T's rows are X's columns; the accumulator lives in tensor memory, two
-//     buffers of 256 columns so the epilogue of one unit overlaps the next unit's
-//     products. Warps 2-5 read the accumulator with tcgen05.ld, scale by alpha and
-//     add into H with vector fp32 reductions (units of the same tile from different
-//     token parts meet there).
+//     buffers of 256 columns so the epilogue of one chunk overlaps the next chunk's
+//     products. The tensor core accumulates only CHUNK k-iterations (512 tokens) in a
+//     buffer; warps 2-9 read each chunk with tcgen05.ld and add it into fp32
+//     registers with round-to-nearest, which keeps the Hessian's error near that of
+//     rounded fp32 summation (the tensor core's own long accumulations drift low).
+//     At the end of a unit the register sums, scaled by alpha, go into H with vector
+//     fp32 reductions (units of the same tile from different token parts meet there).
 //   * Every wait is bounded; on a timeout the CTA raises the library's device error
 //     word, drains its own copies and products, frees tensor memory and returns.
 #include <cudaTypedefs.h>
@@ -41,7 +44,8 @@ constexpr int BOX_BYTES = BOX * BK * 2;       // 8 KB
 constexpr int A_BYTES = BM * BK * 2;          // 16 KB
 constexpr int B_BYTES = BN * BK * 2;          // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int THREADS = 192;
+constexpr int THREADS = 320;                  // TMA, MMA, 8 epilogue warps
+constexpr int CHUNK = 8;                      // k-iterations (512 tokens) per tensor-memory accumulation
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 constexpr uint32_t IDESC = umma_idesc(/*bf16*/ 1, /*A MN-major*/ true, /*B MN-major*/ true, BM, BN);
@@ -53,39 +57,42 @@ constexpr uint32_t SBO = 1024;
 constexpr uint32_t LBO = BOX_BYTES;
 
 struct Geometry {
-  int d, nr, nc, tiles, parts;
-  long long kiters;
+  int d, nr, nc, tiles, parts, kiters;
 };
 
 // number of upper-triangle tiles in row-tiles [0, r)
-__device__ __forceinline__ long long tiles_before_row(int r, int nc) {
-  long long a = r / 2;
-  long long s = (r & 1) ? a * a : a * (a - 1);   // sum_{r' < r} floor(r' / 2)
-  return (long long)r * nc - s;
+__device__ __forceinline__ int tiles_before_row(int r, int nc) {
+  const int a = r >> 1;
+  const int s = (r & 1) ? a * a : a * (a - 1);   // sum_{r' < r} floor(r' / 2)
+  return r * nc - s;
 }
 
-__device__ __forceinline__ void decode_tile(long long t, int nr, int nc, int& r, int& c) {
+__device__ __forceinline__ void decode_tile(int t, int nr, int nc, int& r, int& c) {
   int lo = 0, hi = nr - 1;
   while (lo < hi) {
     int mid = (lo + hi + 1) >> 1;
     if (tiles_before_row(mid, nc) <= t) lo = mid; else hi = mid - 1;
   }
   r = lo;
-  c = (lo / 2) + (int)(t - tiles_before_row(lo, nc));
+  c = (lo >> 1) + (t - tiles_before_row(lo, nc));
 }
 
 struct Unit {
   int r, c;
-  long long k0, k1;
+  int k0, k1;
 };
 
-__device__ __forceinline__ Unit decode_unit(long long u, const Geometry& g) {
+// 32-bit arithmetic only (a 64-bit division is an out-of-line call that would force
+// the epilogue's register sums to the stack): units < 2^31, parts <= 64 and
+// k-iterations < 2^25 keep part * kiters below 2^32.
+__device__ __forceinline__ Unit decode_unit(int u, const Geometry& g) {
   Unit w;
-  long long part = u / g.tiles;
-  long long t = u - part * g.tiles;
+  const unsigned part = (unsigned)u / (unsigned)g.tiles;
+  const int t = u - (int)part * g.tiles;
   decode_tile(t, g.nr, g.nc, w.r, w.c);
-  w.k0 = part * g.kiters / g.parts;
-  w.k1 = (part + 1) * g.kiters / g.parts;
+  const unsigned kit = (unsigned)g.kiters;
+  w.k0 = (int)(part * kit / (unsigned)g.parts);
+  w.k1 = (int)((part + 1u) * kit / (unsigned)g.parts);
   return w;
 }
 
@@ -113,7 +120,7 @@ syrk_kernel(const __grid_constant__ CUtensorMap tmap, float* __restrict__ H, lon
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tmem_full[b], 1);
-      mbar_init(&tmem_empty[b], 4);
+      mbar_init(&tmem_empty[b], 8);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -126,66 +133,69 @@ syrk_kernel(const __grid_constant__ CUtensorMap tmap, float* __restrict__ H, lon
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const long long num_units = (long long)g.tiles * g.parts;
+  const int num_units = g.tiles * g.parts;
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer ----------------
     int stage = 0;
     uint32_t phase = 0;
     uint32_t armed = 0;            // stages that were ever armed
-    uint32_t last_phase[STAGES];
+    uint32_t last_phase = 0;       // bit s: phase of stage s's last arming
     bool ok = true;
-    for (long long u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
+    for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
       Unit w = decode_unit(u, g);
-      for (long long k = w.k0; k < w.k1; ++k) {
+      for (int k = w.k0; k < w.k1; ++k) {
         if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
         uint8_t* sA = smem + stage * STAGE_BYTES;
         uint8_t* sB = sA + A_BYTES;
         mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-        const int tok = (int)(k * BK);
+        const int tok = k * BK;
 #pragma unroll
         for (int h = 0; h < BM / BOX; ++h) tma_load_2d(sA + h * BOX_BYTES, &tmap, &full[stage], w.r * BM + h * BOX, tok);
 #pragma unroll
         for (int h = 0; h < BN / BOX; ++h) tma_load_2d(sB + h * BOX_BYTES, &tmap, &full[stage], w.c * BN + h * BOX, tok);
         armed |= 1u << stage;
-        last_phase[stage] = phase;
+        last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
     }
     if (!ok) { *abort_flag = 1; report_device_error(err_word, DEVERR_TIMEOUT); }
     // every armed load lands whatever the consumer did; wait for them before exit
     for (int s = 0; s < STAGES; ++s)
-      if (armed & (1u << s)) mbar_wait_bounded(&full[s], last_phase[s], nullptr);
+      if (armed & (1u << s)) mbar_wait_bounded(&full[s], (last_phase >> s) & 1u, nullptr);
   } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer ----------------
+    // ---------------- MMA issuer: one accumulator per chunk of CHUNK k-iterations ----------------
     int stage = 0;
     uint32_t phase = 0;
-    uint32_t it = 0;
+    uint32_t it = 0;               // chunks issued (tensor-memory buffer rotation)
     bool ok = true, issued = false;
     const uint32_t sbase = smem_u32(smem);
-    for (long long u = blockIdx.x; ok && u < num_units; u += gridDim.x, ++it) {
+    for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
       Unit w = decode_unit(u, g);
-      const uint32_t buf = it & 1u;
-      if (!mbar_wait_bounded(&tmem_empty[buf], ((it >> 1) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t d_tmem = tmem_base + buf * BN;
-      for (long long k = w.k0; k < w.k1; ++k) {
-        if (!mbar_wait_bounded(&full[stage], phase, abort_flag)) { ok = false; break; }
+      for (int kc = w.k0; ok && kc < w.k1; kc += CHUNK, ++it) {
+        const int ke = (kc + CHUNK < w.k1) ? kc + CHUNK : w.k1;
+        const uint32_t buf = it & 1u;
+        if (!mbar_wait_bounded(&tmem_empty[buf], ((it >> 1) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t a0 = sbase + stage * STAGE_BYTES;
-        const uint32_t b0 = a0 + A_BYTES;
+        const uint32_t d_tmem = tmem_base + buf * BN;
+        for (int k = kc; k < ke; ++k) {
+          if (!mbar_wait_bounded(&full[stage], phase, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a0 = sbase + stage * STAGE_BYTES;
+          const uint32_t b0 = a0 + A_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint64_t da = umma_sdesc_sw128(a0 + kk * KSTEP_BYTES, LBO, SBO);
-          const uint64_t db = umma_sdesc_sw128(b0 + kk * KSTEP_BYTES, LBO, SBO);
-          umma_f16(d_tmem, da, db, IDESC, (k > w.k0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t da = umma_sdesc_sw128(a0 + kk * KSTEP_BYTES, LBO, SBO);
+            const uint64_t db = umma_sdesc_sw128(b0 + kk * KSTEP_BYTES, LBO, SBO);
+            umma_f16(d_tmem, da, db, IDESC, (k > kc || kk > 0) ? 1u : 0u);
+          }
+          issued = true;
+          umma_commit(&empty[stage]);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
-        issued = true;
-        umma_commit(&empty[stage]);
-        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        if (!ok) break;
+        umma_commit(&tmem_full[buf]);
       }
-      if (!ok) break;
-      umma_commit(&tmem_full[buf]);
     }
     if (!ok) { *abort_flag = 1; report_device_error(err_word, DEVERR_TIMEOUT); }
     if (issued) {
@@ -193,46 +203,71 @@ syrk_kernel(const __grid_constant__ CUtensorMap tmap, float* __restrict__ H, lon
       mbar_wait_bounded(drain, 0, nullptr);
     }
   } else if (warp >= 2) {
-    // ---------------- epilogue: TMEM -> alpha * acc -> red.add into H ----------------
+    // ---------------- epilogue: chunk sums from tensor memory, added in fp32 registers
+    // (round to nearest), then alpha * sum reduced into H once per unit ----------------
     const int q = warp & 3;                  // TMEM lane quadrant this warp may access
+    const int h = (warp - 2) >> 2;           // which 128-column half of the tile
     const int row = q * 32 + lane;
     uint32_t it = 0;
-    for (long long u = blockIdx.x; u < num_units; u += gridDim.x, ++it) {
+    bool ok = true;
+    float acc[BN / 2];
+    for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
       Unit w = decode_unit(u, g);
-      const uint32_t buf = it & 1u;
-      if (!mbar_wait_bounded(&tmem_full[buf], (it >> 1) & 1u, abort_flag)) {
-        *abort_flag = 1;
-        report_device_error(err_word, DEVERR_TIMEOUT);
-        break;
-      }
-      tc_fence_after();
       const int i = w.r * BM + row;
       const int i_warp = w.r * BM + q * 32;
-      float* hrow = H + (long long)i * ldh;
-#pragma unroll 1
-      for (int cc = 0; cc < BN / 32; ++cc) {
-        const int j0 = w.c * BN + cc * 32;
-        if (j0 + 31 < i_warp || j0 >= g.d) continue;   // warp-uniform: nothing on or above the diagonal
-        float v[32];
-        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN + cc * 32, v);
-        if (i < g.d) {
+      const int jh = w.c * BN + h * (BN / 2);
+      for (int kc = w.k0; kc < w.k1; kc += CHUNK, ++it) {
+        const uint32_t buf = it & 1u;
+        if (!mbar_wait_bounded(&tmem_full[buf], (it >> 1) & 1u, abort_flag)) {
+          *abort_flag = 1;
+          report_device_error(err_word, DEVERR_TIMEOUT);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const bool first = (kc == w.k0);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int j = j0 + 4 * e;
-            if (j >= i && j + 3 < g.d) {
-              atomicAdd(reinterpret_cast<float4*>(hrow + j),
-                        make_float4(alpha * v[4 * e], alpha * v[4 * e + 1], alpha * v[4 * e + 2], alpha * v[4 * e + 3]));
-            } else {
+        for (int cc = 0; cc < BN / 64; ++cc) {
+          const int j0 = jh + cc * 32;
+          if (j0 + 31 < i_warp || j0 >= g.d) continue;   // warp-uniform: nothing on or above the diagonal
 #pragma unroll
-              for (int x = 0; x < 4; ++x)
-                if (j + x >= i && j + x < g.d) atomicAdd(hrow + j + x, alpha * v[4 * e + x]);
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t v[16];
+            tmem_ld_32x32b_x16_nowait(tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN + h * (BN / 2) + cc * 32 + hh * 16, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+              const float f = __uint_as_float(v[x]);
+              acc[cc * 32 + hh * 16 + x] = first ? f : acc[cc * 32 + hh * 16 + x] + f;
             }
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tmem_empty[buf]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tmem_empty[buf]);
+      if (!ok) break;
+      if (i < g.d) {
+        float* hrow = H + (long long)i * ldh;
+#pragma unroll
+        for (int x = 0; x < BN / 2; ++x) acc[x] *= alpha;
+#pragma unroll
+        for (int cc = 0; cc < BN / 64; ++cc) {
+          const int j0 = jh + cc * 32;
+          if (j0 + 31 < i_warp || j0 >= g.d) continue;
+          if (j0 >= i_warp + 31 && j0 + 31 < g.d) {          // whole group above the diagonal
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              atomicAdd(reinterpret_cast<float4*>(hrow + j0 + 4 * e),
+                        make_float4(acc[cc * 32 + 4 * e], acc[cc * 32 + 4 * e + 1], acc[cc * 32 + 4 * e + 2],
+                                    acc[cc * 32 + 4 * e + 3]));
+          } else {
+#pragma unroll
+            for (int x = 0; x < 32; ++x)
+              if (j0 + x >= i && j0 + x < g.d) atomicAdd(hrow + j0 + x, acc[cc * 32 + x]);
+          }
+        }
+      }
     }
   }
 
@@ -313,7 +348,7 @@ gptq_status syrk_accumulate(const uint16_t* X, long long n, long long d, long lo
   long long tiles = 0;
   for (int r = 0; r < g.nr; ++r) tiles += g.nc - (r * BM) / BN;
   g.tiles = (int)tiles;
-  g.kiters = (n + BK - 1) / BK;
+  g.kiters = (int)((n + BK - 1) / BK);
   const int sms = sm_count();
   g.parts = choose_parts(tiles, g.kiters, sms);
   const long long units = tiles * g.parts;
