@@ -242,6 +242,20 @@ gptq_status gptq_quantize_layer(const void* W, int w_dtype, int64_t m, int64_t d
 gptq_status gptq_unpack_codes(const uint32_t* qweight, int64_t m, int64_t d, int bits,
                               uint8_t* codes, gptq_stream_t stream);
 
+/*
+ * Helper for checks: C = beta * C + alpha * A B (fp32, single batch) with the GEMM the
+ * library uses for its block updates. engine 0: tensor cores, 3 x TF32 products with
+ * fp32 accumulation of 32-deep partial products; engine 1: FFMA. a_kmajor != 0 means
+ * A(i, k) = A[i * lda + k], else A[k * lda + i]; b_kmajor != 0 means
+ * B(k, j) = B[j * ldb + k], else B[k * ldb + j]. lower_tiles != 0 (square C only)
+ * skips 128 x 128 output tiles strictly above the diagonal. Device pointers; no
+ * synchronization.
+ */
+gptq_status gptq_gemm_f32(int engine, int a_kmajor, int b_kmajor, int64_t M, int64_t N, int64_t K,
+                          const float* A, int64_t lda, const float* B, int64_t ldb, float* C,
+                          int64_t ldc, float alpha, float beta, int lower_tiles,
+                          gptq_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -13,14 +13,16 @@
 //
 // Kernels:
 //   prep_kernel        fp32 working copy of W in processing order; NaN/Inf check
-//   colblock_kernel<BS> one thread per row, the block as 32-column sub-blocks whose
-//                      weights stay in registers (the block's later columns wait in
-//                      shared memory); the Hinv1 diagonal block sits in shared memory
-//                      (every thread reads the same entry: broadcast); codes are packed into the
+//   colblock_kernel<BS> eight lanes per row (4 rows per warp, 32 per CTA), the block as
+//                      32-column register sub-blocks (the block's later columns wait
+//                      in shared memory), the Hinv1 diagonal block in shared memory,
+//                      group min/max by shuffles; codes are packed into the
 //                      output bitstream as they are produced; Err1 is written
-//                      column-major (coalesced) for the lazy update; per-column loss
-//                      partial sums come from warp-shuffle reductions
-//   lazy_update_kernel W[:, i2:] -= Err1 @ Hinv1[i1:i2, i2:], FFMA tiles 128 x 128
+//                      row-major for the lazy update; per-column loss partial
+//                      sums of each CTA's 32 rows in a fixed order
+//   transpose_kernel   Ut = Hinv1^T once per call
+//   tc_gemm            lazy update W[:, i2:] -= Err1 @ Hinv1[i1:i2, i2:] on the tensor cores
+//                      (3 x TF32, both operands K-major: Err1 rows, Ut rows)
 //   loss_finalize      col_losses = sum of partials in a fixed order, un-permuted
 //   pack_perm          act-order: gather codes back to the original column order
 //
@@ -96,235 +98,172 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// State of one row (one thread) while a block is processed.
-struct RowState {
-  const float* wrow;      // the row of the working copy (global)
-  float* wsm;             // the row's block columns in shared memory (stride 1)
-  float s, z, inv_s;      // current group's scale, zero and RN(1 / scale)
-  uint64_t acc;           // code bits not yet stored
-  int nacc, widx;         // bits held in acc; next output word
-};
+// Column block, LANES lanes per row.
+//
+// A warp holds 32 / LANES rows; the LANES lanes of a row own the block's columns
+// c = LANES k + q round-robin (q = lane % LANES). At each column the owner broadcasts
+// the current weight with one shuffle and all lanes of the row quantize it
+// identically, then each lane applies the rank-one update to its own later columns.
+// Within a 32-column sub-block the lane's columns sit in registers and are rotated by
+// one slot every LANES columns, so the column about to be quantized is always slot 0
+// of its owner and the loop body stays a few hundred instructions long. When a sub-block is done, its 32
+// errors update the block's later columns (kept in shared memory) column by column in
+// the same order, so the rounding is that of updating every column after every step.
+constexpr int LANES = 8;                             // lanes per row
+constexpr int ROWS_PER_WARP = 32 / LANES;            // 4
+constexpr int WARPS_PER_CTA = ROWS_PER_CTA / ROWS_PER_WARP;   // 8
+constexpr int CB_THREADS = WARPS_PER_CTA * 32;      // 256
+constexpr int SUB = 32;                              // columns per register sub-block
+constexpr int SLOTS = SUB / LANES;                   // 4 registers per lane
+constexpr int ELD = SUB + 1;                         // padded row stride of the error tile
 
-struct BlockArgs {
-  const float* Us;        // Hinv1 diagonal block (shared memory), row-major BS x BS
-  const float* inv_u;     // RN(1 / Hinv1[j][j]) of the block (shared memory)
-  int m, d, i1, ncols, g, G, wpr, lde, bits, r, lane, bs;
-  bool active, natural;
-  float qmax, inv_qmax;
-  uint32_t* qweight;
-  uint8_t* codes8;
-  float *scales, *zeros, *errT, *part;
-};
-
-constexpr int SUB = 32;   // columns per register-resident sub-block
-
-// Column T of sub-block c0 (block-local column c0 + T). T is a compile-time constant so
-// that w[] and e[] stay in registers; the sub-block's other columns live in w[].
-template <int T>
-__device__ __forceinline__ void column_step(float (&w)[SUB], float (&e)[SUB], RowState& st, const BlockArgs& a,
-                                            int c0) {
-  const int t = c0 + T;
-  if (t >= a.ncols) return;
-  const int j = a.i1 + t;
-  if constexpr (T == 0) {
-    if ((j % a.g) == 0) {
-      // group statistics over the current weights of columns [j, j + g): this
-      // sub-block (registers), the block's later columns (shared memory, already
-      // updated by the earlier sub-blocks) and, for groups wider than the block, the
-      // working copy (already updated by the lazy updates)
-      float mn = INFINITY, mx = -INFINITY;
-#pragma unroll
-      for (int u = 0; u < SUB; ++u)
-        if (c0 + u < a.ncols && u < a.g) { mn = fminf(mn, w[u]); mx = fmaxf(mx, w[u]); }
-      for (int u = c0 + SUB; u < a.ncols && u - c0 < a.g; ++u) {
-        const float v = st.wsm[u];
-        mn = fminf(mn, v);
-        mx = fmaxf(mx, v);
-      }
-      for (int c = a.i1 + a.ncols; c < j + a.g && c < a.d; ++c) {
-        const float v = st.wrow[c];
-        mn = fminf(mn, v);
-        mx = fmaxf(mx, v);
-      }
-      st.s = fmaxf(div_mk(__fsub_rn(mx, mn), a.qmax, a.inv_qmax), 1e-8f);
-      st.inv_s = rcp_rn(st.s);
-      st.z = fminf(fmaxf(rintf(div_mk(-mn, st.s, st.inv_s)), 0.0f), a.qmax);
-      if (a.active) {
-        a.scales[(long long)a.r * a.G + j / a.g] = st.s;
-        a.zeros[(long long)a.r * a.G + j / a.g] = st.z;
-      }
-    }
-  }
-  const float x = w[T];
-  const float q = fminf(fmaxf(rintf(__fadd_rn(div_mk(x, st.s, st.inv_s), st.z)), 0.0f), a.qmax);
-  const float wq = __fmul_rn(__fsub_rn(q, st.z), st.s);
-  const float err = a.active ? div_mk(__fsub_rn(x, wq), a.Us[t * a.bs + t], a.inv_u[t]) : 0.0f;
-  e[T] = err;
-  a.errT[(long long)t * a.lde + a.r] = err;
-  const float lsum = warp_sum(__fmul_rn(__fmul_rn(err, err), 0.5f));
-  if (a.lane == 0) a.part[(long long)blockIdx.x * a.d + j] = lsum;
-  const uint32_t qi = (uint32_t)q;
-  if (a.natural) {
-    st.acc |= (uint64_t)qi << st.nacc;
-    st.nacc += a.bits;
-    if (st.nacc >= 32) {
-      if (a.active) a.qweight[(long long)a.r * a.wpr + st.widx] = (uint32_t)st.acc;
-      ++st.widx;
-      st.acc >>= 32;
-      st.nacc -= 32;
-    }
-  } else if (a.active) {
-    a.codes8[(long long)a.r * a.d + j] = (uint8_t)qi;
-  }
-  // rank-one update of the sub-block's remaining columns (same rounding as w - e * u)
-  const float4* urow = reinterpret_cast<const float4*>(a.Us + t * a.bs + c0);
-#pragma unroll
-  for (int u4 = (T + 1) / 4; u4 < SUB / 4; ++u4) {
-    const float4 uv = urow[u4];
-    if (4 * u4 + 0 > T) w[4 * u4 + 0] = __fsub_rn(w[4 * u4 + 0], __fmul_rn(err, uv.x));
-    if (4 * u4 + 1 > T) w[4 * u4 + 1] = __fsub_rn(w[4 * u4 + 1], __fmul_rn(err, uv.y));
-    if (4 * u4 + 2 > T) w[4 * u4 + 2] = __fsub_rn(w[4 * u4 + 2], __fmul_rn(err, uv.z));
-    if (4 * u4 + 3 > T) w[4 * u4 + 3] = __fsub_rn(w[4 * u4 + 3], __fmul_rn(err, uv.w));
-  }
-}
-
-template <int... Ts>
-__device__ __forceinline__ void sub_block_steps(std::integer_sequence<int, Ts...>, float (&w)[SUB], float (&e)[SUB],
-                                                RowState& st, const BlockArgs& a, int c0) {
-  (column_step<Ts>(w, e, st, a, c0), ...);
-}
-
-// One row per thread. The block's BS columns are processed as BS / 32 sub-blocks: a
-// sub-block's 32 weights sit in registers and take their rank-one updates there; when
-// the sub-block is done its 32 errors are applied to the block's later columns, kept
-// in shared memory, in the same per-column order (so the rounding matches updating
-// every column after every step).
 template <int BS>
-__global__ void __launch_bounds__(ROWS_PER_CTA)
+__global__ void __launch_bounds__(CB_THREADS)
 colblock_kernel(const float* __restrict__ Wf, int m, int d, const float* __restrict__ U, int i1, int bits, int g,
                 uint32_t* __restrict__ qweight, int wpr, uint8_t* __restrict__ codes8, float* __restrict__ scales,
-                float* __restrict__ zeros, int G, float* __restrict__ errT, int lde, float* __restrict__ part) {
-  extern __shared__ __align__(16) float Us[];   // BS x BS Hinv1 block, BS reciprocals, 32 x (BS + 1) rows
-  float* inv_u = Us + BS * BS;
-  float* Wsm = inv_u + BS;
-  constexpr int WLD = BS + 1;                    // padded row stride: lanes hit distinct banks
-  const int lane = threadIdx.x;
-  const int ncols = min(BS, d - i1);
-  for (int idx = lane; idx < BS * BS; idx += ROWS_PER_CTA) {
-    const int t = idx / BS, u = idx % BS;
-    Us[idx] = (t < ncols && u < ncols && u >= t) ? U[(long long)(i1 + t) * d + i1 + u] : 0.0f;
-  }
-  // the CTA's 32 rows of the block, one coalesced row at a time
+                float* __restrict__ zeros, int G, float* __restrict__ err, float* __restrict__ part) {
+  extern __shared__ __align__(16) float smem[];
+  float* Us = smem;                                  // BS x BS: Us[t * BS + u] = Hinv1[i1 + t][i1 + u]
+  float* inv_u = Us + BS * BS;                       // RN(1 / Hinv1[j][j])
+  float* Wsm = inv_u + BS;                           // ROWS_PER_CTA x (BS + 1): the block's weights
+  float* Es = Wsm + ROWS_PER_CTA * (BS + 1);         // ROWS_PER_CTA x ELD: the sub-block's errors
+  constexpr int WLD = BS + 1;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q = lane % LANES;                        // position within the row's lanes
+  const int qbase = lane - q;                        // lane owning the row's column 0
+  const int row = warp * ROWS_PER_WARP + lane / LANES;  // row within the CTA
   const int r0 = blockIdx.x * ROWS_PER_CTA;
-  for (int rr = 0; rr < ROWS_PER_CTA; ++rr) {
-    const bool ok = r0 + rr < m;
-    for (int c = lane; c < BS; c += ROWS_PER_CTA)
-      Wsm[rr * WLD + c] = (ok && c < ncols) ? Wf[(long long)(r0 + rr) * d + i1 + c] : 0.0f;
-  }
-  __syncwarp();
-  for (int t = lane; t < BS; t += ROWS_PER_CTA) inv_u[t] = (t < ncols) ? __frcp_rn(Us[t * BS + t]) : 0.0f;
-  __syncwarp();
+  const int r = r0 + row;
+  const bool active = r < m;
+  const int ncols = min(BS, d - i1);
 
-  BlockArgs a;
-  a.Us = Us;
-  a.inv_u = inv_u;
-  a.m = m;
-  a.d = d;
-  a.i1 = i1;
-  a.ncols = ncols;
-  a.g = g;
-  a.G = G;
-  a.wpr = wpr;
-  a.lde = lde;
-  a.bits = bits;
-  a.bs = BS;
-  a.r = r0 + lane;
-  a.lane = lane;
-  a.active = a.r < m;
-  a.natural = (codes8 == nullptr);
-  a.qmax = (float)((1 << bits) - 1);
-  a.inv_qmax = __frcp_rn(a.qmax);
-  a.qweight = qweight;
-  a.codes8 = codes8;
-  a.scales = scales;
-  a.zeros = zeros;
-  a.errT = errT;
-  a.part = part;
+  // the Hinv1 block (only its upper triangle is ever read) and the CTA's rows of W
+  load_tile<CB_THREADS, BS, BS>(Us, BS, U + (long long)i1 * d + i1, d, ncols, ncols);
+  load_tile<CB_THREADS, ROWS_PER_CTA, BS>(Wsm, WLD, Wf + (long long)r0 * d + i1, d, min(ROWS_PER_CTA, m - r0), ncols);
+  __syncthreads();
+  for (int t = tid; t < BS; t += CB_THREADS) inv_u[t] = (t < ncols) ? __frcp_rn(Us[t * BS + t]) : 0.0f;
+  __syncthreads();
 
-  RowState st;
-  st.wrow = Wf + (long long)(a.active ? a.r : 0) * d;
-  st.wsm = Wsm + lane * WLD;
-  st.s = 1.0f;
-  st.z = 0.0f;
-  if ((i1 % g) != 0 && a.active) {   // the block continues a group that began in an earlier block
-    st.s = scales[(long long)a.r * G + i1 / g];
-    st.z = zeros[(long long)a.r * G + i1 / g];
+  float* wsm = Wsm + row * WLD;
+  float* es = Es + row * ELD;
+  const float* wrow = Wf + (long long)(active ? r : 0) * d;
+  const float qmax = (float)((1 << bits) - 1);
+  const float inv_qmax = __frcp_rn(qmax);
+  float s = 1.0f, z = 0.0f;
+  if ((i1 % g) != 0 && active) {   // the block continues a group that began in an earlier block
+    s = scales[(long long)r * G + i1 / g];
+    z = zeros[(long long)r * G + i1 / g];
   }
-  st.inv_s = rcp_rn(st.s);
-  st.acc = 0;
-  st.nacc = 0;
-  st.widx = (int)(((long long)i1 * bits) >> 5);
+  float inv_s = rcp_rn(s);
+  const bool natural = (codes8 == nullptr);
+  const bool packer = natural && q == 0 && active;
+  uint64_t acc = 0;
+  int nacc = 0;
+  int widx = (int)(((long long)i1 * bits) >> 5);
 
 #pragma unroll 1
   for (int c0 = 0; c0 < ncols; c0 += SUB) {
-    float w[SUB], e[SUB];
-#pragma unroll
-    for (int u = 0; u < SUB; ++u) w[u] = st.wsm[c0 + u];
-    sub_block_steps(std::make_integer_sequence<int, SUB>{}, w, e, st, a, c0);
-    // the sub-block's errors move the block's later columns, column by column
     const int nsub = min(SUB, ncols - c0);
+    float w[SLOTS];
+#pragma unroll
+    for (int k = 0; k < SLOTS; ++k) w[k] = wsm[c0 + LANES * k + q];   // column c0 + LANES k + q (zero-padded)
+
+    const int j0 = i1 + c0;
+    if ((j0 % g) == 0) {
+      // group statistics over the current weights of columns [j0, j0 + g), each lane over
+      // its own columns, then combined across the row's lanes
+      float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < SLOTS; ++k) {
+        const int c = LANES * k + q;
+        if (c < nsub && c < g) { mn = fminf(mn, w[k]); mx = fmaxf(mx, w[k]); }
+      }
+      for (int c = c0 + SUB + q; c < ncols && c - c0 < g; c += LANES) {
+        const float v = wsm[c];
+        mn = fminf(mn, v);
+        mx = fmaxf(mx, v);
+      }
+      for (int c = i1 + ncols + q; c < j0 + g && c < d; c += LANES) {
+        const float v = wrow[c];
+        mn = fminf(mn, v);
+        mx = fmaxf(mx, v);
+      }
+#pragma unroll
+      for (int o = 1; o < LANES; o <<= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      }
+      s = fmaxf(div_mk(__fsub_rn(mx, mn), qmax, inv_qmax), 1e-8f);
+      inv_s = rcp_rn(s);
+      z = fminf(fmaxf(rintf(div_mk(-mn, s, inv_s)), 0.0f), qmax);
+      if (active && q == 0) {
+        scales[(long long)r * G + j0 / g] = s;
+        zeros[(long long)r * G + j0 / g] = z;
+      }
+    }
+
 #pragma unroll 1
-    for (int c = c0 + SUB; c < ncols; ++c) {
-      float x = st.wsm[c];
+    for (int cb = c0; cb < c0 + nsub; cb += LANES) {   // LANES columns per iteration
+#pragma unroll
+      for (int i = 0; i < LANES; ++i) {
+        const int t = cb + i;
+        if (t < ncols) {                                 // warp-uniform
+          const float x = __shfl_sync(0xffffffffu, w[0], qbase + i);
+          const float qv = fminf(fmaxf(rintf(__fadd_rn(div_mk(x, s, inv_s), z)), 0.0f), qmax);
+          const float wq = __fmul_rn(__fsub_rn(qv, z), s);
+          const float e = active ? div_mk(__fsub_rn(x, wq), Us[t * BS + t], inv_u[t]) : 0.0f;
+          if (q == 0) {
+            es[t - c0] = e;
+            err[(long long)(r0 + row) * BS + t] = e;
+          }
+          const uint32_t qi = (uint32_t)qv;
+          if (packer) {
+            acc |= (uint64_t)qi << nacc;
+            nacc += bits;
+            if (nacc >= 32) {
+              qweight[(long long)r * wpr + widx] = (uint32_t)acc;
+              ++widx;
+              acc >>= 32;
+              nacc -= 32;
+            }
+          } else if (!natural && q == 0 && active) {
+            codes8[(long long)r * d + i1 + t] = (uint8_t)qi;
+          }
+          // rank-one update of the lane's later columns of the sub-block: slot k holds
+          // column cb + LANES k + q, later than t unless k == 0 and q <= i
+          const float* urow = Us + t * BS + cb + q;
+#pragma unroll
+          for (int k = 0; k < SLOTS; ++k)
+            if (k > 0 || q > i) w[k] = __fsub_rn(w[k], __fmul_rn(e, urow[LANES * k]));
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < SLOTS - 1; ++k) w[k] = w[k + 1];
+      w[SLOTS - 1] = 0.0f;
+    }
+    __syncwarp();
+    // the sub-block's errors move the block's later columns (this lane's share), in order
+#pragma unroll 1
+    for (int c = c0 + SUB + q; c < ncols; c += LANES) {
+      float x = wsm[c];
 #pragma unroll
       for (int u = 0; u < SUB; ++u)
-        if (u < nsub) x = __fsub_rn(x, __fmul_rn(e[u], Us[(c0 + u) * BS + c]));
-      st.wsm[c] = x;
+        if (u < nsub) x = __fsub_rn(x, __fmul_rn(es[u], Us[(c0 + u) * BS + c]));
+      wsm[c] = x;
     }
-  }
-
-  if (a.natural && st.nacc > 0 && a.active) qweight[(long long)a.r * wpr + st.widx] = (uint32_t)st.acc;
-}
-
-// Wf[r][c] -= sum_{k < nb} errT[k][r] * U[i1 + k][c]  for r < m, c in [c0, d)
-__global__ void __launch_bounds__(simt::THREADS)
-lazy_update_kernel(float* __restrict__ Wf, int m, int d, const float* __restrict__ errT, int lde,
-                   const float* __restrict__ U, int i1, int nb, int c0) {
-  using simt::KC;
-  using simt::TILE;
-  __shared__ __align__(16) float As[KC][TILE];
-  __shared__ __align__(16) float Bs[KC][TILE];
-  const int r0 = blockIdx.y * TILE;
-  const int j0 = c0 + blockIdx.x * TILE;
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  simt::Acc acc;
-  simt::zero(acc);
-  for (int kc = 0; kc < nb; kc += KC) {
-    const int kn = min(KC, nb - kc);
     __syncthreads();
-    for (int idx = threadIdx.x; idx < TILE * KC; idx += simt::THREADS) {
-      const int c = idx % TILE, k = idx / TILE;
-      float va = 0.0f, vb = 0.0f;
-      if (k < kn) {
-        if (r0 + c < m) va = errT[(long long)(kc + k) * lde + r0 + c];
-        if (j0 + c < d) vb = U[(long long)(i1 + kc + k) * d + j0 + c];
+    // per-column loss partial sums of the CTA's 32 rows, in a fixed order
+    if (tid < nsub) {
+      float lsum = 0.0f;
+      for (int rr = 0; rr < ROWS_PER_CTA; ++rr) {
+        const float e = Es[rr * ELD + tid];
+        lsum = __fadd_rn(lsum, __fmul_rn(__fmul_rn(e, e), 0.5f));
       }
-      As[k][c] = va;
-      Bs[k][c] = vb;
+      part[(long long)blockIdx.x * d + i1 + c0 + tid] = lsum;
     }
     __syncthreads();
-    simt::mma_chunk(As, Bs, kn, tx, ty, acc);
   }
-#pragma unroll
-  for (int a = 0; a < 8; ++a) {
-    const int r = r0 + simt::micro_row(a, ty);
-    if (r >= m) continue;
-#pragma unroll
-    for (int b = 0; b < 8; ++b) {
-      const int c = j0 + simt::micro_row(b, tx);
-      if (c < d) Wf[(long long)r * d + c] = __fsub_rn(Wf[(long long)r * d + c], acc.v[a][b]);
-    }
-  }
+  if (packer && nacc > 0) qweight[(long long)r * wpr + widx] = (uint32_t)acc;
 }
 
 __global__ void loss_finalize_kernel(const float* __restrict__ part, int nrg, int d, const int* __restrict__ perm,
@@ -371,20 +310,36 @@ __global__ void unpack_kernel(const uint32_t* __restrict__ qweight, int m, int d
   codes[idx] = (uint8_t)(v & ((1u << bits) - 1u));
 }
 
+// Ut = Hinv1^T (the lazy update reads Hinv1's rows as K-major operand columns)
+__global__ void transpose_kernel(const float* __restrict__ U, float* __restrict__ Ut, int d) {
+  __shared__ float tile[32][33];
+  const int bx = blockIdx.x * 32, by = blockIdx.y * 32;
+  for (int yy = threadIdx.y; yy < 32; yy += 8) {
+    const int r = by + yy, c = bx + threadIdx.x;
+    tile[yy][threadIdx.x] = (r < d && c < d) ? U[(long long)r * d + c] : 0.0f;
+  }
+  __syncthreads();
+  for (int yy = threadIdx.y; yy < 32; yy += 8) {
+    const int r = bx + yy, c = by + threadIdx.x;
+    if (r < d && c < d) Ut[(long long)r * d + c] = tile[threadIdx.x][yy];
+  }
+}
+
 struct Layout {
-  size_t hdr, wf, errT, part, codes8, inv, total;
-  int lde, nrg;
+  size_t hdr, wf, err, ut, part, codes8, inv, total;
+  int nrg;
 };
 
 Layout layout(long long m, long long d, int blocksize) {
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
   Layout L;
-  L.lde = (int)((m + 127) / 128 * 128);
   L.nrg = (int)((m + ROWS_PER_CTA - 1) / ROWS_PER_CTA);
+  const size_t mpad = (size_t)L.nrg * ROWS_PER_CTA;
   L.hdr = 0;
   L.wf = kHeaderBytes;
-  L.errT = L.wf + al((size_t)m * d * 4);
-  L.part = L.errT + al((size_t)blocksize * L.lde * 4);
+  L.err = L.wf + al((size_t)m * d * 4);
+  L.ut = L.err + al(mpad * (size_t)blocksize * 4);
+  L.part = L.ut + al((size_t)d * d * 4);
   L.codes8 = L.part + al((size_t)L.nrg * d * 4);
   L.inv = L.codes8 + al((size_t)m * d);
   L.total = L.inv + al((size_t)d * 4);
@@ -392,10 +347,10 @@ Layout layout(long long m, long long d, int blocksize) {
 }
 
 template <int BS>
-gptq_status run_blocks(float* Wf, int m, int d, const float* U, int bits, int g, uint32_t* qweight, int wpr,
-                       uint8_t* codes8, float* scales, float* zeros, int G, float* errT, int lde, float* part,
+gptq_status run_blocks(float* Wf, int m, int d, const float* U, const float* Ut, int bits, int g, uint32_t* qweight,
+                       int wpr, uint8_t* codes8, float* scales, float* zeros, int G, float* err, float* part,
                        cudaStream_t s) {
-  const size_t smem = (size_t)(BS * BS + BS + ROWS_PER_CTA * (BS + 1)) * sizeof(float);
+  const size_t smem = (size_t)(BS * BS + BS + ROWS_PER_CTA * (BS + 1) + ROWS_PER_CTA * ELD) * sizeof(float);
   static bool attr = false;
   if (!attr) {
     if (cudaFuncSetAttribute(colblock_kernel<BS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
@@ -405,14 +360,24 @@ gptq_status run_blocks(float* Wf, int m, int d, const float* U, int bits, int g,
   const int nrg = (m + ROWS_PER_CTA - 1) / ROWS_PER_CTA;
   for (int i1 = 0; i1 < d; i1 += BS) {
     const int nb = std::min(BS, d - i1);
-    colblock_kernel<BS><<<nrg, ROWS_PER_CTA, smem, s>>>(Wf, m, d, U, i1, bits, g, qweight, wpr, codes8, scales,
-                                                        zeros, G, errT, lde, part);
-    count_launch();
+    {
+      ProfScope ps("quantize.colblock", s);
+      colblock_kernel<BS><<<nrg, CB_THREADS, smem, s>>>(Wf, m, d, U, i1, bits, g, qweight, wpr, codes8, scales,
+                                                          zeros, G, err, part);
+      count_launch();
+    }
     const int i2 = i1 + nb;
     if (i2 < d) {
-      dim3 grid((unsigned)((d - i2 + simt::TILE - 1) / simt::TILE), (unsigned)((m + simt::TILE - 1) / simt::TILE));
-      lazy_update_kernel<<<grid, simt::THREADS, 0, s>>>(Wf, m, d, errT, lde, U, i1, nb, i2);
-      count_launch();
+      // W[:, i2:] -= Err1 @ Hinv1[i1:i2, i2:];  A = Err1 (rows of BS), B(k, j) = Ut[i2 + j][i1 + k]
+      simt::GemmArgs ga{};
+      ga.M = m; ga.N = d - i2; ga.K = nb; ga.M_last = m; ga.K_last = nb;
+      ga.A = err; ga.lda = BS;
+      ga.B = Ut + (long long)i2 * d + i1; ga.ldb = d;
+      ga.C = Wf + i2; ga.ldc = d;
+      ga.alpha = -1.0f; ga.beta = 1.0f;
+      ga.vec = (d % 4 == 0) && simt::aligned16(Wf) && simt::aligned16(Ut) && simt::aligned16(err);
+      ProfScope ps2("quantize.lazy_gemm", s);
+      if (gptq_status st = tc_gemm(ga, 1, true, true, s)) return st;
     }
   }
   return check_launch("column-loop kernels");
@@ -433,7 +398,8 @@ gptq_status quantize_launch(const void* W, int w_dtype, long long m_, long long 
   uint8_t* base = reinterpret_cast<uint8_t*>(ws);
   QHeader* hdr = reinterpret_cast<QHeader*>(base + L.hdr);
   float* Wf = reinterpret_cast<float*>(base + L.wf);
-  float* errT = reinterpret_cast<float*>(base + L.errT);
+  float* err = reinterpret_cast<float*>(base + L.err);
+  float* Ut = reinterpret_cast<float*>(base + L.ut);
   float* part = reinterpret_cast<float*>(base + L.part);
   uint8_t* codes8 = perm ? base + L.codes8 : nullptr;
   int* inv = reinterpret_cast<int*>(base + L.inv);
@@ -444,15 +410,18 @@ gptq_status quantize_launch(const void* W, int w_dtype, long long m_, long long 
   if (cudaMemsetAsync(hdr, 0, sizeof(QHeader), s) != cudaSuccess)
     return set_error(GPTQ_ERR_CUDA, "cudaMemsetAsync failed");
   {
+    ProfScope ps("quantize.prep", s);
     dim3 grid((unsigned)std::min(8, (d + 255) / 256), (unsigned)std::min(m, 65535));
     prep_kernel<<<grid, 256, 0, s>>>(W, w_dtype, m, d, ldw, perm, Wf, hdr);
-    count_launch();
+    dim3 tg((unsigned)((d + 31) / 32), (unsigned)((d + 31) / 32));
+    transpose_kernel<<<tg, dim3(32, 8), 0, s>>>(Hinv1, Ut, d);
+    count_launch(2);
   }
   gptq_status st;
   switch (blocksize) {
-    case 32: st = run_blocks<32>(Wf, m, d, Hinv1, bits, g, qweight, wpr, codes8, scales, zeros, G, errT, L.lde, part, s); break;
-    case 64: st = run_blocks<64>(Wf, m, d, Hinv1, bits, g, qweight, wpr, codes8, scales, zeros, G, errT, L.lde, part, s); break;
-    default: st = run_blocks<128>(Wf, m, d, Hinv1, bits, g, qweight, wpr, codes8, scales, zeros, G, errT, L.lde, part, s); break;
+    case 32: st = run_blocks<32>(Wf, m, d, Hinv1, Ut, bits, g, qweight, wpr, codes8, scales, zeros, G, err, part, s); break;
+    case 64: st = run_blocks<64>(Wf, m, d, Hinv1, Ut, bits, g, qweight, wpr, codes8, scales, zeros, G, err, part, s); break;
+    default: st = run_blocks<128>(Wf, m, d, Hinv1, Ut, bits, g, qweight, wpr, codes8, scales, zeros, G, err, part, s); break;
   }
   if (st) return st;
   loss_finalize_kernel<<<(d + 255) / 256, 256, 0, s>>>(part, L.nrg, d, perm, col_losses);

@@ -18,6 +18,31 @@ namespace gptq {
 // ------------------------------------------------------------------------------
 gptq_status set_error(gptq_status st, const char* fmt, ...);
 void count_launch(int n = 1);
+
+// Opt-in launch timing (environment variable GPTQ_PROFILE=1): a ProfScope records a
+// CUDA event pair around the launches it encloses, on their stream; per-name totals
+// are printed to stderr when the process exits. Disabled, a scope costs one branch.
+bool profiling_enabled();
+void profile_record(const char* name, cudaEvent_t start, cudaEvent_t stop);
+cudaEvent_t profile_event();
+struct ProfScope {
+  const char* name;
+  cudaStream_t stream;
+  cudaEvent_t start = nullptr;
+  ProfScope(const char* n, cudaStream_t s) : name(n), stream(s) {
+    if (profiling_enabled()) {
+      start = profile_event();
+      cudaEventRecord(start, stream);
+    }
+  }
+  ~ProfScope() {
+    if (start) {
+      cudaEvent_t stop = profile_event();
+      cudaEventRecord(stop, stream);
+      profile_record(name, start, stop);
+    }
+  }
+};
 gptq_status check_launch(const char* what);
 int sm_count();
 int* device_error_word();   // device address of the library's error word
@@ -90,6 +115,19 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, uint64_
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
       ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
       : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, uint64_t* bar, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Make this thread's ordinary shared-memory writes visible to the async proxy (TMA,
+// tensor-core operand reads) before signalling the consumer.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
@@ -193,6 +231,30 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16_nowait(uint32_t taddr, uint32
 }
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Copy a PR x PC fp32 tile into shared memory (row stride ldd): element (i, c) is
+// src[i * lds + c] when i < rows and c < cols, else 0. Each thread issues UNROLL
+// independent global loads before storing any of them, so a tile costs a few memory
+// round trips rather than one per loop iteration.
+template <int NT, int PR, int PC, int UNROLL = 8>
+__device__ __forceinline__ void load_tile(float* __restrict__ dst, int ldd, const float* __restrict__ src, long long lds,
+                                          int rows, int cols) {
+  constexpr int TOTAL = PR * PC;
+  for (int base = threadIdx.x; base < TOTAL; base += NT * UNROLL) {
+    float v[UNROLL];
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const int idx = base + u * NT;
+      const int i = idx / PC, c = idx % PC;
+      v[u] = (idx < TOTAL && i < rows && c < cols) ? src[(long long)i * lds + c] : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const int idx = base + u * NT;
+      if (idx < TOTAL) dst[(idx / PC) * ldd + idx % PC] = v[u];
+    }
+  }
+}
 
 __device__ __forceinline__ void report_device_error(int* word, int bits) {
   if (word) atomicOr(word, bits);

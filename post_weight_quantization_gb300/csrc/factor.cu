@@ -13,20 +13,28 @@
 // uniqueness of the Cholesky factor with positive diagonal, Hinv1 = J L^-1 J.
 // Cost 2/3 d^3 instead of 4/3 d^3 flops, and one fewer factorization to lose accuracy.
 //
-// Kernels (fp32, FFMA; all bounded, no spin-waits):
-//   diag_stats   lambda and the finiteness check of diag(H)
-//   perm_rank    stable descending sort of diag(H) by rank counting (act-order)
-//   gather       P[a][b] = H_d[p(d-1-a)][p(d-1-b)] (lower triangle), p = act-order
-//   chol_panel   factor a 64-wide diagonal block in shared memory (every CTA) and
-//                solve the panel below it (L21 = A21 L11^-T), one 64-row slab per CTA
-//   chol_update  trailing A22 -= L21 L21^T, 128 x 128 tiles of the lower triangle
-//   eye          Hinv1 = I
-//   trtri_panel  block row K of X = L^-1: X[K][:k1] = L_KK^-1 X[K][:k1]
-//   trtri_update X[rows > K][:k1] -= L[rows > K][K] X[K][:k1]
-// X lives directly in Hinv1 at reversed coordinates: X[a][b] is Hinv1[d-1-a][d-1-b].
+// Kernels (fp32, FFMA; no spin-waits):
+//   diag_stats      lambda and the finiteness check of diag(H)
+//   perm_rank       stable descending sort of diag(H) by rank counting (act-order)
+//   gather          P[a][b] = H_d[p(d-1-a)][p(d-1-b)] (lower triangle), p = act-order
+//   Cholesky, 64-wide blocks, right-looking:
+//     chol_panel    one launch per 64-wide panel: every CTA factors the diagonal block
+//                   in shared memory (16-column pieces), CTA 0 writes it back and the
+//                   others solve 64 rows each below it (x L11^T = a, four lanes per row)
+//     tc_gemm       trailing update A22 -= L21 L21^T (lower tiles; tensor cores,
+//                   3 x TF32, both operands K-major)
+//   Triangular inverse X = L^-1 (natural order, inside Hinv1):
+//     diag_inverse  every 64 x 64 diagonal block at once (thread c solves L x = e_c)
+//     gemm x 2 per level, recursive doubling over block pairs (A, C):
+//                   T = L[C][A] X[A][A];  X[C][A] = -X[C][C] T   (T lives in P's unused
+//                   strict upper triangle)
+//     reverse       Hinv1 = J X J in place
+// A failed pivot sets a flag in the workspace header that every later kernel checks.
+
 #include <algorithm>
 #include <climits>
 #include <cmath>
+#include <utility>
 
 #include "common.cuh"
 #include "simt_gemm.cuh"
@@ -35,15 +43,13 @@ namespace gptq {
 namespace factor {
 
 constexpr int NB = 64;        // panel width
-using simt::TILE;
-using simt::KC;
-constexpr int UPD_THREADS = simt::THREADS;
 
 struct Header {               // at the start of the factor workspace
   float lambda;
   int nonfinite;
   int fail_pivot;             // INT_MAX when the factorization succeeded
   int d;
+  int failed;                 // non-zero once a pivot failed or diag(H) is not finite
 };
 constexpr size_t kHeaderBytes = 256;
 
@@ -71,6 +77,7 @@ __global__ void diag_stats_kernel(const float* __restrict__ H, int d, float perc
     hdr->nonfinite = bad_s;
     hdr->fail_pivot = INT_MAX;
     hdr->d = d;
+    hdr->failed = bad_s;
   }
 }
 
@@ -110,215 +117,225 @@ __global__ void gather_kernel(const float* __restrict__ H, int d, const int* __r
 }
 
 // ---------------------------------------------------------------------------------
-// Cholesky panel: every CTA factors the diagonal block (nb <= 64) in shared memory;
-// CTA 0 writes it back, CTA b >= 1 solves rows [k1 + 64 (b-1), +64) of the panel.
-__global__ void __launch_bounds__(256) chol_panel_kernel(float* __restrict__ P, int d, int k0, Header* hdr) {
-  __shared__ float A[NB][NB + 1];
-  __shared__ float R[64][NB + 1];
-  __shared__ int failed;
-  if (hdr->fail_pivot != INT_MAX || hdr->nonfinite) return;   // an earlier panel failed
-  const int nb = min(NB, d - k0);
-  const int tid = threadIdx.x;
-  for (int idx = tid; idx < nb * nb; idx += blockDim.x) {
-    const int i = idx / nb, l = idx % nb;
-    A[i][l] = (l <= i) ? P[(long long)(k0 + i) * d + k0 + l] : 0.0f;
-  }
-  if (tid == 0) failed = 0;
+// Cholesky of the 64 x 64 diagonal block at k0, blocked in 4 panels of 16 columns:
+//   (a) warp 0 factors the panel's 16 x 16 diagonal piece, lane i holding row i in
+//       registers; column values move between lanes by shuffles;
+//   (b) one thread per row below solves that row against the piece (x L^T = a);
+//   (c) all threads apply the rank-16 update to the lower part right of the panel.
+// Three barriers per panel.
+constexpr int DP = 16;   // panel width inside the diagonal block
+
+template <int... Js>
+__device__ __forceinline__ bool panel_factor(std::integer_sequence<int, Js...>, float (&R)[DP], int lane, int np,
+                                             float* dpiv, int& fail) {
+  bool ok = true;
+  auto step = [&](auto jc) {
+    constexpr int j = decltype(jc)::value;
+    if (!ok || j >= np) return;
+    const float piv = __shfl_sync(0xffffffffu, R[j], j);
+    if (!(piv > 0.0f) || !isfinite(piv)) {
+      ok = false;
+      fail = j;
+      return;
+    }
+    const float dj = sqrtf(piv);
+    const float inv = __fdiv_rn(1.0f, dj);
+    const float li = (lane > j) ? R[j] * inv : 0.0f;
+#pragma unroll
+    for (int c = j + 1; c < DP; ++c) {
+      const float lc = __shfl_sync(0xffffffffu, li, c);      // L[c][j]
+      if (lane >= c) R[c] = fmaf(-li, lc, R[c]);
+    }
+    if (lane == j) R[j] = dj;
+    else if (lane > j) R[j] = li;
+    if (lane == 0) dpiv[j] = inv;
+  };
+  (step(std::integral_constant<int, Js>{}), ...);
+  return ok;
+}
+
+// Factor the nb x nb block held in A (lower triangle) in place; returns the failing
+// pivot (block-relative) or -1. All 256 threads of the CTA take part.
+__device__ int factor_diag_block(float (*A)[NB + 1], float* dinv, int* fail_s, int nb) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) *fail_s = -1;
   __syncthreads();
-  for (int j = 0; j < nb; ++j) {
-    if (tid == 0) {
-      const float piv = A[j][j];
-      if (!(piv > 0.0f) || !isfinite(piv)) {
-        failed = 1;
-        if (blockIdx.x == 0) atomicMin(&hdr->fail_pivot, k0 + j);
-      } else {
-        A[j][j] = sqrtf(piv);
+  for (int p0 = 0; p0 < nb; p0 += DP) {
+    const int np = min(DP, nb - p0);
+    // (a) diagonal piece
+    if (warp == 0) {
+      float R[DP];
+#pragma unroll
+      for (int c = 0; c < DP; ++c) R[c] = (lane < np && c <= lane) ? A[p0 + lane][p0 + c] : 0.0f;
+      int fail = -1;
+      const bool ok = panel_factor(std::make_integer_sequence<int, DP>{}, R, lane, np, dinv, fail);
+      if (!ok && lane == 0) *fail_s = p0 + fail;
+      if (lane < np) {
+#pragma unroll
+        for (int c = 0; c < DP; ++c)
+          if (c <= lane) A[p0 + lane][p0 + c] = R[c];
       }
     }
     __syncthreads();
-    if (failed) return;
-    const float djj = A[j][j];
-    for (int i = j + 1 + tid; i < nb; i += blockDim.x) A[i][j] = __fdiv_rn(A[i][j], djj);
+    if (*fail_s >= 0) return *fail_s;
+    // (b) rows below the piece: x L^T = a
+    const int r = p0 + DP + tid;
+    if (tid < NB - p0 - DP && r < nb) {
+      float x[DP];
+#pragma unroll
+      for (int c = 0; c < DP; ++c) x[c] = (c < np) ? A[r][p0 + c] : 0.0f;
+#pragma unroll
+      for (int j = 0; j < DP; ++j) {
+        x[j] *= dinv[j];
+#pragma unroll
+        for (int c = j + 1; c < DP; ++c) x[c] = fmaf(-x[j], A[p0 + c][p0 + j], x[c]);
+      }
+#pragma unroll
+      for (int c = 0; c < DP; ++c)
+        if (c < np) A[r][p0 + c] = x[c];
+    }
     __syncthreads();
-    const int rem = nb - j - 1;
-    for (int idx = tid; idx < rem * rem; idx += blockDim.x) {
-      const int i = j + 1 + idx / rem, l = j + 1 + idx % rem;
-      if (l <= i) A[i][l] = fmaf(-A[i][j], A[l][j], A[i][l]);
+    // (c) rank-16 update of the lower part right of the panel
+    const int q0 = p0 + np, rem = nb - q0;
+    for (int idx = tid; idx < rem * rem; idx += 256) {
+      const int i = q0 + idx / rem, c = q0 + idx % rem;
+      if (c <= i) {
+        float acc = A[i][c];
+#pragma unroll
+        for (int k = 0; k < DP; ++k)
+          if (k < np) acc = fmaf(-A[i][p0 + k], A[c][p0 + k], acc);
+        A[i][c] = acc;
+      }
     }
     __syncthreads();
   }
-  if (blockIdx.x == 0) {
-    for (int idx = tid; idx < nb * nb; idx += blockDim.x) {
-      const int i = idx / nb, l = idx % nb;
-      if (l <= i) P[(long long)(k0 + i) * d + k0 + l] = A[i][l];
+  return -1;
+}
+
+// One Cholesky step for the 64-wide panel at k0, in one launch: every CTA factors the
+// diagonal block in shared memory (the same arithmetic in each, so every copy is the
+// same); CTA 0 writes it back and CTA b >= 1 solves rows [k1 + 64 (b - 1), + 64) of the
+// panel below against it (x L11^T = a, four lanes per row, pivots broadcast by shuffle).
+constexpr int TR_LANES = 4;
+constexpr int TR_SLOTS = NB / TR_LANES;        // 16
+constexpr int PANEL_THREADS = 256;             // 64 rows per CTA
+constexpr int TR_ROWS = PANEL_THREADS / TR_LANES;
+
+__global__ void __launch_bounds__(PANEL_THREADS) chol_panel_kernel(float* __restrict__ P, int d, int k0, Header* hdr) {
+  __shared__ float A[NB][NB + 1];
+  __shared__ float dinv[DP];
+  __shared__ float invd[NB];
+  __shared__ int fail_s;
+  if (hdr->failed) return;
+  const int nb = min(NB, d - k0), k1 = k0 + nb;
+  const int tid = threadIdx.x;
+  load_tile<PANEL_THREADS, NB, NB>(&A[0][0], NB + 1, P + (long long)k0 * d + k0, d, nb, nb);   // upper part unused
+  __syncthreads();
+  const int fail = factor_diag_block(A, dinv, &fail_s, nb);
+  if (fail >= 0) {
+    if (blockIdx.x == 0 && tid == 0) {
+      atomicMin(&hdr->fail_pivot, k0 + fail);
+      hdr->failed = 1;
     }
     return;
   }
-  // rows of the panel below: X L11^T = A21  (forward substitution over columns)
-  const int r0 = k0 + nb + (blockIdx.x - 1) * 64;
-  const int nr = min(64, d - r0);
-  if (nr <= 0) return;
-  for (int idx = tid; idx < nr * nb; idx += blockDim.x) {
-    const int i = idx / nb, l = idx % nb;
-    R[i][l] = P[(long long)(r0 + i) * d + k0 + l];
+  if (blockIdx.x == 0) {
+    for (int idx = tid; idx < nb * nb; idx += PANEL_THREADS) {
+      const int i = idx / nb, c = idx % nb;
+      if (c <= i) P[(long long)(k0 + i) * d + k0 + c] = A[i][c];
+    }
+    return;
   }
+  for (int j = tid; j < NB; j += PANEL_THREADS) invd[j] = (j < nb) ? __fdiv_rn(1.0f, A[j][j]) : 0.0f;
   __syncthreads();
-  for (int j = 0; j < nb; ++j) {
-    const float djj = A[j][j];
-    for (int i = tid; i < nr; i += blockDim.x) R[i][j] = __fdiv_rn(R[i][j], djj);
-    __syncthreads();
-    const int rem = nb - j - 1;
-    for (int idx = tid; idx < nr * rem; idx += blockDim.x) {
-      const int i = idx / rem, l = j + 1 + idx % rem;
-      R[i][l] = fmaf(-R[i][j], A[l][j], R[i][l]);
-    }
-    __syncthreads();
-  }
-  for (int idx = tid; idx < nr * nb; idx += blockDim.x) {
-    const int i = idx / nb, l = idx % nb;
-    P[(long long)(r0 + i) * d + k0 + l] = R[i][l];
-  }
-}
-
-// ---------------------------------------------------------------------------------
-// trailing update of the Cholesky: for tiles (I, J), J <= I, of rows/cols >= k1:
-//   P[i][j] -= sum_{l < nb} P[i][k0 + l] * P[j][k0 + l]
-__global__ void __launch_bounds__(UPD_THREADS) chol_update_kernel(float* __restrict__ P, int d, int k0, int nb,
-                                                                  const Header* __restrict__ hdr) {
-  __shared__ __align__(16) float As[KC][TILE];
-  __shared__ __align__(16) float Bs[KC][TILE];
-  if (hdr->fail_pivot != INT_MAX || hdr->nonfinite) return;
-  const int k1 = k0 + nb;
-  // lower-triangular tile index -> (I, J)
-  const long long t = blockIdx.x;
-  int I = (int)((sqrt(8.0 * (double)t + 1.0) - 1.0) * 0.5);
-  while ((long long)(I + 1) * (I + 2) / 2 <= t) ++I;
-  while ((long long)I * (I + 1) / 2 > t) --I;
-  const int J = (int)(t - (long long)I * (I + 1) / 2);
-  const int i0 = k1 + I * TILE, j0 = k1 + J * TILE;
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  simt::Acc acc;
+  const int lane = tid & 31, q = lane & (TR_LANES - 1), qbase = lane - q;
+  const int r = k1 + (blockIdx.x - 1) * TR_ROWS + tid / TR_LANES;
+  const bool active = r < d;
+  float* row = P + (long long)(active ? r : k0) * d + k0;
+  float x[TR_SLOTS];
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
+  for (int k = 0; k < TR_SLOTS; ++k) {
+    const int c = TR_LANES * k + q;
+    x[k] = (active && c < nb) ? row[c] : 0.0f;
+  }
+#pragma unroll 1
+  for (int jb = 0; jb < nb; jb += TR_LANES) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc.v[i][j] = 0.0f;
-  for (int kc = 0; kc < nb; kc += KC) {
-    const int kn = min(KC, nb - kc);
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < TILE * KC; idx += UPD_THREADS) {
-      const int r = idx % TILE, k = idx / TILE;
-      float va = 0.0f, vb = 0.0f;
-      if (k < kn) {
-        if (i0 + r < d) va = P[(long long)(i0 + r) * d + k0 + kc + k];
-        if (j0 + r < d) vb = P[(long long)(j0 + r) * d + k0 + kc + k];
+    for (int i = 0; i < TR_LANES; ++i) {
+      const int j = jb + i;
+      if (j < nb) {                                           // warp-uniform
+        const float xj = __shfl_sync(0xffffffffu, x[0], qbase + i) * invd[j];
+        if (q == i && active) row[j] = xj;
+        // slot k holds column jb + 4k + q: later than j unless k == 0 and q <= i
+#pragma unroll
+        for (int k = 0; k < TR_SLOTS; ++k) {
+          const int c = jb + TR_LANES * k + q;
+          if ((k > 0 || q > i) && c < NB) x[k] = fmaf(-xj, A[c][j], x[k]);
+        }
       }
-      As[k][r] = va;
-      Bs[k][r] = vb;
     }
-    __syncthreads();
-    simt::mma_chunk(As, Bs, kn, tx, ty, acc);
-  }
 #pragma unroll
-  for (int a = 0; a < 8; ++a) {
-    const int i = i0 + simt::micro_row(a, ty);
-    if (i >= d) continue;
-#pragma unroll
-    for (int b = 0; b < 8; ++b) {
-      const int j = j0 + simt::micro_row(b, tx);
-      if (j <= i) P[(long long)i * d + j] -= acc.v[a][b];
-    }
+    for (int k = 0; k < TR_SLOTS - 1; ++k) x[k] = x[k + 1];
+    x[TR_SLOTS - 1] = 0.0f;
   }
 }
 
-// ---------------------------------------------------------------------------------
-__global__ void eye_kernel(float* __restrict__ M, int d) {
-  const long long n = (long long)d * d;
-  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n; idx += (long long)gridDim.x * blockDim.x)
-    M[idx] = (idx / d == idx % d) ? 1.0f : 0.0f;
+// Inverse of every 64 x 64 diagonal block of L, written into X's diagonal blocks
+// (X = L^-1 in natural order). Thread c solves L x = e_c (column c of the inverse).
+template <int... Js>
+__device__ __forceinline__ void inv_column(std::integer_sequence<int, Js...>, float (&x)[NB], const float (*L)[NB + 1],
+                                           const float* invd) {
+  auto step = [&](auto jc) {
+    constexpr int j = decltype(jc)::value;
+    x[j] *= invd[j];
+#pragma unroll
+    for (int q = j + 1; q < NB; ++q) x[q] = fmaf(-L[q][j], x[j], x[q]);
+  };
+  (step(std::integral_constant<int, Js>{}), ...);
 }
 
-__device__ __forceinline__ long long rev_index(int a, int b, int d) {
-  return (long long)(d - 1 - a) * d + (d - 1 - b);
-}
-
-// X[K][c0 : c0 + 64) = L_KK^-1 X[K][c0 : c0 + 64), K = [k0, k0 + nb), columns < k1
-__global__ void __launch_bounds__(256) trtri_panel_kernel(const float* __restrict__ P, float* __restrict__ U, int d,
-                                                          int k0, const Header* __restrict__ hdr) {
-  __shared__ float A[NB][NB + 1];
-  __shared__ float Xs[NB][64 + 1];
-  if (hdr->fail_pivot != INT_MAX || hdr->nonfinite) return;
+__global__ void __launch_bounds__(64) diag_inverse_kernel(const float* __restrict__ P, float* __restrict__ X, int d,
+                                                          const Header* hdr) {
+  __shared__ float L[NB][NB + 1];
+  __shared__ float invd[NB];
+  if (hdr->failed) return;
+  const int k0 = blockIdx.x * NB;
   const int nb = min(NB, d - k0);
-  const int k1 = k0 + nb;
-  const int c0 = blockIdx.x * 64;
-  const int nc = min(64, k1 - c0);
-  const int tid = threadIdx.x;
-  for (int idx = tid; idx < nb * nb; idx += blockDim.x) {
-    const int i = idx / nb, l = idx % nb;
-    A[i][l] = (l <= i) ? P[(long long)(k0 + i) * d + k0 + l] : 0.0f;
-  }
-  for (int idx = tid; idx < nb * 64; idx += blockDim.x) {
-    const int i = idx / 64, c = idx % 64;
-    Xs[i][c] = (c < nc) ? U[rev_index(k0 + i, c0 + c, d)] : 0.0f;
+  load_tile<NB, NB, NB>(&L[0][0], NB + 1, P + (long long)k0 * d + k0, d, nb, nb);
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < NB * NB; idx += blockDim.x) {   // lower triangle; identity past the block
+    const int i = idx / NB, c = idx % NB;
+    if (c > i || i >= nb) L[i][c] = (i == c) ? 1.0f : 0.0f;
   }
   __syncthreads();
-  for (int j = 0; j < nb; ++j) {
-    const float djj = A[j][j];
-    for (int c = tid; c < 64; c += blockDim.x) Xs[j][c] = __fdiv_rn(Xs[j][c], djj);
-    __syncthreads();
-    const int rem = nb - j - 1;
-    for (int idx = tid; idx < rem * 64; idx += blockDim.x) {
-      const int i = j + 1 + idx / 64, c = idx % 64;
-      Xs[i][c] = fmaf(-A[i][j], Xs[j][c], Xs[i][c]);
-    }
-    __syncthreads();
-  }
-  for (int idx = tid; idx < nb * 64; idx += blockDim.x) {
-    const int i = idx / 64, c = idx % 64;
-    if (c < nc && c0 + c <= k0 + i) U[rev_index(k0 + i, c0 + c, d)] = Xs[i][c];
-  }
+  for (int j = threadIdx.x; j < NB; j += blockDim.x) invd[j] = __fdiv_rn(1.0f, L[j][j]);
+  __syncthreads();
+  const int c = threadIdx.x;
+  float x[NB];
+#pragma unroll
+  for (int q = 0; q < NB; ++q) x[q] = (q == c) ? 1.0f : 0.0f;
+  inv_column(std::make_integer_sequence<int, NB>{}, x, L, invd);
+  if (c >= nb) return;
+#pragma unroll
+  for (int q = 0; q < NB; ++q)
+    if (q < nb && q >= c) X[(long long)(k0 + q) * d + k0 + c] = x[q];
 }
 
-// X[i][j] -= sum_{l < nb} L[i][k0 + l] X[k0 + l][j] for i >= k1, j < k1
-__global__ void __launch_bounds__(UPD_THREADS) trtri_update_kernel(const float* __restrict__ P, float* __restrict__ U,
-                                                                   int d, int k0, int nb,
-                                                                   const Header* __restrict__ hdr) {
-  __shared__ __align__(16) float As[KC][TILE];
-  __shared__ __align__(16) float Bs[KC][TILE];
-  if (hdr->fail_pivot != INT_MAX || hdr->nonfinite) return;
-  const int k1 = k0 + nb;
-  const int i0 = k1 + blockIdx.y * TILE;
-  const int j0 = blockIdx.x * TILE;
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  simt::Acc acc;
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc.v[i][j] = 0.0f;
-  for (int kc = 0; kc < nb; kc += KC) {
-    const int kn = min(KC, nb - kc);
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < TILE * KC; idx += UPD_THREADS) {
-      const int r = idx % TILE, k = idx / TILE;
-      float va = 0.0f, vb = 0.0f;
-      if (k < kn) {
-        if (i0 + r < d) va = P[(long long)(i0 + r) * d + k0 + kc + k];
-        if (j0 + r < k1) vb = U[rev_index(k0 + kc + k, j0 + r, d)];
-      }
-      As[k][r] = va;
-      Bs[k][r] = vb;
-    }
-    __syncthreads();
-    simt::mma_chunk(As, Bs, kn, tx, ty, acc);
-  }
-#pragma unroll
-  for (int a = 0; a < 8; ++a) {
-    const int i = i0 + simt::micro_row(a, ty);
-    if (i >= d) continue;
-#pragma unroll
-    for (int b = 0; b < 8; ++b) {
-      const int j = j0 + simt::micro_row(b, tx);
-      if (j < k1) U[rev_index(i, j, d)] -= acc.v[a][b];
-    }
+__global__ void zero_kernel(float* __restrict__ M, long long n) {
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n; idx += (long long)gridDim.x * blockDim.x)
+    M[idx] = 0.0f;
+}
+
+// In place: M[a][b] <-> M[d-1-a][d-1-b] (turns X = L^-1, lower, into J X J, upper).
+__global__ void reverse_kernel(float* __restrict__ M, int d, const Header* hdr) {
+  if (hdr->failed) return;
+  const long long n = (long long)d * d;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n / 2;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const long long jdx = n - 1 - idx;         // the partner of idx
+    const float t = M[idx];
+    M[idx] = M[jdx];
+    M[jdx] = t;
   }
 }
 
@@ -334,7 +351,11 @@ gptq_status factor_launch(const float* H, long long d_, float percdamp, int act_
   const int d = (int)d_;
   Header* hdr = reinterpret_cast<Header*>(ws);
   float* P = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + kHeaderBytes);
+  const int* failed = &hdr->failed;
+  const bool vec = (d % 4 == 0) && simt::aligned16(P) && simt::aligned16(Hinv1);
 
+  {
+  ProfScope ps_setup("factor.setup", s);
   diag_stats_kernel<<<1, 1024, 0, s>>>(H, d, percdamp, hdr);
   count_launch();
   if (act_order) {
@@ -346,35 +367,71 @@ gptq_status factor_launch(const float* H, long long d_, float percdamp, int act_
     gather_kernel<<<grid, dim3(32, 8), 0, s>>>(H, d, act_order ? perm_out : nullptr, hdr, P);
     count_launch();
   }
+  }
   if (gptq_status st = check_launch("factor setup kernels")) return st;
 
+  // ---- Cholesky P = L L^T, 64-wide blocks, right-looking
   for (int k0 = 0; k0 < d; k0 += NB) {
-    const int nb = std::min(NB, d - k0);
-    const int below = d - k0 - nb;
-    chol_panel_kernel<<<1 + (below + 63) / 64, 256, 0, s>>>(P, d, k0, hdr);
-    count_launch();
-    if (below > 0) {
-      const long long nt = (below + TILE - 1) / TILE;
-      chol_update_kernel<<<(unsigned)(nt * (nt + 1) / 2), UPD_THREADS, 0, s>>>(P, d, k0, nb, hdr);
+    const int nb = std::min(NB, d - k0), k1 = k0 + nb, below = d - k1;
+    {
+      ProfScope ps("factor.chol_panel", s);
+      chol_panel_kernel<<<1 + (below + TR_ROWS - 1) / TR_ROWS, PANEL_THREADS, 0, s>>>(P, d, k0, hdr);
       count_launch();
+    }
+    if (below > 0) {
+      simt::GemmArgs g{};
+      g.M = g.N = below; g.K = nb; g.M_last = below; g.K_last = nb;
+      g.A = P + (long long)k1 * d + k0; g.lda = d;
+      g.B = g.A; g.ldb = d;
+      g.C = P + (long long)k1 * d + k1; g.ldc = d;
+      g.alpha = -1.0f; g.beta = 1.0f;
+      g.lower_tiles = 1;
+      g.vec = vec;
+      g.skip = failed;
+      ProfScope ps("factor.chol_update_gemm", s);
+      if (gptq_status st = tc_gemm(g, 1, true, true, s)) return st;
     }
   }
   if (gptq_status st = check_launch("Cholesky kernels")) return st;
 
-  eye_kernel<<<std::max(1, std::min(4096, (int)(((long long)d * d + 255) / 256))), 256, 0, s>>>(Hinv1, d);
-  count_launch();
-  for (int k0 = 0; k0 < d; k0 += NB) {
-    const int nb = std::min(NB, d - k0);
-    const int k1 = k0 + nb;
-    trtri_panel_kernel<<<(k1 + 63) / 64, 256, 0, s>>>(P, Hinv1, d, k0, hdr);
-    count_launch();
-    const int below = d - k1;
-    if (below > 0) {
-      dim3 grid((unsigned)((k1 + TILE - 1) / TILE), (unsigned)((below + TILE - 1) / TILE));
-      trtri_update_kernel<<<grid, UPD_THREADS, 0, s>>>(P, Hinv1, d, k0, nb, hdr);
-      count_launch();
-    }
+  // ---- X = L^-1 in natural order inside Hinv1: diagonal blocks, then recursive doubling
+  {
+    ProfScope ps("factor.zero_diag_inverse", s);
+    zero_kernel<<<std::max(1, std::min(4096, (int)(((long long)d * d + 255) / 256))), 256, 0, s>>>(Hinv1, (long long)d * d);
+    diag_inverse_kernel<<<(d + NB - 1) / NB, NB, 0, s>>>(P, Hinv1, d, hdr);
   }
+  count_launch(2);
+  for (int sz = NB; sz < d; sz *= 2) {
+    // pairs p: A block [2p sz, 2p sz + sz) (full), C block [2p sz + sz, min(2p sz + 2sz, d))
+    int np = 0;
+    while (2LL * np * sz + sz < d) ++np;
+    const int c_last = std::min(sz, d - (2 * (np - 1) * sz + sz));
+    const long long pair = 2LL * sz * d + 2LL * sz;
+    // T_p = L[C][A] X[A][A], stored in P's strict upper triangle at rows p sz, columns d - sz
+    simt::GemmArgs g1{};
+    g1.M = sz; g1.N = sz; g1.K = sz; g1.M_last = c_last; g1.K_last = sz;
+    g1.A = P + (long long)sz * d; g1.lda = d; g1.a_bs = pair;
+    g1.B = Hinv1; g1.ldb = d; g1.b_bs = pair; g1.b_lower = 1;
+    g1.C = P + (d - sz); g1.ldc = d; g1.c_bs = (long long)sz * d;
+    g1.alpha = 1.0f; g1.beta = 0.0f;
+    g1.vec = vec;
+    g1.skip = failed;
+    ProfScope ps("factor.trtri_gemms", s);
+    if (gptq_status st = simt::gemm(g1, np, true, false, s)) return st;
+    // X[C][A] = -X[C][C] T_p
+    simt::GemmArgs g2{};
+    g2.M = sz; g2.N = sz; g2.K = sz; g2.M_last = c_last; g2.K_last = c_last;
+    g2.A = Hinv1 + (long long)sz * d + sz; g2.lda = d; g2.a_bs = pair; g2.a_lower = 1;
+    g2.B = P + (d - sz); g2.ldb = d; g2.b_bs = (long long)sz * d;
+    g2.C = Hinv1 + (long long)sz * d; g2.ldc = d; g2.c_bs = pair;
+    g2.alpha = -1.0f; g2.beta = 0.0f;
+    g2.vec = vec;
+    g2.skip = failed;
+    if (gptq_status st = simt::gemm(g2, np, true, false, s)) return st;
+  }
+  ProfScope ps_rev("factor.reverse", s);
+  reverse_kernel<<<std::max(1, std::min(4096, (int)(((long long)d * d / 2 + 255) / 256))), 256, 0, s>>>(Hinv1, d, hdr);
+  count_launch();
   return check_launch("triangular-inverse kernels");
 }
 

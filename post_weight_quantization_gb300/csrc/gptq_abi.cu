@@ -4,10 +4,15 @@
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <string>
+#include <vector>
 
 #include "common.cuh"
+#include "simt_gemm.cuh"
 
 namespace gptq {
 
@@ -58,6 +63,61 @@ gptq_status check_launch(const char* what) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(GPTQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
   return GPTQ_OK;
+}
+
+// ---- opt-in launch timing ----
+namespace {
+struct ProfEntry {
+  const char* name;
+  cudaEvent_t start, stop;
+};
+std::mutex g_prof_mu;
+std::vector<ProfEntry>* g_prof = nullptr;
+int g_prof_state = -1;   // -1 unknown, 0 off, 1 on
+
+void profile_dump() {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (!g_prof) return;
+  cudaDeviceSynchronize();
+  std::map<std::string, std::pair<int, double>> tot;
+  for (const ProfEntry& e : *g_prof) {
+    float ms = 0.0f;
+    if (cudaEventElapsedTime(&ms, e.start, e.stop) == cudaSuccess) {
+      auto& t = tot[e.name];
+      t.first += 1;
+      t.second += ms;
+    }
+  }
+  double all = 0.0;
+  for (auto& kv : tot) all += kv.second.second;
+  fprintf(stderr, "[gptq profile] %zu scopes, %.3f ms total\n", g_prof->size(), all);
+  for (auto& kv : tot)
+    fprintf(stderr, "[gptq profile] %-28s %6d x  %10.3f ms  (%8.2f us each)\n", kv.first.c_str(), kv.second.first,
+            kv.second.second, 1e3 * kv.second.second / kv.second.first);
+}
+}  // namespace
+
+bool profiling_enabled() {
+  if (g_prof_state < 0) {
+    const char* v = getenv("GPTQ_PROFILE");
+    g_prof_state = (v && v[0] == '1') ? 1 : 0;
+    if (g_prof_state) {
+      g_prof = new std::vector<ProfEntry>();
+      atexit(profile_dump);
+    }
+  }
+  return g_prof_state == 1;
+}
+
+cudaEvent_t profile_event() {
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+void profile_record(const char* name, cudaEvent_t start, cudaEvent_t stop) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (g_prof) g_prof->push_back({name, start, stop});
 }
 
 int sm_count() {
@@ -226,6 +286,28 @@ gptq_status gptq_unpack_codes(const uint32_t* qweight, int64_t m, int64_t d, int
   if (m < 0 || d < 0) return set_error(GPTQ_ERR_INVALID_ARG, "negative size");
   if (bits != 2 && bits != 3 && bits != 4 && bits != 8) return set_error(GPTQ_ERR_INVALID_ARG, "bits must be 2, 3, 4 or 8");
   return unpack_launch(qweight, m, d, bits, codes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gptq_status gptq_gemm_f32(int engine, int a_kmajor, int b_kmajor, int64_t M, int64_t N, int64_t K, const float* A,
+                          int64_t lda, const float* B, int64_t ldb, float* C, int64_t ldc, float alpha, float beta,
+                          int lower_tiles, gptq_stream_t stream) {
+  g_last_error[0] = 0;
+  if (!A || !B || !C) return set_error(GPTQ_ERR_INVALID_ARG, "NULL pointer");
+  if (M < 0 || N < 0 || K < 0 || M > (1 << 30) || N > (1 << 30) || K > (1 << 30))
+    return set_error(GPTQ_ERR_INVALID_ARG, "size out of range");
+  if (lower_tiles && M != N) return set_error(GPTQ_ERR_INVALID_ARG, "lower_tiles needs M == N");
+  if (ldc < N || lda < (a_kmajor ? K : M) || ldb < (b_kmajor ? K : N))
+    return set_error(GPTQ_ERR_INVALID_ARG, "leading dimension too small");
+  if (engine != 0 && engine != 1) return set_error(GPTQ_ERR_INVALID_ARG, "engine must be 0 or 1");
+  simt::GemmArgs g{};
+  g.M = (int)M; g.N = (int)N; g.K = (int)K; g.M_last = (int)M; g.K_last = (int)K;
+  g.A = A; g.lda = lda; g.B = B; g.ldb = ldb; g.C = C; g.ldc = ldc;
+  g.alpha = alpha; g.beta = beta;
+  g.lower_tiles = lower_tiles;
+  g.vec = simt::aligned16(A) && simt::aligned16(B) && simt::aligned16(C) && lda % 4 == 0 && ldb % 4 == 0 && ldc % 4 == 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (M == 0 || N == 0) return GPTQ_OK;
+  return engine == 0 ? tc_gemm(g, 1, a_kmajor != 0, b_kmajor != 0, s) : simt::gemm(g, 1, a_kmajor != 0, b_kmajor != 0, s);
 }
 
 }  // extern "C"

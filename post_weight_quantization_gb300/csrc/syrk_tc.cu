@@ -360,6 +360,7 @@ gptq_status syrk_accumulate(const uint16_t* X, long long n, long long d, long lo
       return set_error(GPTQ_ERR_CUDA, "cudaFuncSetAttribute(syrk_kernel) failed");
     attr_set = true;
   }
+  ProfScope ps("hessian.syrk", stream);
   syrk_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(tmap, H, ldh, g, alpha, device_error_word());
   count_launch();
   return check_launch("syrk_kernel");

@@ -1,0 +1,451 @@
+// FP32-accurate GEMM on the 5th-generation tensor cores (3 x TF32):
+//
+//     C = beta * C + alpha * A B        (per batch z, 128 x 128 output tiles)
+//
+// with A(i, k) = A[i * lda + k] and B(k, j) = B[j * ldb + k] (both K-major: the tf32
+// tensor-core path reads only K-major operands; an MN-major tf32 operand yields zeros,
+// so those calls take the FFMA GEMM of simt_gemm.cuh).
+//
+// Each fp32 operand x is split as x = hi + lo, hi = x with its 13 low mantissa bits
+// cleared (what the tf32 tensor-core path reads from an fp32 word) and lo = x - hi
+// (exact); A B is formed as hi_A hi_B + hi_A lo_B + lo_A hi_B, which carries about 21
+// significant bits per product.
+//
+// Design (sm_103a), one persistent CTA per SM, tiles taken round-robin:
+//   warp 0      TMA producer: 32-deep k chunks of A and B into a 3-stage ring
+//   warps 2-5   converters: lo parts of each stage into their own buffers (the
+//               128-byte swizzle permutes 16-byte chunks, so an elementwise pass keeps
+//               the layout), zeroing k past the extent of a ragged last batch
+//   warp 1      MMA issuer: per chunk 4 k-steps x 3 products, tcgen05.mma kind::tf32
+//               M = 128, N = 128, K = 8, into a fresh tensor-memory buffer (four
+//               buffers of 128 columns rotate, so the products run ahead of the
+//               epilogue's memory traffic)
+//   warps 6-13  epilogue: each chunk's partial product is added into fp32 registers
+//               with round-to-nearest (the tensor core's own accumulator truncates, so
+//               long accumulations in it drift), and at the end of a tile
+//               C = beta C + alpha acc is written
+// Every wait is bounded; a timeout raises the device error word.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdlib>
+
+#include "common.cuh"
+#include "simt_gemm.cuh"
+
+namespace gptq {
+namespace tc {
+
+constexpr int BM = 128, BN = 128, BK = 32;     // BK fp32 = 128 bytes: one swizzle row
+constexpr int STAGES = 3;
+constexpr int OP_BYTES = BM * BK * 4;          // 16 KB per operand per stage
+constexpr int STAGE_BYTES = 4 * OP_BYTES;      // A, B, A_lo, B_lo
+constexpr int THREADS = 14 * 32;
+constexpr int CONV_WARP0 = 2, NCONV = 4;
+constexpr int EPI_WARP0 = 6, NEPI = 8;
+constexpr int NBUF = 4;                       // chunk accumulators in tensor memory
+constexpr uint32_t TMEM_COLS = NBUF * BN;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+
+struct Params {
+  int M, N, K, M_last, K_last, batches;
+  int tiles_per_batch, mt, nt;
+  int lower_tiles, a_lower, b_lower;
+  float alpha, beta;
+  float* C;
+  long long ldc, c_bs;
+  const int* skip;
+};
+
+struct Tile {
+  int z, I, J, kbeg, kend, M, K;
+};
+
+__device__ __forceinline__ Tile decode(int t, const Params& p) {
+  Tile w;
+  w.z = t / p.tiles_per_batch;
+  const int u = t - w.z * p.tiles_per_batch;
+  if (p.lower_tiles) {
+    int I = (int)((sqrtf(8.0f * (float)u + 1.0f) - 1.0f) * 0.5f);
+    while ((I + 1) * (I + 2) / 2 <= u) ++I;
+    while (I * (I + 1) / 2 > u) --I;
+    w.I = I;
+    w.J = u - I * (I + 1) / 2;
+  } else {
+    w.I = u / p.nt;
+    w.J = u - w.I * p.nt;
+  }
+  const bool last = (w.z == p.batches - 1);
+  w.M = last ? p.M_last : p.M;
+  w.K = last ? p.K_last : p.K;
+  w.kbeg = 0;
+  w.kend = w.K;
+  if (p.a_lower) w.kend = min(w.kend, (w.I + 1) * BM);
+  if (p.b_lower) w.kbeg = w.J * BN;
+  if (w.kbeg >= w.kend || w.I * BM >= w.M) w.kend = w.kbeg;   // nothing to multiply
+  return w;
+}
+
+__device__ __forceinline__ int nchunks(const Tile& w) { return (w.kend - w.kbeg + BK - 1) / BK; }
+
+// smem descriptors: K-major SW128 (rows of 128 bytes along k, 8-row groups 1024 B
+// apart) and MN-major SW128 (32-element MN chunks are separate TMA boxes 4 KB apart,
+// 8-row k groups 1024 B apart).
+__device__ __forceinline__ uint64_t desc_kmaj(uint32_t base, int kk) { return umma_sdesc_sw128(base + kk * 32, 16, 1024); }
+__device__ __forceinline__ uint64_t desc_mnmaj(uint32_t base, int kk) { return umma_sdesc_sw128(base + kk * 1024, 4096, 1024); }
+
+// Load one operand's 32-deep chunk: K-major = one box {32 k, 128 rows};
+// MN-major = four boxes {32 rows, 32 k}.
+template <bool KMAJ>
+__device__ __forceinline__ void load_operand(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int r0, int k0, int z) {
+  if constexpr (KMAJ) {
+    tma_load_3d(dst, map, bar, k0, r0, z);
+  } else {
+#pragma unroll
+    for (int b = 0; b < 4; ++b) tma_load_3d(dst + b * 4096, map, bar, r0 + 32 * b, k0, z);
+  }
+}
+
+// x -> (hi, lo) for one operand's chunk, hi written in place; elements with k >= kend
+// are zeroed in both buffers. `kbase` is the chunk's first k.
+template <bool KMAJ>
+__device__ __forceinline__ void split_operand(uint8_t* raw, uint8_t* lo, int kbase, int kend, int ctid) {
+  float4* r4 = reinterpret_cast<float4*>(raw);
+  float4* l4 = reinterpret_cast<float4*>(lo);
+  const bool ragged = kbase + BK > kend;
+  for (int idx = ctid; idx < OP_BYTES / 16; idx += NCONV * 32) {
+    float4 x = r4[idx];
+    if (ragged) {
+      // 16-byte chunk idx: byte offset idx * 16
+      int k_of_elem0, step;
+      if constexpr (KMAJ) {
+        const int row = idx >> 3, pc = idx & 7;           // 8 chunks per 128-byte row
+        const int lc = pc ^ (row & 7);                    // logical chunk (128-byte swizzle)
+        k_of_elem0 = kbase + 4 * lc;
+        step = 1;
+      } else {
+        const int krow = (idx >> 3) & 31;                 // 32 k-rows per 4 KB box
+        k_of_elem0 = kbase + krow;
+        step = 0;
+      }
+      if (k_of_elem0 + 0 * step >= kend) x.x = 0.0f;
+      if (k_of_elem0 + 1 * step >= kend) x.y = 0.0f;
+      if (k_of_elem0 + 2 * step >= kend) x.z = 0.0f;
+      if (k_of_elem0 + 3 * step >= kend) x.w = 0.0f;
+    }
+    float4 hi, l;
+    hi.x = __uint_as_float(__float_as_uint(x.x) & 0xFFFFE000u);
+    hi.y = __uint_as_float(__float_as_uint(x.y) & 0xFFFFE000u);
+    hi.z = __uint_as_float(__float_as_uint(x.z) & 0xFFFFE000u);
+    hi.w = __uint_as_float(__float_as_uint(x.w) & 0xFFFFE000u);
+    l.x = x.x - hi.x;
+    l.y = x.y - hi.y;
+    l.z = x.z - hi.z;
+    l.w = x.w - hi.w;
+    r4[idx] = hi;   // hi has no bits below the tf32 mantissa, so hi + lo == x exactly
+    l4[idx] = l;
+  }
+}
+
+template <bool A_KMAJ, bool B_KMAJ>
+__global__ void __launch_bounds__(THREADS, 1)
+tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b, Params p,
+               int* __restrict__ err_word) {
+  if (p.skip && *p.skip) return;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* conv = full + STAGES;
+  uint64_t* empty = conv + STAGES;
+  uint64_t* tmem_full = empty + STAGES;
+  uint64_t* tmem_empty = tmem_full + NBUF;
+  uint64_t* drain = tmem_empty + NBUF;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&conv[s], NCONV);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < NBUF; ++b) {
+      mbar_init(&tmem_full[b], 1);
+      mbar_init(&tmem_empty[b], NEPI);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&map_a);
+    prefetch_tmap(&map_b);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int ntiles = p.tiles_per_batch * p.batches;
+  constexpr uint32_t IDESC = umma_idesc(/*tf32*/ 2, !A_KMAJ, !B_KMAJ, BM, BN);
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer ----------------
+    int stage = 0;
+    uint32_t phase = 0, armed = 0, last_phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+      const Tile w = decode(t, p);
+      for (int k0 = w.kbeg; k0 < w.kend; k0 += BK) {
+        if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
+        uint8_t* sa = smem + stage * STAGE_BYTES;
+        mbar_arrive_expect_tx(&full[stage], 2 * OP_BYTES);
+        load_operand<A_KMAJ>(sa, &map_a, &full[stage], w.I * BM, k0, w.z);
+        load_operand<B_KMAJ>(sa + OP_BYTES, &map_b, &full[stage], w.J * BN, k0, w.z);
+        armed |= 1u << stage;
+        last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (!ok) { *abort_flag = 1; report_device_error(err_word, DEVERR_TIMEOUT); }
+    for (int s = 0; s < STAGES; ++s)
+      if (armed & (1u << s)) mbar_wait_bounded(&full[s], (last_phase >> s) & 1u, nullptr);
+  } else if (warp >= CONV_WARP0 && warp < CONV_WARP0 + NCONV) {
+    // ---------------- converters: lo parts ----------------
+    const int ctid = threadIdx.x - CONV_WARP0 * 32;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+      const Tile w = decode(t, p);
+      for (int k0 = w.kbeg; k0 < w.kend; k0 += BK) {
+        if (!mbar_wait_bounded(&full[stage], phase, abort_flag)) { ok = false; break; }
+        uint8_t* sa = smem + stage * STAGE_BYTES;
+        split_operand<A_KMAJ>(sa, sa + 2 * OP_BYTES, k0, w.kend, ctid);
+        split_operand<B_KMAJ>(sa + OP_BYTES, sa + 3 * OP_BYTES, k0, w.kend, ctid);
+        fence_proxy_async_smem();   // generic-proxy writes must be visible to the tensor core
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&conv[stage]);
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (!ok) { *abort_flag = 1; report_device_error(err_word, DEVERR_TIMEOUT); }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer ----------------
+    int stage = 0;
+    uint32_t phase = 0, it = 0;
+    bool ok = true, issued = false;
+    const uint32_t sbase = smem_u32(smem);
+    for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+      const Tile w = decode(t, p);
+      for (int k0 = w.kbeg; k0 < w.kend; k0 += BK, ++it) {
+        const uint32_t buf = it % NBUF;
+        if (!mbar_wait_bounded(&tmem_empty[buf], ((it / NBUF) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+        if (!mbar_wait_bounded(&conv[stage], phase, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * BN;
+        const uint32_t a = sbase + stage * STAGE_BYTES, b = a + OP_BYTES;
+        const uint32_t alo = a + 2 * OP_BYTES, blo = a + 3 * OP_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BK / 8; ++kk) {
+          const uint64_t da = A_KMAJ ? desc_kmaj(a, kk) : desc_mnmaj(a, kk);
+          const uint64_t dal = A_KMAJ ? desc_kmaj(alo, kk) : desc_mnmaj(alo, kk);
+          const uint64_t db = B_KMAJ ? desc_kmaj(b, kk) : desc_mnmaj(b, kk);
+          const uint64_t dbl = B_KMAJ ? desc_kmaj(blo, kk) : desc_mnmaj(blo, kk);
+          umma_tf32(d_tmem, da, dbl, IDESC, kk > 0 ? 1u : 0u);
+          umma_tf32(d_tmem, dal, db, IDESC, 1u);
+          umma_tf32(d_tmem, da, db, IDESC, 1u);
+        }
+        issued = true;
+        umma_commit(&empty[stage]);
+        umma_commit(&tmem_full[buf]);
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (!ok) { *abort_flag = 1; report_device_error(err_word, DEVERR_TIMEOUT); }
+    if (issued) {
+      umma_commit(drain);
+      mbar_wait_bounded(drain, 0, nullptr);
+    }
+  } else if (warp >= EPI_WARP0) {
+    // ---------------- epilogue ----------------
+    const int q = warp & 3;                       // TMEM lane quadrant
+    const int h = (warp - EPI_WARP0) >> 2;        // 64-column half of the tile
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+      const Tile w = decode(t, p);
+      float acc[64];
+#pragma unroll
+      for (int x = 0; x < 64; ++x) acc[x] = 0.0f;
+      const int nc = nchunks(w);
+      for (int c = 0; c < nc; ++c, ++it) {
+        const uint32_t buf = it % NBUF;
+        if (!mbar_wait_bounded(&tmem_full[buf], (it / NBUF) & 1u, abort_flag)) {
+          *abort_flag = 1;
+          report_device_error(err_word, DEVERR_TIMEOUT);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint32_t v[16];
+          tmem_ld_32x32b_x16_nowait(tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN + h * 64 + g * 16, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int x = 0; x < 16; ++x) acc[g * 16 + x] += __uint_as_float(v[x]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tmem_empty[buf]);
+      }
+      if (!ok) break;
+      const int i = w.I * BM + q * 32 + lane;
+      if (w.I * BM < w.M && i < w.M) {
+        float* crow = p.C + (long long)w.z * p.c_bs + (long long)i * p.ldc;
+        const int j0 = w.J * BN + h * 64;
+        if (j0 + 63 < p.N) {
+          // 32 columns at a time: every load is issued before any store, so a tile
+          // costs one memory round trip per half instead of one per float4
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            float4 o[8];
+            float4* cp = reinterpret_cast<float4*>(crow + j0 + 32 * half);
+#pragma unroll
+            for (int x = 0; x < 8; ++x) o[x] = (p.beta != 0.0f) ? __ldcg(cp + x) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+              const int b = 32 * half + 4 * x;
+              o[x].x = fmaf(p.alpha, acc[b], p.beta * o[x].x);
+              o[x].y = fmaf(p.alpha, acc[b + 1], p.beta * o[x].y);
+              o[x].z = fmaf(p.alpha, acc[b + 2], p.beta * o[x].z);
+              o[x].w = fmaf(p.alpha, acc[b + 3], p.beta * o[x].w);
+            }
+#pragma unroll
+            for (int x = 0; x < 8; ++x) __stcg(cp + x, o[x]);
+          }
+        } else {
+#pragma unroll
+          for (int x = 0; x < 64; ++x) {
+            const int j = j0 + x;
+            if (j < p.N) {
+              const float old = (p.beta != 0.0f) ? crow[j] : 0.0f;
+              crow[j] = fmaf(p.alpha, acc[x], p.beta * old);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 3-D fp32 map over (inner, outer, batch) with the given box.
+bool make_map(CUtensorMap* m, const float* base, long long inner, long long outer, long long ld, int batches,
+              long long bstride, uint32_t box_inner, uint32_t box_outer) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)outer, (cuuint64_t)std::max(1, batches)};
+  cuuint64_t strides[2] = {(cuuint64_t)ld * 4, (cuuint64_t)std::max<long long>(bstride, 1) * 4};
+  if (batches <= 1) strides[1] = (cuuint64_t)ld * 4 * (cuuint64_t)std::max<long long>(outer, 1);
+  cuuint32_t box[3] = {box_inner, box_outer, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace tc
+
+// Operand extents: A is M x K (K-major: rows M of k; MN-major: rows K of m), B is K x N.
+// Falls back to the FFMA GEMM when an operand cannot be described to TMA (16-byte
+// alignment of bases and strides).
+gptq_status tc_gemm(const simt::GemmArgs& g, int batches, bool a_kmaj, bool b_kmaj, cudaStream_t s) {
+  using namespace tc;
+  if (g.M <= 0 || g.N <= 0 || batches <= 0) return GPTQ_OK;
+  static const bool force_ffma = [] {
+    const char* v = getenv("GPTQ_FFMA_GEMM");
+    return v && v[0] == '1';
+  }();
+  if (force_ffma) return simt::gemm(g, batches, a_kmaj, b_kmaj, s);
+  if (batches > 1 && (g.M_last != g.M || g.K_last != g.K)) {
+    // a ragged last batch gets its own launch with exact extents, so no tensor map
+    // describes memory past the end of an operand
+    simt::GemmArgs full = g;
+    full.M_last = g.M;
+    full.K_last = g.K;
+    if (gptq_status st = tc_gemm(full, batches - 1, a_kmaj, b_kmaj, s)) return st;
+    simt::GemmArgs last = g;
+    last.A = g.A + (long long)(batches - 1) * g.a_bs;
+    last.B = g.B + (long long)(batches - 1) * g.b_bs;
+    last.C = g.C + (long long)(batches - 1) * g.c_bs;
+    last.M = last.M_last = g.M_last;
+    last.K = last.K_last = g.K_last;
+    return tc_gemm(last, 1, a_kmaj, b_kmaj, s);
+  }
+  const bool aligned = g.vec && simt::aligned16(g.A) && simt::aligned16(g.B) && simt::aligned16(g.C) &&
+                       (g.lda % 4 == 0) && (g.ldb % 4 == 0) && (g.ldc % 4 == 0) && (g.a_bs % 4 == 0) &&
+                       (g.b_bs % 4 == 0) && (g.c_bs % 4 == 0);
+  // tcgen05 kind::tf32 reads K-major operands only (an MN-major tf32 operand yields
+  // zeros), so other layouts and unaligned operands take the FFMA GEMM
+  if (!aligned || !a_kmaj || !b_kmaj) return simt::gemm(g, batches, a_kmaj, b_kmaj, s);
+  CUtensorMap ma, mb;
+  // logical extents cover every batch (the last batch can only be smaller)
+  bool ok;
+  if (a_kmaj) ok = make_map(&ma, g.A, g.K, g.M, g.lda, batches, g.a_bs, BK, BM);
+  else ok = make_map(&ma, g.A, g.M, g.K, g.lda, batches, g.a_bs, 32, BK);
+  if (ok) {
+    if (b_kmaj) ok = make_map(&mb, g.B, g.K, g.N, g.ldb, batches, g.b_bs, BK, BN);
+    else ok = make_map(&mb, g.B, g.N, g.K, g.ldb, batches, g.b_bs, 32, BK);
+  }
+  if (!ok) return simt::gemm(g, batches, a_kmaj, b_kmaj, s);
+
+  Params p{};
+  p.M = g.M; p.N = g.N; p.K = g.K; p.M_last = g.M_last; p.K_last = g.K_last; p.batches = batches;
+  p.mt = (g.M + BM - 1) / BM;
+  p.nt = (g.N + BN - 1) / BN;
+  p.tiles_per_batch = g.lower_tiles ? p.mt * (p.mt + 1) / 2 : p.mt * p.nt;
+  p.lower_tiles = g.lower_tiles; p.a_lower = g.a_lower; p.b_lower = g.b_lower;
+  p.alpha = g.alpha; p.beta = g.beta;
+  p.C = g.C; p.ldc = g.ldc; p.c_bs = g.c_bs;
+  p.skip = g.skip;
+  const int ntiles = p.tiles_per_batch * batches;
+  const int grid = std::min(ntiles, sm_count());
+
+  auto launch = [&](auto kern) -> gptq_status {
+    static bool attr_done[4] = {false, false, false, false};
+    const int key = (a_kmaj ? 2 : 0) + (b_kmaj ? 1 : 0);
+    if (!attr_done[key]) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
+        return set_error(GPTQ_ERR_CUDA, "cudaFuncSetAttribute(tc_gemm_kernel) failed");
+      attr_done[key] = true;
+    }
+    kern<<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, p, device_error_word());
+    count_launch();
+    return check_launch("tc_gemm_kernel");
+  };
+  return launch(tc_gemm_kernel<true, true>);
+}
+
+}  // namespace gptq

@@ -48,6 +48,8 @@ SIGNATURES = {
     "gptq_quantize_layer": (_c_int, [_vp, _c_int, _c_i64, _c_i64, _c_i64, _vp, _vp, _c_int, _c_int, _c_int, _vp, _vp,
                                      _vp, _vp, _vp, _c_size, ctypes.POINTER(_c_i64), _vp]),
     "gptq_unpack_codes": (_c_int, [_vp, _c_i64, _c_i64, _c_int, _vp, _vp]),
+    "gptq_gemm_f32": (_c_int, [_c_int, _c_int, _c_int, _c_i64, _c_i64, _c_i64, _vp, _c_i64, _vp, _c_i64, _vp, _c_i64,
+                               _c_float, _c_float, _c_int, _vp]),
 }
 
 
@@ -246,6 +248,25 @@ def gptq_unpack_codes(qweight: torch.Tensor, m: int, d: int, bits: int, stream=N
     codes = torch.empty((m, d), dtype=torch.uint8, device=qweight.device)
     _check(_lib.gptq_unpack_codes(_ptr(qweight), m, d, bits, _ptr(codes), _stream(stream)), "gptq_unpack_codes")
     return codes
+
+
+def gptq_gemm_f32(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, a_kmajor: bool, b_kmajor: bool,
+                  alpha: float = 1.0, beta: float = 0.0, engine: int = 0, lower_tiles: bool = False,
+                  stream=None) -> torch.Tensor:
+    """C = beta C + alpha A B with the library's block-update GEMM (test helper).
+
+    a_kmajor: A is stored (M, K) row-major, else (K, M); b_kmajor: B is stored (N, K),
+    else (K, N). C is (M, N)."""
+    for t, nm in ((A, "A"), (B, "B"), (C, "C")):
+        _need_cuda(t, nm, (torch.float32,))
+        if t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError(f"{nm} must be 2-D with unit column stride")
+    M, N = C.shape
+    K = A.shape[1] if a_kmajor else A.shape[0]
+    _check(_lib.gptq_gemm_f32(engine, int(a_kmajor), int(b_kmajor), M, N, K, _ptr(A), A.stride(0), _ptr(B),
+                              B.stride(0), _ptr(C), C.stride(0), float(alpha), float(beta), int(lower_tiles),
+                              _stream(stream)), "gptq_gemm_f32")
+    return C
 
 
 # ----------------------------------------------------------------------------------
