@@ -13,13 +13,13 @@
 //
 // Kernels:
 //   prep_kernel        fp32 working copy of W in processing order; NaN/Inf check
-//   colblock_kernel<BS> eight lanes per row (4 rows per warp, 32 per CTA), the block as
-//                      32-column register sub-blocks (the block's later columns wait
-//                      in shared memory), the Hinv1 diagonal block in shared memory,
-//                      group min/max by shuffles; codes are packed into the
-//                      output bitstream as they are produced; Err1 is written
-//                      row-major for the lazy update; per-column loss partial
-//                      sums of each CTA's 32 rows in a fixed order
+//   rowstats_kernel    per-channel mode: scale and zero of every row from W before any update
+//   diag_info_kernel   per column: Hinv1[j][j], RN(1 / Hinv1[j][j]) and Hinv1[j][j+1]
+//   colblock_kernel<BS> eight lanes per row (4 rows per warp, 32 per CTA); the whole
+//                      block of each row in registers; Hinv1's diagonal block by bulk
+//                      asynchronous copies; group min/max by shuffles; Err1, codes and
+//                      per-column loss partials (the CTA's 32 rows in a fixed order)
+//                      leave from shared memory at the end of the block
 //   transpose_kernel   Ut = Hinv1^T once per call
 //   tc_gemm            lazy update W[:, i2:] -= Err1 @ Hinv1[i1:i2, i2:] on the tensor cores
 //                      (3 x TF32, both operands K-major: Err1 rows, Ut rows)
@@ -92,178 +92,338 @@ __device__ __forceinline__ float rcp_rn(float s) {
   return __double2float_rn(y);
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
+// Scale, its reciprocal and zero of one group from the group's min and max: the
+// quantizer range of "GPTQ-style round-to-nearest with Hessian weighting", in float32
+// with correctly rounded quotients.
+__device__ __forceinline__ void group_params(float mn, float mx, float qmax, float inv_qmax, float& s, float& inv_s,
+                                             float& z) {
+  s = fmaxf(div_mk(__fsub_rn(mx, mn), qmax, inv_qmax), 1e-8f);
+  inv_s = rcp_rn(s);
+  z = fminf(fmaxf(rintf(div_mk(-mn, s, inv_s)), 0.0f), qmax);
 }
 
-// Column block, LANES lanes per row.
+// Per-channel quantization (one group per row): statistics of W before any update,
+// one warp per row.
+__global__ void rowstats_kernel(const float* __restrict__ Wf, int m, int d, int bits, float* __restrict__ scales,
+                                float* __restrict__ zeros) {
+  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (r >= m) return;
+  const float* row = Wf + (long long)r * d;
+  float mn = INFINITY, mx = -INFINITY;
+  for (int c = lane; c < d; c += 32) {
+    const float v = row[c];
+    mn = fminf(mn, v);
+    mx = fmaxf(mx, v);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  if (lane == 0) {
+    const float qmax = (float)((1 << bits) - 1);
+    float s, inv_s, z;
+    group_params(mn, mx, qmax, rcp_rn(qmax), s, inv_s, z);
+    scales[r] = s;
+    zeros[r] = z;
+  }
+}
+
+// Per column j: {Hinv1[j][j], RN(1 / Hinv1[j][j]), Hinv1[j][j+1], 0}
+__global__ void diag_info_kernel(const float* __restrict__ U, int d, float4* __restrict__ dinfo) {
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= d) return;
+  const float u = U[(long long)j * d + j];
+  dinfo[j] = make_float4(u, rcp_rn(u), (j + 1 < d) ? U[(long long)j * d + j + 1] : 0.0f, 0.0f);
+}
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+// ---------------------------------------------------------------------------------
+// Column block. Four lanes per row, eight rows per warp, four warps (32 rows) per CTA.
 //
-// A warp holds 32 / LANES rows; the LANES lanes of a row own the block's columns
-// c = LANES k + q round-robin (q = lane % LANES). At each column the owner broadcasts
-// the current weight with one shuffle and all lanes of the row quantize it
-// identically, then each lane applies the rank-one update to its own later columns.
-// Within a 32-column sub-block the lane's columns sit in registers and are rotated by
-// one slot every LANES columns, so the column about to be quantized is always slot 0
-// of its owner and the loop body stays a few hundred instructions long. When a sub-block is done, its 32
-// errors update the block's later columns (kept in shared memory) column by column in
-// the same order, so the rounding is that of updating every column after every step.
+// The block's weights stay in registers for the whole block: lane q of a row holds
+// columns 16 k + 4 q + j (slot 4 k + j). Columns are visited in 16-column steps; after
+// each step the slots move down by four, so the step's columns are always slots 0..3
+// and the loop body is the same for every step. Steps come in pairs, and every pair
+// drops the four slots that no longer hold a live column (triangular work).
+//
+// At column t all four lanes of a row hold its current value x and quantize it
+// identically; every lane then moves all its slots by -Err1 * Hinv1[t][col]
+// (multiply, then subtract: the listing's float32 rounding). The value of column t+1
+// is fetched from its owner by a shuffle BEFORE that update and updated locally with
+// the same two operations, so the shuffle is off the dependent chain of a column.
+//
+// Hinv1's diagonal block arrives by bulk asynchronous copies of each row's upper part,
+// one mbarrier per 16-row step. Errors and codes collect in shared memory and leave at
+// the end: Err1 row-major for the lazy update, codes packed into the output bitstream
+// (or as bytes for act-order), per-column loss sums over the CTA's rows in a fixed
+// order.
 constexpr int LANES = 8;                             // lanes per row
 constexpr int ROWS_PER_WARP = 32 / LANES;            // 4
-constexpr int WARPS_PER_CTA = ROWS_PER_CTA / ROWS_PER_WARP;   // 8
-constexpr int CB_THREADS = WARPS_PER_CTA * 32;      // 256
-constexpr int SUB = 32;                              // columns per register sub-block
-constexpr int SLOTS = SUB / LANES;                   // 4 registers per lane
-constexpr int ELD = SUB + 1;                         // padded row stride of the error tile
+constexpr int CB_WARPS = ROWS_PER_CTA / ROWS_PER_WARP;   // 8
+constexpr int CB_THREADS = CB_WARPS * 32;           // 256
+constexpr int KW = 4 * LANES;                        // columns per step
 
 template <int BS>
-__global__ void __launch_bounds__(CB_THREADS)
-colblock_kernel(const float* __restrict__ Wf, int m, int d, const float* __restrict__ U, int i1, int bits, int g,
-                uint32_t* __restrict__ qweight, int wpr, uint8_t* __restrict__ codes8, float* __restrict__ scales,
-                float* __restrict__ zeros, int G, float* __restrict__ err, float* __restrict__ part) {
-  extern __shared__ __align__(16) float smem[];
-  float* Us = smem;                                  // BS x BS: Us[t * BS + u] = Hinv1[i1 + t][i1 + u]
-  float* inv_u = Us + BS * BS;                       // RN(1 / Hinv1[j][j])
-  float* Wsm = inv_u + BS;                           // ROWS_PER_CTA x (BS + 1): the block's weights
-  float* Es = Wsm + ROWS_PER_CTA * (BS + 1);         // ROWS_PER_CTA x ELD: the sub-block's errors
-  constexpr int WLD = BS + 1;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int q = lane % LANES;                        // position within the row's lanes
-  const int qbase = lane - q;                        // lane owning the row's column 0
-  const int row = warp * ROWS_PER_WARP + lane / LANES;  // row within the CTA
-  const int r0 = blockIdx.x * ROWS_PER_CTA;
-  const int r = r0 + row;
-  const bool active = r < m;
-  const int ncols = min(BS, d - i1);
+struct CBSmem {
+  static constexpr int ELD = BS + 1;                 // padded row of the error tile
+  static constexpr int CLD = BS + 4;                 // padded row of the code tile (bytes)
+  static constexpr size_t us = 0;
+  static constexpr size_t dinfo = us + sizeof(float) * BS * BS;
+  static constexpr size_t es = dinfo + sizeof(float4) * BS;
+  static constexpr size_t cs = es + sizeof(float) * ROWS_PER_CTA * ELD;
+  static constexpr size_t bars = (cs + ROWS_PER_CTA * CLD + 15) & ~(size_t)15;
+  static constexpr size_t flag = bars + sizeof(uint64_t) * (BS / KW);
+  static constexpr size_t total = flag + 16;
+};
 
-  // the Hinv1 block (only its upper triangle is ever read) and the CTA's rows of W
-  load_tile<CB_THREADS, BS, BS>(Us, BS, U + (long long)i1 * d + i1, d, ncols, ncols);
-  load_tile<CB_THREADS, ROWS_PER_CTA, BS>(Wsm, WLD, Wf + (long long)r0 * d + i1, d, min(ROWS_PER_CTA, m - r0), ncols);
-  __syncthreads();
-  for (int t = tid; t < BS; t += CB_THREADS) inv_u[t] = (t < ncols) ? __frcp_rn(Us[t * BS + t]) : 0.0f;
-  __syncthreads();
+struct CBArgs {
+  const float* Wf;
+  int m, d;
+  const float* U;
+  const float4* dinfo;        // {U[j][j], RN(1 / U[j][j]), U[j][j+1], 0}
+  int i1, bits, g;
+  int stats_given;            // scale/zero of every group precomputed (per-channel)
+  uint32_t* qweight;
+  int wpr;
+  uint8_t* codes8;            // non-null: act-order, codes as bytes in processing order
+  float* scales;
+  float* zeros;
+  int G;
+  float* err;                 // mpad x BS
+  float* part;                // loss partials, one row of d per CTA
+  int bulk;                   // U rows 16-byte aligned: bulk asynchronous copies
+  int vecw;                   // Wf rows 16-byte aligned: vector loads
+  int* err_word;
+};
 
-  float* wsm = Wsm + row * WLD;
-  float* es = Es + row * ELD;
-  const float* wrow = Wf + (long long)(active ? r : 0) * d;
-  const float qmax = (float)((1 << bits) - 1);
-  const float inv_qmax = __frcp_rn(qmax);
-  float s = 1.0f, z = 0.0f;
-  if ((i1 % g) != 0 && active) {   // the block continues a group that began in an earlier block
-    s = scales[(long long)r * G + i1 / g];
-    z = zeros[(long long)r * G + i1 / g];
-  }
-  float inv_s = rcp_rn(s);
-  const bool natural = (codes8 == nullptr);
-  const bool packer = natural && q == 0 && active;
-  uint64_t acc = 0;
-  int nacc = 0;
-  int widx = (int)(((long long)i1 * bits) >> 5);
-
+template <int NSA, int BS>
+__device__ __forceinline__ void cb_step(float (&w)[BS / LANES], float& x, int k, int q, int qbase, int row, float s,
+                                        float inv_s, float z, float qmax, const float* __restrict__ Us,
+                                        const float4* __restrict__ dinfo, float* __restrict__ Es,
+                                        uint8_t* __restrict__ Cs) {
+  constexpr int ELD = CBSmem<BS>::ELD, CLD = CBSmem<BS>::CLD;
+  // Branch-free column bodies, so the scheduler can overlap one column's updates with
+  // the next column's shuffle, loads and quantization. Columns past the end of a ragged
+  // block, and rows past m, run on dead values whose stores are never read back; their
+  // reads stay inside the shared allocation (a row of Us is followed by the next row or
+  // by dinfo).
 #pragma unroll 1
-  for (int c0 = 0; c0 < ncols; c0 += SUB) {
-    const int nsub = min(SUB, ncols - c0);
-    float w[SLOTS];
+  for (int i = 0; i < LANES; ++i) {
 #pragma unroll
-    for (int k = 0; k < SLOTS; ++k) w[k] = wsm[c0 + LANES * k + q];   // column c0 + LANES k + q (zero-padded)
+    for (int j = 0; j < 4; ++j) {
+      const int t = KW * k + 4 * i + j;
+      // the next column before this column's update, from its owner
+      float nsrc;
+      if (j < 3) nsrc = w[j + 1];
+      else if constexpr (NSA > 4) nsrc = (i < LANES - 1) ? w[0] : w[4];
+      else nsrc = w[0];
+      const int nowner = qbase + ((j < 3) ? i : ((i + 1) & (LANES - 1)));
+      const float xn_pre = __shfl_sync(0xffffffffu, nsrc, nowner);
+      const float* urow = Us + t * BS;
+      const float4 di = dinfo[t];                            // U[t][t], 1 / U[t][t], U[t][t+1]
+      // quantize, dequantize, error
+      const float qv = fminf(fmaxf(rintf(__fadd_rn(div_mk(x, s, inv_s), z)), 0.0f), qmax);
+      const float wq = __fmul_rn(__fsub_rn(qv, z), s);
+      const float e = div_mk(__fsub_rn(x, wq), di.x, di.y);
+      Es[row * ELD + t] = e;                                 // the row's lanes store the same value
+      Cs[row * CLD + t] = (uint8_t)(int)qv;
+      // move every slot by -e * U[t][col]; slots at or before t are dead and ignored
+      const float* ucol = urow + KW * k + 4 * q;
+#pragma unroll
+      for (int kk = 0; kk < NSA / 4; ++kk) {
+        const float4 u4 = *reinterpret_cast<const float4*>(ucol + KW * kk);
+        w[4 * kk + 0] = __fsub_rn(w[4 * kk + 0], __fmul_rn(e, u4.x));
+        w[4 * kk + 1] = __fsub_rn(w[4 * kk + 1], __fmul_rn(e, u4.y));
+        w[4 * kk + 2] = __fsub_rn(w[4 * kk + 2], __fmul_rn(e, u4.z));
+        w[4 * kk + 3] = __fsub_rn(w[4 * kk + 3], __fmul_rn(e, u4.w));
+      }
+      x = __fsub_rn(xn_pre, __fmul_rn(e, di.z));
+    }
+  }
+  // the step is done: its slots retire, the rest move down
+#pragma unroll
+  for (int sl = 0; sl < NSA - 4; ++sl) w[sl] = w[sl + 4];
+}
 
-    const int j0 = i1 + c0;
-    if ((j0 % g) == 0) {
-      // group statistics over the current weights of columns [j0, j0 + g), each lane over
-      // its own columns, then combined across the row's lanes
-      float mn = INFINITY, mx = -INFINITY;
-#pragma unroll
-      for (int k = 0; k < SLOTS; ++k) {
-        const int c = LANES * k + q;
-        if (c < nsub && c < g) { mn = fminf(mn, w[k]); mx = fmaxf(mx, w[k]); }
+template <int NS, class F, int... P>
+__device__ __forceinline__ void for_phases(F&& f, std::integer_sequence<int, P...>) {
+  (f(std::integral_constant<int, NS - 8 * P>{}, 2 * P), ...);
+}
+
+template <int BS>
+__global__ void __launch_bounds__(CB_THREADS, 1) colblock_kernel(CBArgs a) {
+  constexpr int NS = BS / LANES;                     // slots per lane
+  constexpr int KS = BS / KW;                        // steps
+  using SL = CBSmem<BS>;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  float* Us = reinterpret_cast<float*>(smem_raw + SL::us);      // Us[t * BS + c] = Hinv1[i1 + t][i1 + c], c >= t
+  float4* dinfo = reinterpret_cast<float4*>(smem_raw + SL::dinfo);
+  float* Es = reinterpret_cast<float*>(smem_raw + SL::es);
+  uint8_t* Cs = smem_raw + SL::cs;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + SL::bars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + SL::flag);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q = lane & (LANES - 1), qbase = lane - q;
+  const int row = warp * ROWS_PER_WARP + lane / LANES;
+  const int r0 = blockIdx.x * ROWS_PER_CTA, r = r0 + row;
+  const bool active = r < a.m;
+  const int d = a.d, i1 = a.i1;
+  const int ncols = min(BS, d - i1);
+  const int nks = (ncols + KW - 1) / KW;
+
+  // ---- Hinv1's diagonal block: row t from column (t & ~3) on
+  if (tid == 0) {
+    *abort_flag = 0;
+    if (a.bulk) {
+      for (int k = 0; k < KS; ++k) mbar_init(&bars[k], 1);
+      fence_mbar_init();
+    }
+  }
+  __syncthreads();
+  if (a.bulk) {
+    if (warp == 0) {
+      if (lane < nks) {
+        uint32_t bytes = 0;
+        for (int t = KW * lane; t < min(KW * lane + KW, ncols); ++t) bytes += (uint32_t)(ncols - (t & ~3)) * 4u;
+        mbar_arrive_expect_tx(&bars[lane], bytes);
       }
-      for (int c = c0 + SUB + q; c < ncols && c - c0 < g; c += LANES) {
-        const float v = wsm[c];
-        mn = fminf(mn, v);
-        mx = fmaxf(mx, v);
-      }
-      for (int c = i1 + ncols + q; c < j0 + g && c < d; c += LANES) {
-        const float v = wrow[c];
-        mn = fminf(mn, v);
-        mx = fmaxf(mx, v);
-      }
-#pragma unroll
-      for (int o = 1; o < LANES; o <<= 1) {
-        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      }
-      s = fmaxf(div_mk(__fsub_rn(mx, mn), qmax, inv_qmax), 1e-8f);
-      inv_s = rcp_rn(s);
-      z = fminf(fmaxf(rintf(div_mk(-mn, s, inv_s)), 0.0f), qmax);
-      if (active && q == 0) {
-        scales[(long long)r * G + j0 / g] = s;
-        zeros[(long long)r * G + j0 / g] = z;
+      __syncwarp();
+      for (int t = lane; t < ncols; t += 32) {
+        const int c0 = t & ~3;
+        bulk_load(Us + t * BS + c0, a.U + (long long)(i1 + t) * d + i1 + c0, (uint32_t)(ncols - c0) * 4u,
+                  &bars[t / KW]);
       }
     }
+  } else {
+    load_tile<CB_THREADS, BS, BS>(Us, BS, a.U + (long long)i1 * d + i1, d, ncols, ncols);
+  }
+  for (int t = tid; t < BS; t += CB_THREADS) dinfo[t] = (t < ncols) ? a.dinfo[i1 + t] : make_float4(1.f, 1.f, 0.f, 0.f);
 
+  // ---- the row's block of W into registers: slot 4k + j <- column 16k + 4q + j
+  float w[NS];
+  {
+    const float* wrow = a.Wf + (long long)(active ? r : 0) * d + i1;
+#pragma unroll
+    for (int k = 0; k < KS; ++k) {
+      const int c = KW * k + 4 * q;
+      if (a.vecw && active && c < ncols) {
+        const float4 v = *reinterpret_cast<const float4*>(wrow + c);
+        w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) w[4 * k + j] = (active && c + j < ncols) ? wrow[c + j] : 0.0f;
+      }
+    }
+  }
+
+  const float qmax = (float)((1 << a.bits) - 1);
+  const float inv_qmax = rcp_rn(qmax);
+  float s = 1.0f, inv_s = 1.0f, z = 0.0f;
+  if (active && (a.stats_given || (i1 % a.g) != 0)) {   // statistics from an earlier block or precomputed
+    s = a.scales[(long long)r * a.G + i1 / a.g];
+    z = a.zeros[(long long)r * a.G + i1 / a.g];
+    inv_s = rcp_rn(s);
+  }
+  __syncthreads();                                    // dinfo (and the fallback tile) visible
+
+  float x = __shfl_sync(0xffffffffu, w[0], qbase);    // column 0 (slot 0 of lane 0)
+
+  // One phase: two 16-column steps with NSA live slots per lane (inlined once per
+  // phase; the two steps share the code).
+  auto phase = [&](auto nsa_c, int kbeg) {
+    constexpr int NSA = decltype(nsa_c)::value;
 #pragma unroll 1
-    for (int cb = c0; cb < c0 + nsub; cb += LANES) {   // LANES columns per iteration
-#pragma unroll
-      for (int i = 0; i < LANES; ++i) {
-        const int t = cb + i;
-        if (t < ncols) {                                 // warp-uniform
-          const float x = __shfl_sync(0xffffffffu, w[0], qbase + i);
-          const float qv = fminf(fmaxf(rintf(__fadd_rn(div_mk(x, s, inv_s), z)), 0.0f), qmax);
-          const float wq = __fmul_rn(__fsub_rn(qv, z), s);
-          const float e = active ? div_mk(__fsub_rn(x, wq), Us[t * BS + t], inv_u[t]) : 0.0f;
-          if (q == 0) {
-            es[t - c0] = e;
-            err[(long long)(r0 + row) * BS + t] = e;
-          }
-          const uint32_t qi = (uint32_t)qv;
-          if (packer) {
-            acc |= (uint64_t)qi << nacc;
-            nacc += bits;
-            if (nacc >= 32) {
-              qweight[(long long)r * wpr + widx] = (uint32_t)acc;
-              ++widx;
-              acc >>= 32;
-              nacc -= 32;
-            }
-          } else if (!natural && q == 0 && active) {
-            codes8[(long long)r * d + i1 + t] = (uint8_t)qi;
-          }
-          // rank-one update of the lane's later columns of the sub-block: slot k holds
-          // column cb + LANES k + q, later than t unless k == 0 and q <= i
-          const float* urow = Us + t * BS + cb + q;
-#pragma unroll
-          for (int k = 0; k < SLOTS; ++k)
-            if (k > 0 || q > i) w[k] = __fsub_rn(w[k], __fmul_rn(e, urow[LANES * k]));
+    for (int k = kbeg; k < kbeg + 2 && k < nks; ++k) {
+      if (a.bulk) {
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[k], 0, abort_flag));
+        if (!ok && lane == 0) {
+          *abort_flag = 1;
+          report_device_error(a.err_word, DEVERR_TIMEOUT);
         }
       }
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) return;
+      const int j0 = i1 + KW * k;
+      if (!a.stats_given && (j0 % a.g) == 0) {
+        // the group's current weights: this lane's live slots, then columns beyond the block
+        float mn = INFINITY, mx = -INFINITY;
 #pragma unroll
-      for (int k = 0; k < SLOTS - 1; ++k) w[k] = w[k + 1];
-      w[SLOTS - 1] = 0.0f;
-    }
-    __syncwarp();
-    // the sub-block's errors move the block's later columns (this lane's share), in order
-#pragma unroll 1
-    for (int c = c0 + SUB + q; c < ncols; c += LANES) {
-      float x = wsm[c];
+        for (int sl = 0; sl < NSA; ++sl) {
+          const int c = KW * (k + sl / 4) + 4 * q + (sl & 3);
+          if (c < ncols && c - KW * k < a.g) { mn = fminf(mn, w[sl]); mx = fmaxf(mx, w[sl]); }
+        }
+        const float* wrow = a.Wf + (long long)(active ? r : 0) * d;
+        for (int c = i1 + ncols + q; c < j0 + a.g && c < d; c += LANES) {
+          const float v = wrow[c];
+          mn = fminf(mn, v);
+          mx = fmaxf(mx, v);
+        }
 #pragma unroll
-      for (int u = 0; u < SUB; ++u)
-        if (u < nsub) x = __fsub_rn(x, __fmul_rn(es[u], Us[(c0 + u) * BS + c]));
-      wsm[c] = x;
-    }
-    __syncthreads();
-    // per-column loss partial sums of the CTA's 32 rows, in a fixed order
-    if (tid < nsub) {
-      float lsum = 0.0f;
-      for (int rr = 0; rr < ROWS_PER_CTA; ++rr) {
-        const float e = Es[rr * ELD + tid];
-        lsum = __fadd_rn(lsum, __fmul_rn(__fmul_rn(e, e), 0.5f));
+        for (int o = 1; o < LANES; o <<= 1) {
+          mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        }
+        group_params(mn, mx, qmax, inv_qmax, s, inv_s, z);
+        if (active && q == 0) {
+          a.scales[(long long)r * a.G + j0 / a.g] = s;
+          a.zeros[(long long)r * a.G + j0 / a.g] = z;
+        }
       }
-      part[(long long)blockIdx.x * d + i1 + c0 + tid] = lsum;
+      cb_step<NSA, BS>(w, x, k, q, qbase, row, s, inv_s, z, qmax, Us, dinfo, Es, Cs);
     }
-    __syncthreads();
+  };
+  // each phase runs with the slots that can still hold a live column
+  for_phases<NS>(phase, std::make_integer_sequence<int, (KS + 1) / 2>{});
+
+  __syncthreads();
+  if (*abort_flag) return;
+
+  // ---- Err1 out (row-major, BS per row), loss partials, codes
+  constexpr int ELD = SL::ELD, CLD = SL::CLD;
+  for (int idx = tid; idx < ROWS_PER_CTA * BS; idx += CB_THREADS) {
+    const int rr = idx / BS, t = idx % BS;
+    if (t < ncols && r0 + rr < a.m) a.err[(long long)(r0 + rr) * BS + t] = Es[rr * ELD + t];
   }
-  if (packer && nacc > 0) qweight[(long long)r * wpr + widx] = (uint32_t)acc;
+  for (int t = tid; t < ncols; t += CB_THREADS) {
+    float lsum = 0.0f;
+    for (int rr = 0; rr < ROWS_PER_CTA; ++rr) {
+      const float e = (r0 + rr < a.m) ? Es[rr * ELD + t] : 0.0f;
+      lsum = __fadd_rn(lsum, __fmul_rn(__fmul_rn(e, e), 0.5f));
+    }
+    a.part[(long long)blockIdx.x * d + i1 + t] = lsum;
+  }
+  if (a.codes8) {
+    for (int idx = tid; idx < ROWS_PER_CTA * BS; idx += CB_THREADS) {
+      const int rr = idx / BS, t = idx % BS;
+      if (t < ncols && r0 + rr < a.m) a.codes8[(long long)(r0 + rr) * d + i1 + t] = Cs[rr * CLD + t];
+    }
+  } else {
+    // words [i1 b / 32, ceil((i1 + ncols) b / 32)) of each row; i1 b is a multiple of 32
+    const int bits = a.bits;
+    const int wb = (int)(((long long)i1 * bits) >> 5);
+    const int we = (int)(((long long)(i1 + ncols) * bits + 31) >> 5);
+    const int nw = we - wb;
+    for (int idx = tid; idx < ROWS_PER_CTA * nw; idx += CB_THREADS) {
+      const int rr = idx / nw, wi = wb + idx % nw;
+      if (r0 + rr >= a.m) continue;
+      const long long b0 = (long long)wi * 32;
+      const int jf = (int)(b0 / bits);
+      const int jl = min(i1 + ncols - 1, (int)((b0 + 31) / bits));
+      uint64_t v = 0;
+      for (int j = jf; j <= jl; ++j) {
+        const uint64_t code = Cs[rr * CLD + (j - i1)];
+        const long long sh = (long long)j * bits - b0;
+        v |= (sh >= 0) ? (code << sh) : (code >> (-sh));
+      }
+      a.qweight[(long long)(r0 + rr) * a.wpr + wi] = (uint32_t)v;
+    }
+  }
 }
 
 __global__ void loss_finalize_kernel(const float* __restrict__ part, int nrg, int d, const int* __restrict__ perm,
@@ -326,7 +486,7 @@ __global__ void transpose_kernel(const float* __restrict__ U, float* __restrict_
 }
 
 struct Layout {
-  size_t hdr, wf, err, ut, part, codes8, inv, total;
+  size_t hdr, wf, err, ut, part, codes8, inv, dinfo, total;
   int nrg;
 };
 
@@ -342,28 +502,25 @@ Layout layout(long long m, long long d, int blocksize) {
   L.part = L.ut + al((size_t)d * d * 4);
   L.codes8 = L.part + al((size_t)L.nrg * d * 4);
   L.inv = L.codes8 + al((size_t)m * d);
-  L.total = L.inv + al((size_t)d * 4);
+  L.dinfo = L.inv + al((size_t)d * 4);
+  L.total = L.dinfo + al((size_t)d * 16);
   return L;
 }
 
 template <int BS>
-gptq_status run_blocks(float* Wf, int m, int d, const float* U, const float* Ut, int bits, int g, uint32_t* qweight,
-                       int wpr, uint8_t* codes8, float* scales, float* zeros, int G, float* err, float* part,
-                       cudaStream_t s) {
-  const size_t smem = (size_t)(BS * BS + BS + ROWS_PER_CTA * (BS + 1) + ROWS_PER_CTA * ELD) * sizeof(float);
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(colblock_kernel<BS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-      return set_error(GPTQ_ERR_CUDA, "cudaFuncSetAttribute(colblock_kernel) failed");
-    attr = true;
-  }
+gptq_status run_blocks(CBArgs a, const float* Ut, cudaStream_t s) {
+  using SL = CBSmem<BS>;
+  if (cudaFuncSetAttribute(colblock_kernel<BS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SL::total) !=
+      cudaSuccess)
+    return set_error(GPTQ_ERR_CUDA, "cudaFuncSetAttribute(colblock_kernel) failed");
+  const int m = a.m, d = a.d;
   const int nrg = (m + ROWS_PER_CTA - 1) / ROWS_PER_CTA;
   for (int i1 = 0; i1 < d; i1 += BS) {
     const int nb = std::min(BS, d - i1);
+    a.i1 = i1;
     {
       ProfScope ps("quantize.colblock", s);
-      colblock_kernel<BS><<<nrg, CB_THREADS, smem, s>>>(Wf, m, d, U, i1, bits, g, qweight, wpr, codes8, scales,
-                                                          zeros, G, err, part);
+      colblock_kernel<BS><<<nrg, CB_THREADS, SL::total, s>>>(a);
       count_launch();
     }
     const int i2 = i1 + nb;
@@ -371,11 +528,11 @@ gptq_status run_blocks(float* Wf, int m, int d, const float* U, const float* Ut,
       // W[:, i2:] -= Err1 @ Hinv1[i1:i2, i2:];  A = Err1 (rows of BS), B(k, j) = Ut[i2 + j][i1 + k]
       simt::GemmArgs ga{};
       ga.M = m; ga.N = d - i2; ga.K = nb; ga.M_last = m; ga.K_last = nb;
-      ga.A = err; ga.lda = BS;
+      ga.A = a.err; ga.lda = BS;
       ga.B = Ut + (long long)i2 * d + i1; ga.ldb = d;
-      ga.C = Wf + i2; ga.ldc = d;
+      ga.C = const_cast<float*>(a.Wf) + i2; ga.ldc = d;
       ga.alpha = -1.0f; ga.beta = 1.0f;
-      ga.vec = (d % 4 == 0) && simt::aligned16(Wf) && simt::aligned16(Ut) && simt::aligned16(err);
+      ga.vec = (d % 4 == 0) && simt::aligned16(a.Wf) && simt::aligned16(Ut) && simt::aligned16(a.err);
       ProfScope ps2("quantize.lazy_gemm", s);
       if (gptq_status st = tc_gemm(ga, 1, true, true, s)) return st;
     }
@@ -403,6 +560,7 @@ gptq_status quantize_launch(const void* W, int w_dtype, long long m_, long long 
   float* part = reinterpret_cast<float*>(base + L.part);
   uint8_t* codes8 = perm ? base + L.codes8 : nullptr;
   int* inv = reinterpret_cast<int*>(base + L.inv);
+  float4* dinfo = reinterpret_cast<float4*>(base + L.dinfo);
   const int g = (group_size < 0) ? d : group_size;
   const int G = d / g;
   const int wpr = (int)(((long long)d * bits + 31) / 32);
@@ -415,13 +573,27 @@ gptq_status quantize_launch(const void* W, int w_dtype, long long m_, long long 
     prep_kernel<<<grid, 256, 0, s>>>(W, w_dtype, m, d, ldw, perm, Wf, hdr);
     dim3 tg((unsigned)((d + 31) / 32), (unsigned)((d + 31) / 32));
     transpose_kernel<<<tg, dim3(32, 8), 0, s>>>(Hinv1, Ut, d);
-    count_launch(2);
+    diag_info_kernel<<<(d + 255) / 256, 256, 0, s>>>(Hinv1, d, dinfo);
+    count_launch(3);
+    if (group_size < 0) {
+      rowstats_kernel<<<(m + 7) / 8, 256, 0, s>>>(Wf, m, d, bits, scales, zeros);
+      count_launch();
+    }
   }
+  CBArgs a{};
+  a.Wf = Wf; a.m = m; a.d = d; a.U = Hinv1; a.dinfo = dinfo;
+  a.bits = bits; a.g = g; a.stats_given = group_size < 0;
+  a.qweight = qweight; a.wpr = wpr; a.codes8 = codes8;
+  a.scales = scales; a.zeros = zeros; a.G = G;
+  a.err = err; a.part = part;
+  a.bulk = (d % 4 == 0) && simt::aligned16(Hinv1);
+  a.vecw = (d % 4 == 0) && simt::aligned16(Wf);
+  a.err_word = device_error_word();
   gptq_status st;
   switch (blocksize) {
-    case 32: st = run_blocks<32>(Wf, m, d, Hinv1, Ut, bits, g, qweight, wpr, codes8, scales, zeros, G, err, part, s); break;
-    case 64: st = run_blocks<64>(Wf, m, d, Hinv1, Ut, bits, g, qweight, wpr, codes8, scales, zeros, G, err, part, s); break;
-    default: st = run_blocks<128>(Wf, m, d, Hinv1, Ut, bits, g, qweight, wpr, codes8, scales, zeros, G, err, part, s); break;
+    case 32: st = run_blocks<32>(a, Ut, s); break;
+    case 64: st = run_blocks<64>(a, Ut, s); break;
+    default: st = run_blocks<128>(a, Ut, s); break;
   }
   if (st) return st;
   loss_finalize_kernel<<<(d + 255) / 256, 256, 0, s>>>(part, L.nrg, d, perm, col_losses);
