@@ -304,6 +304,10 @@ __global__ void __launch_bounds__(CB_THREADS, 1) colblock_kernel(CBArgs a) {
   } else {
     load_tile<CB_THREADS, BS, BS>(Us, BS, a.U + (long long)i1 * d + i1, d, ncols, ncols);
   }
+  // Hinv1 is final before this kernel's stream predecessor starts; W, dinfo and the
+  // statistics may come from the kernel just before (and Err1 is still being read by it)
+  grid_dep_launch();
+  grid_dep_wait();
   for (int t = tid; t < BS; t += CB_THREADS) dinfo[t] = (t < ncols) ? a.dinfo[i1 + t] : make_float4(1.f, 1.f, 0.f, 0.f);
 
   // ---- the row's block of W into registers: slot 4k + j <- column 16k + 4q + j
@@ -520,7 +524,8 @@ gptq_status run_blocks(CBArgs a, const float* Ut, cudaStream_t s) {
     a.i1 = i1;
     {
       ProfScope ps("quantize.colblock", s);
-      colblock_kernel<BS><<<nrg, CB_THREADS, SL::total, s>>>(a);
+      if (launch_pdl(colblock_kernel<BS>, dim3(nrg), dim3(CB_THREADS), SL::total, s, a) != cudaSuccess)
+        return check_launch("colblock_kernel");
       count_launch();
     }
     const int i2 = i1 + nb;

@@ -9,6 +9,8 @@
 #include <stdint.h>
 #include <stddef.h>
 
+#include <utility>
+
 #include "../../include/gptq.h"
 
 namespace gptq {
@@ -254,6 +256,31 @@ __device__ __forceinline__ void load_tile(float* __restrict__ dst, int ldd, cons
       if (idx < TOTAL) dst[(idx / PC) * ldd + idx % PC] = v[u];
     }
   }
+}
+
+// Programmatic dependent launch. A kernel launched with launch_pdl may start while the
+// kernel before it in the stream is still running; it must call grid_dep_wait (which
+// returns once that kernel has completed and its writes are visible, and at once when
+// there is no such dependency) before it reads anything an earlier kernel wrote or
+// writes anything an earlier kernel reads. grid_dep_launch lets the next kernel's
+// launch begin early; correctness never depends on where it is called.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 __device__ __forceinline__ void report_device_error(int* word, int bits) {

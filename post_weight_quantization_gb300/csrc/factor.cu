@@ -19,8 +19,8 @@
 //   gather          P[a][b] = H_d[p(d-1-a)][p(d-1-b)] (lower triangle), p = act-order
 //   Cholesky, 64-wide blocks, right-looking:
 //     chol_panel    one launch per 64-wide panel: every CTA factors the diagonal block
-//                   in shared memory (16-column pieces), CTA 0 writes it back and the
-//                   others solve 64 rows each below it (x L11^T = a, four lanes per row)
+//                   together with 64 rows below it, right-looking in 8-column steps in
+//                   shared memory; CTA 0 writes L11, the others their rows of L21
 //     tc_gemm       trailing update A22 -= L21 L21^T (lower tiles; tensor cores,
 //                   3 x TF32, both operands K-major)
 //   Triangular inverse X = L^-1 (natural order, inside Hinv1):
@@ -117,168 +117,169 @@ __global__ void gather_kernel(const float* __restrict__ H, int d, const int* __r
 }
 
 // ---------------------------------------------------------------------------------
-// Cholesky of the 64 x 64 diagonal block at k0, blocked in 4 panels of 16 columns:
-//   (a) warp 0 factors the panel's 16 x 16 diagonal piece, lane i holding row i in
-//       registers; column values move between lanes by shuffles;
-//   (b) one thread per row below solves that row against the piece (x L^T = a);
-//   (c) all threads apply the rank-16 update to the lower part right of the panel.
-// Three barriers per panel.
-constexpr int DP = 16;   // panel width inside the diagonal block
+// One Cholesky step for the 64-wide panel at k0, in one launch. Every CTA factors the
+// tall panel made of the 64 x 64 diagonal block and (CTA b >= 1) rows
+// [k1 + 64 (b - 1), + 64) below it, right-looking in steps of 8 columns, all in shared
+// memory:
+//   (a) warp 0 factors the step's 8 columns of the diagonal block (lane i holding rows
+//       i and i + 32, pivots and column values broadcast by shuffles);
+//   (b) 64 threads solve the same 8 columns of the rows below (x L^T = a);
+//   (c) all threads subtract the step's rank-8 product from the columns to its right.
+// The diagonal block's arithmetic is the same in every CTA, so every copy agrees;
+// CTA 0 writes it back, the others write their rows. A ragged last block is padded
+// with the identity.
+constexpr int PANEL_THREADS = 256;
+constexpr int PLD = NB + 1;                    // padded row of the shared tiles
+constexpr int PS = 8;                          // columns per step
 
+// 1 / sqrt(x) for x > 0: the hardware estimate refined by one Newton step
+// y <- y (3 - x y^2) / 2 (about one ulp); no call, no slow path.
+__device__ __forceinline__ float rsqrt_nr(float x) {
+  const float y = rsqrtf(x);
+  return y * fmaf(-0.5f * x * y, y, 1.5f);
+}
+
+// 1 / x for a normal x: the hardware estimate refined by one Newton step
+// y <- y + y (1 - x y).
+__device__ __forceinline__ float rcp_nr(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return fmaf(y, fmaf(-x, y, 1.0f), y);
+}
+
+// Step (a): columns [pc, pc + 8) of the diagonal block, rows pc..63, by one warp.
 template <int... Js>
-__device__ __forceinline__ bool panel_factor(std::integer_sequence<int, Js...>, float (&R)[DP], int lane, int np,
-                                             float* dpiv, int& fail) {
-  bool ok = true;
-  auto step = [&](auto jc) {
-    constexpr int j = decltype(jc)::value;
-    if (!ok || j >= np) return;
-    const float piv = __shfl_sync(0xffffffffu, R[j], j);
-    if (!(piv > 0.0f) || !isfinite(piv)) {
-      ok = false;
-      fail = j;
-      return;
-    }
-    const float dj = sqrtf(piv);
-    const float inv = __fdiv_rn(1.0f, dj);
-    const float li = (lane > j) ? R[j] * inv : 0.0f;
+__device__ __forceinline__ void panel8(std::integer_sequence<int, Js...>, float* A, float* dinv, int pc, int lane,
+                                       int& fail) {
+  const int r0 = lane, r1 = lane + 32;
+  float v0[PS], v1[PS];
 #pragma unroll
-    for (int c = j + 1; c < DP; ++c) {
-      const float lc = __shfl_sync(0xffffffffu, li, c);      // L[c][j]
-      if (lane >= c) R[c] = fmaf(-li, lc, R[c]);
+  for (int c = 0; c < PS; ++c) {
+    v0[c] = (r0 >= pc + c) ? A[r0 * PLD + pc + c] : 0.0f;
+    v1[c] = (r1 >= pc + c) ? A[r1 * PLD + pc + c] : 0.0f;
+  }
+  const bool hi = pc >= 32;                    // warp-uniform: the step's pivots lie in rows 32..63
+  auto step = [&](auto jc) {
+    constexpr int jj = decltype(jc)::value;
+    const int j = pc + jj;
+    const float piv = __shfl_sync(0xffffffffu, hi ? v1[jj] : v0[jj], j & 31);
+    if (!(piv > 0.0f && piv < INFINITY) && fail < 0) fail = j;
+    const float inv = rsqrt_nr(piv);
+    const float l0 = v0[jj] * inv, l1 = v1[jj] * inv;
+#pragma unroll
+    for (int cc = jj + 1; cc < PS; ++cc) {
+      const int c = pc + cc;
+      const float lc = __shfl_sync(0xffffffffu, hi ? l1 : l0, c & 31);   // L[c][j]
+      v0[cc] = (r0 >= c) ? fmaf(-l0, lc, v0[cc]) : v0[cc];
+      v1[cc] = (r1 >= c) ? fmaf(-l1, lc, v1[cc]) : v1[cc];
     }
-    if (lane == j) R[j] = dj;
-    else if (lane > j) R[j] = li;
-    if (lane == 0) dpiv[j] = inv;
+    v0[jj] = (r0 == j) ? piv * inv : ((r0 > j) ? l0 : v0[jj]);
+    v1[jj] = (r1 == j) ? piv * inv : ((r1 > j) ? l1 : v1[jj]);
+    if (lane == 0) dinv[j] = inv;
   };
   (step(std::integral_constant<int, Js>{}), ...);
-  return ok;
-}
-
-// Factor the nb x nb block held in A (lower triangle) in place; returns the failing
-// pivot (block-relative) or -1. All 256 threads of the CTA take part.
-__device__ int factor_diag_block(float (*A)[NB + 1], float* dinv, int* fail_s, int nb) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) *fail_s = -1;
-  __syncthreads();
-  for (int p0 = 0; p0 < nb; p0 += DP) {
-    const int np = min(DP, nb - p0);
-    // (a) diagonal piece
-    if (warp == 0) {
-      float R[DP];
 #pragma unroll
-      for (int c = 0; c < DP; ++c) R[c] = (lane < np && c <= lane) ? A[p0 + lane][p0 + c] : 0.0f;
-      int fail = -1;
-      const bool ok = panel_factor(std::make_integer_sequence<int, DP>{}, R, lane, np, dinv, fail);
-      if (!ok && lane == 0) *fail_s = p0 + fail;
-      if (lane < np) {
-#pragma unroll
-        for (int c = 0; c < DP; ++c)
-          if (c <= lane) A[p0 + lane][p0 + c] = R[c];
-      }
-    }
-    __syncthreads();
-    if (*fail_s >= 0) return *fail_s;
-    // (b) rows below the piece: x L^T = a
-    const int r = p0 + DP + tid;
-    if (tid < NB - p0 - DP && r < nb) {
-      float x[DP];
-#pragma unroll
-      for (int c = 0; c < DP; ++c) x[c] = (c < np) ? A[r][p0 + c] : 0.0f;
-#pragma unroll
-      for (int j = 0; j < DP; ++j) {
-        x[j] *= dinv[j];
-#pragma unroll
-        for (int c = j + 1; c < DP; ++c) x[c] = fmaf(-x[j], A[p0 + c][p0 + j], x[c]);
-      }
-#pragma unroll
-      for (int c = 0; c < DP; ++c)
-        if (c < np) A[r][p0 + c] = x[c];
-    }
-    __syncthreads();
-    // (c) rank-16 update of the lower part right of the panel
-    const int q0 = p0 + np, rem = nb - q0;
-    for (int idx = tid; idx < rem * rem; idx += 256) {
-      const int i = q0 + idx / rem, c = q0 + idx % rem;
-      if (c <= i) {
-        float acc = A[i][c];
-#pragma unroll
-        for (int k = 0; k < DP; ++k)
-          if (k < np) acc = fmaf(-A[i][p0 + k], A[c][p0 + k], acc);
-        A[i][c] = acc;
-      }
-    }
-    __syncthreads();
+  for (int c = 0; c < PS; ++c) {
+    if (r0 >= pc + c) A[r0 * PLD + pc + c] = v0[c];
+    if (r1 >= pc + c) A[r1 * PLD + pc + c] = v1[c];
   }
-  return -1;
 }
-
-// One Cholesky step for the 64-wide panel at k0, in one launch: every CTA factors the
-// diagonal block in shared memory (the same arithmetic in each, so every copy is the
-// same); CTA 0 writes it back and CTA b >= 1 solves rows [k1 + 64 (b - 1), + 64) of the
-// panel below against it (x L11^T = a, four lanes per row, pivots broadcast by shuffle).
-constexpr int TR_LANES = 4;
-constexpr int TR_SLOTS = NB / TR_LANES;        // 16
-constexpr int PANEL_THREADS = 256;             // 64 rows per CTA
-constexpr int TR_ROWS = PANEL_THREADS / TR_LANES;
 
 __global__ void __launch_bounds__(PANEL_THREADS) chol_panel_kernel(float* __restrict__ P, int d, int k0, Header* hdr) {
-  __shared__ float A[NB][NB + 1];
-  __shared__ float dinv[DP];
-  __shared__ float invd[NB];
-  __shared__ int fail_s;
+  extern __shared__ float psm[];
+  float* A = psm;                      // 64 x PLD: the diagonal block, then L11 (lower)
+  float* Xs = A + NB * PLD;            // 64 x PLD: this CTA's rows of the panel below
+  float* dinv = Xs + NB * PLD;         // 64
+  int* fail_s = reinterpret_cast<int*>(dinv + NB);
+  grid_dep_wait();                     // the previous trailing update
+  grid_dep_launch();
   if (hdr->failed) return;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tx = tid & 15, ty = tid >> 4;
   const int nb = min(NB, d - k0), k1 = k0 + nb;
-  const int tid = threadIdx.x;
-  load_tile<PANEL_THREADS, NB, NB>(&A[0][0], NB + 1, P + (long long)k0 * d + k0, d, nb, nb);   // upper part unused
+  const bool below = blockIdx.x > 0;
+  const int rbeg = k1 + (blockIdx.x - 1) * NB;              // first panel row of this CTA
+  const int nr = below ? min(NB, d - rbeg) : 0;
+
+  // many loads in flight per thread; zeros outside the block
+  load_tile<PANEL_THREADS, NB, NB>(A, PLD, P + (long long)k0 * d + k0, d, nb, nb);
+  if (below) load_tile<PANEL_THREADS, NB, NB>(Xs, PLD, P + (long long)rbeg * d + k0, d, nr, nb);
+  if (tid == 0) *fail_s = -1;
   __syncthreads();
-  const int fail = factor_diag_block(A, dinv, &fail_s, nb);
-  if (fail >= 0) {
+  if (tid >= nb && tid < NB) A[tid * PLD + tid] = 1.0f;   // identity padding of a ragged block
+  __syncthreads();
+
+#pragma unroll 1
+  for (int pc = 0; pc < NB; pc += PS) {
+    if (warp == 0) {
+      int fail = -1;
+      panel8(std::make_integer_sequence<int, PS>{}, A, dinv, pc, lane, fail);
+      if (lane == 0 && fail >= 0 && fail < nb && *fail_s < 0) *fail_s = fail;
+    }
+    __syncthreads();
+    if (*fail_s >= 0) break;
+    const int q0 = pc + PS, rem = NB - q0;
+    if (below && tid < NB) {
+      // (b) row tid of Xs, columns [pc, pc + 8)
+      float* xr = Xs + tid * PLD + pc;
+      float x[PS];
+#pragma unroll
+      for (int c = 0; c < PS; ++c) x[c] = xr[c];
+#pragma unroll
+      for (int jj = 0; jj < PS; ++jj) {
+        x[jj] *= dinv[pc + jj];
+#pragma unroll
+        for (int cc = jj + 1; cc < PS; ++cc) x[cc] = fmaf(-x[jj], A[(pc + cc) * PLD + pc + jj], x[cc]);
+      }
+#pragma unroll
+      for (int c = 0; c < PS; ++c) xr[c] = x[c];
+    }
+    // (c) diagonal block: A[i][c] -= sum_k L[i][pc+k] L[c][pc+k], q0 <= c <= i
+    for (int a = ty; a < rem; a += 16) {
+      const int i = q0 + a;
+      for (int b = tx; b <= a; b += 16) {
+        const int c = q0 + b;
+        float acc = A[i * PLD + c];
+#pragma unroll
+        for (int k = 0; k < PS; ++k) acc = fmaf(-A[i * PLD + pc + k], A[c * PLD + pc + k], acc);
+        A[i * PLD + c] = acc;
+      }
+    }
+    __syncthreads();
+    if (below) {
+      // (c) rows below: Xs[r][c] -= sum_k Xs[r][pc+k] L[c][pc+k], c >= q0
+      for (int r = ty; r < NB; r += 16) {
+        for (int b = tx; b < rem; b += 16) {
+          const int c = q0 + b;
+          float acc = Xs[r * PLD + c];
+#pragma unroll
+          for (int k = 0; k < PS; ++k) acc = fmaf(-Xs[r * PLD + pc + k], A[c * PLD + pc + k], acc);
+          Xs[r * PLD + c] = acc;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  if (*fail_s >= 0) {
     if (blockIdx.x == 0 && tid == 0) {
-      atomicMin(&hdr->fail_pivot, k0 + fail);
+      atomicMin(&hdr->fail_pivot, k0 + *fail_s);
       hdr->failed = 1;
     }
     return;
   }
-  if (blockIdx.x == 0) {
-    for (int idx = tid; idx < nb * nb; idx += PANEL_THREADS) {
-      const int i = idx / nb, c = idx % nb;
-      if (c <= i) P[(long long)(k0 + i) * d + k0 + c] = A[i][c];
+  if (!below) {
+    for (int idx = tid; idx < NB * NB; idx += PANEL_THREADS) {
+      const int i = idx >> 6, c = idx & 63;
+      if (i < nb && c <= i) P[(long long)(k0 + i) * d + k0 + c] = A[i * PLD + c];
     }
-    return;
-  }
-  for (int j = tid; j < NB; j += PANEL_THREADS) invd[j] = (j < nb) ? __fdiv_rn(1.0f, A[j][j]) : 0.0f;
-  __syncthreads();
-  const int lane = tid & 31, q = lane & (TR_LANES - 1), qbase = lane - q;
-  const int r = k1 + (blockIdx.x - 1) * TR_ROWS + tid / TR_LANES;
-  const bool active = r < d;
-  float* row = P + (long long)(active ? r : k0) * d + k0;
-  float x[TR_SLOTS];
-#pragma unroll
-  for (int k = 0; k < TR_SLOTS; ++k) {
-    const int c = TR_LANES * k + q;
-    x[k] = (active && c < nb) ? row[c] : 0.0f;
-  }
-#pragma unroll 1
-  for (int jb = 0; jb < nb; jb += TR_LANES) {
-#pragma unroll
-    for (int i = 0; i < TR_LANES; ++i) {
-      const int j = jb + i;
-      if (j < nb) {                                           // warp-uniform
-        const float xj = __shfl_sync(0xffffffffu, x[0], qbase + i) * invd[j];
-        if (q == i && active) row[j] = xj;
-        // slot k holds column jb + 4k + q: later than j unless k == 0 and q <= i
-#pragma unroll
-        for (int k = 0; k < TR_SLOTS; ++k) {
-          const int c = jb + TR_LANES * k + q;
-          if ((k > 0 || q > i) && c < NB) x[k] = fmaf(-xj, A[c][j], x[k]);
-        }
-      }
+  } else {
+    for (int idx = tid; idx < NB * NB; idx += PANEL_THREADS) {
+      const int i = idx >> 6, c = idx & 63;
+      if (i < nr && c < nb) P[(long long)(rbeg + i) * d + k0 + c] = Xs[i * PLD + c];
     }
-#pragma unroll
-    for (int k = 0; k < TR_SLOTS - 1; ++k) x[k] = x[k + 1];
-    x[TR_SLOTS - 1] = 0.0f;
   }
 }
+constexpr size_t PANEL_SMEM = (size_t)(2 * NB * PLD + NB + 4) * sizeof(float);
 
 // Inverse of every 64 x 64 diagonal block of L, written into X's diagonal blocks
 // (X = L^-1 in natural order). Thread c solves L x = e_c (column c of the inverse).
@@ -308,7 +309,7 @@ __global__ void __launch_bounds__(64) diag_inverse_kernel(const float* __restric
     if (c > i || i >= nb) L[i][c] = (i == c) ? 1.0f : 0.0f;
   }
   __syncthreads();
-  for (int j = threadIdx.x; j < NB; j += blockDim.x) invd[j] = __fdiv_rn(1.0f, L[j][j]);
+  for (int j = threadIdx.x; j < NB; j += blockDim.x) invd[j] = rcp_nr(L[j][j]);
   __syncthreads();
   const int c = threadIdx.x;
   float x[NB];
@@ -370,12 +371,18 @@ gptq_status factor_launch(const float* H, long long d_, float percdamp, int act_
   }
   if (gptq_status st = check_launch("factor setup kernels")) return st;
 
+  if (cudaFuncSetAttribute(chol_panel_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PANEL_SMEM) !=
+      cudaSuccess)
+    return set_error(GPTQ_ERR_CUDA, "cudaFuncSetAttribute(chol_panel_kernel) failed");
+
   // ---- Cholesky P = L L^T, 64-wide blocks, right-looking
   for (int k0 = 0; k0 < d; k0 += NB) {
     const int nb = std::min(NB, d - k0), k1 = k0 + nb, below = d - k1;
     {
       ProfScope ps("factor.chol_panel", s);
-      chol_panel_kernel<<<1 + (below + TR_ROWS - 1) / TR_ROWS, PANEL_THREADS, 0, s>>>(P, d, k0, hdr);
+      if (launch_pdl(chol_panel_kernel, dim3(1 + (below + NB - 1) / NB), dim3(PANEL_THREADS), PANEL_SMEM, s, P, d, k0,
+                     hdr) != cudaSuccess)
+        return check_launch("chol_panel_kernel");
       count_launch();
     }
     if (below > 0) {

@@ -151,7 +151,6 @@ template <bool A_KMAJ, bool B_KMAJ>
 __global__ void __launch_bounds__(THREADS, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b, Params p,
                int* __restrict__ err_word) {
-  if (p.skip && *p.skip) return;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -186,7 +185,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int ntiles = p.tiles_per_batch * p.batches;
+  // everything above touched no global data; the operands and C come from earlier kernels
+  grid_dep_launch();
+  grid_dep_wait();
+  const int ntiles = (p.skip && *p.skip) ? 0 : p.tiles_per_batch * p.batches;
   constexpr uint32_t IDESC = umma_idesc(/*tf32*/ 2, !A_KMAJ, !B_KMAJ, BM, BN);
 
   if (warp == 0 && lane == 0) {
@@ -441,7 +443,8 @@ gptq_status tc_gemm(const simt::GemmArgs& g, int batches, bool a_kmaj, bool b_km
         return set_error(GPTQ_ERR_CUDA, "cudaFuncSetAttribute(tc_gemm_kernel) failed");
       attr_done[key] = true;
     }
-    kern<<<grid, THREADS, SMEM_BYTES, s>>>(ma, mb, p, device_error_word());
+    if (launch_pdl(kern, dim3(grid), dim3(THREADS), SMEM_BYTES, s, ma, mb, p, device_error_word()) != cudaSuccess)
+      return check_launch("tc_gemm_kernel");
     count_launch();
     return check_launch("tc_gemm_kernel");
   };
