@@ -20,6 +20,7 @@ import json
 import os
 import statistics
 import subprocess
+import threading
 import sys
 import time
 
@@ -37,7 +38,7 @@ L2_FLUSH_BYTES = 256 << 20
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["gptq", "reference"], default="gptq")
     ap.add_argument("--workload", default="llama_4096_g128")
@@ -115,13 +116,16 @@ def oracle_sample(wl, layer, X_bits_sample, W_bits_rows, n_total, rows_total):
 
 # ----------------------------------------------------------------------------------
 class Clocks:
+    """nvidia-smi sampled every 100 ms by a reader thread; stop(t0, t1) keeps the samples
+    taken inside the timed region [t0, t1] (perf_counter seconds)."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int, enabled: bool):
         self.proc = None
-        self.index = index
+        self.lines = []
+        self.ready = threading.Event()
         if enabled:
             try:
                 self.proc = subprocess.Popen(
@@ -129,19 +133,30 @@ class Clocks:
                      "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             except OSError:
                 self.proc = None
+        if self.proc is not None:
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            self.ready.wait(timeout=10.0)      # sampler running before the timed region starts
 
-    def stop(self):
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.perf_counter(), line))
+            self.ready.set()
+
+    def stop(self, t0: float, t1: float):
         if self.proc is None:
             return None
+        time.sleep(0.25)                       # the sample that closes the window
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-            out, _ = self.proc.communicate()
+        self.thread.join(timeout=5)
+        inside = [ln for t, ln in self.lines if t0 <= t <= t1 + 0.15]
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.splitlines():
+        for line in inside:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 8:
                 continue
@@ -293,17 +308,19 @@ def run_gpu(args):
     launches0 = g.gptq_launch_count()
     events = []
     t_wall = time.perf_counter()
+    t_region0 = t_wall
     for _ in range(args.steps):
         flush.zero_()                       # L2 flush between steps, outside the step's events
         ev = mk()
         step(ev)
         events.append(ev)
     torch.cuda.synchronize()
-    t_wall = time.perf_counter() - t_wall
+    t_region1 = time.perf_counter()
+    t_wall = t_region1 - t_wall
     if world > 1:
         dist.barrier()
     launches = g.gptq_launch_count() - launches0
-    clk = clocks.stop()
+    clk = clocks.stop(t_region0, t_region1)
     g.gptq_device_check()
 
     st_ms = {"syrk": [], "factor": [], "quantize": []}
