@@ -1,0 +1,194 @@
+"""Parity of the larger configurations: the Llama-7B MLP (gate/up 11008 x 4096 sharing one
+4096^2 Hessian, down 4096 x 11008 with an 11008^2 Hessian; 262144 tokens) and the
+70B-shaped decoder block (q/k/v and o at hidden 8192, gate/up 28672 x 8192, down
+8192 x 28672 with a 28672^2 Hessian; 131072 tokens; 4-bit g128 and 2-bit g64).
+
+Each case runs the path as a user would: the Hessian accumulated over all tokens in
+streamed batches, one factor call, one column-loop call on the stacked rows of the
+layers that share the Hessian. The oracle cannot redo these layers in seconds, so it
+checks what it can compute exactly:
+  * Hessian entries of sampled channels, summed in float64 from the same tokens;
+  * Hinv1's trailing k x k block, which is exactly the Hinv1 of H_d's trailing k x k
+    block (Hinv1 = J L^-1 J with J H_d J = L L^T: the first k pivots of L only see that
+    block), by the oracle's float64 three-step chain;
+  * U H_d U^T = I on sampled rows (any size);
+  * sampled rows of the column loop with the same Hinv1 (rows are independent) against
+    the float32 and float64 oracle;
+  * the loss identity and the code range over the whole layer.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import gptq_oracle as orc
+from synth import bf16_bits_to_f32, gen_activations_into, workload
+
+pytestmark = pytest.mark.gpu
+
+CODE_TOL = 0.005
+SCALE_RTOL = 1e-4
+ERR_RTOL = 0.02
+TOKENS_PER_BATCH = 16384
+TAIL = 2048                # trailing block checked against the oracle chain
+
+CASES = [
+    ("llama7b_mlp", "mlp_in", ("gate", "up"), 4, 128),
+    ("llama7b_mlp", "mlp_down", ("down",), 4, 128),
+    ("llama70b_block", "attn_in", ("q", "k", "v"), 4, 128),
+    ("llama70b_block", "attn_out", ("o",), 2, 64),
+    ("llama70b_block", "mlp_in", ("gate", "up"), 4, 128),
+    ("llama70b_block", "mlp_down", ("down",), 4, 128),
+    ("llama70b_block", "mlp_down", ("down",), 2, 64),
+]
+
+
+@pytest.fixture(scope="module")
+def g():
+    from post_weight_quantization_gb300 import build as b
+    b.build()
+    from post_weight_quantization_gb300 import gptq
+    return gptq
+
+
+_HCACHE = {}
+
+
+def hessian(g, wl_name, key):
+    """GPU Hessian over all tokens (streamed batches) and exact float64 sums of sampled
+    channels from the same bf16 tokens."""
+    if (wl_name, key) in _HCACHE:
+        return _HCACHE[(wl_name, key)]
+    _HCACHE.clear()
+    torch.cuda.empty_cache()
+    spec = workload(wl_name).acts[key]
+    n, d = spec.n, spec.d
+    ch = np.sort(np.random.default_rng(7).choice(d, size=24, replace=False))
+    ref = np.zeros((24, 24))
+    aref = np.zeros((24, 24))
+    H = torch.empty((d, d), dtype=torch.float32, device="cuda")
+    buf = np.empty((TOKENS_PER_BATCH, d), dtype=np.uint16)
+    for t0 in range(0, n, TOKENS_PER_BATCH):
+        t1 = min(n, t0 + TOKENS_PER_BATCH)
+        xb = buf[: t1 - t0]
+        gen_activations_into(spec, xb, token_range=(t0, t1))
+        Xd = torch.from_numpy(xb.view(np.int16)).cuda()
+        g.gptq_hessian_accumulate(Xd, H, alpha=2.0, zero_first=(t0 == 0))
+        xs = bf16_bits_to_f32(xb[:, ch]).astype(np.float64)
+        ref += xs.T @ xs
+        ax = np.abs(xs)
+        aref += ax.T @ ax
+        torch.cuda.synchronize()
+    g.gptq_device_check()
+    out = (H, ch, 2.0 * ref, 2.0 * aref, n)
+    _HCACHE[(wl_name, key)] = out
+    return out
+
+
+def lambda_max(A, iters=40):
+    """Largest eigenvalue of a symmetric positive definite matrix by power iteration
+    (a lower bound that converges from below)."""
+    v = torch.ones(A.shape[0], dtype=A.dtype, device=A.device)
+    lam = 0.0
+    for _ in range(iters):
+        w = A @ v
+        lam = float(torch.dot(v, w) / torch.dot(v, v))
+        v = w / torch.linalg.vector_norm(w)
+    return lam
+
+
+def sym64(H):
+    """The symmetric float64 matrix of a GPU Hessian whose upper triangle is authoritative."""
+    Hu = torch.triu(H.double())
+    return Hu + torch.triu(Hu, 1).T
+
+
+@pytest.mark.parametrize("wl_name,key,names,bits,gs", CASES)
+def test_large_config(g, wl_name, key, names, bits, gs):
+    wl = workload(wl_name)
+    H, ch, ref, aref, n = hessian(g, wl_name, key)
+    d = H.shape[0]
+
+    # ---- Hessian: sampled entries within the worst-case bound of fp32 summation
+    got = H[torch.from_numpy(ch).cuda()][:, torch.from_numpy(ch).cuda()].cpu().numpy().astype(np.float64)
+    iu = np.triu_indices(len(ch))
+    bound = 2 * n * 2.0 ** -24 * aref
+    assert np.all(np.abs(got - ref)[iu] <= bound[iu])
+
+    # ---- factor
+    U, perm, info = g.gptq_factor(H, percdamp=0.01, act_order=False)
+    assert info == -1 and perm is None
+    assert bool(torch.all(torch.diagonal(U) > 0)) and bool(torch.all(torch.tril(U, -1) == 0))
+    Hs = sym64(H)
+    lam = 0.01 * float(torch.diagonal(Hs).mean())
+    Hd = Hs + lam * torch.eye(d, dtype=torch.float64, device="cuda")
+    # trailing block against the oracle chain on the same (damped) Hessian
+    Hd_tail = Hd[d - TAIL:, d - TAIL:].cpu().numpy()
+    Uo = orc.hinv1(Hd_tail)
+    Ug = U[d - TAIL:, d - TAIL:].cpu().numpy().astype(np.float64)
+    ev = np.linalg.eigvalsh(Hd_tail)
+    kappa = ev[-1] / ev[0]
+    rel = np.linalg.norm(Ug - Uo) / np.linalg.norm(Uo)
+    print(f"[{wl_name}/{key}] trailing-block rel {rel:.3e}, kappa {kappa:.3e}")
+    assert rel < kappa * 2.0 ** -24, (rel, kappa)
+    # U H_d U^T = I on sampled rows of the whole matrix
+    rows_u = torch.from_numpy(np.sort(np.random.default_rng(3).choice(d, size=8, replace=False))).cuda()
+    U64 = U.double()
+    cols = U64 @ (Hd @ U64[rows_u].T)                 # columns rows_u of U H_d U^T
+    E = torch.zeros_like(cols)
+    E[rows_u, torch.arange(len(rows_u), device="cuda")] = 1.0
+    res = float((cols - E).abs().max())
+    kap = 1.02 * lambda_max(Hd) / lam           # lambda_min(H_d) >= lam
+    print(f"[{wl_name}/{key}] residual of U H_d U^T - I {res:.3e}, kappa <= {kap:.3e}")
+    assert res < kap * 2.0 ** -24, (res, kap)
+    del cols, U64
+
+    # ---- column loop on the stacked rows of the layers sharing this Hessian
+    layers = [l for l in wl.layers if l.name in names]
+    W_bits = np.concatenate([wl.weight(l) for l in layers], axis=0)
+    m = W_bits.shape[0]
+    Wd = torch.from_numpy(W_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    q = g.gptq_quantize_layer(Wd, U, None, bits=bits, group_size=gs, blocksize=128, sync=True)
+    torch.cuda.synchronize()
+    g.gptq_device_check()
+    codes_all = g.gptq_unpack_codes(q.qweight, m, d, bits)
+    assert int(codes_all.min()) >= 0 and int(codes_all.max()) <= 2 ** bits - 1
+
+    rows = np.sort(np.random.default_rng(5).choice(m, size=24, replace=False))
+    W = bf16_bits_to_f32(W_bits[rows])
+    Uh = U.cpu().numpy()
+    res32 = orc.gptq_columns(np.ascontiguousarray(W), Uh, bits, gs, 128, dtype=np.float32)
+    res64 = orc.gptq_columns(W.astype(np.float64), Uh.astype(np.float64), bits, gs, 128)
+    del Uh
+    codes = codes_all.cpu().numpy().astype(np.int64)[rows]
+    scales = q.scales.cpu().numpy()[rows].astype(np.float64)
+    zeros = q.zeros.cpu().numpy()[rows].astype(np.float64)
+    mism = np.mean(codes != res32["codes"])
+    print(f"[{wl_name}/{key}/{bits}b g{gs}] code mismatch vs float32 oracle {mism:.4f}")
+    assert mism <= CODE_TOL, mism
+    s32, z32 = orc.quant_params(np.ascontiguousarray(W[:, :gs]), bits)
+    assert np.array_equal(scales[:, 0].astype(np.float32), s32)
+    assert np.array_equal(zeros[:, 0].astype(np.float32), z32)
+    assert np.max(np.abs(scales[:, 0] - res64["scales"][:, 0]) / res64["scales"][:, 0]) <= SCALE_RTOL
+    gi = torch.arange(d, device="cuda") // gs
+    sel = torch.from_numpy(rows).cuda()
+    W64 = torch.from_numpy(W).cuda().double()
+
+    def out_err(What):
+        dW = W64 - What
+        return float(((dW @ Hs) * dW).sum() / ((W64 @ Hs) * W64).sum()) ** 0.5
+
+    What_g = (codes_all[sel].double() - q.zeros[sel].double()[:, gi]) * q.scales[sel].double()[:, gi]
+    e_gpu = out_err(What_g)
+    for res_o in (res64, res32):
+        e_orc = out_err(torch.from_numpy(res_o["W_hat"].astype(np.float64)).cuda())
+        print(f"[{wl_name}/{key}/{bits}b g{gs}] output error gpu {e_gpu:.5f} oracle {e_orc:.5f}")
+        assert abs(e_gpu - e_orc) <= ERR_RTOL * e_orc, (e_gpu, e_orc)
+
+    # ---- loss identity over the whole layer: sum of Losses1 = 1/2 tr(dW H_d dW^T)
+    Hd32 = Hd.float()
+    del Hd, Hs
+    What = (codes_all.float() - q.zeros[:, gi]) * q.scales[:, gi]
+    dW = Wd.float() - What
+    quad = 0.5 * float(((dW @ Hd32).double() * dW.double()).sum())
+    total = float(q.col_losses.double().sum())
+    assert abs(total - quad) <= 1e-2 * quad, (total, quad)
