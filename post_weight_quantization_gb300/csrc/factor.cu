@@ -25,10 +25,11 @@
 //                   3 x TF32, both operands K-major)
 //   Triangular inverse X = L^-1 (natural order, inside Hinv1):
 //     diag_inverse  every 64 x 64 diagonal block at once (thread c solves L x = e_c)
-//     gemm x 2 per level, recursive doubling over block pairs (A, C):
-//                   T = L[C][A] X[A][A];  X[C][A] = -X[C][C] T   (T lives in P's unused
-//                   strict upper triangle)
-//     reverse       Hinv1 = J X J in place
+//     tc_gemm x 2 + a transpose per level, recursive doubling over block pairs (A, C)
+//                   with X below the diagonal and Y = X^T above it:
+//                   T = Y[A][A] L[C][A]^T;  X[C][A] = -X[C][C] T^T;  Y[A][C] = X[C][A]^T
+//                   (T lives in P's unused strict upper triangle; both operands K-major)
+//     reverse       Hinv1 = J X J in place, lower triangle cleared
 // A failed pivot sets a flag in the workspace header that every later kernel checks.
 
 #include <algorithm>
@@ -318,8 +319,10 @@ __global__ void __launch_bounds__(64) diag_inverse_kernel(const float* __restric
   inv_column(std::make_integer_sequence<int, NB>{}, x, L, invd);
   if (c >= nb) return;
 #pragma unroll
-  for (int q = 0; q < NB; ++q)
+  for (int q = 0; q < NB; ++q) {
     if (q < nb && q >= c) X[(long long)(k0 + q) * d + k0 + c] = x[q];
+    if (q < nb && q > c) X[(long long)(k0 + c) * d + k0 + q] = x[q];   // the transpose, above
+  }
 }
 
 __global__ void zero_kernel(float* __restrict__ M, long long n) {
@@ -327,16 +330,40 @@ __global__ void zero_kernel(float* __restrict__ M, long long n) {
     M[idx] = 0.0f;
 }
 
-// In place: M[a][b] <-> M[d-1-a][d-1-b] (turns X = L^-1, lower, into J X J, upper).
+// In place: M[a][b] <-> M[d-1-a][d-1-b], then the strict lower triangle cleared: turns
+// X = L^-1 (lower, with its transpose stored above) into J X J (upper, lower zero).
 __global__ void reverse_kernel(float* __restrict__ M, int d, const Header* hdr) {
   if (hdr->failed) return;
   const long long n = (long long)d * d;
   for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n / 2;
        idx += (long long)gridDim.x * blockDim.x) {
     const long long jdx = n - 1 - idx;         // the partner of idx
+    const long long a = idx / d, b = idx - a * d;   // idx: row a, column b; jdx: d-1-a, d-1-b
     const float t = M[idx];
-    M[idx] = M[jdx];
-    M[jdx] = t;
+    M[idx] = (a <= b) ? M[jdx] : 0.0f;
+    M[jdx] = (a >= b) ? t : 0.0f;
+  }
+}
+
+// Y[a0 + j][c0 + i] = X[c0 + i][a0 + j] for every pair z of the doubling step: the
+// transpose of the block just computed, stored above the diagonal.
+__global__ void pair_transpose_kernel(float* __restrict__ M, int d, int sz, int np, int c_last,
+                                      const Header* hdr) {
+  __shared__ float tile[32][33];
+  if (hdr->failed) return;
+  const int z = blockIdx.z;
+  const int a0 = 2 * z * sz, c0 = a0 + sz;
+  const int nc = (z == np - 1) ? c_last : sz;
+  const int bi = blockIdx.y * 32, bj = blockIdx.x * 32;      // i over C rows, j over A columns
+  if (bi >= nc) return;
+  for (int yy = threadIdx.y; yy < 32; yy += 8) {
+    const int i = bi + yy, j = bj + threadIdx.x;
+    tile[yy][threadIdx.x] = (i < nc && j < sz) ? M[(long long)(c0 + i) * d + a0 + j] : 0.0f;
+  }
+  __syncthreads();
+  for (int yy = threadIdx.y; yy < 32; yy += 8) {
+    const int j = bj + yy, i = bi + threadIdx.x;
+    if (i < nc && j < sz) M[(long long)(a0 + j) * d + c0 + i] = tile[threadIdx.x][yy];
   }
 }
 
@@ -408,33 +435,48 @@ gptq_status factor_launch(const float* H, long long d_, float percdamp, int act_
     diag_inverse_kernel<<<(d + NB - 1) / NB, NB, 0, s>>>(P, Hinv1, d, hdr);
   }
   count_launch(2);
+  // Doubling over block pairs (A, C) = ([2p sz, 2p sz + sz), [2p sz + sz, ...)): with
+  // X = L^-1 kept below the diagonal of Hinv1 and Y = X^T above it (shared diagonal),
+  //   T = Y[A][A] L[C][A]^T           (= (L[C][A] X[A][A])^T, into P's unused upper part)
+  //   X[C][A] = -X[C][C] T^T          (= -X[C][C] L[C][A] X[A][A])
+  //   Y[A][C] = X[C][A]^T
+  // so every product has both operands K-major (the tensor-core GEMM's layout); the
+  // triangular operands are masked, since their other triangle holds the transpose.
   for (int sz = NB; sz < d; sz *= 2) {
-    // pairs p: A block [2p sz, 2p sz + sz) (full), C block [2p sz + sz, min(2p sz + 2sz, d))
     int np = 0;
     while (2LL * np * sz + sz < d) ++np;
     const int c_last = std::min(sz, d - (2 * (np - 1) * sz + sz));
     const long long pair = 2LL * sz * d + 2LL * sz;
-    // T_p = L[C][A] X[A][A], stored in P's strict upper triangle at rows p sz, columns d - sz
-    simt::GemmArgs g1{};
-    g1.M = sz; g1.N = sz; g1.K = sz; g1.M_last = c_last; g1.K_last = sz;
-    g1.A = P + (long long)sz * d; g1.lda = d; g1.a_bs = pair;
-    g1.B = Hinv1; g1.ldb = d; g1.b_bs = pair; g1.b_lower = 1;
-    g1.C = P + (d - sz); g1.ldc = d; g1.c_bs = (long long)sz * d;
-    g1.alpha = 1.0f; g1.beta = 0.0f;
-    g1.vec = vec;
-    g1.skip = failed;
+    const int nfull = (c_last == sz) ? np : np - 1;
     ProfScope ps("factor.trtri_gemms", s);
-    if (gptq_status st = simt::gemm(g1, np, true, false, s)) return st;
-    // X[C][A] = -X[C][C] T_p
+    auto g1_for = [&](int p0, int nbatch, int ncol) {
+      const long long a0 = 2LL * p0 * sz, c0 = a0 + sz;
+      simt::GemmArgs g1{};
+      g1.M = sz; g1.N = ncol; g1.K = sz; g1.M_last = sz; g1.K_last = sz;
+      g1.A = Hinv1 + a0 * d + a0; g1.lda = d; g1.a_bs = pair; g1.a_tri = 2;
+      g1.B = P + c0 * d + a0; g1.ldb = d; g1.b_bs = pair;
+      g1.C = P + a0 * d + c0; g1.ldc = d; g1.c_bs = pair;
+      g1.alpha = 1.0f; g1.beta = 0.0f;
+      g1.vec = vec;
+      g1.skip = failed;
+      return tc_gemm(g1, nbatch, true, true, s);
+    };
+    if (nfull > 0)
+      if (gptq_status st = g1_for(0, nfull, sz)) return st;
+    if (nfull < np)
+      if (gptq_status st = g1_for(np - 1, 1, c_last)) return st;
     simt::GemmArgs g2{};
     g2.M = sz; g2.N = sz; g2.K = sz; g2.M_last = c_last; g2.K_last = c_last;
-    g2.A = Hinv1 + (long long)sz * d + sz; g2.lda = d; g2.a_bs = pair; g2.a_lower = 1;
-    g2.B = P + (d - sz); g2.ldb = d; g2.b_bs = (long long)sz * d;
+    g2.A = Hinv1 + (long long)sz * d + sz; g2.lda = d; g2.a_bs = pair; g2.a_tri = 1;
+    g2.B = P + sz; g2.ldb = d; g2.b_bs = pair;
     g2.C = Hinv1 + (long long)sz * d; g2.ldc = d; g2.c_bs = pair;
     g2.alpha = -1.0f; g2.beta = 0.0f;
     g2.vec = vec;
     g2.skip = failed;
-    if (gptq_status st = simt::gemm(g2, np, true, false, s)) return st;
+    if (gptq_status st = tc_gemm(g2, np, true, true, s)) return st;
+    dim3 tg((unsigned)((sz + 31) / 32), (unsigned)((sz + 31) / 32), (unsigned)np);
+    pair_transpose_kernel<<<tg, dim3(32, 8), 0, s>>>(Hinv1, d, sz, np, c_last, hdr);
+    count_launch();
   }
   ProfScope ps_rev("factor.reverse", s);
   reverse_kernel<<<std::max(1, std::min(4096, (int)(((long long)d * d / 2 + 255) / 256))), 256, 0, s>>>(Hinv1, d, hdr);

@@ -5,9 +5,11 @@
 // with A(i, k) and B(k, j) read from row-major storage in either of two layouts:
 //   K-major   A(i, k) = A[i * lda + k]      B(k, j) = B[j * ldb + k]
 //   MN-major  A(i, k) = A[k * lda + i]      B(k, j) = B[k * ldb + j]
-// Options: only the lower-triangular tiles of a square C; A lower triangular
-// (A(i, k) = 0 for k > i) or B lower triangular (B(k, j) = 0 for k < j), which trims
-// the k range per tile; batches with a smaller last batch (ragged pairs).
+// Options: only the lower-triangular tiles of a square C; A read as lower triangular
+// (a_tri = 1: A(i, k) taken as 0 for k > i) or upper triangular (a_tri = 2: 0 for
+// k < i), whatever the other triangle holds (the k range is trimmed per tile and the
+// elements are masked); B lower triangular with zeros stored (B(k, j) = 0 for k < j,
+// k range trimmed); batches with a smaller last batch (ragged pairs).
 //
 // 256 threads per 128 x 128 tile, each an 8 x 8 register micro-tile (rows and
 // columns split 4 + 4 so shared-memory float4 reads are conflict free); k chunks of
@@ -36,7 +38,7 @@ struct GemmArgs {
   long long ldc, c_bs;
   float alpha, beta;
   int lower_tiles;        // C square: only tiles with J <= I
-  int a_lower;            // A(i, k) == 0 for k > i
+  int a_tri;              // 1: A lower triangular, 2: A upper triangular (masked)
   int b_lower;            // B(k, j) == 0 for k < j
   int vec;                // every operand 16-byte aligned with leading dimensions % 4 == 0
   const int* skip;        // non-null and non-zero: do nothing (an earlier step failed)
@@ -50,9 +52,14 @@ __device__ __forceinline__ int micro_row(int t, int ty) { return (t < 4) ? ty * 
 
 // Load a BK x TILE chunk (k in [k0, k0 + BK), r in [r0, r0 + TILE)) of one operand into
 // 8 registers per thread. Element (r, k) is P[k * ld + r] (MN-major) or P[r * ld + k].
+// tri: 0 none, 1 keep k <= r, 2 keep k >= r (r, k: the element's row and k index)
+__device__ __forceinline__ bool tri_keep(int tri, int r, int k) {
+  return tri == 0 || (tri == 1 ? k <= r : k >= r);
+}
+
 template <bool KMAJ>
 __device__ __forceinline__ void load_chunk(const float* __restrict__ P, long long ld, int r0, int R, int k0, int Kend,
-                                           bool vec, float (&v)[8]) {
+                                           bool vec, float (&v)[8], int tri = 0) {
   const int t = threadIdx.x;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -66,6 +73,11 @@ __device__ __forceinline__ void load_chunk(const float* __restrict__ P, long lon
 #pragma unroll
         for (int c = 0; c < 4; ++c) v[4 * h + c] = (k < Kend && rr + c < R) ? P[(long long)k * ld + rr + c] : 0.0f;
       }
+      if (tri) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          if (!tri_keep(tri, rr + c, k)) v[4 * h + c] = 0.0f;
+      }
     } else {
       const int r = t / 4 + 64 * h, kk = (t % 4) * 4;
       const int k = k0 + kk, rr = r0 + r;
@@ -75,6 +87,11 @@ __device__ __forceinline__ void load_chunk(const float* __restrict__ P, long lon
       } else {
 #pragma unroll
         for (int c = 0; c < 4; ++c) v[4 * h + c] = (rr < R && k + c < Kend) ? P[(long long)rr * ld + k + c] : 0.0f;
+      }
+      if (tri) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          if (!tri_keep(tri, rr, k + c)) v[4 * h + c] = 0.0f;
       }
     }
   }
@@ -123,8 +140,9 @@ __global__ void __launch_bounds__(THREADS) gemm_kernel(GemmArgs g) {
   const float* __restrict__ B = g.B + (long long)z * g.b_bs;
   float* __restrict__ C = g.C + (long long)z * g.c_bs;
   int kbeg = 0, kend = K;
-  if (g.a_lower) kend = min(kend, i0 + TILE);
-  if (g.b_lower) kbeg = j0;
+  if (g.a_tri == 1) kend = min(kend, i0 + TILE);
+  if (g.a_tri == 2) kbeg = i0;
+  if (g.b_lower) kbeg = max(kbeg, j0);
   const bool vec = g.vec != 0;
 
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
@@ -136,7 +154,7 @@ __global__ void __launch_bounds__(THREADS) gemm_kernel(GemmArgs g) {
 
   float va[8], vb[8];
   if (kbeg < kend) {
-    load_chunk<A_KMAJ>(A, g.lda, i0, M, kbeg, kend, vec, va);
+    load_chunk<A_KMAJ>(A, g.lda, i0, M, kbeg, kend, vec, va, g.a_tri);
     load_chunk<B_KMAJ>(B, g.ldb, j0, N, kbeg, kend, vec, vb);
     store_chunk<A_KMAJ>(As[0], va);
     store_chunk<B_KMAJ>(Bs[0], vb);
@@ -146,7 +164,7 @@ __global__ void __launch_bounds__(THREADS) gemm_kernel(GemmArgs g) {
   for (int k0 = kbeg; k0 < kend; k0 += BK) {
     const bool more = k0 + BK < kend;
     if (more) {
-      load_chunk<A_KMAJ>(A, g.lda, i0, M, k0 + BK, kend, vec, va);
+      load_chunk<A_KMAJ>(A, g.lda, i0, M, k0 + BK, kend, vec, va, g.a_tri);
       load_chunk<B_KMAJ>(B, g.ldb, j0, N, k0 + BK, kend, vec, vb);
     }
 #pragma unroll

@@ -50,7 +50,7 @@ constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 struct Params {
   int M, N, K, M_last, K_last, batches;
   int tiles_per_batch, mt, nt;
-  int lower_tiles, a_lower, b_lower;
+  int lower_tiles, a_tri, b_lower;
   float alpha, beta;
   float* C;
   long long ldc, c_bs;
@@ -80,8 +80,9 @@ __device__ __forceinline__ Tile decode(int t, const Params& p) {
   w.K = last ? p.K_last : p.K;
   w.kbeg = 0;
   w.kend = w.K;
-  if (p.a_lower) w.kend = min(w.kend, (w.I + 1) * BM);
-  if (p.b_lower) w.kbeg = w.J * BN;
+  if (p.a_tri == 1) w.kend = min(w.kend, (w.I + 1) * BM);
+  if (p.a_tri == 2) w.kbeg = w.I * BM;
+  if (p.b_lower) w.kbeg = max(w.kbeg, w.J * BN);
   if (w.kbeg >= w.kend || w.I * BM >= w.M) w.kend = w.kbeg;   // nothing to multiply
   return w;
 }
@@ -107,14 +108,34 @@ __device__ __forceinline__ void load_operand(uint8_t* dst, const CUtensorMap* ma
 }
 
 // x -> (hi, lo) for one operand's chunk, hi written in place; elements with k >= kend
-// are zeroed in both buffers. `kbase` is the chunk's first k.
+// are zeroed in both buffers, and so are those outside the triangle `tri` (1: keep
+// k <= row, 2: keep k >= row; K-major operands, rows counted from row0). `kbase` is the
+// chunk's first k.
 template <bool KMAJ>
-__device__ __forceinline__ void split_operand(uint8_t* raw, uint8_t* lo, int kbase, int kend, int ctid) {
+__device__ __forceinline__ void split_operand(uint8_t* raw, uint8_t* lo, int kbase, int kend, int ctid, int tri = 0,
+                                              int row0 = 0) {
   float4* r4 = reinterpret_cast<float4*>(raw);
   float4* l4 = reinterpret_cast<float4*>(lo);
   const bool ragged = kbase + BK > kend;
+  // the chunk meets the tile's diagonal band only if [kbase, kbase + BK) overlaps [row0, row0 + BM)
+  const bool diag = KMAJ && tri != 0 && kbase < row0 + BM && kbase + BK > row0;
   for (int idx = ctid; idx < OP_BYTES / 16; idx += NCONV * 32) {
     float4 x = r4[idx];
+    if (diag) {
+      const int row = idx >> 3, lc = (idx & 7) ^ (row & 7);
+      const int k0 = kbase + 4 * lc, r = row0 + row;
+      if (tri == 1) {
+        if (k0 + 0 > r) x.x = 0.0f;
+        if (k0 + 1 > r) x.y = 0.0f;
+        if (k0 + 2 > r) x.z = 0.0f;
+        if (k0 + 3 > r) x.w = 0.0f;
+      } else {
+        if (k0 + 0 < r) x.x = 0.0f;
+        if (k0 + 1 < r) x.y = 0.0f;
+        if (k0 + 2 < r) x.z = 0.0f;
+        if (k0 + 3 < r) x.w = 0.0f;
+      }
+    }
     if (ragged) {
       // 16-byte chunk idx: byte offset idx * 16
       int k_of_elem0, step;
@@ -223,7 +244,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       for (int k0 = w.kbeg; k0 < w.kend; k0 += BK) {
         if (!mbar_wait_bounded(&full[stage], phase, abort_flag)) { ok = false; break; }
         uint8_t* sa = smem + stage * STAGE_BYTES;
-        split_operand<A_KMAJ>(sa, sa + 2 * OP_BYTES, k0, w.kend, ctid);
+        split_operand<A_KMAJ>(sa, sa + 2 * OP_BYTES, k0, w.kend, ctid, p.a_tri, w.I * BM);
         split_operand<B_KMAJ>(sa + OP_BYTES, sa + 3 * OP_BYTES, k0, w.kend, ctid);
         fence_proxy_async_smem();   // generic-proxy writes must be visible to the tensor core
         __syncwarp();
@@ -428,7 +449,7 @@ gptq_status tc_gemm(const simt::GemmArgs& g, int batches, bool a_kmaj, bool b_km
   p.mt = (g.M + BM - 1) / BM;
   p.nt = (g.N + BN - 1) / BN;
   p.tiles_per_batch = g.lower_tiles ? p.mt * (p.mt + 1) / 2 : p.mt * p.nt;
-  p.lower_tiles = g.lower_tiles; p.a_lower = g.a_lower; p.b_lower = g.b_lower;
+  p.lower_tiles = g.lower_tiles; p.a_tri = g.a_tri; p.b_lower = g.b_lower;
   p.alpha = g.alpha; p.beta = g.beta;
   p.C = g.C; p.ldc = g.ldc; p.c_bs = g.c_bs;
   p.skip = g.skip;
