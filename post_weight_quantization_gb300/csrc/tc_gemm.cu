@@ -45,7 +45,9 @@ constexpr int CONV_WARP0 = 2, NCONV = 4;
 constexpr int EPI_WARP0 = 6, NEPI = 8;
 constexpr int NBUF = 4;                       // chunk accumulators in tensor memory
 constexpr uint32_t TMEM_COLS = NBUF * BN;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+constexpr int EPI_LD = 33;                    // padded row of an epilogue warp's 32 x 32 staging tile
+constexpr int EPI_BYTES = NEPI * 32 * EPI_LD * 4;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256 + EPI_BYTES;
 
 struct Params {
   int M, N, K, M_last, K_last, batches;
@@ -183,6 +185,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   uint64_t* drain = tmem_empty + NBUF;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* epi_stage = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES + 256);   // NEPI x 32 x EPI_LD
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -324,40 +327,36 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         if (lane == 0) mbar_arrive(&tmem_empty[buf]);
       }
       if (!ok) break;
-      const int i = w.I * BM + q * 32 + lane;
-      if (w.I * BM < w.M && i < w.M) {
-        float* crow = p.C + (long long)w.z * p.c_bs + (long long)i * p.ldc;
-        const int j0 = w.J * BN + h * 64;
-        if (j0 + 63 < p.N) {
-          // 32 columns at a time: every load is issued before any store, so a tile
-          // costs one memory round trip per half instead of one per float4
+      // C = beta C + alpha acc through a 32 x 32 staging tile per warp: lane = row while
+      // reading tensor memory, lane = column while touching C, so every load and store
+      // of C is one contiguous 128-byte row segment
+      float* stg = epi_stage + (warp - EPI_WARP0) * 32 * EPI_LD;
+      const int rbase = w.I * BM + q * 32;
+      float* cbase = p.C + (long long)w.z * p.c_bs;
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            float4 o[8];
-            float4* cp = reinterpret_cast<float4*>(crow + j0 + 32 * half);
+      for (int g2 = 0; g2 < 2; ++g2) {
 #pragma unroll
-            for (int x = 0; x < 8; ++x) o[x] = (p.beta != 0.0f) ? __ldcg(cp + x) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c = 0; c < 32; ++c) stg[lane * EPI_LD + c] = acc[32 * g2 + c];
+        __syncwarp();
+        const int j = w.J * BN + h * 64 + 32 * g2 + lane;
+        float o[32];
+        if (p.beta != 0.0f) {
 #pragma unroll
-            for (int x = 0; x < 8; ++x) {
-              const int b = 32 * half + 4 * x;
-              o[x].x = fmaf(p.alpha, acc[b], p.beta * o[x].x);
-              o[x].y = fmaf(p.alpha, acc[b + 1], p.beta * o[x].y);
-              o[x].z = fmaf(p.alpha, acc[b + 2], p.beta * o[x].z);
-              o[x].w = fmaf(p.alpha, acc[b + 3], p.beta * o[x].w);
-            }
-#pragma unroll
-            for (int x = 0; x < 8; ++x) __stcg(cp + x, o[x]);
+          for (int r = 0; r < 32; ++r) {
+            const int i = rbase + r;
+            o[r] = (i < w.M && j < p.N) ? __ldcg(cbase + (long long)i * p.ldc + j) : 0.0f;
           }
         } else {
 #pragma unroll
-          for (int x = 0; x < 64; ++x) {
-            const int j = j0 + x;
-            if (j < p.N) {
-              const float old = (p.beta != 0.0f) ? crow[j] : 0.0f;
-              crow[j] = fmaf(p.alpha, acc[x], p.beta * old);
-            }
-          }
+          for (int r = 0; r < 32; ++r) o[r] = 0.0f;
         }
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+          const int i = rbase + r;
+          if (i < w.M && j < p.N)
+            __stcg(cbase + (long long)i * p.ldc + j, fmaf(p.alpha, stg[r * EPI_LD + lane], p.beta * o[r]));
+        }
+        __syncwarp();
       }
     }
   }
