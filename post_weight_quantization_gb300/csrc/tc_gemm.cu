@@ -17,13 +17,14 @@
 //               128-byte swizzle permutes 16-byte chunks, so an elementwise pass keeps
 //               the layout), zeroing k past the extent of a ragged last batch
 //   warp 1      MMA issuer: per chunk 4 k-steps x 3 products, tcgen05.mma kind::tf32
-//               M = 128, N = 128, K = 8, into a fresh tensor-memory buffer (four
-//               buffers of 128 columns rotate, so the products run ahead of the
-//               epilogue's memory traffic)
-//   warps 6-13  epilogue: each chunk's partial product is added into fp32 registers
+//               M = 128, N = 128, K = 8; two chunks (64 products) go into one
+//               tensor-memory buffer, four buffers of 128 columns rotate, so the
+//               products of the next tile run ahead of the epilogue's memory traffic
+//   warps 6-13  epilogue: each buffer's partial product is added into fp32 registers
 //               with round-to-nearest (the tensor core's own accumulator truncates, so
 //               long accumulations in it drift), and at the end of a tile
-//               C = beta C + alpha acc is written
+//               C = beta C + alpha acc is written through a shared-memory staging
+//               tile in 128-byte rows
 // Every wait is bounded; a timeout raises the device error word.
 #include <cudaTypedefs.h>
 
@@ -44,6 +45,7 @@ constexpr int THREADS = 14 * 32;
 constexpr int CONV_WARP0 = 2, NCONV = 4;
 constexpr int EPI_WARP0 = 6, NEPI = 8;
 constexpr int NBUF = 4;                       // chunk accumulators in tensor memory
+constexpr int ACC_CHUNKS = 2;                 // 32-deep chunks summed in one accumulator (64 products)
 constexpr uint32_t TMEM_COLS = NBUF * BN;
 constexpr int EPI_LD = 33;                    // padded row of an epilogue warp's 32 x 32 staging tile
 constexpr int EPI_BYTES = NEPI * 32 * EPI_LD * 4;
@@ -264,9 +266,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     const uint32_t sbase = smem_u32(smem);
     for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
       const Tile w = decode(t, p);
-      for (int k0 = w.kbeg; k0 < w.kend; k0 += BK, ++it) {
+      int cin = 0;                                 // chunk index within the tile
+      for (int k0 = w.kbeg; k0 < w.kend; k0 += BK, ++cin) {
+        const bool first = (cin % ACC_CHUNKS) == 0;
+        const bool last = (cin % ACC_CHUNKS) == ACC_CHUNKS - 1 || k0 + BK >= w.kend;
         const uint32_t buf = it % NBUF;
-        if (!mbar_wait_bounded(&tmem_empty[buf], ((it / NBUF) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+        if (first && !mbar_wait_bounded(&tmem_empty[buf], ((it / NBUF) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
         if (!mbar_wait_bounded(&conv[stage], phase, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * BN;
@@ -278,13 +283,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
           const uint64_t dal = A_KMAJ ? desc_kmaj(alo, kk) : desc_mnmaj(alo, kk);
           const uint64_t db = B_KMAJ ? desc_kmaj(b, kk) : desc_mnmaj(b, kk);
           const uint64_t dbl = B_KMAJ ? desc_kmaj(blo, kk) : desc_mnmaj(blo, kk);
-          umma_tf32(d_tmem, da, dbl, IDESC, kk > 0 ? 1u : 0u);
+          umma_tf32(d_tmem, da, dbl, IDESC, (kk > 0 || !first) ? 1u : 0u);
           umma_tf32(d_tmem, dal, db, IDESC, 1u);
           umma_tf32(d_tmem, da, db, IDESC, 1u);
         }
         issued = true;
         umma_commit(&empty[stage]);
-        umma_commit(&tmem_full[buf]);
+        if (last) {
+          umma_commit(&tmem_full[buf]);
+          ++it;
+        }
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
     }
@@ -304,7 +312,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       float acc[64];
 #pragma unroll
       for (int x = 0; x < 64; ++x) acc[x] = 0.0f;
-      const int nc = nchunks(w);
+      const int nc = (nchunks(w) + ACC_CHUNKS - 1) / ACC_CHUNKS;   // accumulators of this tile
       for (int c = 0; c < nc; ++c, ++it) {
         const uint32_t buf = it % NBUF;
         if (!mbar_wait_bounded(&tmem_full[buf], (it / NBUF) & 1u, abort_flag)) {
