@@ -97,7 +97,8 @@ def oracle_sample(wl, layer, X_bits_sample, W_bits_rows, n_total, rows_total):
     from synth import bf16_bits_to_f32
 
     t0 = time.perf_counter()
-    Hs = orc.hessian([bf16_bits_to_f32(X_bits_sample)])
+    step = 16384        # the oracle's batches, so a large sample never needs one float64 copy
+    Hs = orc.hessian(bf16_bits_to_f32(X_bits_sample[i:i + step]) for i in range(0, X_bits_sample.shape[0], step))
     t1 = time.perf_counter()
     Hd, _ = orc.damp(Hs, wl.percdamp)
     perm = orc.act_order_perm(Hs) if wl.act_order else np.arange(Hs.shape[0])
@@ -380,8 +381,9 @@ def run_gpu(args):
     # ---- CPU oracle baseline (rank 0, N = 1 only), bounded sample
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n_s = min(n, 2 * CHUNK)
-        rows = min(m, 32)
+        # about 10 s of host work: 1/2 of the tokens, the full factor, 1/8 of the rows
+        n_s = min(n, max(2 * CHUNK, (n // 2) // CHUNK * CHUNK))
+        rows = min(m, max(32, m // 8))
         r = oracle_sample(wl, layer, X_host.numpy().view(np.uint16)[:n_s], W_bits[:rows], n, m)
         cpu = {"value": round(weights / r["total_s"] / 1e6, 6), "unit": "Mweights/s", "cores": blas_threads(),
                "kind": "oracle",

@@ -300,7 +300,7 @@ class HostPipeline:
     """
 
     def __init__(self, m: int, d: int, bits: int = 4, group_size: int = 128, blocksize: int = 128,
-                 percdamp: float = 0.01, act_order: bool = False, chunk_tokens: int = 16384,
+                 percdamp: float = 0.01, act_order: bool = False, chunk_tokens: int = 32768,
                  w_dtype=torch.bfloat16, device="cuda"):
         self.m, self.d, self.bits, self.group_size, self.blocksize = m, d, bits, group_size, blocksize
         self.percdamp, self.act_order, self.chunk = percdamp, act_order, chunk_tokens
@@ -328,6 +328,7 @@ class HostPipeline:
         self.copy_stream = torch.cuda.Stream(device=dev)
         self.copied = [torch.cuda.Event() for _ in range(2)]
         self.consumed = [torch.cuda.Event() for _ in range(2)]
+        self.w_copied = torch.cuda.Event()
 
     def bytes_h2d(self, n_tokens: int) -> int:
         return n_tokens * self.d * 2 + self.W.numel() * self.W.element_size()
@@ -342,6 +343,7 @@ class HostPipeline:
         comp = torch.cuda.current_stream() if stream is None else stream
         n = X_host.shape[0]
         first = True
+        self.copy_stream.wait_stream(comp)          # earlier work on the caller's stream first
         for c, t0 in enumerate(range(0, n, self.chunk)):
             t1 = min(n, t0 + self.chunk)
             b = c & 1
@@ -355,10 +357,12 @@ class HostPipeline:
             gptq_hessian_accumulate(buf, self.H, alpha=2.0, zero_first=first, stream=comp)
             self.consumed[b].record(comp)
             first = False
-        with torch.cuda.stream(comp):
+        with torch.cuda.stream(self.copy_stream):       # W behind the last token chunk
             self.W.copy_(W_host, non_blocking=True)
+            self.w_copied.record(self.copy_stream)
         gptq_factor(self.H, percdamp=self.percdamp, act_order=self.act_order, Hinv1=self.Hinv1, perm_out=self.perm,
                     ws=self.ws_f, sync=False, stream=comp)
+        comp.wait_event(self.w_copied)
         gptq_quantize_layer(self.W, self.Hinv1, self.perm, bits=self.bits, group_size=self.group_size,
                             blocksize=self.blocksize, out=self.out, ws=self.ws_q, stream=comp)
         with torch.cuda.stream(comp):

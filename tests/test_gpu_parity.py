@@ -330,3 +330,34 @@ def test_launch_counter_moves(g):
     torch.cuda.synchronize()
     assert g.gptq_launch_count() > before
     assert float(torch.triu(H).abs().max()) == 0.0
+
+
+@pytest.mark.parametrize("act_order", [False, True])
+def test_host_pipeline_matches_oracle(g, act_order):
+    """The end-to-end host-buffer API: tokens streamed from pinned memory in chunks (two
+    device buffers, a ragged last chunk), W copied, factor and column loop, results
+    copied back; run twice on the same pipeline object."""
+    m, d, n, bits = 520, 768, 3 * 4096 + 1000, 4
+    gs = -1 if act_order else 128
+    W_bits = make_weight(m, d, 41)
+    X_bits = make_activations(ActSpec("heavy_tail", n, d, seed=41))
+    pipe = g.HostPipeline(m, d, bits=bits, group_size=gs, blocksize=128, act_order=act_order, chunk_tokens=4096)
+    W_host = torch.from_numpy(W_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    X_host = torch.from_numpy(X_bits.view(np.int16)).pin_memory()
+    H = orc.hessian([bf16_bits_to_f32(X_bits)])
+    W = bf16_bits_to_f32(W_bits)
+    res64 = orc.gptq_layer(W.astype(np.float64), H, bits, gs, 128, 0.01, act_order)
+    res32 = orc.gptq_layer(W, H.astype(np.float32), bits, gs, 128, 0.01, act_order, dtype=np.float32)
+    for _ in range(2):
+        out = pipe.run(W_host, X_host)
+        torch.cuda.synchronize()
+        g.gptq_device_check()
+        codes = orc.unpack_codes(out.qweight.numpy().view(np.uint32), bits, d).astype(np.int64)
+        p = pipe.perm.cpu().numpy().astype(np.int64) if act_order else None
+        if act_order and not np.array_equal(p, res64["perm"]):
+            hx = np.diag(H)
+            assert np.all(np.abs(hx[p] - hx[res64["perm"]]) <= 1e-6 * hx.max())
+        check_layer(W.astype(np.float64), res64, res32, codes, out.scales.numpy().astype(np.float64),
+                    out.zeros.numpy().astype(np.float64), H, bits, gs, p)
+        total = float(out.col_losses.numpy().astype(np.float64).sum())
+        assert abs(total - float(np.sum(res64["col_losses"]))) <= 1e-2 * total
