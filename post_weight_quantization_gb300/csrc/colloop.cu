@@ -195,7 +195,9 @@ struct CBArgs {
   float* scales;
   float* zeros;
   int G;
-  float* err;                 // mpad x BS
+  float* err;                 // Err1 of the current outer block: mpad x eld, row-major
+  int eld;                    // row stride of err (the outer block width)
+  int eoff;                   // this block's first column within err
   float* part;                // loss partials, one row of d per CTA
   int bulk;                   // U rows 16-byte aligned: bulk asynchronous copies
   int vecw;                   // Wf rows 16-byte aligned: vector loads
@@ -392,7 +394,7 @@ __global__ void __launch_bounds__(CB_THREADS, 1) colblock_kernel(CBArgs a) {
   constexpr int ELD = SL::ELD, CLD = SL::CLD;
   for (int idx = tid; idx < ROWS_PER_CTA * BS; idx += CB_THREADS) {
     const int rr = idx / BS, t = idx % BS;
-    if (t < ncols && r0 + rr < a.m) a.err[(long long)(r0 + rr) * BS + t] = Es[rr * ELD + t];
+    if (t < ncols && r0 + rr < a.m) a.err[(long long)(r0 + rr) * a.eld + a.eoff + t] = Es[rr * ELD + t];
   }
   for (int t = tid; t < ncols; t += CB_THREADS) {
     float lsum = 0.0f;
@@ -489,6 +491,23 @@ __global__ void transpose_kernel(const float* __restrict__ U, float* __restrict_
   }
 }
 
+// The lazy update is blocked on two levels. After a block of BS columns, only the
+// columns up to the end of its outer block of OUTER columns move (K = BS); after an
+// outer block, every column right of it moves at once by Err1 of the whole outer block
+// (K = OUTER). In exact arithmetic this is the pages' update, W[:, i2:] -= Err1 @
+// Hinv1[i1:i2, i2:] after every block, summed in another order: each column still
+// receives every earlier column's correction before it is quantized, and a group's
+// columns are current when its statistics are read, because an outer block holds
+// whole groups. The wide products read and write W's right part once per outer block
+// instead of once per block.
+constexpr int OUTER = 1024;
+
+// Outer block width: OUTER when it holds whole blocks and whole groups, else one block.
+inline int outer_width(int BS, int g, int stats_given) {
+  const bool groups_fit = stats_given || (g > 0 && OUTER % g == 0);
+  return (OUTER % BS == 0 && groups_fit) ? OUTER : BS;
+}
+
 struct Layout {
   size_t hdr, wf, err, ut, part, codes8, inv, dinfo, total;
   int nrg;
@@ -502,7 +521,7 @@ Layout layout(long long m, long long d, int blocksize) {
   L.hdr = 0;
   L.wf = kHeaderBytes;
   L.err = L.wf + al((size_t)m * d * 4);
-  L.ut = L.err + al(mpad * (size_t)blocksize * 4);
+  L.ut = L.err + al(mpad * (size_t)std::max(OUTER, blocksize) * 4);
   L.part = L.ut + al((size_t)d * d * 4);
   L.codes8 = L.part + al((size_t)L.nrg * d * 4);
   L.inv = L.codes8 + al((size_t)m * d);
@@ -519,28 +538,38 @@ gptq_status run_blocks(CBArgs a, const float* Ut, cudaStream_t s) {
     return set_error(GPTQ_ERR_CUDA, "cudaFuncSetAttribute(colblock_kernel) failed");
   const int m = a.m, d = a.d;
   const int nrg = (m + ROWS_PER_CTA - 1) / ROWS_PER_CTA;
-  for (int i1 = 0; i1 < d; i1 += BS) {
-    const int nb = std::min(BS, d - i1);
-    a.i1 = i1;
-    {
-      ProfScope ps("quantize.colblock", s);
-      if (launch_pdl(colblock_kernel<BS>, dim3(nrg), dim3(CB_THREADS), SL::total, s, a) != cudaSuccess)
-        return check_launch("colblock_kernel");
-      count_launch();
+  const int OB = outer_width(BS, a.g, a.stats_given);
+  const bool vec = (d % 4 == 0) && simt::aligned16(a.Wf) && simt::aligned16(Ut) && simt::aligned16(a.err);
+  a.eld = OB;
+  // W[:, c0:c1] -= Err1[:, e0:e0+K] @ Hinv1[k0:k0+K, c0:c1];  B(k, j) = Ut[c0 + j][k0 + k]
+  auto lazy = [&](int e0, int k0, int K, int c0, int c1) -> gptq_status {
+    simt::GemmArgs ga{};
+    ga.M = m; ga.N = c1 - c0; ga.K = K; ga.M_last = m; ga.K_last = K;
+    ga.A = a.err + e0; ga.lda = OB;
+    ga.B = Ut + (long long)c0 * d + k0; ga.ldb = d;
+    ga.C = const_cast<float*>(a.Wf) + c0; ga.ldc = d;
+    ga.alpha = -1.0f; ga.beta = 1.0f;
+    ga.vec = vec;
+    ProfScope ps2("quantize.lazy_gemm", s);
+    return tc_gemm(ga, 1, true, true, s);
+  };
+  for (int o1 = 0; o1 < d; o1 += OB) {
+    const int o2 = std::min(o1 + OB, d);
+    for (int i1 = o1; i1 < o2; i1 += BS) {
+      const int nb = std::min(BS, o2 - i1), i2 = i1 + nb;
+      a.i1 = i1;
+      a.eoff = i1 - o1;
+      {
+        ProfScope ps("quantize.colblock", s);
+        if (launch_pdl(colblock_kernel<BS>, dim3(nrg), dim3(CB_THREADS), SL::total, s, a) != cudaSuccess)
+          return check_launch("colblock_kernel");
+        count_launch();
+      }
+      if (i2 < o2)   // the rest of this outer block
+        if (gptq_status st = lazy(i1 - o1, i1, nb, i2, o2)) return st;
     }
-    const int i2 = i1 + nb;
-    if (i2 < d) {
-      // W[:, i2:] -= Err1 @ Hinv1[i1:i2, i2:];  A = Err1 (rows of BS), B(k, j) = Ut[i2 + j][i1 + k]
-      simt::GemmArgs ga{};
-      ga.M = m; ga.N = d - i2; ga.K = nb; ga.M_last = m; ga.K_last = nb;
-      ga.A = a.err; ga.lda = BS;
-      ga.B = Ut + (long long)i2 * d + i1; ga.ldb = d;
-      ga.C = const_cast<float*>(a.Wf) + i2; ga.ldc = d;
-      ga.alpha = -1.0f; ga.beta = 1.0f;
-      ga.vec = (d % 4 == 0) && simt::aligned16(a.Wf) && simt::aligned16(Ut) && simt::aligned16(a.err);
-      ProfScope ps2("quantize.lazy_gemm", s);
-      if (gptq_status st = tc_gemm(ga, 1, true, true, s)) return st;
-    }
+    if (o2 < d)      // everything right of the outer block
+      if (gptq_status st = lazy(0, o1, o2 - o1, o2, d)) return st;
   }
   return check_launch("column-loop kernels");
 }

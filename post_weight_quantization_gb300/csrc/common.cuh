@@ -258,6 +258,15 @@ __device__ __forceinline__ void load_tile(float* __restrict__ dst, int ldd, cons
   }
 }
 
+// 16-byte asynchronous copy global -> shared (both addresses 16-byte aligned); many
+// can be in flight per thread. cp_async_wait_all waits for this thread's copies.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 // Programmatic dependent launch. A kernel launched with launch_pdl may start while the
 // kernel before it in the stream is still running; it must call grid_dep_wait (which
 // returns once that kernel has completed and its writes are visible, and at once when

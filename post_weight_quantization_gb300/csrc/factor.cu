@@ -17,10 +17,10 @@
 //   diag_stats      lambda and the finiteness check of diag(H)
 //   perm_rank       stable descending sort of diag(H) by rank counting (act-order)
 //   gather          P[a][b] = H_d[p(d-1-a)][p(d-1-b)] (lower triangle), p = act-order
-//   Cholesky, 64-wide blocks, right-looking:
-//     chol_panel    one launch per 64-wide panel: every CTA factors the diagonal block
-//                   together with 64 rows below it, right-looking in 8-column steps in
-//                   shared memory; CTA 0 writes L11, the others their rows of L21
+//   Cholesky, 128-wide blocks, right-looking:
+//     chol_panel    one launch per 128-wide panel: every CTA factors the diagonal block
+//                   (32-column tall panels in one warp's registers) and solves 32 rows
+//                   below it; CTA 0 writes L11, the others their rows of L21
 //     tc_gemm       trailing update A22 -= L21 L21^T (lower tiles; tensor cores,
 //                   3 x TF32, both operands K-major)
 //   Triangular inverse X = L^-1 (natural order, inside Hinv1):
@@ -43,7 +43,6 @@
 namespace gptq {
 namespace factor {
 
-constexpr int NB = 64;        // panel width
 
 struct Header {               // at the start of the factor workspace
   float lambda;
@@ -51,6 +50,7 @@ struct Header {               // at the start of the factor workspace
   int fail_pivot;             // INT_MAX when the factorization succeeded
   int d;
   int failed;                 // non-zero once a pivot failed or diag(H) is not finite
+  int timeout;                // a bounded wait gave up
 };
 constexpr size_t kHeaderBytes = 256;
 
@@ -79,6 +79,7 @@ __global__ void diag_stats_kernel(const float* __restrict__ H, int d, float perc
     hdr->fail_pivot = INT_MAX;
     hdr->d = d;
     hdr->failed = bad_s;
+    hdr->timeout = 0;
   }
 }
 
@@ -118,20 +119,29 @@ __global__ void gather_kernel(const float* __restrict__ H, int d, const int* __r
 }
 
 // ---------------------------------------------------------------------------------
-// One Cholesky step for the 64-wide panel at k0, in one launch. Every CTA factors the
-// tall panel made of the 64 x 64 diagonal block and (CTA b >= 1) rows
-// [k1 + 64 (b - 1), + 64) below it, right-looking in steps of 8 columns, all in shared
-// memory:
-//   (a) warp 0 factors the step's 8 columns of the diagonal block (lane i holding rows
-//       i and i + 32, pivots and column values broadcast by shuffles);
-//   (b) 64 threads solve the same 8 columns of the rows below (x L^T = a);
-//   (c) all threads subtract the step's rank-8 product from the columns to its right.
-// The diagonal block's arithmetic is the same in every CTA, so every copy agrees;
-// CTA 0 writes it back, the others write their rows. A ragged last block is padded
+// One Cholesky step for the 128-wide panel at k0, in one launch. Every CTA factors the
+// 128 x 128 diagonal block (the same arithmetic in every CTA, so every copy agrees;
+// CTA 0 keeps it) and CTA b >= 1 also solves the rows [k1 + 32 (b - 1), + 32) below it
+// (R), all in shared memory. The diagonal block goes in four sub-panels of 32 columns;
+// for sub-panel p, with barriers between the phases:
+//   A  warp 0: L[p][p] = chol(S[p][p]) in registers (lane i holds row i); column j of L
+//      is broadcast through shared memory (Lt[j][*]), the next pivot's own update stays
+//      in its lane, so a column costs one shuffle, one reciprocal square root and a few
+//      dependent operations. Meanwhile warps 1-7 finish the previous sub-panel's
+//      trailing update (every block but the one factored now);
+//   B  one warp per row group (sub-panels i > p of the diagonal block, then R): the
+//      group's 32 x 32 piece of column block p solves x L[p][p]^T = a by forward
+//      substitution, one row per lane;
+//   C  the next diagonal sub-block loses the new sub-panel's product (the one update the
+//      next Cholesky waits for).
+// Values above the diagonal of S are never read as L. A ragged last block is padded
 // with the identity.
+constexpr int NB = 128;                        // panel width
+constexpr int SB = 32;                         // sub-panel width
+constexpr int RB = 32;                         // rows below per CTA
 constexpr int PANEL_THREADS = 256;
-constexpr int PLD = NB + 1;                    // padded row of the shared tiles
-constexpr int PS = 8;                          // columns per step
+constexpr int SLD = NB + 4;                    // padded row of the shared tiles (rows stay 16-byte aligned)
+constexpr int TLD = SB + 4;                    // padded row of Lt
 
 // 1 / sqrt(x) for x > 0: the hardware estimate refined by one Newton step
 // y <- y (3 - x y^2) / 2 (about one ulp); no call, no slow path.
@@ -148,116 +158,259 @@ __device__ __forceinline__ float rcp_nr(float x) {
   return fmaf(y, fmaf(-x, y, 1.0f), y);
 }
 
-// Step (a): columns [pc, pc + 8) of the diagonal block, rows pc..63, by one warp.
-template <int... Js>
-__device__ __forceinline__ void panel8(std::integer_sequence<int, Js...>, float* A, float* dinv, int pc, int lane,
-                                       int& fail) {
-  const int r0 = lane, r1 = lane + 32;
-  float v0[PS], v1[PS];
+// Bulk asynchronous copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from global to shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+// v[c] -= f * Lt[j][c] for c in (j, 32): float4 broadcasts from the aligned piece that
+// holds column j + 1 on (columns <= j in that piece are left alone)
+template <int J>
+__device__ __forceinline__ void axpy_tail(float (&v)[SB], float f, const float* __restrict__ lrow) {
 #pragma unroll
-  for (int c = 0; c < PS; ++c) {
-    v0[c] = (r0 >= pc + c) ? A[r0 * PLD + pc + c] : 0.0f;
-    v1[c] = (r1 >= pc + c) ? A[r1 * PLD + pc + c] : 0.0f;
-  }
-  const bool hi = pc >= 32;                    // warp-uniform: the step's pivots lie in rows 32..63
-  auto step = [&](auto jc) {
-    constexpr int jj = decltype(jc)::value;
-    const int j = pc + jj;
-    const float piv = __shfl_sync(0xffffffffu, hi ? v1[jj] : v0[jj], j & 31);
-    if (!(piv > 0.0f && piv < INFINITY) && fail < 0) fail = j;
-    const float inv = rsqrt_nr(piv);
-    const float l0 = v0[jj] * inv, l1 = v1[jj] * inv;
-#pragma unroll
-    for (int cc = jj + 1; cc < PS; ++cc) {
-      const int c = pc + cc;
-      const float lc = __shfl_sync(0xffffffffu, hi ? l1 : l0, c & 31);   // L[c][j]
-      v0[cc] = (r0 >= c) ? fmaf(-l0, lc, v0[cc]) : v0[cc];
-      v1[cc] = (r1 >= c) ? fmaf(-l1, lc, v1[cc]) : v1[cc];
-    }
-    v0[jj] = (r0 == j) ? piv * inv : ((r0 > j) ? l0 : v0[jj]);
-    v1[jj] = (r1 == j) ? piv * inv : ((r1 > j) ? l1 : v1[jj]);
-    if (lane == 0) dinv[j] = inv;
-  };
-  (step(std::integral_constant<int, Js>{}), ...);
-#pragma unroll
-  for (int c = 0; c < PS; ++c) {
-    if (r0 >= pc + c) A[r0 * PLD + pc + c] = v0[c];
-    if (r1 >= pc + c) A[r1 * PLD + pc + c] = v1[c];
+  for (int c4 = (J + 1) & ~3; c4 < SB; c4 += 4) {
+    const float4 q = *reinterpret_cast<const float4*>(lrow + c4);
+    if (c4 + 0 > J) v[c4 + 0] = fmaf(-f, q.x, v[c4 + 0]);
+    if (c4 + 1 > J) v[c4 + 1] = fmaf(-f, q.y, v[c4 + 1]);
+    if (c4 + 2 > J) v[c4 + 2] = fmaf(-f, q.z, v[c4 + 2]);
+    if (c4 + 3 > J) v[c4 + 3] = fmaf(-f, q.w, v[c4 + 3]);
   }
 }
 
-__global__ void __launch_bounds__(PANEL_THREADS) chol_panel_kernel(float* __restrict__ P, int d, int k0, Header* hdr) {
-  extern __shared__ float psm[];
-  float* A = psm;                      // 64 x PLD: the diagonal block, then L11 (lower)
-  float* Xs = A + NB * PLD;            // 64 x PLD: this CTA's rows of the panel below
-  float* dinv = Xs + NB * PLD;         // 64
+// Phase A, warp 0: S[c0..][c0..] (32 x 32) -> its Cholesky factor (lower), Lt[j][c] =
+// L[c][j], dinv[c0 + j] = 1 / L[j][j].
+template <int... Js>
+__device__ __forceinline__ void chol32(std::integer_sequence<int, Js...>, float* __restrict__ S, int c0,
+                                       float* __restrict__ Lt, float* __restrict__ dinv, int lane, int& fail) {
+  float v[SB];
+  float* row = S + (c0 + lane) * SLD + c0;
+#pragma unroll
+  for (int c = 0; c < SB; c += 4) {
+    const float4 q = *reinterpret_cast<const float4*>(row + c);
+    v[c] = q.x; v[c + 1] = q.y; v[c + 2] = q.z; v[c + 3] = q.w;
+  }
+  float piv = __shfl_sync(0xffffffffu, v[0], 0);
+  auto column = [&](auto jc) {
+    constexpr int j = decltype(jc)::value;
+    if (!(piv > 0.0f && piv < INFINITY) && fail < 0) fail = c0 + j;
+    const float inv = rsqrt_nr(piv);
+    const float l = v[j] * inv;                         // lane j: piv * inv = L[j][j]
+    if constexpr (j + 1 < SB) {
+      const float dn = fmaf(-l, l, v[j + 1]);           // lane j + 1: the next pivot
+      const float pn = __shfl_sync(0xffffffffu, dn, j + 1);
+      Lt[j * TLD + lane] = l;
+      __syncwarp();
+      axpy_tail<j>(v, l, Lt + j * TLD);
+      piv = pn;
+    }
+    v[j] = l;                                           // L[lane][j] (lane >= j)
+    if (lane == 0) dinv[c0 + j] = inv;
+  };
+  (column(std::integral_constant<int, Js>{}), ...);
+#pragma unroll
+  for (int c = 0; c < SB; c += 4) *reinterpret_cast<float4*>(row + c) = make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
+}
+
+// Phase B: row `lane` of a 32 x 32 piece (row stride SLD) solves x L^T = a, L = the
+// current diagonal sub-block, read as Lt.
+template <int... Js>
+__device__ __forceinline__ void solve32(std::integer_sequence<int, Js...>, float* __restrict__ A,
+                                        const float* __restrict__ Lt, const float* __restrict__ dinv, int lane) {
+  float r[SB];
+  float* row = A + lane * SLD;
+#pragma unroll
+  for (int c = 0; c < SB; c += 4) {
+    const float4 q = *reinterpret_cast<const float4*>(row + c);
+    r[c] = q.x; r[c + 1] = q.y; r[c + 2] = q.z; r[c + 3] = q.w;
+  }
+  auto column = [&](auto jc) {
+    constexpr int j = decltype(jc)::value;
+    r[j] *= dinv[j];
+    if constexpr (j + 1 < SB) axpy_tail<j>(r, r[j], Lt + j * TLD);
+  };
+  (column(std::integral_constant<int, Js>{}), ...);
+#pragma unroll
+  for (int c = 0; c < SB; c += 4) *reinterpret_cast<float4*>(row + c) = make_float4(r[c], r[c + 1], r[c + 2], r[c + 3]);
+}
+
+struct BlockTask {
+  float* C;
+  const float* A;
+  const float* B;
+};
+
+// C -= A B^T for one 4 x 4 piece of a 32 x 32 block (k < 32): rows ui + 8a and columns
+// uj + 8b, so the float4 reads of a quarter-warp fall in distinct banks.
+__device__ __forceinline__ void piece_update(const BlockTask& bt, int ui, int uj) {
+  float acc[4][4];
+#pragma unroll
+  for (int x = 0; x < 4; ++x)
+#pragma unroll
+    for (int y = 0; y < 4; ++y) acc[x][y] = 0.0f;
+#pragma unroll 2
+  for (int k = 0; k < SB; k += 4) {
+    float4 a[4], b[4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      a[x] = *reinterpret_cast<const float4*>(bt.A + (ui + 8 * x) * SLD + k);
+      b[x] = *reinterpret_cast<const float4*>(bt.B + (uj + 8 * x) * SLD + k);
+    }
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+      for (int y = 0; y < 4; ++y) {
+        acc[x][y] = fmaf(a[x].x, b[y].x, acc[x][y]);
+        acc[x][y] = fmaf(a[x].y, b[y].y, acc[x][y]);
+        acc[x][y] = fmaf(a[x].z, b[y].z, acc[x][y]);
+        acc[x][y] = fmaf(a[x].w, b[y].w, acc[x][y]);
+      }
+  }
+#pragma unroll
+  for (int x = 0; x < 4; ++x)
+#pragma unroll
+    for (int y = 0; y < 4; ++y) bt.C[(ui + 8 * x) * SLD + uj + 8 * y] -= acc[x][y];
+}
+
+__global__ void __launch_bounds__(PANEL_THREADS, 2) chol_panel_kernel(float* __restrict__ P, float* __restrict__ Lsave,
+                                                                      int d, int k0, int vec, Header* hdr,
+                                                                      int* err_word) {
+  extern __shared__ __align__(16) float psm[];
+  float* S = psm;                      // NB x SLD: the diagonal block, then L11 (lower)
+  float* R = S + NB * SLD;             // RB x SLD: this CTA's rows below, then its rows of L21
+  float* Lt = R + RB * SLD;            // SB x TLD: Lt[j][c] = L[c0 + c][c0 + j] of the current sub-panel
+  float* dinv = Lt + SB * TLD;         // NB
   int* fail_s = reinterpret_cast<int*>(dinv + NB);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(dinv + NB + 2);   // 8-byte aligned
   grid_dep_wait();                     // the previous trailing update
   grid_dep_launch();
   if (hdr->failed) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int tx = tid & 15, ty = tid >> 4;
   const int nb = min(NB, d - k0), k1 = k0 + nb;
   const bool below = blockIdx.x > 0;
-  const int rbeg = k1 + (blockIdx.x - 1) * NB;              // first panel row of this CTA
-  const int nr = below ? min(NB, d - rbeg) : 0;
+  const int rbeg = k1 + (blockIdx.x - 1) * RB;               // first row below handled here
+  const int nr = below ? min(RB, d - rbeg) : 0;
 
-  // many loads in flight per thread; zeros outside the block
-  load_tile<PANEL_THREADS, NB, NB>(A, PLD, P + (long long)k0 * d + k0, d, nb, nb);
-  if (below) load_tile<PANEL_THREADS, NB, NB>(Xs, PLD, P + (long long)rbeg * d + k0, d, nr, nb);
+  // The lower triangle of the diagonal block (pieces of four columns up to the
+  // diagonal) and the rows below; the identity past a ragged end.
+  if (vec) {
+    // one bulk asynchronous copy per row: row i of the diagonal block up to the end of
+    // the four-column piece holding the diagonal, full rows of R
+    if (tid == 0) {
+      mbar_init(bar, 1);
+      fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t bytes = 0;
+      for (int i = 0; i < nb; ++i) bytes += 4u * (uint32_t)min((i | 3) + 1, nb);
+      bytes += 4u * (uint32_t)(nr * nb);
+      mbar_arrive_expect_tx(bar, bytes);
+    }
+    __syncthreads();
+    if (tid < nb) bulk_g2s(S + tid * SLD, P + (long long)(k0 + tid) * d + k0, 4u * (uint32_t)min((tid | 3) + 1, nb), bar);
+    else if (tid >= NB && tid - NB < nr)
+      bulk_g2s(R + (tid - NB) * SLD, P + (long long)(rbeg + tid - NB) * d + k0, 4u * (uint32_t)nb, bar);
+    const bool landed = mbar_wait_bounded(bar, 0, nullptr);
+    if (__syncthreads_or(!landed)) {
+      // the copies did not land in time: nothing is written, later kernels skip their
+      // work, and the status reports a timeout
+      if (tid == 0) {
+        report_device_error(err_word, DEVERR_TIMEOUT);
+        hdr->timeout = 1;
+        hdr->failed = 1;
+      }
+      return;
+    }
+  } else {
+    for (int idx = tid; idx < nb * nb; idx += PANEL_THREADS) {
+      const int i = idx / nb, c = idx - i * nb;
+      if (c <= i) S[i * SLD + c] = P[(long long)(k0 + i) * d + k0 + c];
+    }
+    for (int idx = tid; idx < nr * nb; idx += PANEL_THREADS) {
+      const int i = idx / nb, c = idx - i * nb;
+      R[i * SLD + c] = P[(long long)(rbeg + i) * d + k0 + c];
+    }
+  }
+  if (nb < NB || (below && nr < RB)) {                       // ragged: pad
+    for (int idx = tid; idx < NB * NB; idx += PANEL_THREADS) {
+      const int i = idx / NB, c = idx % NB;
+      if ((i >= nb || c >= nb) && c <= i) S[i * SLD + c] = (i == c) ? 1.0f : 0.0f;
+    }
+    if (below)
+      for (int idx = tid; idx < RB * NB; idx += PANEL_THREADS) {
+        const int i = idx / NB, c = idx % NB;
+        if (i >= nr || c >= nb) R[i * SLD + c] = 0.0f;
+      }
+  }
   if (tid == 0) *fail_s = -1;
-  __syncthreads();
-  if (tid >= nb && tid < NB) A[tid * PLD + tid] = 1.0f;   // identity padding of a ragged block
   __syncthreads();
 
 #pragma unroll 1
-  for (int pc = 0; pc < NB; pc += PS) {
+  for (int p = 0; p < 4; ++p) {
+    const int c0 = SB * p;
+    // ---- A: Cholesky of the sub-block; the rest of the previous trailing update
     if (warp == 0) {
       int fail = -1;
-      panel8(std::make_integer_sequence<int, PS>{}, A, dinv, pc, lane, fail);
-      if (lane == 0 && fail >= 0 && fail < nb && *fail_s < 0) *fail_s = fail;
+      chol32(std::make_integer_sequence<int, SB>{}, S, c0, Lt, dinv, lane, fail);
+      fail = __reduce_min_sync(0xffffffffu, fail < 0 ? INT_MAX : fail);
+      if (lane == 0 && fail != INT_MAX && fail < nb) *fail_s = fail;
+    } else if (p > 0) {
+      // blocks (I, J), p <= J <= I <= 3, but not (p, p); then R[:, q], q >= p; all
+      // against column block p - 1
+      const int q0 = c0 - SB;
+      const int ndiag = (4 - p) * (5 - p) / 2 - 1;
+      const int ntask = ndiag + (below ? 4 - p : 0);
+      for (int u = tid - 32; u < ntask * 64; u += PANEL_THREADS - 32) {
+        const int t = u >> 6;
+        BlockTask bt;
+        if (t < ndiag) {
+          int I = p, n = t + 1;                                // skip (p, p)
+          while (n > I - p) { n -= I - p + 1; ++I; }
+          const int J = p + n;
+          bt = BlockTask{S + SB * I * SLD + SB * J, S + SB * I * SLD + q0, S + SB * J * SLD + q0};
+        } else {
+          const int q = p + (t - ndiag);
+          bt = BlockTask{R + SB * q, R + q0, S + SB * q * SLD + q0};
+        }
+        piece_update(bt, (u & 63) >> 3, u & 7);
+      }
     }
     __syncthreads();
     if (*fail_s >= 0) break;
-    const int q0 = pc + PS, rem = NB - q0;
-    if (below && tid < NB) {
-      // (b) row tid of Xs, columns [pc, pc + 8)
-      float* xr = Xs + tid * PLD + pc;
-      float x[PS];
-#pragma unroll
-      for (int c = 0; c < PS; ++c) x[c] = xr[c];
-#pragma unroll
-      for (int jj = 0; jj < PS; ++jj) {
-        x[jj] *= dinv[pc + jj];
-#pragma unroll
-        for (int cc = jj + 1; cc < PS; ++cc) x[cc] = fmaf(-x[jj], A[(pc + cc) * PLD + pc + jj], x[cc]);
-      }
-#pragma unroll
-      for (int c = 0; c < PS; ++c) xr[c] = x[c];
-    }
-    // (c) diagonal block: A[i][c] -= sum_k L[i][pc+k] L[c][pc+k], q0 <= c <= i
-    for (int a = ty; a < rem; a += 16) {
-      const int i = q0 + a;
-      for (int b = tx; b <= a; b += 16) {
-        const int c = q0 + b;
-        float acc = A[i * PLD + c];
-#pragma unroll
-        for (int k = 0; k < PS; ++k) acc = fmaf(-A[i * PLD + pc + k], A[c * PLD + pc + k], acc);
-        A[i * PLD + c] = acc;
-      }
+    // ---- B: column block p of the row groups below the sub-block
+    {
+      const int ngrp = 3 - p;
+      if (warp < ngrp) solve32(std::make_integer_sequence<int, SB>{}, S + (c0 + SB * (warp + 1)) * SLD + c0, Lt,
+                               dinv + c0, lane);
+      else if (warp == ngrp && below) solve32(std::make_integer_sequence<int, SB>{}, R + c0, Lt, dinv + c0, lane);
     }
     __syncthreads();
-    if (below) {
-      // (c) rows below: Xs[r][c] -= sum_k Xs[r][pc+k] L[c][pc+k], c >= q0
-      for (int r = ty; r < NB; r += 16) {
-        for (int b = tx; b < rem; b += 16) {
-          const int c = q0 + b;
-          float acc = Xs[r * PLD + c];
-#pragma unroll
-          for (int k = 0; k < PS; ++k) acc = fmaf(-Xs[r * PLD + pc + k], A[c * PLD + pc + k], acc);
-          Xs[r * PLD + c] = acc;
-        }
+    // ---- C: the next diagonal sub-block, 2 x 2 outputs per thread (rows ri + 16a,
+    // columns rj + 16b)
+    if (p < 3) {
+      const int n0 = c0 + SB;
+      const int ri = tid >> 4, rj = tid & 15;
+      const float* A0 = S + n0 * SLD + c0;
+      float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+#pragma unroll 4
+      for (int k = 0; k < SB; k += 4) {
+        const float4 x0 = *reinterpret_cast<const float4*>(A0 + ri * SLD + k);
+        const float4 x1 = *reinterpret_cast<const float4*>(A0 + (ri + 16) * SLD + k);
+        const float4 y0 = *reinterpret_cast<const float4*>(A0 + rj * SLD + k);
+        const float4 y1 = *reinterpret_cast<const float4*>(A0 + (rj + 16) * SLD + k);
+        a00 = fmaf(x0.x, y0.x, fmaf(x0.y, y0.y, fmaf(x0.z, y0.z, fmaf(x0.w, y0.w, a00))));
+        a01 = fmaf(x0.x, y1.x, fmaf(x0.y, y1.y, fmaf(x0.z, y1.z, fmaf(x0.w, y1.w, a01))));
+        a10 = fmaf(x1.x, y0.x, fmaf(x1.y, y0.y, fmaf(x1.z, y0.z, fmaf(x1.w, y0.w, a10))));
+        a11 = fmaf(x1.x, y1.x, fmaf(x1.y, y1.y, fmaf(x1.z, y1.z, fmaf(x1.w, y1.w, a11))));
       }
+      float* C0 = S + n0 * SLD + n0;
+      C0[ri * SLD + rj] -= a00;
+      C0[ri * SLD + rj + 16] -= a01;
+      C0[(ri + 16) * SLD + rj] -= a10;
+      C0[(ri + 16) * SLD + rj + 16] -= a11;
       __syncthreads();
     }
   }
@@ -270,56 +423,77 @@ __global__ void __launch_bounds__(PANEL_THREADS) chol_panel_kernel(float* __rest
   }
   if (!below) {
     for (int idx = tid; idx < NB * NB; idx += PANEL_THREADS) {
-      const int i = idx >> 6, c = idx & 63;
-      if (i < nb && c <= i) P[(long long)(k0 + i) * d + k0 + c] = A[i * PLD + c];
+      const int i = idx / NB, c = idx % NB;
+      if (i < nb && c <= i) Lsave[(long long)(k0 + i) * d + k0 + c] = S[i * SLD + c];
+    }
+  } else if (vec) {
+    const int nq = nb >> 2;
+    for (int idx = tid; idx < nr * nq; idx += PANEL_THREADS) {
+      const int i = idx / nq, c4 = idx - i * nq;
+      *reinterpret_cast<float4*>(P + (long long)(rbeg + i) * d + k0 + 4 * c4) =
+          *reinterpret_cast<const float4*>(R + i * SLD + 4 * c4);
     }
   } else {
-    for (int idx = tid; idx < NB * NB; idx += PANEL_THREADS) {
-      const int i = idx >> 6, c = idx & 63;
-      if (i < nr && c < nb) P[(long long)(rbeg + i) * d + k0 + c] = Xs[i * PLD + c];
+    for (int idx = tid; idx < RB * NB; idx += PANEL_THREADS) {
+      const int i = idx / NB, c = idx % NB;
+      if (i < nr && c < nb) P[(long long)(rbeg + i) * d + k0 + c] = R[i * SLD + c];
     }
   }
 }
-constexpr size_t PANEL_SMEM = (size_t)(2 * NB * PLD + NB + 4) * sizeof(float);
+constexpr size_t PANEL_SMEM = (size_t)((NB + RB) * SLD + SB * TLD + NB + 4) * sizeof(float);   // + flag, mbarrier
+
+// P[k0 + i][k0 + c] = Lsave[k0 + i][k0 + c] for the lower triangle of every diagonal
+// block (blockIdx.y = block, 8 rows per CTA in x)
+__global__ void place_diag_kernel(float* __restrict__ P, const float* __restrict__ Lsave, int d, const Header* hdr) {
+  if (hdr->failed) return;
+  const int k0 = blockIdx.y * NB;
+  const int nb = min(NB, d - k0);
+  const int i = blockIdx.x * 8 + threadIdx.y;
+  if (i >= nb) return;
+  const long long row = (long long)(k0 + i) * d + k0;
+  for (int c = threadIdx.x; c <= i; c += 32) P[row + c] = Lsave[row + c];
+}
+
+constexpr int NBI = 64;       // diagonal blocks inverted at once before the doubling steps
 
 // Inverse of every 64 x 64 diagonal block of L, written into X's diagonal blocks
 // (X = L^-1 in natural order). Thread c solves L x = e_c (column c of the inverse).
 template <int... Js>
-__device__ __forceinline__ void inv_column(std::integer_sequence<int, Js...>, float (&x)[NB], const float (*L)[NB + 1],
+__device__ __forceinline__ void inv_column(std::integer_sequence<int, Js...>, float (&x)[NBI], const float (*L)[NBI + 1],
                                            const float* invd) {
   auto step = [&](auto jc) {
     constexpr int j = decltype(jc)::value;
     x[j] *= invd[j];
 #pragma unroll
-    for (int q = j + 1; q < NB; ++q) x[q] = fmaf(-L[q][j], x[j], x[q]);
+    for (int q = j + 1; q < NBI; ++q) x[q] = fmaf(-L[q][j], x[j], x[q]);
   };
   (step(std::integral_constant<int, Js>{}), ...);
 }
 
 __global__ void __launch_bounds__(64) diag_inverse_kernel(const float* __restrict__ P, float* __restrict__ X, int d,
                                                           const Header* hdr) {
-  __shared__ float L[NB][NB + 1];
-  __shared__ float invd[NB];
+  __shared__ float L[NBI][NBI + 1];
+  __shared__ float invd[NBI];
   if (hdr->failed) return;
-  const int k0 = blockIdx.x * NB;
-  const int nb = min(NB, d - k0);
-  load_tile<NB, NB, NB>(&L[0][0], NB + 1, P + (long long)k0 * d + k0, d, nb, nb);
+  const int k0 = blockIdx.x * NBI;
+  const int nb = min(NBI, d - k0);
+  load_tile<NBI, NBI, NBI>(&L[0][0], NBI + 1, P + (long long)k0 * d + k0, d, nb, nb);
   __syncthreads();
-  for (int idx = threadIdx.x; idx < NB * NB; idx += blockDim.x) {   // lower triangle; identity past the block
-    const int i = idx / NB, c = idx % NB;
+  for (int idx = threadIdx.x; idx < NBI * NBI; idx += blockDim.x) {   // lower triangle; identity past the block
+    const int i = idx / NBI, c = idx % NBI;
     if (c > i || i >= nb) L[i][c] = (i == c) ? 1.0f : 0.0f;
   }
   __syncthreads();
-  for (int j = threadIdx.x; j < NB; j += blockDim.x) invd[j] = rcp_nr(L[j][j]);
+  for (int j = threadIdx.x; j < NBI; j += blockDim.x) invd[j] = rcp_nr(L[j][j]);
   __syncthreads();
   const int c = threadIdx.x;
-  float x[NB];
+  float x[NBI];
 #pragma unroll
-  for (int q = 0; q < NB; ++q) x[q] = (q == c) ? 1.0f : 0.0f;
-  inv_column(std::make_integer_sequence<int, NB>{}, x, L, invd);
+  for (int q = 0; q < NBI; ++q) x[q] = (q == c) ? 1.0f : 0.0f;
+  inv_column(std::make_integer_sequence<int, NBI>{}, x, L, invd);
   if (c >= nb) return;
 #pragma unroll
-  for (int q = 0; q < NB; ++q) {
+  for (int q = 0; q < NBI; ++q) {
     if (q < nb && q >= c) X[(long long)(k0 + q) * d + k0 + c] = x[q];
     if (q < nb && q > c) X[(long long)(k0 + c) * d + k0 + q] = x[q];   // the transpose, above
   }
@@ -407,8 +581,8 @@ gptq_status factor_launch(const float* H, long long d_, float percdamp, int act_
     const int nb = std::min(NB, d - k0), k1 = k0 + nb, below = d - k1;
     {
       ProfScope ps("factor.chol_panel", s);
-      if (launch_pdl(chol_panel_kernel, dim3(1 + (below + NB - 1) / NB), dim3(PANEL_THREADS), PANEL_SMEM, s, P, d, k0,
-                     hdr) != cudaSuccess)
+      if (launch_pdl(chol_panel_kernel, dim3(1 + (below + RB - 1) / RB), dim3(PANEL_THREADS), PANEL_SMEM, s, P, Hinv1,
+                     d, k0, vec ? 1 : 0, hdr, device_error_word()) != cudaSuccess)
         return check_launch("chol_panel_kernel");
       count_launch();
     }
@@ -431,8 +605,10 @@ gptq_status factor_launch(const float* H, long long d_, float percdamp, int act_
   // ---- X = L^-1 in natural order inside Hinv1: diagonal blocks, then recursive doubling
   {
     ProfScope ps("factor.zero_diag_inverse", s);
+    place_diag_kernel<<<dim3(NB / 8, (unsigned)((d + NB - 1) / NB)), dim3(32, 8), 0, s>>>(P, Hinv1, d, hdr);
+    count_launch();
     zero_kernel<<<std::max(1, std::min(4096, (int)(((long long)d * d + 255) / 256))), 256, 0, s>>>(Hinv1, (long long)d * d);
-    diag_inverse_kernel<<<(d + NB - 1) / NB, NB, 0, s>>>(P, Hinv1, d, hdr);
+    diag_inverse_kernel<<<(d + NBI - 1) / NBI, NBI, 0, s>>>(P, Hinv1, d, hdr);
   }
   count_launch(2);
   // Doubling over block pairs (A, C) = ([2p sz, 2p sz + sz), [2p sz + sz, ...)): with
@@ -442,7 +618,7 @@ gptq_status factor_launch(const float* H, long long d_, float percdamp, int act_
   //   Y[A][C] = X[C][A]^T
   // so every product has both operands K-major (the tensor-core GEMM's layout); the
   // triangular operands are masked, since their other triangle holds the transpose.
-  for (int sz = NB; sz < d; sz *= 2) {
+  for (int sz = NBI; sz < d; sz *= 2) {
     int np = 0;
     while (2LL * np * sz + sz < d) ++np;
     const int c_last = std::min(sz, d - (2 * (np - 1) * sz + sz));
@@ -489,6 +665,10 @@ gptq_status factor_read_status(const void* ws, long long* info, cudaStream_t s) 
   if (cudaStreamSynchronize(s) != cudaSuccess) return set_error(GPTQ_ERR_CUDA, "cudaStreamSynchronize failed");
   if (cudaMemcpy(&h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess)
     return set_error(GPTQ_ERR_CUDA, "reading the factor status failed");
+  if (h.timeout) {
+    if (info) *info = -1;
+    return set_error(GPTQ_ERR_TIMEOUT, "a wait for the panel's copies gave up");
+  }
   if (h.nonfinite) {
     if (info) *info = 0;
     return set_error(GPTQ_ERR_NONFINITE, "diag(H) holds a NaN or an Inf");
