@@ -171,7 +171,7 @@ gptq_status gptq_factor_status(const void* ws, int64_t* info, gptq_stream_t stre
  * The pages have no counterpart of this call; it exists only for such callers.
  *
  * Same arguments, results and status codes as gptq_factor, minus ws / ws_bytes. The
- * scratch is a device array inside the library sized for d <= 2048 (16 MiB + 256
+ * scratch is a device array inside the library sized for d <= 2048 (17 MiB + 256
  * bytes), held on every GPU that loads the library until the process exits;
  * d > 2048 returns GPTQ_ERR_INVALID_ARG before anything is launched. The call
  * allocates nothing.

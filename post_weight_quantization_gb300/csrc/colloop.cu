@@ -196,6 +196,7 @@ struct CBArgs {
   float* zeros;
   int G;
   float* err;                 // Err1 of the current outer block: mpad x eld, row-major
+  float* err_lo;              // its low parts (err - err with the 13 low mantissa bits cleared)
   int eld;                    // row stride of err (the outer block width)
   int eoff;                   // this block's first column within err
   float* part;                // loss partials, one row of d per CTA
@@ -394,7 +395,12 @@ __global__ void __launch_bounds__(CB_THREADS, 1) colblock_kernel(CBArgs a) {
   constexpr int ELD = SL::ELD, CLD = SL::CLD;
   for (int idx = tid; idx < ROWS_PER_CTA * BS; idx += CB_THREADS) {
     const int rr = idx / BS, t = idx % BS;
-    if (t < ncols && r0 + rr < a.m) a.err[(long long)(r0 + rr) * a.eld + a.eoff + t] = Es[rr * ELD + t];
+    if (t < ncols && r0 + rr < a.m) {
+      const float e = Es[rr * ELD + t];
+      const long long o = (long long)(r0 + rr) * a.eld + a.eoff + t;
+      a.err[o] = e;
+      a.err_lo[o] = e - __uint_as_float(__float_as_uint(e) & 0xFFFFE000u);
+    }
   }
   for (int t = tid; t < ncols; t += CB_THREADS) {
     float lsum = 0.0f;
@@ -476,8 +482,10 @@ __global__ void unpack_kernel(const uint32_t* __restrict__ qweight, int m, int d
   codes[idx] = (uint8_t)(v & ((1u << bits) - 1u));
 }
 
-// Ut = Hinv1^T (the lazy update reads Hinv1's rows as K-major operand columns)
-__global__ void transpose_kernel(const float* __restrict__ U, float* __restrict__ Ut, int d) {
+// Ut = Hinv1^T (the lazy update reads Hinv1's rows as K-major operand columns) and
+// its low parts Ut_lo = Ut - Ut with the 13 low mantissa bits cleared
+__global__ void transpose_kernel(const float* __restrict__ U, float* __restrict__ Ut, float* __restrict__ Ut_lo,
+                                 int d) {
   __shared__ float tile[32][33];
   const int bx = blockIdx.x * 32, by = blockIdx.y * 32;
   for (int yy = threadIdx.y; yy < 32; yy += 8) {
@@ -487,7 +495,11 @@ __global__ void transpose_kernel(const float* __restrict__ U, float* __restrict_
   __syncthreads();
   for (int yy = threadIdx.y; yy < 32; yy += 8) {
     const int r = bx + yy, c = by + threadIdx.x;
-    if (r < d && c < d) Ut[(long long)r * d + c] = tile[threadIdx.x][yy];
+    if (r < d && c < d) {
+      const float x = tile[threadIdx.x][yy];
+      Ut[(long long)r * d + c] = x;
+      Ut_lo[(long long)r * d + c] = x - __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+    }
   }
 }
 
@@ -509,7 +521,7 @@ inline int outer_width(int BS, int g, int stats_given) {
 }
 
 struct Layout {
-  size_t hdr, wf, err, ut, part, codes8, inv, dinfo, total;
+  size_t hdr, wf, err, errlo, ut, utlo, part, codes8, inv, dinfo, total;
   int nrg;
 };
 
@@ -521,8 +533,10 @@ Layout layout(long long m, long long d, int blocksize) {
   L.hdr = 0;
   L.wf = kHeaderBytes;
   L.err = L.wf + al((size_t)m * d * 4);
-  L.ut = L.err + al(mpad * (size_t)std::max(OUTER, blocksize) * 4);
-  L.part = L.ut + al((size_t)d * d * 4);
+  L.errlo = L.err + al(mpad * (size_t)std::max(OUTER, blocksize) * 4);
+  L.ut = L.errlo + al(mpad * (size_t)std::max(OUTER, blocksize) * 4);
+  L.utlo = L.ut + al((size_t)d * d * 4);
+  L.part = L.utlo + al((size_t)d * d * 4);
   L.codes8 = L.part + al((size_t)L.nrg * d * 4);
   L.inv = L.codes8 + al((size_t)m * d);
   L.dinfo = L.inv + al((size_t)d * 4);
@@ -531,7 +545,7 @@ Layout layout(long long m, long long d, int blocksize) {
 }
 
 template <int BS>
-gptq_status run_blocks(CBArgs a, const float* Ut, cudaStream_t s) {
+gptq_status run_blocks(CBArgs a, const float* Ut, const float* Ut_lo, cudaStream_t s) {
   using SL = CBSmem<BS>;
   if (cudaFuncSetAttribute(colblock_kernel<BS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SL::total) !=
       cudaSuccess)
@@ -547,6 +561,8 @@ gptq_status run_blocks(CBArgs a, const float* Ut, cudaStream_t s) {
     ga.M = m; ga.N = c1 - c0; ga.K = K; ga.M_last = m; ga.K_last = K;
     ga.A = a.err + e0; ga.lda = OB;
     ga.B = Ut + (long long)c0 * d + k0; ga.ldb = d;
+    ga.A_lo = a.err_lo + e0; ga.lda_lo = OB;
+    ga.B_lo = Ut_lo + (long long)c0 * d + k0; ga.ldb_lo = d;
     ga.C = const_cast<float*>(a.Wf) + c0; ga.ldc = d;
     ga.alpha = -1.0f; ga.beta = 1.0f;
     ga.vec = vec;
@@ -590,7 +606,9 @@ gptq_status quantize_launch(const void* W, int w_dtype, long long m_, long long 
   QHeader* hdr = reinterpret_cast<QHeader*>(base + L.hdr);
   float* Wf = reinterpret_cast<float*>(base + L.wf);
   float* err = reinterpret_cast<float*>(base + L.err);
+  float* err_lo = reinterpret_cast<float*>(base + L.errlo);
   float* Ut = reinterpret_cast<float*>(base + L.ut);
+  float* Ut_lo = reinterpret_cast<float*>(base + L.utlo);
   float* part = reinterpret_cast<float*>(base + L.part);
   uint8_t* codes8 = perm ? base + L.codes8 : nullptr;
   int* inv = reinterpret_cast<int*>(base + L.inv);
@@ -606,7 +624,7 @@ gptq_status quantize_launch(const void* W, int w_dtype, long long m_, long long 
     dim3 grid((unsigned)std::min(8, (d + 255) / 256), (unsigned)std::min(m, 65535));
     prep_kernel<<<grid, 256, 0, s>>>(W, w_dtype, m, d, ldw, perm, Wf, hdr);
     dim3 tg((unsigned)((d + 31) / 32), (unsigned)((d + 31) / 32));
-    transpose_kernel<<<tg, dim3(32, 8), 0, s>>>(Hinv1, Ut, d);
+    transpose_kernel<<<tg, dim3(32, 8), 0, s>>>(Hinv1, Ut, Ut_lo, d);
     diag_info_kernel<<<(d + 255) / 256, 256, 0, s>>>(Hinv1, d, dinfo);
     count_launch(3);
     if (group_size < 0) {
@@ -619,15 +637,15 @@ gptq_status quantize_launch(const void* W, int w_dtype, long long m_, long long 
   a.bits = bits; a.g = g; a.stats_given = group_size < 0;
   a.qweight = qweight; a.wpr = wpr; a.codes8 = codes8;
   a.scales = scales; a.zeros = zeros; a.G = G;
-  a.err = err; a.part = part;
+  a.err = err; a.err_lo = err_lo; a.part = part;
   a.bulk = (d % 4 == 0) && simt::aligned16(Hinv1);
   a.vecw = (d % 4 == 0) && simt::aligned16(Wf);
   a.err_word = device_error_word();
   gptq_status st;
   switch (blocksize) {
-    case 32: st = run_blocks<32>(a, Ut, s); break;
-    case 64: st = run_blocks<64>(a, Ut, s); break;
-    default: st = run_blocks<128>(a, Ut, s); break;
+    case 32: st = run_blocks<32>(a, Ut, Ut_lo, s); break;
+    case 64: st = run_blocks<64>(a, Ut, Ut_lo, s); break;
+    default: st = run_blocks<128>(a, Ut, Ut_lo, s); break;
   }
   if (st) return st;
   loss_finalize_kernel<<<(d + 255) / 256, 256, 0, s>>>(part, L.nrg, d, perm, col_losses);

@@ -275,8 +275,8 @@ __device__ __forceinline__ void piece_update(const BlockTask& bt, int ui, int uj
 }
 
 __global__ void __launch_bounds__(PANEL_THREADS, 2) chol_panel_kernel(float* __restrict__ P, float* __restrict__ Lsave,
-                                                                      int d, int k0, int vec, Header* hdr,
-                                                                      int* err_word) {
+                                                                      float* __restrict__ Plo, int d, int k0, int vec,
+                                                                      Header* hdr, int* err_word) {
   extern __shared__ __align__(16) float psm[];
   float* S = psm;                      // NB x SLD: the diagonal block, then L11 (lower)
   float* R = S + NB * SLD;             // RB x SLD: this CTA's rows below, then its rows of L21
@@ -427,11 +427,19 @@ __global__ void __launch_bounds__(PANEL_THREADS, 2) chol_panel_kernel(float* __r
       if (i < nb && c <= i) Lsave[(long long)(k0 + i) * d + k0 + c] = S[i * SLD + c];
     }
   } else if (vec) {
+    // L21 rows, and their low parts for the trailing update's tensor-core product
+    // (Plo[row][c] = x - x with the 13 low mantissa bits cleared)
     const int nq = nb >> 2;
     for (int idx = tid; idx < nr * nq; idx += PANEL_THREADS) {
       const int i = idx / nq, c4 = idx - i * nq;
-      *reinterpret_cast<float4*>(P + (long long)(rbeg + i) * d + k0 + 4 * c4) =
-          *reinterpret_cast<const float4*>(R + i * SLD + 4 * c4);
+      const float4 x = *reinterpret_cast<const float4*>(R + i * SLD + 4 * c4);
+      *reinterpret_cast<float4*>(P + (long long)(rbeg + i) * d + k0 + 4 * c4) = x;
+      float4 l;
+      l.x = x.x - __uint_as_float(__float_as_uint(x.x) & 0xFFFFE000u);
+      l.y = x.y - __uint_as_float(__float_as_uint(x.y) & 0xFFFFE000u);
+      l.z = x.z - __uint_as_float(__float_as_uint(x.z) & 0xFFFFE000u);
+      l.w = x.w - __uint_as_float(__float_as_uint(x.w) & 0xFFFFE000u);
+      *reinterpret_cast<float4*>(Plo + (long long)(rbeg + i) * NB + 4 * c4) = l;
     }
   } else {
     for (int idx = tid; idx < RB * NB; idx += PANEL_THREADS) {
@@ -543,8 +551,10 @@ __global__ void pair_transpose_kernel(float* __restrict__ M, int d, int sz, int 
 
 }  // namespace factor
 
+// header | P (d x d) | Plo (d x 128: low parts of the current panel's L21)
 size_t factor_workspace_bytes(long long d) {
-  return factor::kHeaderBytes + (((size_t)d * (size_t)d * sizeof(float) + 255) & ~(size_t)255);
+  auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  return factor::kHeaderBytes + al((size_t)d * (size_t)d * sizeof(float)) + al((size_t)d * factor::NB * sizeof(float));
 }
 
 gptq_status factor_launch(const float* H, long long d_, float percdamp, int act_order, int32_t* perm_out,
@@ -553,6 +563,8 @@ gptq_status factor_launch(const float* H, long long d_, float percdamp, int act_
   const int d = (int)d_;
   Header* hdr = reinterpret_cast<Header*>(ws);
   float* P = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + kHeaderBytes);
+  float* Plo = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + kHeaderBytes +
+                                        (((size_t)d * (size_t)d * sizeof(float) + 255) & ~(size_t)255));
   const int* failed = &hdr->failed;
   const bool vec = (d % 4 == 0) && simt::aligned16(P) && simt::aligned16(Hinv1);
 
@@ -582,7 +594,7 @@ gptq_status factor_launch(const float* H, long long d_, float percdamp, int act_
     {
       ProfScope ps("factor.chol_panel", s);
       if (launch_pdl(chol_panel_kernel, dim3(1 + (below + RB - 1) / RB), dim3(PANEL_THREADS), PANEL_SMEM, s, P, Hinv1,
-                     d, k0, vec ? 1 : 0, hdr, device_error_word()) != cudaSuccess)
+                     Plo, d, k0, vec ? 1 : 0, hdr, device_error_word()) != cudaSuccess)
         return check_launch("chol_panel_kernel");
       count_launch();
     }
@@ -591,6 +603,8 @@ gptq_status factor_launch(const float* H, long long d_, float percdamp, int act_
       g.M = g.N = below; g.K = nb; g.M_last = below; g.K_last = nb;
       g.A = P + (long long)k1 * d + k0; g.lda = d;
       g.B = g.A; g.ldb = d;
+      g.A_lo = Plo + (long long)k1 * NB; g.lda_lo = NB;
+      g.B_lo = g.A_lo; g.ldb_lo = NB;
       g.C = P + (long long)k1 * d + k1; g.ldc = d;
       g.alpha = -1.0f; g.beta = 1.0f;
       g.lower_tiles = 1;

@@ -37,6 +37,13 @@ struct GemmArgs {
   float* C;
   long long ldc, c_bs;
   float alpha, beta;
+  // Optional low parts for the tensor-core GEMM (K-major, same extents as A and B):
+  // A_lo = A - tf32(A) and B_lo = B - tf32(B), tf32 = the 13 low mantissa bits cleared.
+  // Given both, the operands are loaded pre-split and no conversion pass runs.
+  const float* A_lo;
+  long long lda_lo;
+  const float* B_lo;
+  long long ldb_lo;
   int lower_tiles;        // C square: only tiles with J <= I
   int a_tri;              // 1: A lower triangular, 2: A upper triangular (masked)
   int b_lower;            // B(k, j) == 0 for k < j

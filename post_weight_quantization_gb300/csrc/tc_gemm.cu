@@ -7,15 +7,19 @@
 // so those calls take the FFMA GEMM of simt_gemm.cuh).
 //
 // Each fp32 operand x is split as x = hi + lo, hi = x with its 13 low mantissa bits
-// cleared (what the tf32 tensor-core path reads from an fp32 word) and lo = x - hi
-// (exact); A B is formed as hi_A hi_B + hi_A lo_B + lo_A hi_B, which carries about 21
-// significant bits per product.
+// cleared and lo = x - hi (exact); A B is formed as hi_A hi_B + hi_A lo_B + lo_A hi_B,
+// which carries about 21 significant bits per product. The tf32 tensor-core path reads
+// an fp32 word as its hi part (the low mantissa bits are ignored; checked against an
+// fp64 product on this GPU), so the raw operand serves as hi and only lo is stored.
+// Callers that already hold the lo parts pass them (GemmArgs::A_lo / B_lo) and the
+// tiles are loaded pre-split; otherwise converter warps form lo in shared memory.
 //
 // Design (sm_103a), one persistent CTA per SM, tiles taken round-robin:
 //   warp 0      TMA producer: 32-deep k chunks of A and B into a 3-stage ring
-//   warps 2-5   converters: lo parts of each stage into their own buffers (the
-//               128-byte swizzle permutes 16-byte chunks, so an elementwise pass keeps
-//               the layout), zeroing k past the extent of a ragged last batch
+//   warps 2-5   converters (operands without lo parts): lo parts of each stage into
+//               their own buffers (the 128-byte swizzle permutes 16-byte chunks, so an
+//               elementwise pass keeps the layout), zeroing k past the extent of a
+//               ragged last batch and outside a triangular operand
 //   warp 1      MMA issuer: per chunk 4 k-steps x 3 products, tcgen05.mma kind::tf32
 //               M = 128, N = 128, K = 8; two chunks (64 products) go into one
 //               tensor-memory buffer, four buffers of 128 columns rotate, so the
@@ -41,9 +45,12 @@ constexpr int BM = 128, BN = 128, BK = 32;     // BK fp32 = 128 bytes: one swizz
 constexpr int STAGES = 3;
 constexpr int OP_BYTES = BM * BK * 4;          // 16 KB per operand per stage
 constexpr int STAGE_BYTES = 4 * OP_BYTES;      // A, B, A_lo, B_lo
-constexpr int THREADS = 14 * 32;
 constexpr int CONV_WARP0 = 2, NCONV = 4;
-constexpr int EPI_WARP0 = 6, NEPI = 8;
+constexpr int NEPI = 8;
+// warps 0-1 TMA and MMA, then the converters (operands without lo parts), then the
+// epilogue warps
+template <bool PRESPLIT> constexpr int epi_warp0() { return PRESPLIT ? 2 : CONV_WARP0 + NCONV; }
+template <bool PRESPLIT> constexpr int threads() { return (epi_warp0<PRESPLIT>() + NEPI) * 32; }
 constexpr int NBUF = 4;                       // chunk accumulators in tensor memory
 constexpr int ACC_CHUNKS = 2;                 // 32-deep chunks summed in one accumulator (64 products)
 constexpr uint32_t TMEM_COLS = NBUF * BN;
@@ -158,23 +165,20 @@ __device__ __forceinline__ void split_operand(uint8_t* raw, uint8_t* lo, int kba
       if (k_of_elem0 + 2 * step >= kend) x.z = 0.0f;
       if (k_of_elem0 + 3 * step >= kend) x.w = 0.0f;
     }
-    float4 hi, l;
-    hi.x = __uint_as_float(__float_as_uint(x.x) & 0xFFFFE000u);
-    hi.y = __uint_as_float(__float_as_uint(x.y) & 0xFFFFE000u);
-    hi.z = __uint_as_float(__float_as_uint(x.z) & 0xFFFFE000u);
-    hi.w = __uint_as_float(__float_as_uint(x.w) & 0xFFFFE000u);
-    l.x = x.x - hi.x;
-    l.y = x.y - hi.y;
-    l.z = x.z - hi.z;
-    l.w = x.w - hi.w;
-    r4[idx] = hi;   // hi has no bits below the tf32 mantissa, so hi + lo == x exactly
+    float4 l;
+    l.x = x.x - __uint_as_float(__float_as_uint(x.x) & 0xFFFFE000u);
+    l.y = x.y - __uint_as_float(__float_as_uint(x.y) & 0xFFFFE000u);
+    l.z = x.z - __uint_as_float(__float_as_uint(x.z) & 0xFFFFE000u);
+    l.w = x.w - __uint_as_float(__float_as_uint(x.w) & 0xFFFFE000u);
+    if (ragged || diag) r4[idx] = x;   // the masked operand; untouched chunks stay as loaded
     l4[idx] = l;
   }
 }
 
-template <bool A_KMAJ, bool B_KMAJ>
-__global__ void __launch_bounds__(THREADS, 1)
-tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b, Params p,
+template <bool A_KMAJ, bool B_KMAJ, bool PRESPLIT>
+__global__ void __launch_bounds__(threads<PRESPLIT>(), 1)
+tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+               const __grid_constant__ CUtensorMap map_alo, const __grid_constant__ CUtensorMap map_blo, Params p,
                int* __restrict__ err_word) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -205,6 +209,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     fence_mbar_init();
     prefetch_tmap(&map_a);
     prefetch_tmap(&map_b);
+    if constexpr (PRESPLIT) {
+      prefetch_tmap(&map_alo);
+      prefetch_tmap(&map_blo);
+    }
   }
   if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
   tc_fence_before();
@@ -227,9 +235,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       for (int k0 = w.kbeg; k0 < w.kend; k0 += BK) {
         if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
         uint8_t* sa = smem + stage * STAGE_BYTES;
-        mbar_arrive_expect_tx(&full[stage], 2 * OP_BYTES);
+        mbar_arrive_expect_tx(&full[stage], (PRESPLIT ? 4 : 2) * OP_BYTES);
         load_operand<A_KMAJ>(sa, &map_a, &full[stage], w.I * BM, k0, w.z);
         load_operand<B_KMAJ>(sa + OP_BYTES, &map_b, &full[stage], w.J * BN, k0, w.z);
+        if constexpr (PRESPLIT) {
+          load_operand<A_KMAJ>(sa + 2 * OP_BYTES, &map_alo, &full[stage], w.I * BM, k0, w.z);
+          load_operand<B_KMAJ>(sa + 3 * OP_BYTES, &map_blo, &full[stage], w.J * BN, k0, w.z);
+        }
         armed |= 1u << stage;
         last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -238,7 +250,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     if (!ok) { *abort_flag = 1; report_device_error(err_word, DEVERR_TIMEOUT); }
     for (int s = 0; s < STAGES; ++s)
       if (armed & (1u << s)) mbar_wait_bounded(&full[s], (last_phase >> s) & 1u, nullptr);
-  } else if (warp >= CONV_WARP0 && warp < CONV_WARP0 + NCONV) {
+  } else if (!PRESPLIT && warp >= CONV_WARP0 && warp < CONV_WARP0 + NCONV) {
     // ---------------- converters: lo parts ----------------
     const int ctid = threadIdx.x - CONV_WARP0 * 32;
     int stage = 0;
@@ -272,7 +284,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         const bool last = (cin % ACC_CHUNKS) == ACC_CHUNKS - 1 || k0 + BK >= w.kend;
         const uint32_t buf = it % NBUF;
         if (first && !mbar_wait_bounded(&tmem_empty[buf], ((it / NBUF) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
-        if (!mbar_wait_bounded(&conv[stage], phase, abort_flag)) { ok = false; break; }
+        if (!mbar_wait_bounded(PRESPLIT ? &full[stage] : &conv[stage], phase, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * BN;
         const uint32_t a = sbase + stage * STAGE_BYTES, b = a + OP_BYTES;
@@ -301,14 +313,25 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       umma_commit(drain);
       mbar_wait_bounded(drain, 0, nullptr);
     }
-  } else if (warp >= EPI_WARP0) {
+  } else if (warp >= epi_warp0<PRESPLIT>()) {
     // ---------------- epilogue ----------------
+    constexpr int EPI_WARP0 = epi_warp0<PRESPLIT>();
     const int q = warp & 3;                       // TMEM lane quadrant
     const int h = (warp - EPI_WARP0) >> 2;        // 64-column half of the tile
     uint32_t it = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
       const Tile w = decode(t, p);
+      // Pull this thread's 64-column segment of C into L2 while the tile's products are
+      // computed, so the read-modify-write below waits on L2 rather than on DRAM
+      // (whole segments only; a ragged edge is read as it is).
+      if (p.beta != 0.0f) {
+        const int i = w.I * BM + q * 32 + lane, j0 = w.J * BN + h * 64;
+        if (i < w.M && j0 + 64 <= p.N) {
+          const float* seg = p.C + (long long)w.z * p.c_bs + (long long)i * p.ldc + j0;
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], 256;" ::"l"(seg) : "memory");
+        }
+      }
       float acc[64];
 #pragma unroll
       for (int x = 0; x < 64; ++x) acc[x] = 0.0f;
@@ -437,6 +460,9 @@ gptq_status tc_gemm(const simt::GemmArgs& g, int batches, bool a_kmaj, bool b_km
   const bool aligned = g.vec && simt::aligned16(g.A) && simt::aligned16(g.B) && simt::aligned16(g.C) &&
                        (g.lda % 4 == 0) && (g.ldb % 4 == 0) && (g.ldc % 4 == 0) && (g.a_bs % 4 == 0) &&
                        (g.b_bs % 4 == 0) && (g.c_bs % 4 == 0);
+  // pre-split operands: both lo parts given, aligned, one batch, no triangular masks
+  const bool presplit = g.A_lo && g.B_lo && batches == 1 && !g.a_tri && !g.b_lower && simt::aligned16(g.A_lo) &&
+                        simt::aligned16(g.B_lo) && (g.lda_lo % 4 == 0) && (g.ldb_lo % 4 == 0);
   // tcgen05 kind::tf32 reads K-major operands only (an MN-major tf32 operand yields
   // zeros), so other layouts and unaligned operands take the FFMA GEMM
   if (!aligned || !a_kmaj || !b_kmaj) return simt::gemm(g, batches, a_kmaj, b_kmaj, s);
@@ -450,6 +476,9 @@ gptq_status tc_gemm(const simt::GemmArgs& g, int batches, bool a_kmaj, bool b_km
     else ok = make_map(&mb, g.B, g.N, g.K, g.ldb, batches, g.b_bs, 32, BK);
   }
   if (!ok) return simt::gemm(g, batches, a_kmaj, b_kmaj, s);
+  CUtensorMap malo = ma, mblo = mb;
+  const bool split = presplit && make_map(&malo, g.A_lo, g.K, g.M, g.lda_lo, 1, 0, BK, BM) &&
+                     make_map(&mblo, g.B_lo, g.K, g.N, g.ldb_lo, 1, 0, BK, BN);
 
   Params p{};
   p.M = g.M; p.N = g.N; p.K = g.K; p.M_last = g.M_last; p.K_last = g.K_last; p.batches = batches;
@@ -463,20 +492,20 @@ gptq_status tc_gemm(const simt::GemmArgs& g, int batches, bool a_kmaj, bool b_km
   const int ntiles = p.tiles_per_batch * batches;
   const int grid = std::min(ntiles, sm_count());
 
-  auto launch = [&](auto kern) -> gptq_status {
-    static bool attr_done[4] = {false, false, false, false};
-    const int key = (a_kmaj ? 2 : 0) + (b_kmaj ? 1 : 0);
+  auto launch = [&](auto kern, int key) -> gptq_status {
+    static bool attr_done[2] = {false, false};
     if (!attr_done[key]) {
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
         return set_error(GPTQ_ERR_CUDA, "cudaFuncSetAttribute(tc_gemm_kernel) failed");
       attr_done[key] = true;
     }
-    if (launch_pdl(kern, dim3(grid), dim3(THREADS), SMEM_BYTES, s, ma, mb, p, device_error_word()) != cudaSuccess)
+    if (launch_pdl(kern, dim3(grid), dim3(key ? threads<true>() : threads<false>()), SMEM_BYTES, s, ma, mb, malo,
+                   mblo, p, device_error_word()) != cudaSuccess)
       return check_launch("tc_gemm_kernel");
     count_launch();
     return check_launch("tc_gemm_kernel");
   };
-  return launch(tc_gemm_kernel<true, true>);
+  return split ? launch(tc_gemm_kernel<true, true, true>, 1) : launch(tc_gemm_kernel<true, true, false>, 0);
 }
 
 }  // namespace gptq
