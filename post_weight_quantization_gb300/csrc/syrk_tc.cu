@@ -58,6 +58,7 @@ constexpr uint32_t LBO = BOX_BYTES;
 
 struct Geometry {
   int d, nr, nc, tiles, parts, kiters;
+  int npairs;                 // paired mode: 256 x 256 pair-tiles (rows 2p, 2p + 1 of the 128-row tiles)
 };
 
 // number of upper-triangle tiles in row-tiles [0, r)
@@ -82,6 +83,9 @@ struct Unit {
   int k0, k1;
 };
 
+// pair-tiles (p, c), c >= p, row-major: sum_{p' < p} (nc - p')
+__device__ __forceinline__ int pairs_before_row(int p, int nc) { return p * nc - (p * (p - 1)) / 2; }
+
 // 32-bit arithmetic only (a 64-bit division is an out-of-line call that would force
 // the epilogue's register sums to the stack): units < 2^31, parts <= 64 and
 // k-iterations < 2^25 keep part * kiters below 2^32.
@@ -96,6 +100,29 @@ __device__ __forceinline__ Unit decode_unit(int u, const Geometry& g) {
   return w;
 }
 
+// Paired mode (d a multiple of 256): a cluster of two CTAs takes (pair-tile, part)
+// units; CTA `rank` computes the 128 x 256 tile of row 2p + rank. Both tiles need the
+// same 256 channels of X as their B operand, so each CTA loads half of that slab with
+// a multicast copy into both CTAs' shared memory (one third less traffic from L2 than
+// two independent tiles); a stage is free again once both CTAs' products have read it.
+__device__ __forceinline__ Unit decode_pair_unit(int u, const Geometry& g, int rank) {
+  Unit w;
+  const unsigned part = (unsigned)u / (unsigned)g.npairs;
+  const int t = u - (int)part * g.npairs;
+  int lo = 0, hi = g.nr / 2 - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pairs_before_row(mid, g.nc) <= t) lo = mid; else hi = mid - 1;
+  }
+  w.r = 2 * lo + rank;
+  w.c = lo + (t - pairs_before_row(lo, g.nc));
+  const unsigned kit = (unsigned)g.kiters;
+  w.k0 = (int)(part * kit / (unsigned)g.parts);
+  w.k1 = (int)((part + 1u) * kit / (unsigned)g.parts);
+  return w;
+}
+
+template <bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
 syrk_kernel(const __grid_constant__ CUtensorMap tmap, float* __restrict__ H, long long ldh, Geometry g,
             float alpha, int* __restrict__ err_word) {
@@ -112,11 +139,15 @@ syrk_kernel(const __grid_constant__ CUtensorMap tmap, float* __restrict__ H, lon
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int rank = PAIR ? (int)cluster_ctarank() : 0;
+  const int cid = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;       // cluster (or CTA) index
+  const int ncl = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  auto unit_of = [&](int u) { return PAIR ? decode_pair_unit(u, g, rank) : decode_unit(u, g); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], PAIR ? 2 : 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tmem_full[b], 1);
@@ -131,9 +162,10 @@ syrk_kernel(const __grid_constant__ CUtensorMap tmap, float* __restrict__ H, lon
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if constexpr (PAIR) cluster_sync();      // the peer's barriers exist before anything targets them
   const uint32_t tmem_base = *tmem_slot;
 
-  const int num_units = g.tiles * g.parts;
+  const int num_units = (PAIR ? g.npairs : g.tiles) * g.parts;
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer ----------------
@@ -142,8 +174,8 @@ syrk_kernel(const __grid_constant__ CUtensorMap tmap, float* __restrict__ H, lon
     uint32_t armed = 0;            // stages that were ever armed
     uint32_t last_phase = 0;       // bit s: phase of stage s's last arming
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
-      Unit w = decode_unit(u, g);
+    for (int u = cid; ok && u < num_units; u += ncl) {
+      Unit w = unit_of(u);
       for (int k = w.k0; k < w.k1; ++k) {
         if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
         uint8_t* sA = smem + stage * STAGE_BYTES;
@@ -152,8 +184,15 @@ syrk_kernel(const __grid_constant__ CUtensorMap tmap, float* __restrict__ H, lon
         const int tok = k * BK;
 #pragma unroll
         for (int h = 0; h < BM / BOX; ++h) tma_load_2d(sA + h * BOX_BYTES, &tmap, &full[stage], w.r * BM + h * BOX, tok);
+        if constexpr (PAIR) {
 #pragma unroll
-        for (int h = 0; h < BN / BOX; ++h) tma_load_2d(sB + h * BOX_BYTES, &tmap, &full[stage], w.c * BN + h * BOX, tok);
+          for (int h = 2 * rank; h < 2 * rank + 2; ++h)
+            tma_load_2d_mc(sB + h * BOX_BYTES, &tmap, &full[stage], w.c * BN + h * BOX, tok, (uint16_t)3);
+        } else {
+#pragma unroll
+          for (int h = 0; h < BN / BOX; ++h)
+            tma_load_2d(sB + h * BOX_BYTES, &tmap, &full[stage], w.c * BN + h * BOX, tok);
+        }
         armed |= 1u << stage;
         last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -170,8 +209,8 @@ syrk_kernel(const __grid_constant__ CUtensorMap tmap, float* __restrict__ H, lon
     uint32_t it = 0;               // chunks issued (tensor-memory buffer rotation)
     bool ok = true, issued = false;
     const uint32_t sbase = smem_u32(smem);
-    for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
-      Unit w = decode_unit(u, g);
+    for (int u = cid; ok && u < num_units; u += ncl) {
+      Unit w = unit_of(u);
       for (int kc = w.k0; ok && kc < w.k1; kc += CHUNK, ++it) {
         const int ke = (kc + CHUNK < w.k1) ? kc + CHUNK : w.k1;
         const uint32_t buf = it & 1u;
@@ -190,7 +229,8 @@ syrk_kernel(const __grid_constant__ CUtensorMap tmap, float* __restrict__ H, lon
             umma_f16(d_tmem, da, db, IDESC, (k > kc || kk > 0) ? 1u : 0u);
           }
           issued = true;
-          umma_commit(&empty[stage]);
+          if constexpr (PAIR) umma_commit_mc(&empty[stage], (uint16_t)3);   // both CTAs' copies of the stage
+          else umma_commit(&empty[stage]);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
@@ -211,8 +251,8 @@ syrk_kernel(const __grid_constant__ CUtensorMap tmap, float* __restrict__ H, lon
     uint32_t it = 0;
     bool ok = true;
     float acc[BN / 2];
-    for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
-      Unit w = decode_unit(u, g);
+    for (int u = cid; ok && u < num_units; u += ncl) {
+      Unit w = unit_of(u);
       const int i = w.r * BM + row;
       const int i_warp = w.r * BM + q * 32;
       const int jh = w.c * BN + h * (BN / 2);
@@ -278,6 +318,8 @@ syrk_kernel(const __grid_constant__ CUtensorMap tmap, float* __restrict__ H, lon
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
   }
+  // neither CTA leaves while the other may still deliver copies or arrivals to it
+  if constexpr (PAIR) cluster_sync();
 }
 
 // zero the upper triangle (i <= j) of H
@@ -349,19 +391,64 @@ gptq_status syrk_accumulate(const uint16_t* X, long long n, long long d, long lo
   for (int r = 0; r < g.nr; ++r) tiles += g.nc - (r * BM) / BN;
   g.tiles = (int)tiles;
   g.kiters = (int)((n + BK - 1) / BK);
+  g.npairs = 0;
   const int sms = sm_count();
-  g.parts = choose_parts(tiles, g.kiters, sms);
-  const long long units = tiles * g.parts;
-  const int grid = (int)std::min<long long>(units, sms);
 
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(syrk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
-      return set_error(GPTQ_ERR_CUDA, "cudaFuncSetAttribute(syrk_kernel) failed");
-    attr_set = true;
+  static bool attr_set[2] = {false, false};
+  for (int k = 0; k < 2; ++k)
+    if (!attr_set[k]) {
+      if (cudaFuncSetAttribute(k ? syrk_kernel<true> : syrk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               SMEM_BYTES) != cudaSuccess)
+        return set_error(GPTQ_ERR_CUDA, "cudaFuncSetAttribute(syrk_kernel) failed");
+      attr_set[k] = true;
+    }
+
+  // Paired mode when every 128-row tile has its partner: d a multiple of 256.
+  int clusters = 0;
+  if (d % BN == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * (sms / 2)));
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&clusters, syrk_kernel<true>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      clusters = 0;
+    }
   }
   ProfScope ps("hessian.syrk", stream);
-  syrk_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(tmap, H, ldh, g, alpha, device_error_word());
+  if (clusters > 0) {
+    g.npairs = (g.nc * (g.nc + 1)) / 2;
+    g.parts = choose_parts(g.npairs, g.kiters, clusters);
+    const long long units = (long long)g.npairs * g.parts;
+    const int ncl = (int)std::min<long long>(units, clusters);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * ncl));
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, syrk_kernel<true>, tmap, H, ldh, g, alpha, device_error_word()) != cudaSuccess)
+      return check_launch("syrk_kernel (paired)");
+  } else {
+    g.parts = choose_parts(tiles, g.kiters, sms);
+    const long long units = tiles * g.parts;
+    const int grid = (int)std::min<long long>(units, sms);
+    syrk_kernel<false><<<grid, THREADS, SMEM_BYTES, stream>>>(tmap, H, ldh, g, alpha, device_error_word());
+  }
   count_launch();
   return check_launch("syrk_kernel");
 }
