@@ -15,7 +15,7 @@
 //   prep_kernel        fp32 working copy of W in processing order; NaN/Inf check
 //   rowstats_kernel    per-channel mode: scale and zero of every row from W before any update
 //   diag_info_kernel   per column: Hinv1[j][j], RN(1 / Hinv1[j][j]) and Hinv1[j][j+1]
-//   colblock_kernel<BS> eight lanes per row (4 rows per warp, 32 per CTA); the whole
+//   colblock_kernel<BS, LANES> 8 or 16 lanes per row (32 rows per CTA); the whole
 //                      block of each row in registers; Hinv1's diagonal block by bulk
 //                      asynchronous copies; group min/max by shuffles; Err1, codes and
 //                      per-column loss partials (the CTA's 32 rows in a fixed order)
@@ -144,33 +144,38 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 }
 
 // ---------------------------------------------------------------------------------
-// Column block. Four lanes per row, eight rows per warp, four warps (32 rows) per CTA.
+// Column block. LANES lanes per row (8 or 16), 32 / LANES rows per warp, 32 rows per
+// CTA.
 //
 // The block's weights stay in registers for the whole block: lane q of a row holds
-// columns 16 k + 4 q + j (slot 4 k + j). Columns are visited in 16-column steps; after
-// each step the slots move down by four, so the step's columns are always slots 0..3
-// and the loop body is the same for every step. Steps come in pairs, and every pair
-// drops the four slots that no longer hold a live column (triangular work).
+// columns KW k + 4 q + j (slot 4 k + j), KW = 4 LANES. Columns are visited in
+// KW-column steps; after each step the slots move down by four, so the step's columns
+// are always slots 0..3 and the loop body is the same for every step. Later phases
+// drop the slots that no longer hold a live column (triangular work).
 //
-// At column t all four lanes of a row hold its current value x and quantize it
+// At column t all lanes of a row hold its current value x and quantize it
 // identically; every lane then moves all its slots by -Err1 * Hinv1[t][col]
 // (multiply, then subtract: the listing's float32 rounding). The value of column t+1
 // is fetched from its owner by a shuffle BEFORE that update and updated locally with
 // the same two operations, so the shuffle is off the dependent chain of a column.
 //
 // Hinv1's diagonal block arrives by bulk asynchronous copies of each row's upper part,
-// one mbarrier per 16-row step. Errors and codes collect in shared memory and leave at
-// the end: Err1 row-major for the lazy update, codes packed into the output bitstream
-// (or as bytes for act-order), per-column loss sums over the CTA's rows in a fixed
-// order.
-constexpr int LANES = 8;                             // lanes per row
-constexpr int ROWS_PER_WARP = 32 / LANES;            // 4
-constexpr int CB_WARPS = ROWS_PER_CTA / ROWS_PER_WARP;   // 8
-constexpr int CB_THREADS = CB_WARPS * 32;           // 256
-constexpr int KW = 4 * LANES;                        // columns per step
+// one mbarrier per step. Errors and codes collect in shared memory and leave at the
+// end: Err1 row-major for the lazy update, codes packed into the output bitstream (or
+// as bytes for act-order), per-column loss sums over the CTA's rows in a fixed order.
+//
+// Lanes per row (LANES): 16 for 128-column blocks whose groups start on 64-column
+// steps (two rows per warp, 16 warps per CTA, so each scheduler has four warps to hide
+// the column chain's latency), else 8. A step of 4 * LANES columns must fit in the
+// block, and group statistics are taken at step starts.
+template <int LANES> constexpr int cb_threads() { return ROWS_PER_CTA * LANES; }
+// Steps per phase: a phase is one inlined copy of the step with a fixed number of live
+// slots; with 16 lanes a block has only two steps, so each gets its own.
+template <int LANES> constexpr int cb_steps_per_phase() { return LANES >= 16 ? 1 : 2; }
 
-template <int BS>
+template <int BS, int LANES>
 struct CBSmem {
+  static constexpr int KW = 4 * LANES;               // columns per step
   static constexpr int ELD = BS + 1;                 // padded row of the error tile
   static constexpr int CLD = BS + 4;                 // padded row of the code tile (bytes)
   static constexpr size_t us = 0;
@@ -205,12 +210,13 @@ struct CBArgs {
   int* err_word;
 };
 
-template <int NSA, int BS>
+template <int NSA, int BS, int LANES>
 __device__ __forceinline__ void cb_step(float (&w)[BS / LANES], float& x, int k, int q, int qbase, int row, float s,
                                         float inv_s, float z, float qmax, const float* __restrict__ Us,
                                         const float4* __restrict__ dinfo, float* __restrict__ Es,
                                         uint8_t* __restrict__ Cs) {
-  constexpr int ELD = CBSmem<BS>::ELD, CLD = CBSmem<BS>::CLD;
+  using SL = CBSmem<BS, LANES>;
+  constexpr int ELD = SL::ELD, CLD = SL::CLD, KW = SL::KW;
   // Branch-free column bodies, so the scheduler can overlap one column's updates with
   // the next column's shuffle, loads and quantization. Columns past the end of a ragged
   // block, and rows past m, run on dead values whose stores are never read back; their
@@ -254,16 +260,23 @@ __device__ __forceinline__ void cb_step(float (&w)[BS / LANES], float& x, int k,
   for (int sl = 0; sl < NSA - 4; ++sl) w[sl] = w[sl + 4];
 }
 
-template <int NS, class F, int... P>
+// Phase P covers steps [SPP P, SPP P + SPP) with the NS - 4 SPP P slots that can still
+// hold a live column there.
+template <int NS, int SPP, class F, int... P>
 __device__ __forceinline__ void for_phases(F&& f, std::integer_sequence<int, P...>) {
-  (f(std::integral_constant<int, NS - 8 * P>{}, 2 * P), ...);
+  (f(std::integral_constant<int, NS - 4 * SPP * P>{}, SPP * P), ...);
 }
 
-template <int BS>
-__global__ void __launch_bounds__(CB_THREADS, 1) colblock_kernel(CBArgs a) {
+template <int BS, int LANES>
+__global__ void __launch_bounds__(cb_threads<LANES>(), 1) colblock_kernel(CBArgs a) {
+  constexpr int ROWS_PER_WARP = 32 / LANES;
+  constexpr int CB_THREADS = cb_threads<LANES>();
+  constexpr int SPP = cb_steps_per_phase<LANES>();
+  constexpr int KW = 4 * LANES;                      // columns per step
   constexpr int NS = BS / LANES;                     // slots per lane
   constexpr int KS = BS / KW;                        // steps
-  using SL = CBSmem<BS>;
+  static_assert(KS >= 1 && BS % KW == 0, "a block holds whole steps");
+  using SL = CBSmem<BS, LANES>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   float* Us = reinterpret_cast<float*>(smem_raw + SL::us);      // Us[t * BS + c] = Hinv1[i1 + t][i1 + c], c >= t
   float4* dinfo = reinterpret_cast<float4*>(smem_raw + SL::dinfo);
@@ -342,12 +355,12 @@ __global__ void __launch_bounds__(CB_THREADS, 1) colblock_kernel(CBArgs a) {
 
   float x = __shfl_sync(0xffffffffu, w[0], qbase);    // column 0 (slot 0 of lane 0)
 
-  // One phase: two 16-column steps with NSA live slots per lane (inlined once per
-  // phase; the two steps share the code).
+  // One phase: SPP steps of KW columns with NSA live slots per lane (inlined once per
+  // phase; the phase's steps share the code).
   auto phase = [&](auto nsa_c, int kbeg) {
     constexpr int NSA = decltype(nsa_c)::value;
 #pragma unroll 1
-    for (int k = kbeg; k < kbeg + 2 && k < nks; ++k) {
+    for (int k = kbeg; k < kbeg + SPP && k < nks; ++k) {
       if (a.bulk) {
         const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[k], 0, abort_flag));
         if (!ok && lane == 0) {
@@ -382,11 +395,11 @@ __global__ void __launch_bounds__(CB_THREADS, 1) colblock_kernel(CBArgs a) {
           a.zeros[(long long)r * a.G + j0 / a.g] = z;
         }
       }
-      cb_step<NSA, BS>(w, x, k, q, qbase, row, s, inv_s, z, qmax, Us, dinfo, Es, Cs);
+      cb_step<NSA, BS, LANES>(w, x, k, q, qbase, row, s, inv_s, z, qmax, Us, dinfo, Es, Cs);
     }
   };
   // each phase runs with the slots that can still hold a live column
-  for_phases<NS>(phase, std::make_integer_sequence<int, (KS + 1) / 2>{});
+  for_phases<NS, SPP>(phase, std::make_integer_sequence<int, (KS + SPP - 1) / SPP>{});
 
   __syncthreads();
   if (*abort_flag) return;
@@ -544,11 +557,11 @@ Layout layout(long long m, long long d, int blocksize) {
   return L;
 }
 
-template <int BS>
+template <int BS, int LANES>
 gptq_status run_blocks(CBArgs a, const float* Ut, const float* Ut_lo, cudaStream_t s) {
-  using SL = CBSmem<BS>;
-  if (cudaFuncSetAttribute(colblock_kernel<BS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SL::total) !=
-      cudaSuccess)
+  using SL = CBSmem<BS, LANES>;
+  if (cudaFuncSetAttribute(colblock_kernel<BS, LANES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)SL::total) != cudaSuccess)
     return set_error(GPTQ_ERR_CUDA, "cudaFuncSetAttribute(colblock_kernel) failed");
   const int m = a.m, d = a.d;
   const int nrg = (m + ROWS_PER_CTA - 1) / ROWS_PER_CTA;
@@ -577,7 +590,8 @@ gptq_status run_blocks(CBArgs a, const float* Ut, const float* Ut_lo, cudaStream
       a.eoff = i1 - o1;
       {
         ProfScope ps("quantize.colblock", s);
-        if (launch_pdl(colblock_kernel<BS>, dim3(nrg), dim3(CB_THREADS), SL::total, s, a) != cudaSuccess)
+        if (launch_pdl(colblock_kernel<BS, LANES>, dim3(nrg), dim3(cb_threads<LANES>()), SL::total, s, a) !=
+            cudaSuccess)
           return check_launch("colblock_kernel");
         count_launch();
       }
@@ -643,9 +657,12 @@ gptq_status quantize_launch(const void* W, int w_dtype, long long m_, long long 
   a.err_word = device_error_word();
   gptq_status st;
   switch (blocksize) {
-    case 32: st = run_blocks<32>(a, Ut, Ut_lo, s); break;
-    case 64: st = run_blocks<64>(a, Ut, Ut_lo, s); break;
-    default: st = run_blocks<128>(a, Ut, Ut_lo, s); break;
+    case 32: st = run_blocks<32, 8>(a, Ut, Ut_lo, s); break;
+    case 64: st = run_blocks<64, 8>(a, Ut, Ut_lo, s); break;
+    default:
+      // 64-column steps need groups that start on them
+      st = (a.stats_given || g % 64 == 0) ? run_blocks<128, 16>(a, Ut, Ut_lo, s) : run_blocks<128, 8>(a, Ut, Ut_lo, s);
+      break;
   }
   if (st) return st;
   loss_finalize_kernel<<<(d + 255) / 256, 256, 0, s>>>(part, L.nrg, d, perm, col_losses);
