@@ -17,12 +17,14 @@
 //   diag_stats      lambda and the finiteness check of diag(H)
 //   perm_rank       stable descending sort of diag(H) by rank counting (act-order)
 //   gather          P[a][b] = H_d[p(d-1-a)][p(d-1-b)] (lower triangle), p = act-order
-//   Cholesky, 128-wide blocks, right-looking:
+//   Cholesky, 128-wide blocks, right-looking with a look-ahead of one panel:
 //     chol_panel    one launch per 128-wide panel: every CTA factors the diagonal block
-//                   (32-column tall panels in one warp's registers) and solves 32 rows
+//                   (32-column tall panels in one warp's registers) and solves 128 rows
 //                   below it; CTA 0 writes L11, the others their rows of L21
-//     tc_gemm       trailing update A22 -= L21 L21^T (lower tiles; tensor cores,
-//                   3 x TF32, both operands K-major)
+//     tc_gemm       trailing update A22 -= L21 L21^T (tensor cores, 3 x TF32, both
+//                   operands K-major) in two launches: the next panel's column block
+//                   first, then the lower tiles right of it, which run on the SMs the
+//                   next panel leaves free while that panel is factored
 //   Triangular inverse X = L^-1 (natural order, inside Hinv1):
 //     diag_inverse  every 64 x 64 diagonal block at once (thread c solves L x = e_c)
 //     tc_gemm x 2 + a transpose per level, recursive doubling over block pairs (A, C)
@@ -51,6 +53,7 @@ struct Header {               // at the start of the factor workspace
   int d;
   int failed;                 // non-zero once a pivot failed or diag(H) is not finite
   int timeout;                // a bounded wait gave up
+  unsigned ready;             // warps of trailing-update tiles of tile column 0 stored so far
 };
 constexpr size_t kHeaderBytes = 256;
 
@@ -80,6 +83,7 @@ __global__ void diag_stats_kernel(const float* __restrict__ H, int d, float perc
     hdr->d = d;
     hdr->failed = bad_s;
     hdr->timeout = 0;
+    hdr->ready = 0;
   }
 }
 
@@ -138,7 +142,7 @@ __global__ void gather_kernel(const float* __restrict__ H, int d, const int* __r
 // with the identity.
 constexpr int NB = 128;                        // panel width
 constexpr int SB = 32;                         // sub-panel width
-constexpr int RB = 32;                         // rows below per CTA
+constexpr int RB = 64;                         // rows below per CTA (RB / SB row groups)
 constexpr int PANEL_THREADS = 256;
 constexpr int SLD = NB + 4;                    // padded row of the shared tiles (rows stay 16-byte aligned)
 constexpr int TLD = SB + 4;                    // padded row of Lt
@@ -274,9 +278,13 @@ __device__ __forceinline__ void piece_update(const BlockTask& bt, int ui, int uj
     for (int y = 0; y < 4; ++y) bt.C[(ui + 8 * x) * SLD + uj + 8 * y] -= acc[x][y];
 }
 
-__global__ void __launch_bounds__(PANEL_THREADS, 2) chol_panel_kernel(float* __restrict__ P, float* __restrict__ Lsave,
-                                                                      float* __restrict__ Plo, int d, int k0, int vec,
-                                                                      Header* hdr, int* err_word) {
+static_assert(RB % SB == 0 && RB <= PANEL_THREADS - NB, "one copy-issuing thread per row below");
+static_assert(3 + RB / SB <= PANEL_THREADS / 32, "one warp per row group in phase B");
+
+// The panel step; `plain` loads its tiles with ordinary loads (they were published by a
+// counter, see chol_panel_kernel) instead of bulk asynchronous copies.
+__device__ __noinline__ void chol_panel_body(float* __restrict__ P, float* __restrict__ Lsave, float* __restrict__ Plo,
+                                                int d, int k0, int vec, bool plain, Header* hdr, int* err_word) {
   extern __shared__ __align__(16) float psm[];
   float* S = psm;                      // NB x SLD: the diagonal block, then L11 (lower)
   float* R = S + NB * SLD;             // RB x SLD: this CTA's rows below, then its rows of L21
@@ -284,18 +292,32 @@ __global__ void __launch_bounds__(PANEL_THREADS, 2) chol_panel_kernel(float* __r
   float* dinv = Lt + SB * TLD;         // NB
   int* fail_s = reinterpret_cast<int*>(dinv + NB);
   uint64_t* bar = reinterpret_cast<uint64_t*>(dinv + NB + 2);   // 8-byte aligned
-  grid_dep_wait();                     // the previous trailing update
-  grid_dep_launch();
   if (hdr->failed) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nb = min(NB, d - k0), k1 = k0 + nb;
   const bool below = blockIdx.x > 0;
   const int rbeg = k1 + (blockIdx.x - 1) * RB;               // first row below handled here
   const int nr = below ? min(RB, d - rbeg) : 0;
+  const int nrg = (nr + SB - 1) / SB;                        // row groups of R in use
 
   // The lower triangle of the diagonal block (pieces of four columns up to the
   // diagonal) and the rows below; the identity past a ragged end.
-  if (vec) {
+  if (vec && plain) {
+    // whole rows (the part above the diagonal is never read as L), 16 bytes at a time
+    constexpr int Q = NB / 4;
+    for (int idx = tid; idx < nb * Q; idx += PANEL_THREADS) {
+      const int i = idx / Q, c4 = 4 * (idx - i * Q);
+      if (c4 < nb)
+        *reinterpret_cast<float4*>(S + i * SLD + c4) =
+            *reinterpret_cast<const float4*>(P + (long long)(k0 + i) * d + k0 + c4);
+    }
+    for (int idx = tid; idx < nr * Q; idx += PANEL_THREADS) {
+      const int i = idx / Q, c4 = 4 * (idx - i * Q);
+      if (c4 < nb)
+        *reinterpret_cast<float4*>(R + i * SLD + c4) =
+            *reinterpret_cast<const float4*>(P + (long long)(rbeg + i) * d + k0 + c4);
+    }
+  } else if (vec) {
     // one bulk asynchronous copy per row: row i of the diagonal block up to the end of
     // the four-column piece holding the diagonal, full rows of R
     if (tid == 0) {
@@ -358,11 +380,11 @@ __global__ void __launch_bounds__(PANEL_THREADS, 2) chol_panel_kernel(float* __r
       fail = __reduce_min_sync(0xffffffffu, fail < 0 ? INT_MAX : fail);
       if (lane == 0 && fail != INT_MAX && fail < nb) *fail_s = fail;
     } else if (p > 0) {
-      // blocks (I, J), p <= J <= I <= 3, but not (p, p); then R[:, q], q >= p; all
-      // against column block p - 1
+      // blocks (I, J), p <= J <= I <= 3, but not (p, p); then R[g][q], q >= p, for every
+      // row group g of R; all against column block p - 1
       const int q0 = c0 - SB;
       const int ndiag = (4 - p) * (5 - p) / 2 - 1;
-      const int ntask = ndiag + (below ? 4 - p : 0);
+      const int ntask = ndiag + nrg * (4 - p);
       for (int u = tid - 32; u < ntask * 64; u += PANEL_THREADS - 32) {
         const int t = u >> 6;
         BlockTask bt;
@@ -372,8 +394,9 @@ __global__ void __launch_bounds__(PANEL_THREADS, 2) chol_panel_kernel(float* __r
           const int J = p + n;
           bt = BlockTask{S + SB * I * SLD + SB * J, S + SB * I * SLD + q0, S + SB * J * SLD + q0};
         } else {
-          const int q = p + (t - ndiag);
-          bt = BlockTask{R + SB * q, R + q0, S + SB * q * SLD + q0};
+          const int tt = t - ndiag, q = p + tt % (4 - p);
+          float* Rg = R + (tt / (4 - p)) * SB * SLD;
+          bt = BlockTask{Rg + SB * q, Rg + q0, S + SB * q * SLD + q0};
         }
         piece_update(bt, (u & 63) >> 3, u & 7);
       }
@@ -385,7 +408,8 @@ __global__ void __launch_bounds__(PANEL_THREADS, 2) chol_panel_kernel(float* __r
       const int ngrp = 3 - p;
       if (warp < ngrp) solve32(std::make_integer_sequence<int, SB>{}, S + (c0 + SB * (warp + 1)) * SLD + c0, Lt,
                                dinv + c0, lane);
-      else if (warp == ngrp && below) solve32(std::make_integer_sequence<int, SB>{}, R + c0, Lt, dinv + c0, lane);
+      else if (warp - ngrp < nrg)
+        solve32(std::make_integer_sequence<int, SB>{}, R + (warp - ngrp) * SB * SLD + c0, Lt, dinv + c0, lane);
     }
     __syncthreads();
     // ---- C: the next diagonal sub-block, 2 x 2 outputs per thread (rows ri + 16a,
@@ -449,6 +473,51 @@ __global__ void __launch_bounds__(PANEL_THREADS, 2) chol_panel_kernel(float* __r
   }
 }
 constexpr size_t PANEL_SMEM = (size_t)((NB + RB) * SLD + SB * TLD + NB + 4) * sizeof(float);   // + flag, mbarrier
+// Shared memory reserved per panel CTA: more than half an SM's, so no two CTAs of the
+// latency-bound panel share an SM (the trailing update leaves it a few free SMs at a time).
+constexpr size_t PANEL_SMEM_RESERVED = PANEL_SMEM > 120 * 1024 ? PANEL_SMEM : 120 * 1024;
+
+// Wait until *ctr >= target (wrapping compare), reading with acquire semantics at gpu
+// scope; gives up after kWaitLimitNs.
+__device__ __forceinline__ bool wait_counter_bounded(const unsigned* ctr, unsigned target) {
+  const unsigned long long t0 = global_timer_ns();
+  for (;;) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if ((int)(v - target) >= 0) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    __nanosleep(128);
+  }
+}
+
+// One 128-wide panel step. Without `ready` it waits for the kernel before it (the
+// previous trailing update) to complete. With it (look-ahead), that update is still
+// running: it publishes its tiles of this panel's column block by adding to *ready,
+// and this panel starts once *ready reaches ready_target; only the completion of this
+// grid waits for the update's, so the next kernel still sees both.
+__global__ void __launch_bounds__(PANEL_THREADS, 2) chol_panel_kernel(float* __restrict__ P, float* __restrict__ Lsave,
+                                                                      float* __restrict__ Plo, int d, int k0, int vec,
+                                                                      const unsigned* ready, unsigned ready_target,
+                                                                      Header* hdr, int* err_word) {
+  if (!ready) {
+    grid_dep_wait();
+    grid_dep_launch();
+    chol_panel_body(P, Lsave, Plo, d, k0, vec, false, hdr, err_word);
+    return;
+  }
+  grid_dep_launch();
+  __shared__ int ok_s;
+  if (threadIdx.x == 0) ok_s = wait_counter_bounded(ready, ready_target) ? 1 : 0;
+  __syncthreads();
+  if (ok_s) {
+    chol_panel_body(P, Lsave, Plo, d, k0, vec, true, hdr, err_word);
+  } else if (threadIdx.x == 0) {
+    report_device_error(err_word, DEVERR_TIMEOUT);
+    hdr->timeout = 1;
+    hdr->failed = 1;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) grid_dep_wait();
+}
 
 // P[k0 + i][k0 + c] = Lsave[k0 + i][k0 + c] for the lower triangle of every diagonal
 // block (blockIdx.y = block, 8 rows per CTA in x)
@@ -551,10 +620,13 @@ __global__ void pair_transpose_kernel(float* __restrict__ M, int d, int sz, int 
 
 }  // namespace factor
 
-// header | P (d x d) | Plo (d x 128: low parts of the current panel's L21)
+// header | P (d x d) | Plo[2] (d x 128 each: low parts of L21 of the even and the odd
+// panels; a panel writes its own while the trailing update of the one before still reads
+// the other)
 size_t factor_workspace_bytes(long long d) {
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  return factor::kHeaderBytes + al((size_t)d * (size_t)d * sizeof(float)) + al((size_t)d * factor::NB * sizeof(float));
+  return factor::kHeaderBytes + al((size_t)d * (size_t)d * sizeof(float)) +
+         2 * al((size_t)d * factor::NB * sizeof(float));
 }
 
 gptq_status factor_launch(const float* H, long long d_, float percdamp, int act_order, int32_t* perm_out,
@@ -563,8 +635,10 @@ gptq_status factor_launch(const float* H, long long d_, float percdamp, int act_
   const int d = (int)d_;
   Header* hdr = reinterpret_cast<Header*>(ws);
   float* P = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + kHeaderBytes);
-  float* Plo = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + kHeaderBytes +
-                                        (((size_t)d * (size_t)d * sizeof(float) + 255) & ~(size_t)255));
+  float* Plo0 = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + kHeaderBytes +
+                                         (((size_t)d * (size_t)d * sizeof(float) + 255) & ~(size_t)255));
+  const size_t plo_stride = (((size_t)d * NB * sizeof(float) + 255) & ~(size_t)255) / sizeof(float);
+  auto plo = [&](int k0) { return Plo0 + ((k0 / NB) & 1) * plo_stride; };
   const int* failed = &hdr->failed;
   const bool vec = (d % 4 == 0) && simt::aligned16(P) && simt::aligned16(Hinv1);
 
@@ -584,32 +658,49 @@ gptq_status factor_launch(const float* H, long long d_, float percdamp, int act_
   }
   if (gptq_status st = check_launch("factor setup kernels")) return st;
 
-  if (cudaFuncSetAttribute(chol_panel_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PANEL_SMEM) !=
+  if (cudaFuncSetAttribute(chol_panel_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PANEL_SMEM_RESERVED) !=
       cudaSuccess)
     return set_error(GPTQ_ERR_CUDA, "cudaFuncSetAttribute(chol_panel_kernel) failed");
 
-  // ---- Cholesky P = L L^T, 64-wide blocks, right-looking
+  // ---- Cholesky P = L L^T, 128-wide panels, right-looking with a look-ahead of one
+  // panel. The trailing update after panel k computes its tiles column by column, so
+  // panel k+1's column block comes first; each stored tile of it is published on
+  // hdr->ready (8 per tile), and panel k+1, already resident, starts when all of them
+  // are, while the rest of the update runs on the SMs it leaves free. (Through the FFMA
+  // GEMM, which publishes nothing, the panels wait for whole kernels instead.)
+  auto panel_ctas = [](int below) { return 1 + (below + RB - 1) / RB; };
+  const bool lookahead = vec && tc_gemm_available();
+  unsigned ready_target = 0;
   for (int k0 = 0; k0 < d; k0 += NB) {
     const int nb = std::min(NB, d - k0), k1 = k0 + nb, below = d - k1;
+    const bool flagged = lookahead && k0 > 0;
     {
       ProfScope ps("factor.chol_panel", s);
-      if (launch_pdl(chol_panel_kernel, dim3(1 + (below + RB - 1) / RB), dim3(PANEL_THREADS), PANEL_SMEM, s, P, Hinv1,
-                     Plo, d, k0, vec ? 1 : 0, hdr, device_error_word()) != cudaSuccess)
+      if (launch_pdl(chol_panel_kernel, dim3(panel_ctas(below)), dim3(PANEL_THREADS), PANEL_SMEM_RESERVED, s, P, Hinv1,
+                     plo(k0), d, k0, vec ? 1 : 0, flagged ? &hdr->ready : nullptr, ready_target, hdr,
+                     device_error_word()) != cudaSuccess)
         return check_launch("chol_panel_kernel");
       count_launch();
     }
     if (below > 0) {
+      // A22 -= L21 L21^T over the lower tiles of P[k1:, k1:]
       simt::GemmArgs g{};
       g.M = g.N = below; g.K = nb; g.M_last = below; g.K_last = nb;
       g.A = P + (long long)k1 * d + k0; g.lda = d;
       g.B = g.A; g.ldb = d;
-      g.A_lo = Plo + (long long)k1 * NB; g.lda_lo = NB;
+      g.A_lo = plo(k0) + (long long)k1 * NB; g.lda_lo = NB;
       g.B_lo = g.A_lo; g.ldb_lo = NB;
       g.C = P + (long long)k1 * d + k1; g.ldc = d;
       g.alpha = -1.0f; g.beta = 1.0f;
-      g.lower_tiles = 1;
+      g.lower_tiles = lookahead ? 2 : 1;
       g.vec = vec;
       g.skip = failed;
+      if (lookahead) {
+        const int below_next = below - std::min(NB, below);
+        g.signal = &hdr->ready;
+        g.max_ctas = std::max(1, sm_count() - panel_ctas(below_next));
+        ready_target += 8u * (unsigned)((below + 127) / 128);   // tiles of tile column 0
+      }
       ProfScope ps("factor.chol_update_gemm", s);
       if (gptq_status st = tc_gemm(g, 1, true, true, s)) return st;
     }

@@ -29,9 +29,9 @@ namespace {
 
 constexpr long long kStaticMaxD = 2048;
 // status header (256 bytes) + the d x d fp32 matrix the factorization works in + the
-// low parts of one 128-column panel (d x 128 fp32)
+// low parts of two 128-column panels (2 x d x 128 fp32)
 constexpr size_t kStaticScratchBytes =
-    256 + (size_t)kStaticMaxD * kStaticMaxD * sizeof(float) + (size_t)kStaticMaxD * 128 * sizeof(float);
+    256 + (size_t)kStaticMaxD * kStaticMaxD * sizeof(float) + 2 * (size_t)kStaticMaxD * 128 * sizeof(float);
 
 static __device__ __align__(256) unsigned char g_factor_scratch[kStaticScratchBytes];
 

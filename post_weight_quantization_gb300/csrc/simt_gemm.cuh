@@ -44,11 +44,16 @@ struct GemmArgs {
   long long lda_lo;
   const float* B_lo;
   long long ldb_lo;
-  int lower_tiles;        // C square: only tiles with J <= I
+  int lower_tiles;        // C square: only tiles with J <= I (1: row by row; 2: column by column,
+                          // so tile column 0 is computed in the first round)
   int a_tri;              // 1: A lower triangular, 2: A upper triangular (masked)
   int b_lower;            // B(k, j) == 0 for k < j
   int vec;                // every operand 16-byte aligned with leading dimensions % 4 == 0
   const int* skip;        // non-null and non-zero: do nothing (an earlier step failed)
+  // Tensor-core GEMM only (the FFMA GEMM ignores them):
+  int max_ctas;           // > 0: at most this many persistent CTAs (leave SMs to the next kernel)
+  unsigned* signal;       // lower_tiles == 2: +1 per epilogue warp (8 per tile) once a tile of
+                          // tile column 0 is stored, after a gpu-scope fence
 };
 
 struct Acc {
@@ -249,5 +254,8 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // Same operation on the tensor cores (3 x TF32, tc_gemm.cu); falls back to simt::gemm
 // when TMA cannot describe an operand, or when GPTQ_FFMA_GEMM=1.
 gptq_status tc_gemm(const simt::GemmArgs& g, int batches, bool a_kmaj, bool b_kmaj, cudaStream_t s);
+// True when tc_gemm runs its K-major, 16-byte-aligned, single-batch calls on the tensor
+// cores (the driver's tensor-map entry point resolves and GPTQ_FFMA_GEMM is not set).
+bool tc_gemm_available();
 
 }  // namespace gptq

@@ -62,6 +62,7 @@ struct Params {
   int M, N, K, M_last, K_last, batches;
   int tiles_per_batch, mt, nt;
   int lower_tiles, a_tri, b_lower;
+  unsigned* signal;
   float alpha, beta;
   float* C;
   long long ldc, c_bs;
@@ -76,7 +77,13 @@ __device__ __forceinline__ Tile decode(int t, const Params& p) {
   Tile w;
   w.z = t / p.tiles_per_batch;
   const int u = t - w.z * p.tiles_per_batch;
-  if (p.lower_tiles) {
+  if (p.lower_tiles == 2) {
+    // column by column: tile column J starts at J mt - J (J - 1) / 2
+    int J = 0;
+    while (J + 1 < p.mt && u >= (J + 1) * p.mt - (J + 1) * J / 2) ++J;
+    w.J = J;
+    w.I = J + (u - (J * p.mt - J * (J - 1) / 2));
+  } else if (p.lower_tiles) {
     int I = (int)((sqrtf(8.0f * (float)u + 1.0f) - 1.0f) * 0.5f);
     while ((I + 1) * (I + 2) / 2 <= u) ++I;
     while (I * (I + 1) / 2 > u) --I;
@@ -389,6 +396,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         }
         __syncwarp();
       }
+      if (p.signal && w.J == 0) {
+        // this warp's part of a tile of column 0 is stored: publish it (gpu scope)
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(p.signal, 1u);
+      }
     }
   }
 
@@ -434,14 +447,20 @@ bool make_map(CUtensorMap* m, const float* base, long long inner, long long oute
 // Operand extents: A is M x K (K-major: rows M of k; MN-major: rows K of m), B is K x N.
 // Falls back to the FFMA GEMM when an operand cannot be described to TMA (16-byte
 // alignment of bases and strides).
-gptq_status tc_gemm(const simt::GemmArgs& g, int batches, bool a_kmaj, bool b_kmaj, cudaStream_t s) {
-  using namespace tc;
-  if (g.M <= 0 || g.N <= 0 || batches <= 0) return GPTQ_OK;
-  static const bool force_ffma = [] {
+static bool force_ffma() {
+  static const bool f = [] {
     const char* v = getenv("GPTQ_FFMA_GEMM");
     return v && v[0] == '1';
   }();
-  if (force_ffma) return simt::gemm(g, batches, a_kmaj, b_kmaj, s);
+  return f;
+}
+
+bool tc_gemm_available() { return !force_ffma() && tc::encode_fn() != nullptr; }
+
+gptq_status tc_gemm(const simt::GemmArgs& g, int batches, bool a_kmaj, bool b_kmaj, cudaStream_t s) {
+  using namespace tc;
+  if (g.M <= 0 || g.N <= 0 || batches <= 0) return GPTQ_OK;
+  if (force_ffma()) return simt::gemm(g, batches, a_kmaj, b_kmaj, s);
   if (batches > 1 && (g.M_last != g.M || g.K_last != g.K)) {
     // a ragged last batch gets its own launch with exact extents, so no tensor map
     // describes memory past the end of an operand
@@ -486,11 +505,12 @@ gptq_status tc_gemm(const simt::GemmArgs& g, int batches, bool a_kmaj, bool b_km
   p.nt = (g.N + BN - 1) / BN;
   p.tiles_per_batch = g.lower_tiles ? p.mt * (p.mt + 1) / 2 : p.mt * p.nt;
   p.lower_tiles = g.lower_tiles; p.a_tri = g.a_tri; p.b_lower = g.b_lower;
+  p.signal = (g.lower_tiles == 2) ? g.signal : nullptr;
   p.alpha = g.alpha; p.beta = g.beta;
   p.C = g.C; p.ldc = g.ldc; p.c_bs = g.c_bs;
   p.skip = g.skip;
   const int ntiles = p.tiles_per_batch * batches;
-  const int grid = std::min(ntiles, sm_count());
+  const int grid = std::min(ntiles, g.max_ctas > 0 ? std::min(g.max_ctas, sm_count()) : sm_count());
 
   auto launch = [&](auto kern, int key) -> gptq_status {
     static bool attr_done[2] = {false, false};
