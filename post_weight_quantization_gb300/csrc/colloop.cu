@@ -579,6 +579,7 @@ gptq_status run_blocks(CBArgs a, const float* Ut, const float* Ut_lo, cudaStream
     ga.C = const_cast<float*>(a.Wf) + c0; ga.ldc = d;
     ga.alpha = -1.0f; ga.beta = 1.0f;
     ga.vec = vec;
+    ga.b_final = 1;             // Ut is written once, before the first column block
     ProfScope ps2("quantize.lazy_gemm", s);
     return tc_gemm(ga, 1, true, true, s);
   };

@@ -54,6 +54,9 @@ struct GemmArgs {
   int max_ctas;           // > 0: at most this many persistent CTAs (leave SMs to the next kernel)
   unsigned* signal;       // lower_tiles == 2: +1 per epilogue warp (8 per tile) once a tile of
                           // tile column 0 is stored, after a gpu-scope fence
+  int b_final;            // B (and B_lo) were final before the kernel ahead of this GEMM in the
+                          // stream started: their first loads may start before the dependency
+                          // wait (needs skip == nullptr)
 };
 
 struct Acc {

@@ -63,6 +63,7 @@ struct Params {
   int tiles_per_batch, mt, nt;
   int lower_tiles, a_tri, b_lower;
   unsigned* signal;
+  int b_final;
   float alpha, beta;
   float* C;
   long long ldc, c_bs;
@@ -228,26 +229,43 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   const uint32_t tmem_base = *tmem_slot;
   // everything above touched no global data; the operands and C come from earlier kernels
   grid_dep_launch();
+  const bool producer = (warp == 0 && lane == 0);
+  // With a final B, the producer first loads the B parts of its first tile's first
+  // stages (their barriers armed for the whole stage), then waits like everyone else.
+  int pre = 0;
+  if (producer && p.b_final && !p.skip && (int)blockIdx.x < p.tiles_per_batch * p.batches) {
+    const Tile w = decode(blockIdx.x, p);
+    pre = min(nchunks(w), STAGES);
+    for (int c = 0; c < pre; ++c) {
+      uint8_t* sa = smem + c * STAGE_BYTES;
+      const int k0 = w.kbeg + c * BK;
+      mbar_arrive_expect_tx(&full[c], (PRESPLIT ? 4 : 2) * OP_BYTES);
+      load_operand<B_KMAJ>(sa + OP_BYTES, &map_b, &full[c], w.J * BN, k0, w.z);
+      if constexpr (PRESPLIT) load_operand<B_KMAJ>(sa + 3 * OP_BYTES, &map_blo, &full[c], w.J * BN, k0, w.z);
+    }
+  }
   grid_dep_wait();
   const int ntiles = (p.skip && *p.skip) ? 0 : p.tiles_per_batch * p.batches;
   constexpr uint32_t IDESC = umma_idesc(/*tf32*/ 2, !A_KMAJ, !B_KMAJ, BM, BN);
 
-  if (warp == 0 && lane == 0) {
+  if (producer) {
     // ---------------- TMA producer ----------------
     int stage = 0;
     uint32_t phase = 0, armed = 0, last_phase = 0;
     bool ok = true;
+    int seq = 0;                                   // chunks issued so far
     for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
       const Tile w = decode(t, p);
-      for (int k0 = w.kbeg; k0 < w.kend; k0 += BK) {
+      for (int k0 = w.kbeg; k0 < w.kend; k0 += BK, ++seq) {
         if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
         uint8_t* sa = smem + stage * STAGE_BYTES;
-        mbar_arrive_expect_tx(&full[stage], (PRESPLIT ? 4 : 2) * OP_BYTES);
+        const bool preloaded = seq < pre;          // B parts already on their way
+        if (!preloaded) mbar_arrive_expect_tx(&full[stage], (PRESPLIT ? 4 : 2) * OP_BYTES);
         load_operand<A_KMAJ>(sa, &map_a, &full[stage], w.I * BM, k0, w.z);
-        load_operand<B_KMAJ>(sa + OP_BYTES, &map_b, &full[stage], w.J * BN, k0, w.z);
+        if (!preloaded) load_operand<B_KMAJ>(sa + OP_BYTES, &map_b, &full[stage], w.J * BN, k0, w.z);
         if constexpr (PRESPLIT) {
           load_operand<A_KMAJ>(sa + 2 * OP_BYTES, &map_alo, &full[stage], w.I * BM, k0, w.z);
-          load_operand<B_KMAJ>(sa + 3 * OP_BYTES, &map_blo, &full[stage], w.J * BN, k0, w.z);
+          if (!preloaded) load_operand<B_KMAJ>(sa + 3 * OP_BYTES, &map_blo, &full[stage], w.J * BN, k0, w.z);
         }
         armed |= 1u << stage;
         last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
@@ -339,6 +357,18 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
           asm volatile("cp.async.bulk.prefetch.L2.global [%0], 256;" ::"l"(seg) : "memory");
         }
       }
+      // Pre-split mode: this thread's C values of the first 32-column half are loaded
+      // now, so their latency hides behind the tile's loads and products.
+      float o_early[32];
+      if constexpr (PRESPLIT) {
+        const int j = w.J * BN + h * 64 + lane;
+        const float* cb = p.C + (long long)w.z * p.c_bs;
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+          const int i = w.I * BM + q * 32 + r;
+          o_early[r] = (p.beta != 0.0f && i < w.M && j < p.N) ? __ldcg(cb + (long long)i * p.ldc + j) : 0.0f;
+        }
+      }
       float acc[64];
 #pragma unroll
       for (int x = 0; x < 64; ++x) acc[x] = 0.0f;
@@ -378,7 +408,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         __syncwarp();
         const int j = w.J * BN + h * 64 + 32 * g2 + lane;
         float o[32];
-        if (p.beta != 0.0f) {
+        if (PRESPLIT && g2 == 0) {
+#pragma unroll
+          for (int r = 0; r < 32; ++r) o[r] = o_early[r];
+        } else if (p.beta != 0.0f) {
 #pragma unroll
           for (int r = 0; r < 32; ++r) {
             const int i = rbase + r;
@@ -506,6 +539,7 @@ gptq_status tc_gemm(const simt::GemmArgs& g, int batches, bool a_kmaj, bool b_km
   p.tiles_per_batch = g.lower_tiles ? p.mt * (p.mt + 1) / 2 : p.mt * p.nt;
   p.lower_tiles = g.lower_tiles; p.a_tri = g.a_tri; p.b_lower = g.b_lower;
   p.signal = (g.lower_tiles == 2) ? g.signal : nullptr;
+  p.b_final = (g.b_final && !g.skip) ? 1 : 0;
   p.alpha = g.alpha; p.beta = g.beta;
   p.C = g.C; p.ldc = g.ldc; p.c_bs = g.c_bs;
   p.skip = g.skip;
