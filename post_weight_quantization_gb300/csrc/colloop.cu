@@ -13,6 +13,7 @@
 //
 // Kernels:
 //   prep_kernel        fp32 working copy of W in processing order; NaN/Inf check
+//                      (prep_bf16x8_kernel: bf16 in natural order, 16-byte loads)
 //   rowstats_kernel    per-channel mode: scale and zero of every row from W before any update
 //   diag_info_kernel   per column: Hinv1[j][j], RN(1 / Hinv1[j][j]) and Hinv1[j][j+1]
 //   colblock_kernel<BS, LANES> 8 or 16 lanes per row (32 rows per CTA); the whole
@@ -59,6 +60,33 @@ __global__ void prep_kernel(const void* __restrict__ W, int w_dtype, int m, int 
       bad |= !isfinite(v);
       Wf[(long long)r * d + j] = v;
     }
+  }
+  if (bad) atomicOr(&hdr->nonfinite, 1);
+}
+
+// The same for bf16 W in natural order, rows 16-byte aligned: eight columns per thread.
+__global__ void prep_bf16x8_kernel(const uint16_t* __restrict__ W, int m, int d, long long ldw, float* __restrict__ Wf,
+                                   QHeader* hdr) {
+  const int q8 = d >> 3;
+  const long long n = (long long)m * q8;
+  int bad = 0;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const long long r = idx / q8;
+    const int c = (int)(idx - r * q8) << 3;
+    const uint4 v = *reinterpret_cast<const uint4*>(W + r * ldw + c);
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    float f[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      f[2 * k] = __uint_as_float(u[k] << 16);
+      f[2 * k + 1] = __uint_as_float(u[k] & 0xFFFF0000u);
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) bad |= !isfinite(f[k]);
+    float4* dst = reinterpret_cast<float4*>(Wf + r * d + c);
+    dst[0] = make_float4(f[0], f[1], f[2], f[3]);
+    dst[1] = make_float4(f[4], f[5], f[6], f[7]);
   }
   if (bad) atomicOr(&hdr->nonfinite, 1);
 }
@@ -415,13 +443,22 @@ __global__ void __launch_bounds__(cb_threads<LANES>(), 1) colblock_kernel(CBArgs
       a.err_lo[o] = e - __uint_as_float(__float_as_uint(e) & 0xFFFFE000u);
     }
   }
-  for (int t = tid; t < ncols; t += CB_THREADS) {
-    float lsum = 0.0f;
-    for (int rr = 0; rr < ROWS_PER_CTA; ++rr) {
-      const float e = (r0 + rr < a.m) ? Es[rr * ELD + t] : 0.0f;
-      lsum = __fadd_rn(lsum, __fmul_rn(__fmul_rn(e, e), 0.5f));
+  {
+    // per column, LPC adjacent lanes sum RPL rows each, then combine in a fixed order
+    constexpr int LPC = (CB_THREADS / BS) < 8 ? (CB_THREADS / BS) : 8;    // 2, 4 or 8
+    constexpr int RPL = ROWS_PER_CTA / LPC;
+    for (int base = 0; base < BS; base += CB_THREADS / LPC) {
+      const int t = base + tid / LPC, part = tid % LPC;
+      float lsum = 0.0f;
+      if (t < ncols)
+        for (int rr = part * RPL; rr < part * RPL + RPL; ++rr) {
+          const float e = (r0 + rr < a.m) ? Es[rr * ELD + t] : 0.0f;
+          lsum = __fadd_rn(lsum, __fmul_rn(__fmul_rn(e, e), 0.5f));
+        }
+#pragma unroll
+      for (int o = 1; o < LPC; o <<= 1) lsum = __fadd_rn(lsum, __shfl_xor_sync(0xffffffffu, lsum, o));
+      if (t < ncols && part == 0) a.part[(long long)blockIdx.x * d + i1 + t] = lsum;
     }
-    a.part[(long long)blockIdx.x * d + i1 + t] = lsum;
   }
   if (a.codes8) {
     for (int idx = tid; idx < ROWS_PER_CTA * BS; idx += CB_THREADS) {
@@ -636,8 +673,12 @@ gptq_status quantize_launch(const void* W, int w_dtype, long long m_, long long 
     return set_error(GPTQ_ERR_CUDA, "cudaMemsetAsync failed");
   {
     ProfScope ps("quantize.prep", s);
-    dim3 grid((unsigned)std::min(8, (d + 255) / 256), (unsigned)std::min(m, 65535));
-    prep_kernel<<<grid, 256, 0, s>>>(W, w_dtype, m, d, ldw, perm, Wf, hdr);
+    if (!perm && w_dtype == 1 && d % 8 == 0 && ldw % 8 == 0 && simt::aligned16(W) && simt::aligned16(Wf)) {
+      prep_bf16x8_kernel<<<8 * sm_count(), 256, 0, s>>>(reinterpret_cast<const uint16_t*>(W), m, d, ldw, Wf, hdr);
+    } else {
+      dim3 grid((unsigned)std::min(8, (d + 255) / 256), (unsigned)std::min(m, 65535));
+      prep_kernel<<<grid, 256, 0, s>>>(W, w_dtype, m, d, ldw, perm, Wf, hdr);
+    }
     dim3 tg((unsigned)((d + 31) / 32), (unsigned)((d + 31) / 32));
     transpose_kernel<<<tg, dim3(32, 8), 0, s>>>(Hinv1, Ut, Ut_lo, d);
     diag_info_kernel<<<(d + 255) / 256, 256, 0, s>>>(Hinv1, d, dinfo);

@@ -125,14 +125,15 @@ __global__ void gather_kernel(const float* __restrict__ H, int d, const int* __r
 // ---------------------------------------------------------------------------------
 // One Cholesky step for the 128-wide panel at k0, in one launch. Every CTA factors the
 // 128 x 128 diagonal block (the same arithmetic in every CTA, so every copy agrees;
-// CTA 0 keeps it) and CTA b >= 1 also solves the rows [k1 + 32 (b - 1), + 32) below it
-// (R), all in shared memory. The diagonal block goes in four sub-panels of 32 columns;
-// for sub-panel p, with barriers between the phases:
+// CTA 0 keeps it) and CTA b >= 1 also solves the RB rows [k1 + RB (b - 1), + RB) below
+// it (R), all in shared memory. The diagonal block goes in four sub-panels of 32
+// columns; for sub-panel p, with barriers between the phases:
 //   A  warp 0: L[p][p] = chol(S[p][p]) in registers (lane i holds row i); column j of L
 //      is broadcast through shared memory (Lt[j][*]), the next pivot's own update stays
 //      in its lane, so a column costs one shuffle, one reciprocal square root and a few
 //      dependent operations. Meanwhile warps 1-7 finish the previous sub-panel's
-//      trailing update (every block but the one factored now);
+//      trailing update of the diagonal block (every block but the one factored now)
+//      and bring column block p of R up to date with all earlier ones;
 //   B  one warp per row group (sub-panels i > p of the diagonal block, then R): the
 //      group's 32 x 32 piece of column block p solves x L[p][p]^T = a by forward
 //      substitution, one row per lane;
@@ -246,16 +247,17 @@ struct BlockTask {
   const float* B;
 };
 
-// C -= A B^T for one 4 x 4 piece of a 32 x 32 block (k < 32): rows ui + 8a and columns
-// uj + 8b, so the float4 reads of a quarter-warp fall in distinct banks.
-__device__ __forceinline__ void piece_update(const BlockTask& bt, int ui, int uj) {
+// C -= A B^T for one 4 x 4 piece of a 32 x 32 block (k < K, K a multiple of 4): rows
+// ui + 8a and columns uj + 8b, so the float4 reads of a quarter-warp fall in distinct
+// banks.
+__device__ __forceinline__ void piece_update(const BlockTask& bt, int ui, int uj, int K) {
   float acc[4][4];
 #pragma unroll
   for (int x = 0; x < 4; ++x)
 #pragma unroll
     for (int y = 0; y < 4; ++y) acc[x][y] = 0.0f;
 #pragma unroll 2
-  for (int k = 0; k < SB; k += 4) {
+  for (int k = 0; k < K; k += 4) {
     float4 a[4], b[4];
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
@@ -380,25 +382,26 @@ __device__ __noinline__ void chol_panel_body(float* __restrict__ P, float* __res
       fail = __reduce_min_sync(0xffffffffu, fail < 0 ? INT_MAX : fail);
       if (lane == 0 && fail != INT_MAX && fail < nb) *fail_s = fail;
     } else if (p > 0) {
-      // blocks (I, J), p <= J <= I <= 3, but not (p, p); then R[g][q], q >= p, for every
-      // row group g of R; all against column block p - 1
+      // Diagonal block, right-looking: blocks (I, J), p <= J <= I <= 3, but not (p, p),
+      // against column block p - 1. Rows below, left-looking: R[g][p] against all of
+      // R[g][0 .. p) at once (K = 32 p), one task per row group g; R's column blocks
+      // beyond p wait for their own phase, which keeps every phase's share of this work
+      // below the time of the sub-block Cholesky.
       const int q0 = c0 - SB;
       const int ndiag = (4 - p) * (5 - p) / 2 - 1;
-      const int ntask = ndiag + nrg * (4 - p);
+      const int ntask = ndiag + nrg;
       for (int u = tid - 32; u < ntask * 64; u += PANEL_THREADS - 32) {
         const int t = u >> 6;
-        BlockTask bt;
         if (t < ndiag) {
           int I = p, n = t + 1;                                // skip (p, p)
           while (n > I - p) { n -= I - p + 1; ++I; }
           const int J = p + n;
-          bt = BlockTask{S + SB * I * SLD + SB * J, S + SB * I * SLD + q0, S + SB * J * SLD + q0};
+          piece_update(BlockTask{S + SB * I * SLD + SB * J, S + SB * I * SLD + q0, S + SB * J * SLD + q0},
+                       (u & 63) >> 3, u & 7, SB);
         } else {
-          const int tt = t - ndiag, q = p + tt % (4 - p);
-          float* Rg = R + (tt / (4 - p)) * SB * SLD;
-          bt = BlockTask{Rg + SB * q, Rg + q0, S + SB * q * SLD + q0};
+          float* Rg = R + (t - ndiag) * SB * SLD;
+          piece_update(BlockTask{Rg + c0, Rg, S + c0 * SLD}, (u & 63) >> 3, u & 7, c0);
         }
-        piece_update(bt, (u & 63) >> 3, u & 7);
       }
     }
     __syncthreads();
