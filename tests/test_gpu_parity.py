@@ -147,7 +147,7 @@ def _spd(d, n, seed):
     return orc.hessian([X])
 
 
-@pytest.mark.parametrize("d,n", [(256, 1024), (1000, 4096), (1024, 600), (100, 64)])
+@pytest.mark.parametrize("d,n", [(256, 1024), (1000, 4096), (1024, 600), (100, 64), (130, 512)])
 def test_factor_matches_three_step_chain(g, d, n):
     H = _spd(d, n, seed=d)
     Hg = torch.from_numpy(H.astype(np.float32)).cuda()
