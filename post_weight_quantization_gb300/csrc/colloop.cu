@@ -21,7 +21,7 @@
 //                      asynchronous copies; group min/max by shuffles; Err1, codes and
 //                      per-column loss partials (the CTA's 32 rows in a fixed order)
 //                      leave from shared memory at the end of the block
-//   transpose_kernel   Ut = Hinv1^T once per call
+//   transpose_kernel   Ut = Hinv1^T once per call (transpose4_kernel: 16-byte accesses)
 //   tc_gemm            lazy update W[:, i2:] -= Err1 @ Hinv1[i1:i2, i2:] on the tensor cores
 //                      (3 x TF32, both operands K-major: Err1 rows, Ut rows)
 //   loss_finalize      col_losses = sum of partials in a fixed order, un-permuted
@@ -488,13 +488,24 @@ __global__ void __launch_bounds__(cb_threads<LANES>(), 1) colblock_kernel(CBArgs
   }
 }
 
+// col_losses[j] = sum over the CTAs' partials: 32 columns per CTA, the 8 warps each sum
+// every 8th partial, then warp 0 adds the 8 sums (fixed order)
 __global__ void loss_finalize_kernel(const float* __restrict__ part, int nrg, int d, const int* __restrict__ perm,
                                      float* __restrict__ col_losses) {
-  const int j = blockIdx.x * blockDim.x + threadIdx.x;
-  if (j >= d) return;
+  __shared__ float acc[8][33];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int j = blockIdx.x * 32 + lane;
   float s = 0.0f;
-  for (int b = 0; b < nrg; ++b) s += part[(long long)b * d + j];
-  col_losses[perm ? perm[j] : j] = s;
+  if (j < d)
+    for (int b = w; b < nrg; b += 8) s += part[(long long)b * d + j];
+  acc[w][lane] = s;
+  __syncthreads();
+  if (w == 0 && j < d) {
+    float t = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t += acc[k][lane];
+    col_losses[perm ? perm[j] : j] = t;
+  }
 }
 
 __global__ void invperm_kernel(const int* __restrict__ perm, int d, int* __restrict__ inv) {
@@ -530,6 +541,30 @@ __global__ void unpack_kernel(const uint32_t* __restrict__ qweight, int m, int d
   uint64_t v = qweight[(long long)r * wpr + wi] >> off;
   if (off + bits > 32) v |= (uint64_t)qweight[(long long)r * wpr + wi + 1] << (32 - off);
   codes[idx] = (uint8_t)(v & ((1u << bits) - 1u));
+}
+
+// The same for d % 4 == 0 and 16-byte aligned rows: 32 x 32 tiles, one 16-byte load and
+// two 16-byte stores per thread (256 threads: 32 rows x 8 pieces of four).
+__global__ void transpose4_kernel(const float* __restrict__ U, float* __restrict__ Ut, float* __restrict__ Ut_lo,
+                                  int d) {
+  __shared__ float tile[32][33];
+  const int bx = blockIdx.x * 32, by = blockIdx.y * 32;
+  const int r = threadIdx.x >> 3, c4 = (threadIdx.x & 7) * 4;
+  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (by + r < d && bx + c4 < d) v = *reinterpret_cast<const float4*>(U + (long long)(by + r) * d + bx + c4);
+  tile[r][c4] = v.x; tile[r][c4 + 1] = v.y; tile[r][c4 + 2] = v.z; tile[r][c4 + 3] = v.w;
+  __syncthreads();
+  // output row bx + r, columns by + c4 .. + 3 = input column bx + r of rows by + c4 ..
+  if (bx + r < d && by + c4 < d) {
+    const float4 o = make_float4(tile[c4][r], tile[c4 + 1][r], tile[c4 + 2][r], tile[c4 + 3][r]);
+    const long long off = (long long)(bx + r) * d + by + c4;
+    *reinterpret_cast<float4*>(Ut + off) = o;
+    *reinterpret_cast<float4*>(Ut_lo + off) =
+        make_float4(o.x - __uint_as_float(__float_as_uint(o.x) & 0xFFFFE000u),
+                    o.y - __uint_as_float(__float_as_uint(o.y) & 0xFFFFE000u),
+                    o.z - __uint_as_float(__float_as_uint(o.z) & 0xFFFFE000u),
+                    o.w - __uint_as_float(__float_as_uint(o.w) & 0xFFFFE000u));
+  }
 }
 
 // Ut = Hinv1^T (the lazy update reads Hinv1's rows as K-major operand columns) and
@@ -680,7 +715,10 @@ gptq_status quantize_launch(const void* W, int w_dtype, long long m_, long long 
       prep_kernel<<<grid, 256, 0, s>>>(W, w_dtype, m, d, ldw, perm, Wf, hdr);
     }
     dim3 tg((unsigned)((d + 31) / 32), (unsigned)((d + 31) / 32));
-    transpose_kernel<<<tg, dim3(32, 8), 0, s>>>(Hinv1, Ut, Ut_lo, d);
+    if (d % 4 == 0 && simt::aligned16(Hinv1) && simt::aligned16(Ut) && simt::aligned16(Ut_lo))
+      transpose4_kernel<<<tg, 256, 0, s>>>(Hinv1, Ut, Ut_lo, d);
+    else
+      transpose_kernel<<<tg, dim3(32, 8), 0, s>>>(Hinv1, Ut, Ut_lo, d);
     diag_info_kernel<<<(d + 255) / 256, 256, 0, s>>>(Hinv1, d, dinfo);
     count_launch(3);
     if (group_size < 0) {
@@ -707,7 +745,7 @@ gptq_status quantize_launch(const void* W, int w_dtype, long long m_, long long 
       break;
   }
   if (st) return st;
-  loss_finalize_kernel<<<(d + 255) / 256, 256, 0, s>>>(part, L.nrg, d, perm, col_losses);
+  loss_finalize_kernel<<<(d + 31) / 32, 256, 0, s>>>(part, L.nrg, d, perm, col_losses);
   count_launch();
   if (perm) {
     invperm_kernel<<<(d + 255) / 256, 256, 0, s>>>(perm, d, inv);

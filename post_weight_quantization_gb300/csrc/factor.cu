@@ -17,6 +17,7 @@
 //   diag_stats      lambda and the finiteness check of diag(H)
 //   perm_rank       stable descending sort of diag(H) by rank counting (act-order)
 //   gather          P[a][b] = H_d[p(d-1-a)][p(d-1-b)] (lower triangle), p = act-order
+//                   (gather_rev4: natural order, 16-byte loads)
 //   Cholesky, 128-wide blocks, right-looking with a look-ahead of one panel:
 //     chol_panel    one launch per 128-wide panel: every CTA factors the diagonal block
 //                   (32-column tall panels in one warp's registers) and solves 128 rows
@@ -104,6 +105,30 @@ __global__ void perm_rank_kernel(const float* __restrict__ H, int d, int* __rest
     }
   }
   if (j < d) perm[min(rank, d - 1)] = j;
+}
+
+// Natural order, d % 4 == 0 and 16-byte aligned rows: P[a][b] (b <= a) = H_d[d-1-a][d-1-b]
+// = H[d-1-a][d-1-b] (+ lambda on the diagonal), four columns per thread: P[a][4k..4k+3]
+// is H[d-1-a][d-4-4k .. d-1-4k] reversed, one aligned 16-byte load. One warp per row a.
+__global__ void gather_rev4_kernel(const float* __restrict__ H, int d, const Header* __restrict__ hdr,
+                                   float* __restrict__ P) {
+  const int a = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (a >= d) return;
+  const float lam = hdr->lambda;
+  const float* hrow = H + (long long)(d - 1 - a) * d;
+  float* prow = P + (long long)a * d;
+  for (int k = lane; 4 * k <= a; k += 32) {
+    const int b = 4 * k;
+    const float4 v = *reinterpret_cast<const float4*>(hrow + d - 4 - b);
+    float4 o = make_float4(v.w, v.z, v.y, v.x);          // P[a][b + t] = H[d-1-a][d-1-b-t]
+    if (b + 3 <= a) {
+      if (b + 3 == a) o.w += lam;
+      *reinterpret_cast<float4*>(prow + b) = o;
+    } else {                                             // the piece holding the diagonal
+      const float ov[4] = {o.x, o.y, o.z, o.w};
+      for (int t = 0; b + t <= a; ++t) prow[b + t] = (b + t == a) ? ov[t] + lam : ov[t];
+    }
+  }
 }
 
 // P[a][b] (b <= a) = H_d[p(d-1-a)][p(d-1-b)], read from the upper triangle of H
@@ -653,7 +678,10 @@ gptq_status factor_launch(const float* H, long long d_, float percdamp, int act_
     perm_rank_kernel<<<(d + 255) / 256, 256, 0, s>>>(H, d, perm_out);
     count_launch();
   }
-  {
+  if (!act_order && d % 4 == 0 && simt::aligned16(H) && simt::aligned16(P)) {
+    gather_rev4_kernel<<<(unsigned)((d + 7) / 8), 256, 0, s>>>(H, d, hdr, P);
+    count_launch();
+  } else {
     dim3 grid((unsigned)std::min(64, (d + 31) / 32), (unsigned)((d + 7) / 8));
     gather_kernel<<<grid, dim3(32, 8), 0, s>>>(H, d, act_order ? perm_out : nullptr, hdr, P);
     count_launch();

@@ -323,10 +323,21 @@ syrk_kernel(const __grid_constant__ CUtensorMap tmap, float* __restrict__ H, lon
 }
 
 // zero the upper triangle (i <= j) of H
-__global__ void zero_upper_kernel(float* __restrict__ H, long long ldh, int d) {
-  const int i = blockIdx.y;
-  for (int j = i + blockIdx.x * blockDim.x + threadIdx.x; j < d; j += gridDim.x * blockDim.x)
-    H[(long long)i * ldh + j] = 0.0f;
+// H[i][j] = 0 for j >= i: one warp per row, a scalar head up to the first 16-byte
+// boundary (vec: rows 16-byte aligned), then 16-byte stores
+__global__ void zero_upper_kernel(float* __restrict__ H, long long ldh, int d, int vec) {
+  const int i = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (i >= d) return;
+  float* row = H + (long long)i * ldh;
+  if (!vec) {
+    for (int j = i + lane; j < d; j += 32) row[j] = 0.0f;
+    return;
+  }
+  const int j4 = min(d, (i + 3) & ~3);
+  if (i + lane < j4) row[i + lane] = 0.0f;
+  const int q_end = d >> 2;
+  for (int q = (j4 >> 2) + lane; q < q_end; q += 32) reinterpret_cast<float4*>(row)[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = (q_end << 2) + lane; j < d; j += 32) if (j >= j4) row[j] = 0.0f;
 }
 
 }  // namespace syrk
@@ -364,8 +375,8 @@ gptq_status syrk_accumulate(const uint16_t* X, long long n, long long d, long lo
                             float alpha, int zero_first, cudaStream_t stream) {
   using namespace syrk;
   if (zero_first) {
-    dim3 grid((unsigned)std::max<long long>(1, std::min<long long>((d + 255) / 256, 64)), (unsigned)d);
-    zero_upper_kernel<<<grid, 256, 0, stream>>>(H, ldh, (int)d);
+    const int vec = (ldh % 4 == 0) && (reinterpret_cast<uintptr_t>(H) % 16 == 0);
+    zero_upper_kernel<<<(unsigned)((d + 7) / 8), 256, 0, stream>>>(H, ldh, (int)d, vec);
     count_launch();
     if (gptq_status st = check_launch("zero_upper_kernel")) return st;
   }
