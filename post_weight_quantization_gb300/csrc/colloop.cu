@@ -597,7 +597,10 @@ __global__ void transpose_kernel(const float* __restrict__ U, float* __restrict_
 // columns are current when its statistics are read, because an outer block holds
 // whole groups. The wide products read and write W's right part once per outer block
 // instead of once per block.
-constexpr int OUTER = 1024;
+// 640 = five 128-column blocks: every K = BS update after a block then has at most
+// 4 x 128 columns, one round of 128 x 128 tiles on the GPU at m = 4096 (with 1024, the
+// first three of seven took two rounds), for some more K = OUTER work.
+constexpr int OUTER = 640;
 
 // Outer block width: OUTER when it holds whole blocks and whole groups, else one block.
 inline int outer_width(int BS, int g, int stats_given) {

@@ -624,6 +624,25 @@ __global__ void reverse_kernel(float* __restrict__ M, int d, const Header* hdr) 
   }
 }
 
+// The same for d % 4 == 0 and a 16-byte aligned M: elements idx .. idx + 3 (one row) swap
+// with the 16-byte piece at n - 4 - idx, which holds their partners in reverse order.
+__global__ void reverse4_kernel(float* __restrict__ M, int d, const Header* hdr) {
+  if (hdr->failed) return;
+  const long long n = (long long)d * d;
+  float4* M4 = reinterpret_cast<float4*>(M);
+  for (long long k = blockIdx.x * (long long)blockDim.x + threadIdx.x; 4 * k < n / 2;
+       k += (long long)gridDim.x * blockDim.x) {
+    const long long idx = 4 * k;
+    const long long a = idx / d, b = idx - a * d;
+    const float4 lo = M4[k];
+    const float4 hi = M4[(n - 4 - idx) >> 2];          // partners of idx + 3, + 2, + 1, idx
+    M4[k] = make_float4(a <= b ? hi.w : 0.0f, a <= b + 1 ? hi.z : 0.0f, a <= b + 2 ? hi.y : 0.0f,
+                        a <= b + 3 ? hi.x : 0.0f);
+    M4[(n - 4 - idx) >> 2] = make_float4(a >= b + 3 ? lo.w : 0.0f, a >= b + 2 ? lo.z : 0.0f,
+                                         a >= b + 1 ? lo.y : 0.0f, a >= b ? lo.x : 0.0f);
+  }
+}
+
 // Y[a0 + j][c0 + i] = X[c0 + i][a0 + j] for every pair z of the doubling step: the
 // transpose of the block just computed, stored above the diagonal.
 __global__ void pair_transpose_kernel(float* __restrict__ M, int d, int sz, int np, int c_last,
@@ -791,7 +810,12 @@ gptq_status factor_launch(const float* H, long long d_, float percdamp, int act_
     count_launch();
   }
   ProfScope ps_rev("factor.reverse", s);
-  reverse_kernel<<<std::max(1, std::min(4096, (int)(((long long)d * d / 2 + 255) / 256))), 256, 0, s>>>(Hinv1, d, hdr);
+  if (vec)
+    reverse4_kernel<<<std::max(1, std::min(4096, (int)(((long long)d * d / 8 + 255) / 256))), 256, 0, s>>>(Hinv1, d,
+                                                                                                         hdr);
+  else
+    reverse_kernel<<<std::max(1, std::min(4096, (int)(((long long)d * d / 2 + 255) / 256))), 256, 0, s>>>(Hinv1, d,
+                                                                                                        hdr);
   count_launch();
   return check_launch("triangular-inverse kernels");
 }
