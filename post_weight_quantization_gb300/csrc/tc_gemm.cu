@@ -93,6 +93,9 @@ __device__ __forceinline__ Tile decode(int t, const Params& p) {
   } else {
     w.I = u / p.nt;
     w.J = u - w.I * p.nt;
+    // a lower-triangular A (a_tri 1) makes tile rows cost more as I grows: take them
+    // from the bottom so tiles come in order of decreasing cost, as for a_tri 2
+    if (p.a_tri == 1) w.I = p.mt - 1 - w.I;
   }
   const bool last = (w.z == p.batches - 1);
   w.M = last ? p.M_last : p.M;
@@ -107,6 +110,12 @@ __device__ __forceinline__ Tile decode(int t, const Params& p) {
 }
 
 __device__ __forceinline__ int nchunks(const Tile& w) { return (w.kend - w.kbeg + BK - 1) / BK; }
+
+// The k-th tile of CTA b: rounds alternate direction (b, then 2 grid - 1 - b, ...), so a
+// CTA that drew an expensive tile in one round draws a cheap one in the next when tiles
+// come in order of decreasing cost (triangular operands, see decode). The sequence is
+// increasing in k, so the first index past the end ends every role's loop.
+__device__ __forceinline__ int tile_at(int k, int b, int grid) { return (k & 1) ? (k + 1) * grid - 1 - b : k * grid + b; }
 
 // smem descriptors: K-major SW128 (rows of 128 bytes along k, 8-row groups 1024 B
 // apart) and MN-major SW128 (32-element MN chunks are separate TMA boxes 4 KB apart,
@@ -254,7 +263,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     uint32_t phase = 0, armed = 0, last_phase = 0;
     bool ok = true;
     int seq = 0;                                   // chunks issued so far
-    for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+    for (int kt = 0, t = blockIdx.x; ok && t < ntiles; t = tile_at(++kt, blockIdx.x, gridDim.x)) {
       const Tile w = decode(t, p);
       for (int k0 = w.kbeg; k0 < w.kend; k0 += BK, ++seq) {
         if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
@@ -281,7 +290,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+    for (int kt = 0, t = blockIdx.x; ok && t < ntiles; t = tile_at(++kt, blockIdx.x, gridDim.x)) {
       const Tile w = decode(t, p);
       for (int k0 = w.kbeg; k0 < w.kend; k0 += BK) {
         if (!mbar_wait_bounded(&full[stage], phase, abort_flag)) { ok = false; break; }
@@ -301,7 +310,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     uint32_t phase = 0, it = 0;
     bool ok = true, issued = false;
     const uint32_t sbase = smem_u32(smem);
-    for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+    for (int kt = 0, t = blockIdx.x; ok && t < ntiles; t = tile_at(++kt, blockIdx.x, gridDim.x)) {
       const Tile w = decode(t, p);
       int cin = 0;                                 // chunk index within the tile
       for (int k0 = w.kbeg; k0 < w.kend; k0 += BK, ++cin) {
@@ -345,7 +354,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     const int h = (warp - EPI_WARP0) >> 2;        // 64-column half of the tile
     uint32_t it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+    for (int kt = 0, t = blockIdx.x; ok && t < ntiles; t = tile_at(++kt, blockIdx.x, gridDim.x)) {
       const Tile w = decode(t, p);
       // Pull this thread's 64-column segment of C into L2 while the tile's products are
       // computed, so the read-modify-write below waits on L2 rather than on DRAM

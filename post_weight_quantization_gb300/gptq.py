@@ -289,6 +289,22 @@ def quantize_layer(W: torch.Tensor, X_batches, bits: int = 4, group_size: int = 
     return q, H, Hinv1, perm
 
 
+def token_pieces(n: int, chunk: int):
+    """Token ranges for HostPipeline: chunks of `chunk` tokens, the last one cut in four
+    (when it has at least 4096 tokens), so the Hessian of the final piece, the one step
+    that no copy overlaps, is short."""
+    out, t0 = [], 0
+    while t0 < n:
+        t1 = min(n, t0 + chunk)
+        if t1 == n and t1 - t0 >= 4096:
+            q = (t1 - t0) // 4
+            out += [(t0 + k * q, t0 + (k + 1) * q if k < 3 else t1) for k in range(4)]
+        else:
+            out.append((t0, t1))
+        t0 = t1
+    return out
+
+
 class HostPipeline:
     """End-to-end quantization of one layer from host (pinned) buffers.
 
@@ -344,8 +360,7 @@ class HostPipeline:
         n = X_host.shape[0]
         first = True
         self.copy_stream.wait_stream(comp)          # earlier work on the caller's stream first
-        for c, t0 in enumerate(range(0, n, self.chunk)):
-            t1 = min(n, t0 + self.chunk)
+        for c, (t0, t1) in enumerate(token_pieces(n, self.chunk)):
             b = c & 1
             buf = self.xbuf[b][: t1 - t0]
             with torch.cuda.stream(self.copy_stream):

@@ -126,3 +126,16 @@ def test_unpack_argument_checks(g):
     lib = g.library()
     assert lib.gptq_unpack_codes(None, 4, 4, 4, P, None) == g.GPTQ_ERR_INVALID_ARG
     assert lib.gptq_unpack_codes(P, 4, 4, 5, P, None) == g.GPTQ_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("n,chunk", [(262144, 32768), (100, 32768), (5000, 4096), (8192, 4096), (0, 64)])
+def test_host_pipeline_token_pieces(g, n, chunk):
+    pieces = g.token_pieces(n, chunk)
+    # contiguous cover of [0, n), no piece longer than a chunk
+    assert [a for a, _ in pieces[1:]] == [b for _, b in pieces[:-1]]
+    assert (pieces[0][0], pieces[-1][1]) == (0, n) if n else pieces == []
+    assert all(0 < b - a <= chunk for a, b in pieces)
+    # a last chunk of at least 4096 tokens is cut in four
+    last = n - ((n - 1) // chunk) * chunk if n else 0
+    if last >= 4096:
+        assert len(pieces) == (n - last) // chunk + 4
