@@ -412,10 +412,14 @@ __device__ __noinline__ void chol_panel_body(float* __restrict__ P, float* __res
       // R[g][0 .. p) at once (K = 32 p), one task per row group g; R's column blocks
       // beyond p wait for their own phase, which keeps every phase's share of this work
       // below the time of the sub-block Cholesky.
+      // Warp 4 shares warp 0's scheduler and stays out, so the latency-bound Cholesky
+      // issues alone there; warps 1-3 and 5-7 take the pieces.
       const int q0 = c0 - SB;
       const int ndiag = (4 - p) * (5 - p) / 2 - 1;
       const int ntask = ndiag + nrg;
-      for (int u = tid - 32; u < ntask * 64; u += PANEL_THREADS - 32) {
+      constexpr int TASK_THREADS = PANEL_THREADS - 64;
+      const int tw = (warp < 4) ? warp - 1 : warp - 2;       // 0..5 for warps 1-3, 5-7
+      for (int u = (warp == 4) ? ntask * 64 : tw * 32 + lane; u < ntask * 64; u += TASK_THREADS) {
         const int t = u >> 6;
         if (t < ndiag) {
           int I = p, n = t + 1;                                // skip (p, p)
