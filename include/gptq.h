@@ -211,7 +211,10 @@ gptq_status gptq_factor_static(const float* H, int64_t d, float percdamp, int ac
  *              (statistics from W before any update). Otherwise d % group_size == 0
  *              and group_size % blocksize == 0 or blocksize % group_size == 0, so
  *              that a group's statistics are read after all earlier compensation.
- *              With perm != NULL only -1 is supported (GPTQ_ERR_UNSUPPORTED).
+ *              With perm != NULL, groups are formed in processing order: group k
+ *              holds the processed columns k*group_size ... (k+1)*group_size - 1,
+ *              so original column j belongs to group g_idx[j] = p / group_size with
+ *              perm[p] == j (scales and zeros are indexed by that group).
  *   blocksize  lazy-update block width in [1, 256]; this build runs 32, 64 and 128
  *              (the pages use 128) and returns GPTQ_ERR_UNSUPPORTED for others. It
  *              does not change the result in exact arithmetic. Group sizes must be
@@ -219,7 +222,8 @@ gptq_status gptq_factor_static(const float* H, int64_t d, float percdamp, int ac
  *   qweight    device uint32, m x ceil(d*bits/32): per row a little-endian
  *              bitstream, code of column j in bits [j*bits, j*bits + bits).
  *   scales, zeros  device fp32, m x G row-major, G = d / group_size (1 when -1);
- *              w_hat = (code - zero) * scale; zeros hold integers in [0, 2^bits-1].
+ *              w_hat = (code - zero) * scale with the (scale, zero) of the column's
+ *              group; zeros hold integers in [0, 2^bits-1].
  *   col_losses device fp32[d]: for every column, the sum over rows of Err1^2 / 2,
  *              the increase of 1/2 (w - w_hat) H_d (w - w_hat)^T caused by fixing that
  *              column; their total is 1/2 tr(dW H_d dW^T).

@@ -237,12 +237,17 @@ def gptq_layer(W: np.ndarray, H: np.ndarray, bits: int = 4, group_size: int = 12
     return codes, losses and W_hat in the original column order.
 
     Adds ``perm`` (identity without act-order), ``U`` (Hinv1 of the permuted damped
-    H), ``lambda``, ``col_losses`` (losses summed over rows) and ``H_d``.
+    H), ``lambda``, ``col_losses`` (losses summed over rows), ``H_d`` and ``g_idx``.
+
+    With act-order and groups, groups are formed in processing order (the pages name
+    act-order, "The GPTQ Algorithm", ActOrder, and groups of 128 columns, but not how
+    the two combine; this is the plainest reading): the scale and zero of group k come
+    from processed columns k*g ... (k+1)*g - 1, and original column j uses group
+    g_idx[j] = (position of j in perm) // g. ``scales`` and ``zeros`` stay indexed by
+    group.
     """
     W = np.asarray(W, dtype=dtype)
     m, d = W.shape
-    if act_order and group_size not in (-1, 0, None):
-        raise ValueError("act-order is supported with per-channel quantization only")
     Hd, lam = damp(H, percdamp, dtype=dtype)
     perm = act_order_perm(H) if act_order else np.arange(d)
     Hp = Hd[np.ix_(perm, perm)]
@@ -253,7 +258,10 @@ def gptq_layer(W: np.ndarray, H: np.ndarray, bits: int = 4, group_size: int = 12
         a = np.empty_like(res[key])
         a[:, perm] = res[key]
         out[key] = a
-    out.update(perm=perm, U=U, H_d=Hd, col_losses=out["losses"].sum(axis=0))
+    g = d if group_size in (-1, 0, None) else group_size
+    g_idx = np.empty(d, dtype=np.int64)
+    g_idx[perm] = np.arange(d) // g
+    out.update(perm=perm, U=U, H_d=Hd, col_losses=out["losses"].sum(axis=0), g_idx=g_idx)
     out["lambda"] = lam
     return out
 

@@ -264,8 +264,6 @@ gptq_status gptq_quantize_layer(const void* W, int w_dtype, int64_t m, int64_t d
     return set_error(GPTQ_ERR_UNSUPPORTED, "this build runs blocksize 32, 64 or 128");
   if (group_size != -1 && group_size % 32)
     return set_error(GPTQ_ERR_UNSUPPORTED, "this build runs group sizes that are multiples of 32 (or -1)");
-  if (perm && group_size != -1)
-    return set_error(GPTQ_ERR_UNSUPPORTED, "act-order is supported with per-channel quantization (group_size -1)");
   if (!aligned(ws, 256)) return set_error(GPTQ_ERR_INVALID_ARG, "ws must be 256-byte aligned");
   const size_t need = quantize_workspace_bytes(m, d, blocksize);
   if (ws_bytes < need) return set_error(GPTQ_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", ws_bytes, need);

@@ -118,7 +118,6 @@ def test_quantize_argument_checks(g):
     assert call(wsb=ws - 1) == g.GPTQ_ERR_INVALID_ARG
     assert call(bs=16, gs=128) == g.GPTQ_ERR_UNSUPPORTED    # valid, not built
     assert call(gs=16, bs=32) == g.GPTQ_ERR_UNSUPPORTED
-    assert call(perm=P, gs=128) == g.GPTQ_ERR_UNSUPPORTED   # act-order with groups
     assert g.gptq_launch_count() == before
 
 

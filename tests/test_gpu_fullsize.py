@@ -81,7 +81,7 @@ def exact_hessian(layer_inputs):
     return H
 
 
-@pytest.mark.parametrize("bits,gs,act_order", [(4, 128, False), (3, -1, True)])
+@pytest.mark.parametrize("bits,gs,act_order", [(4, 128, False), (3, -1, True), (4, 128, True)])
 def test_end_to_end_full_size(g, layer_inputs, gpu_hessian, exact_hessian, bits, gs, act_order):
     """The whole GPU path (its own Hessian and factor) against the oracle run on the exact
     float64 Hessian, on sampled rows."""
@@ -123,7 +123,7 @@ def test_end_to_end_full_size(g, layer_inputs, gpu_hessian, exact_hessian, bits,
         assert abs(e_gpu - e_orc) <= ERR_RTOL * e_orc, (e_gpu, e_orc)
 
 
-@pytest.mark.parametrize("bits,gs,act_order", [(4, 128, False), (3, -1, True)])
+@pytest.mark.parametrize("bits,gs,act_order", [(4, 128, False), (3, -1, True), (4, 128, True)])
 def test_layer_full_size(g, layer_inputs, gpu_hessian, bits, gs, act_order):
     W_bits, _ = layer_inputs
     H, Hfull = gpu_hessian
@@ -178,7 +178,9 @@ def test_layer_full_size(g, layer_inputs, gpu_hessian, bits, gs, act_order):
     Gn = 1 if gs == -1 else d // gs
     sc = q.scales.double()
     ze = q.zeros.double()
-    gcols = torch.arange(d, device="cuda") // gsz
+    g_idx = np.empty(d, dtype=np.int64)
+    g_idx[p] = np.arange(d) // gsz                 # groups are formed in processing order
+    gcols = torch.from_numpy(g_idx).cuda()
     What = (torch.from_numpy(codes_all).cuda().double() - ze[:, gcols]) * sc[:, gcols]
     dW = Wd.double() - What
     Hdg = torch.from_numpy(Hd).cuda()

@@ -79,7 +79,11 @@ def check_layer(W64, res64, res32, codes, scales, zeros, H0, bits, gs, perm=None
     assert srel <= SCALE_RTOL, srel
     mism32 = np.mean(codes != res32["codes"])
     assert mism32 <= CODE_TOL, mism32
-    gi = np.arange(W64.shape[1]) // (W64.shape[1] if gs == -1 else gs)
+    d = W64.shape[1]
+    gi = np.arange(d) // (d if gs == -1 else gs)
+    if perm is not None:                              # groups are formed in processing order
+        gi = np.empty(d, dtype=np.int64)
+        gi[perm] = np.arange(d) // (d if gs == -1 else gs)
     What = (codes - zeros[:, gi]) * scales[:, gi]
     e_gpu = orc.relative_output_error(W64, What, H0)
     for res in (res64, res32):
@@ -315,7 +319,8 @@ def test_end_to_end_toy_256(g):
 
 
 @pytest.mark.parametrize("m,d,n,bits,gs,ao", [(520, 1024, 16384, 4, 128, False), (640, 768, 8192, 3, -1, True),
-                                              (384, 512, 4096, 2, 64, False), (1000, 1536, 4096, 4, 128, False)])
+                                              (384, 512, 4096, 2, 64, False), (1000, 1536, 4096, 4, 128, False),
+                                              (544, 1024, 8192, 4, 128, True), (300, 640, 4096, 2, 64, True)])
 def test_end_to_end_mid(g, m, d, n, bits, gs, ao):
     W_bits = make_weight(m, d, 31)
     X_bits = make_activations(ActSpec("heavy_tail", n, d, seed=31))

@@ -465,3 +465,54 @@ def test_pack_roundtrip(bits):
     words = orc.pack_codes(codes, bits)
     assert words.shape == (5, (263 * bits + 31) // 32)
     assert np.array_equal(orc.unpack_codes(words, bits, 263), codes)
+
+
+# ----------------------------------------------------------------------------------
+# act-order with groups: groups are formed in processing order
+# ----------------------------------------------------------------------------------
+def test_act_order_groups_diagonal_hessian_is_rtn_in_processing_order():
+    """Diagonal H with distinct entries: no compensation, so act-order with groups is
+    round-to-nearest applied to the columns in processing order (groups of g
+    consecutive processed columns), scattered back; g_idx maps each column to its group."""
+    rng = np.random.default_rng(17)
+    d, g = 256, 64
+    W = rng.normal(0, 0.02, size=(24, d))
+    H = np.diag(rng.permutation(np.linspace(0.5, 3.0, d)))
+    res = orc.gptq_layer(W, H, 4, g, 128, act_order=True)
+    p = res["perm"]
+    assert not np.array_equal(p, np.arange(d))
+    ref = orc.rtn(W[:, p], 4, g)
+    assert np.array_equal(res["codes"][:, p], ref["codes"])
+    assert np.array_equal(res["scales"], ref["scales"]) and np.array_equal(res["zeros"], ref["zeros"])
+    inv = np.empty(d, dtype=np.int64)
+    inv[p] = np.arange(d)
+    assert np.array_equal(res["g_idx"], inv // g)
+    gi = res["g_idx"]
+    np.testing.assert_array_equal(res["W_hat"], (res["codes"] - res["zeros"][:, gi]) * res["scales"][:, gi])
+
+
+def test_act_order_groups_with_equal_diagonal_is_the_natural_order():
+    """Equal diagonal entries (H[i][j] = rho^|i-j|): the stable act-order sort keeps the
+    natural order, so act-order with groups gives the grouped natural-order result."""
+    d = 256
+    i = np.arange(d)
+    H = 0.7 ** np.abs(i[:, None] - i[None, :])
+    W = np.random.default_rng(3).normal(0, 0.02, size=(20, d))
+    a = orc.gptq_layer(W, H, 4, 128, 128, act_order=True)
+    b = orc.gptq_layer(W, H, 4, 128, 128)
+    assert np.array_equal(a["perm"], np.arange(d))
+    for k in ("codes", "scales", "zeros", "W_hat", "losses"):
+        assert np.array_equal(a[k], b[k]), k
+    assert np.array_equal(a["g_idx"], np.arange(d) // 128)
+
+
+def test_act_order_groups_blocksize_invariance():
+    """The pages' blocksize invariance holds with act-order and groups (identical fp64
+    codes for blocksize 1, 32 and 128)."""
+    W, X = _layer(24, 256, 600, seed=12)
+    H = orc.hessian([X])
+    r = [orc.gptq_layer(W, H, 4, 64, bs, act_order=True) for bs in (1, 32, 128)]
+    assert not np.array_equal(r[0]["perm"], np.arange(256))
+    for x in r[1:]:
+        assert np.array_equal(x["codes"], r[0]["codes"])
+        np.testing.assert_allclose(x["scales"], r[0]["scales"], rtol=1e-12)
