@@ -39,6 +39,8 @@ design notes of the repository):
   group's first column; this needs group_size % blocksize == 0 or the reverse.
 * Rounding is round-half-to-even (``np.rint``) and w/scale is a true division.
 * act-order ties keep the lower column index first (stable sort).
+* act-order with groups: groups are formed in processing order; original column j
+  uses group (position of j in the order) // group_size.
 * Code storage: code (r, j) occupies bits [j*b, j*b + b) of row r's stream.
 """
 from __future__ import annotations
