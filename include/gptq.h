@@ -247,6 +247,32 @@ gptq_status gptq_unpack_codes(const uint32_t* qweight, int64_t m, int64_t d, int
                               uint8_t* codes, gptq_stream_t stream);
 
 /*
+ * The quantized layer used again: Y = X W_hat^T computed straight from the packed
+ * form, w_hat[r][j] = (code[r][j] - zero[r][g]) * scale[r][g] with g = g_idx[j], or
+ * j / group_size when g_idx is NULL ("GPTQ: fixing errors as you go": once quantized,
+ * the stored low-bit weights and per-group scales stand in for the layer's weights).
+ * One warp per output row reads each code once; fp32 accumulation.
+ *
+ *   qweight, scales, zeros  as written by gptq_quantize_layer (device; m x
+ *              ceil(d*bits/32) words, m x G floats each). qweight 16-byte aligned
+ *              for 4 and 8 bits, 8-byte for 2.
+ *   g_idx      device int32[d] group of every column (act-order groups), values in
+ *              [0, G); or NULL.
+ *   m, d       rows and columns of W; d a multiple of 32.
+ *   bits       2, 3, 4 or 8.  group_size  -1 or a multiple of 32 dividing d.
+ *   X          device bf16 bits, T x d token-major, row stride ldx (ldx >= d,
+ *              ldx % 8 == 0, 16-byte aligned). T >= 0 tokens (8 per launch inside).
+ *   Y          device fp32, T x m, row stride ldy >= m.
+ * Asynchronous on `stream`; argument errors return GPTQ_ERR_INVALID_ARG before any
+ * launch. This is the use of the stored layer that the pages describe, not a step of
+ * the quantization itself.
+ */
+gptq_status gptq_dequant_gemv(const uint32_t* qweight, const float* scales, const float* zeros,
+                              const int32_t* g_idx, int64_t m, int64_t d, int bits, int group_size,
+                              const uint16_t* X, int64_t T, int64_t ldx, float* Y, int64_t ldy,
+                              gptq_stream_t stream);
+
+/*
  * Helper for checks: C = beta * C + alpha * A B (fp32, single batch) with the GEMM the
  * library uses for its block updates. engine 0: tensor cores, 3 x TF32 products with
  * fp32 accumulation of 32-deep partial products; engine 1: FFMA. a_kmajor != 0 means

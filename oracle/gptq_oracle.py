@@ -19,6 +19,8 @@ What it computes, step by step, in the order and notation of the pages:
                    after it; per-element losses Losses1 = Err1^2 / 2.
 * ``pack_codes`` / ``unpack_codes``  b-bit codes as a little-endian bitstream of
                    uint32 words per row.
+* ``dequantize_packed`` / ``dequant_matmul``  the stored layer used again: W_hat
+                   from packed codes and group scales, and Y = X W_hat^T.
 * ``relative_output_error``  ||(W - W_hat) X^T||_F / ||W X^T||_F through H.
 
 Arithmetic is float64 unless ``dtype=np.float32`` is passed; the float32 mode keeps
@@ -52,6 +54,7 @@ __all__ = [
     "hessian", "hessian_accumulate", "hessian_entries", "damp", "act_order_perm",
     "hinv1", "quant_params", "quantize", "dequantize", "gptq_columns", "gptq_layer",
     "rtn", "pack_codes", "unpack_codes", "packed_words_per_row",
+    "dequantize_packed", "dequant_matmul",
     "relative_output_error", "loss_quadratic_form",
 ]
 
@@ -324,6 +327,32 @@ def unpack_codes(words: np.ndarray, bits: int, d: int) -> np.ndarray:
     bitstream = np.unpackbits(words.view(np.uint8).reshape(m, -1), axis=1, bitorder="little")
     b = bitstream[:, :d * bits].reshape(m, d, bits).astype(np.int64)
     return (b << np.arange(bits)).sum(axis=2)
+
+
+# ----------------------------------------------------------------------------------
+# Using the stored layer: dequantize and multiply
+# ----------------------------------------------------------------------------------
+def dequantize_packed(words: np.ndarray, scales: np.ndarray, zeros: np.ndarray, bits: int, d: int,
+                      group_size: int = 128, g_idx=None) -> np.ndarray:
+    """W_hat (m x d, float64) from packed codes and per-group scale and zero.
+
+    After quantization the layer is used as before ("GPTQ: fixing errors as you go",
+    section on what changes at inference time: the stored low-bit weights and one scale
+    per group stand in for the full-precision ones): w_hat = (code - zero) * scale with
+    the (scale, zero) of the column's group, g_idx[j] (default j // group_size).
+    """
+    codes = unpack_codes(words, bits, d).astype(np.float64)
+    g = d if group_size in (-1, 0, None) else group_size
+    gi = np.arange(d) // g if g_idx is None else np.asarray(g_idx, dtype=np.int64)
+    return dequantize(codes, np.asarray(scales, dtype=np.float64)[:, gi], np.asarray(zeros, dtype=np.float64)[:, gi])
+
+
+def dequant_matmul(X: np.ndarray, words: np.ndarray, scales: np.ndarray, zeros: np.ndarray, bits: int,
+                   group_size: int = 128, g_idx=None) -> np.ndarray:
+    """Y = X W_hat^T in float64 for tokens X (T x d): the layer's output computed from
+    its stored form."""
+    X = np.asarray(X, dtype=np.float64)
+    return X @ dequantize_packed(words, scales, zeros, bits, X.shape[1], group_size, g_idx).T
 
 
 # ----------------------------------------------------------------------------------

@@ -29,6 +29,9 @@ gptq_status quantize_launch(const void* W, int w_dtype, long long m, long long d
                             float* scales, float* zeros, float* col_losses, void* ws, cudaStream_t s);
 gptq_status quantize_read_status(const void* ws, long long* info, cudaStream_t s);
 gptq_status unpack_launch(const uint32_t* qweight, long long m, long long d, int bits, uint8_t* codes, cudaStream_t s);
+gptq_status dequant_gemv_launch(const uint32_t* qweight, const float* scales, const float* zeros, const int32_t* g_idx,
+                                long long m, long long d, int bits, int group_size, const uint16_t* X, long long T,
+                                long long ldx, float* Y, long long ldy, cudaStream_t s);
 
 namespace {
 thread_local char g_last_error[512] = "";
@@ -284,6 +287,25 @@ gptq_status gptq_unpack_codes(const uint32_t* qweight, int64_t m, int64_t d, int
   if (m < 0 || d < 0) return set_error(GPTQ_ERR_INVALID_ARG, "negative size");
   if (bits != 2 && bits != 3 && bits != 4 && bits != 8) return set_error(GPTQ_ERR_INVALID_ARG, "bits must be 2, 3, 4 or 8");
   return unpack_launch(qweight, m, d, bits, codes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gptq_status gptq_dequant_gemv(const uint32_t* qweight, const float* scales, const float* zeros, const int32_t* g_idx,
+                              int64_t m, int64_t d, int bits, int group_size, const uint16_t* X, int64_t T,
+                              int64_t ldx, float* Y, int64_t ldy, gptq_stream_t stream) {
+  g_last_error[0] = 0;
+  if (!qweight || !scales || !zeros || (T > 0 && (!X || !Y))) return set_error(GPTQ_ERR_INVALID_ARG, "NULL pointer");
+  if (m < 1 || m > ((int64_t)1 << 30) || d < 32 || d > 65536 || d % 32)
+    return set_error(GPTQ_ERR_INVALID_ARG, "m >= 1 and d a multiple of 32 in [32, 65536] are required");
+  if (bits != 2 && bits != 3 && bits != 4 && bits != 8) return set_error(GPTQ_ERR_INVALID_ARG, "bits must be 2, 3, 4 or 8");
+  if (group_size != -1 && (group_size < 32 || group_size % 32 || d % group_size))
+    return set_error(GPTQ_ERR_INVALID_ARG, "group_size must be -1 or a multiple of 32 that divides d");
+  if (T < 0 || ldx < d || ldx % 8 || ldy < m) return set_error(GPTQ_ERR_INVALID_ARG, "bad T, ldx or ldy");
+  const size_t qa = (bits == 4 || bits == 8) ? 16 : (bits == 2 ? 8 : 4);
+  if (!aligned(qweight, qa) || (T > 0 && !aligned(X, 16)) || !aligned(scales, 4) || !aligned(zeros, 4))
+    return set_error(GPTQ_ERR_INVALID_ARG, "qweight (16 bytes for 4 and 8 bits, 8 for 2) or X (16 bytes) misaligned");
+  if (T == 0) return GPTQ_OK;
+  return dequant_gemv_launch(qweight, scales, zeros, g_idx, m, d, bits, group_size, X, T, ldx, Y, ldy,
+                             reinterpret_cast<cudaStream_t>(stream));
 }
 
 gptq_status gptq_gemm_f32(int engine, int a_kmajor, int b_kmajor, int64_t M, int64_t N, int64_t K, const float* A,

@@ -48,6 +48,8 @@ SIGNATURES = {
     "gptq_quantize_layer": (_c_int, [_vp, _c_int, _c_i64, _c_i64, _c_i64, _vp, _vp, _c_int, _c_int, _c_int, _vp, _vp,
                                      _vp, _vp, _vp, _c_size, ctypes.POINTER(_c_i64), _vp]),
     "gptq_unpack_codes": (_c_int, [_vp, _c_i64, _c_i64, _c_int, _vp, _vp]),
+    "gptq_dequant_gemv": (_c_int, [_vp, _vp, _vp, _vp, _c_i64, _c_i64, _c_int, _c_int, _vp, _c_i64, _c_i64, _vp, _c_i64,
+                                   _vp]),
     "gptq_gemm_f32": (_c_int, [_c_int, _c_int, _c_int, _c_i64, _c_i64, _c_i64, _vp, _c_i64, _vp, _c_i64, _vp, _c_i64,
                                _c_float, _c_float, _c_int, _vp]),
 }
@@ -248,6 +250,23 @@ def gptq_unpack_codes(qweight: torch.Tensor, m: int, d: int, bits: int, stream=N
     codes = torch.empty((m, d), dtype=torch.uint8, device=qweight.device)
     _check(_lib.gptq_unpack_codes(_ptr(qweight), m, d, bits, _ptr(codes), _stream(stream)), "gptq_unpack_codes")
     return codes
+
+
+def gptq_dequant_gemv(q: "QuantizedLayer", X: torch.Tensor, m: int, g_idx: Optional[torch.Tensor] = None,
+                      Y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Y = X W_hat^T (T x m, fp32) from the packed layer q and bf16 tokens X (T x d)."""
+    _need_cuda(X, "X", (torch.bfloat16, torch.int16))
+    if X.dim() != 2 or X.stride(1) != 1 or X.shape[1] != q.d:
+        raise ValueError("X must be T x d with unit column stride")
+    if g_idx is not None:
+        _need_cuda(g_idx, "g_idx", (torch.int32,))
+    T = X.shape[0]
+    if Y is None:
+        Y = torch.empty((T, m), dtype=torch.float32, device=X.device)
+    st = _lib.gptq_dequant_gemv(_ptr(q.qweight), _ptr(q.scales), _ptr(q.zeros), _ptr(g_idx), m, q.d, q.bits,
+                                q.group_size, _ptr(X), T, X.stride(0), _ptr(Y), Y.stride(0), _stream(stream))
+    _check(st, "gptq_dequant_gemv")
+    return Y
 
 
 def gptq_gemm_f32(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, a_kmajor: bool, b_kmajor: bool,

@@ -138,3 +138,23 @@ def test_host_pipeline_token_pieces(g, n, chunk):
     last = n - ((n - 1) // chunk) * chunk if n else 0
     if last >= 4096:
         assert len(pieces) == (n - last) // chunk + 4
+
+
+def test_dequant_gemv_argument_checks(g):
+    lib = g.library()
+    before = g.gptq_launch_count()
+
+    def call(q=P, s=P, z=P, gi=None, m=64, d=256, bits=4, gs=128, X=P, T=3, ldx=256, Y=P, ldy=64):
+        return lib.gptq_dequant_gemv(q, s, z, gi, m, d, bits, gs, X, T, ldx, Y, ldy, None)
+
+    assert call(q=None) == g.GPTQ_ERR_INVALID_ARG
+    assert call(d=250, ldx=256) == g.GPTQ_ERR_INVALID_ARG          # d not a multiple of 32
+    assert call(bits=5) == g.GPTQ_ERR_INVALID_ARG
+    assert call(gs=48) == g.GPTQ_ERR_INVALID_ARG
+    assert call(gs=96) == g.GPTQ_ERR_INVALID_ARG                    # does not divide d
+    assert call(ldx=252) == g.GPTQ_ERR_INVALID_ARG
+    assert call(ldx=260) == g.GPTQ_ERR_INVALID_ARG                  # not a multiple of 8
+    assert call(ldy=63) == g.GPTQ_ERR_INVALID_ARG
+    assert call(q=P + 4) == g.GPTQ_ERR_INVALID_ARG                  # 4-bit words need 16-byte alignment
+    assert call(T=0, X=None, Y=None) == g.GPTQ_OK                   # nothing to do
+    assert g.gptq_launch_count() == before

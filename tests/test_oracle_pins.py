@@ -516,3 +516,21 @@ def test_act_order_groups_blocksize_invariance():
     for x in r[1:]:
         assert np.array_equal(x["codes"], r[0]["codes"])
         np.testing.assert_allclose(x["scales"], r[0]["scales"], rtol=1e-12)
+
+
+# ----------------------------------------------------------------------------------
+# the stored layer used again: dequantize and multiply
+# ----------------------------------------------------------------------------------
+@pytest.mark.parametrize("bits,gs,ao", [(4, 128, False), (3, -1, True), (2, 64, True), (8, 32, False)])
+def test_dequantize_packed_reproduces_w_hat(bits, gs, ao):
+    """The packed codes with the group scales and zeros (g_idx for act-order) give back
+    exactly the W_hat the quantizer produced, and Y = X W_hat^T follows from it."""
+    W, X = _layer(12, 256, 512, seed=bits + 7)
+    H = orc.hessian([X])
+    res = orc.gptq_layer(W, H, bits, gs, 32 if gs == 32 else 64, act_order=ao)
+    words = orc.pack_codes(res["codes"], bits)
+    What = orc.dequantize_packed(words, res["scales"], res["zeros"], bits, 256, gs, res["g_idx"] if ao else None)
+    assert np.array_equal(What, res["W_hat"])
+    Xt = X[:5]
+    np.testing.assert_allclose(orc.dequant_matmul(Xt, words, res["scales"], res["zeros"], bits, gs,
+                                                  res["g_idx"] if ao else None), Xt @ res["W_hat"].T, rtol=1e-12)
