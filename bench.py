@@ -191,6 +191,24 @@ def kernel_traffic(kernel_file: str, key: str):
 
 
 # ----------------------------------------------------------------------------------
+def slowest_rank_seconds(t_local: float, world: int, device) -> float:
+    """The job's time over `world` replicas: the largest of the ranks' timed regions (the
+    job ends with its last replica). One all-reduce (max) when world > 1."""
+    if world <= 1:
+        return t_local
+    import torch
+    import torch.distributed as dist
+    tt = torch.tensor([t_local], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_rate_mweights(world: int, steps: int, weights: int, t_max: float) -> float:
+    """Whole-job throughput: every replica quantizes `weights` per step."""
+    return world * steps * weights / t_max / 1e6
+
+
+# ----------------------------------------------------------------------------------
 def run_reference(args):
     """The oracle as it stands on the host cores, each step a bounded sample."""
     import torch.distributed as dist  # noqa: F401  (only to honour torchrun env; rank 0 works)
@@ -330,14 +348,9 @@ def run_gpu(args):
         st_ms["factor"].append(ev[1].elapsed_time(ev[2]))
         st_ms["quantize"].append(ev[2].elapsed_time(ev[3]))
     step_ms = [a + b + c for a, b, c in zip(st_ms["syrk"], st_ms["factor"], st_ms["quantize"])]
-    t_local = sum(step_ms) / 1e3
-    t_max = t_local
-    if world > 1:
-        tt = torch.tensor([t_local], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_max = float(tt.item())
+    t_max = slowest_rank_seconds(sum(step_ms) / 1e3, world, dev)
     weights = m * d
-    value = world * args.steps * weights / t_max / 1e6
+    value = job_rate_mweights(world, args.steps, weights, t_max)
     ms_per_step = t_max / args.steps * 1e3
     syrk_ms = statistics.mean(st_ms["syrk"])
     syrk_flops = float(n) * d * (d + 1)
@@ -368,13 +381,9 @@ def run_gpu(args):
             b.record(stream)
             b.synchronize()
             e_ms.append(a.elapsed_time(b))
-        te = sum(e_ms) / 1e3
-        if world > 1:
-            tt = torch.tensor([te], dtype=torch.float64, device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            te = float(tt.item())
+        te = slowest_rank_seconds(sum(e_ms) / 1e3, world, dev)
         g.gptq_device_check()
-        e2e = {"value": round(world * args.steps * weights / te / 1e6, 4), "unit": "Mweights/s",
+        e2e = {"value": round(job_rate_mweights(world, args.steps, weights, te), 4), "unit": "Mweights/s",
                "ms_per_step": round(te / args.steps * 1e3, 4),
                "h2d_bytes_per_step": pipe.bytes_h2d(n), "d2h_bytes_per_step": pipe.bytes_d2h()}
 
