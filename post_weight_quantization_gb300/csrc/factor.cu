@@ -330,19 +330,20 @@ __device__ __noinline__ void chol_panel_body(float* __restrict__ P, float* __res
   // The lower triangle of the diagonal block (pieces of four columns up to the
   // diagonal) and the rows below; the identity past a ragged end.
   if (vec && plain) {
-    // whole rows (the part above the diagonal is never read as L), 16 bytes at a time
+    // whole rows (the part above the diagonal is never read as L), 16 bytes at a time,
+    // from L2 (.cg): the rows were stored by the update kernel still running beside us
     constexpr int Q = NB / 4;
     for (int idx = tid; idx < nb * Q; idx += PANEL_THREADS) {
       const int i = idx / Q, c4 = 4 * (idx - i * Q);
       if (c4 < nb)
         *reinterpret_cast<float4*>(S + i * SLD + c4) =
-            *reinterpret_cast<const float4*>(P + (long long)(k0 + i) * d + k0 + c4);
+            __ldcg(reinterpret_cast<const float4*>(P + (long long)(k0 + i) * d + k0 + c4));
     }
     for (int idx = tid; idx < nr * Q; idx += PANEL_THREADS) {
       const int i = idx / Q, c4 = 4 * (idx - i * Q);
       if (c4 < nb)
         *reinterpret_cast<float4*>(R + i * SLD + c4) =
-            *reinterpret_cast<const float4*>(P + (long long)(rbeg + i) * d + k0 + c4);
+            __ldcg(reinterpret_cast<const float4*>(P + (long long)(rbeg + i) * d + k0 + c4));
     }
   } else if (vec) {
     // one bulk asynchronous copy per row: row i of the diagonal block up to the end of
