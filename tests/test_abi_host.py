@@ -158,3 +158,22 @@ def test_dequant_gemv_argument_checks(g):
     assert call(q=P + 4) == g.GPTQ_ERR_INVALID_ARG                  # 4-bit words need 16-byte alignment
     assert call(T=0, X=None, Y=None) == g.GPTQ_OK                   # nothing to do
     assert g.gptq_launch_count() == before
+
+
+def _prototypes():
+    """name -> parameter count of every function include/gptq.h declares."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(gptq_\w+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
+        args = m.group(2).strip()
+        out[m.group(1)] = 0 if args in ("", "void") else args.count(",") + 1
+    return out
+
+
+def test_binding_signatures_match_the_header(g):
+    """Every declared function has a ctypes signature with the same number of parameters."""
+    protos = _prototypes()
+    assert protos, "no prototypes parsed"
+    for name, nargs in protos.items():
+        assert name in g.SIGNATURES, f"{name} has no binding"
+        assert len(g.SIGNATURES[name][1]) == nargs, (name, nargs, len(g.SIGNATURES[name][1]))
