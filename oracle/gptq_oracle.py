@@ -17,6 +17,8 @@ What it computes, step by step, in the order and notation of the pages:
 * ``gptq_columns`` blocked column loop: quantize, error Err1 = (w - w_hat)/Hinv1[j,j],
                    rank-one update inside the block, lazy Err1 @ Hinv1[block, rest]
                    after it; per-element losses Losses1 = Err1^2 / 2.
+* ``sequential_pass``  layers one after another: each layer's Hessian from the
+                   inputs that the already quantized layers before it produce.
 * ``pack_codes`` / ``unpack_codes``  b-bit codes as a little-endian bitstream of
                    uint32 words per row.
 * ``dequantize_packed`` / ``dequant_matmul``  the stored layer used again: W_hat
@@ -43,6 +45,9 @@ design notes of the repository):
 * act-order ties keep the lower column index first (stable sort).
 * act-order with groups: groups are formed in processing order; original column j
   uses group (position of j in the order) // group_size.
+* Layers one after another: the synthetic model is a chain of linear layers with
+  nothing between them; layer l+1 is calibrated on X_l W_hat_l^T (the quantized
+  outputs), rounded to bfloat16.
 * Code storage: code (r, j) occupies bits [j*b, j*b + b) of row r's stream.
 """
 from __future__ import annotations
@@ -53,7 +58,7 @@ import scipy.linalg
 __all__ = [
     "hessian", "hessian_accumulate", "hessian_entries", "damp", "act_order_perm",
     "hinv1", "quant_params", "quantize", "dequantize", "gptq_columns", "gptq_layer",
-    "rtn", "pack_codes", "unpack_codes", "packed_words_per_row",
+    "rtn", "round_to_bf16", "sequential_pass", "pack_codes", "unpack_codes", "packed_words_per_row",
     "dequantize_packed", "dequant_matmul",
     "relative_output_error", "loss_quadratic_form",
 ]
@@ -292,6 +297,55 @@ def rtn(W: np.ndarray, bits: int, group_size: int = 128, dtype=np.float64) -> di
         What[:, sl] = dequantize(q, s[:, None], z[:, None])
         scales[:, k], zeros[:, k] = s, z
     return {"codes": codes, "W_hat": What, "scales": scales, "zeros": zeros}
+
+
+# ----------------------------------------------------------------------------------
+# Layers one after another
+# ----------------------------------------------------------------------------------
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """Each value rounded to the nearest bfloat16 (8 significant bits, ties to even),
+    returned as float64. Written from the format's definition: x = f * 2^e with
+    0.5 <= |f| < 1, keep rint(f * 2^8) / 2^8. Values are assumed inside bfloat16's
+    normal range (|x| between 2^-126 and 2^128) or zero."""
+    x = np.asarray(x, dtype=np.float64)
+    f, e = np.frexp(x)
+    return np.ldexp(np.rint(np.ldexp(f, 8)), e - 8)
+
+
+def sequential_pass(X0: np.ndarray, weights, bits: int = 4, group_size: int = 128,
+                    blocksize: int = 128, percdamp: float = 0.01, act_order: bool = False,
+                    propagate: str | None = "bf16") -> dict:
+    """Quantize a chain of linear layers one after another, each on the inputs that the
+    layers already quantized hand it.
+
+    "The GPTQ Algorithm" (procedure, steps 1-4) and "GPTQ: fixing errors as you go" (the
+    algorithm in words: record the layer's inputs, build H = 2 X X^T, go through the
+    columns, then move to the next layer). The pages' models are not at hand; the
+    plainest synthetic stand-in is a chain of linear layers W_1 (m_1 x d), W_2 (m_2 x
+    m_1), ... with nothing between them. Layer l's calibration inputs are the outputs
+    of the layers before it with their quantized weights, X_{l+1} = X_l W_hat_l^T,
+    rounded to bfloat16 (the activations' storage type) unless ``propagate`` is None
+    (kept in float64).
+
+    Returns ``layers`` (one ``gptq_layer`` result per layer), ``inputs`` (X_l of every
+    layer, float64), ``H`` (the undamped Hessian of every layer) and ``output`` (the
+    last layer's quantized output X_{L+1} before rounding).
+    """
+    X = np.asarray(X0, dtype=np.float64)
+    layers, inputs, hessians = [], [], []
+    out = None
+    for li, W in enumerate(weights):
+        W = np.asarray(W, dtype=np.float64)
+        if W.shape[1] != X.shape[1]:
+            raise ValueError(f"layer {li}: W has {W.shape[1]} input channels, the inputs {X.shape[1]}")
+        H = hessian([X])
+        res = gptq_layer(W, H, bits, group_size, blocksize, percdamp, act_order)
+        inputs.append(X)
+        hessians.append(H)
+        layers.append(res)
+        out = X @ res["W_hat"].T
+        X = round_to_bf16(out) if propagate == "bf16" else out
+    return {"layers": layers, "inputs": inputs, "H": hessians, "output": out}
 
 
 # ----------------------------------------------------------------------------------

@@ -15,6 +15,7 @@ import pytest
 
 from oracle import gptq_oracle as orc
 from synth import ActSpec, bf16_bits_to_f32, make_activations, make_weight
+from synth.workloads import f32_to_bf16_bits
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -534,3 +535,110 @@ def test_dequantize_packed_reproduces_w_hat(bits, gs, ao):
     Xt = X[:5]
     np.testing.assert_allclose(orc.dequant_matmul(Xt, words, res["scales"], res["zeros"], bits, gs,
                                                   res["g_idx"] if ao else None), Xt @ res["W_hat"].T, rtol=1e-12)
+
+
+# ----------------------------------------------------------------------------------
+# layers one after another
+# ----------------------------------------------------------------------------------
+def _bf16_table():
+    """Every finite positive bfloat16 value, ascending, with its bit pattern."""
+    bits = np.arange(1, 0x7F80, dtype=np.uint32).astype(np.uint16)
+    return bf16_bits_to_f32(bits).astype(np.float64), bits
+
+
+def test_round_to_bf16_is_nearest_with_ties_to_even():
+    """Brute force over the whole bfloat16 table: each result is a bfloat16 value, no
+    other one is nearer, and exact midpoints go to the neighbour with an even last
+    mantissa bit. For float32 inputs it also agrees with the input generators' bit-level
+    float32 rounding, a different construction."""
+    vals, bits = _bf16_table()
+    rng = np.random.default_rng(21)
+    y = rng.standard_normal(4000) * np.exp(rng.uniform(-30, 30, 4000))
+    k = rng.integers(200, len(vals) - 200, 500)
+    mids = 0.5 * (vals[k] + vals[k + 1])                  # exact in float64
+    y = np.concatenate([y, mids, -mids, vals[k], [0.0]])
+    r = orc.round_to_bf16(y)
+    a = np.abs(y)
+    i = np.clip(np.searchsorted(vals, a), 1, len(vals) - 1)
+    lo, hi = vals[i - 1], vals[i]
+    dlo, dhi = a - lo, hi - a
+    want = np.where(dlo < dhi, lo, np.where(dhi < dlo, hi, np.where(bits[i - 1] % 2 == 0, lo, hi)))
+    want = np.where(a == 0, 0.0, np.copysign(want, y))
+    assert np.array_equal(r, want)
+    assert np.all(np.abs(r[len(y) - 1 - 3 * 500:len(y) - 1 - 500]) != 0)
+    x32 = (rng.standard_normal(20000) * np.exp(rng.uniform(-40, 40, 20000))).astype(np.float32)
+    assert np.array_equal(orc.round_to_bf16(x32.astype(np.float64)),
+                          bf16_bits_to_f32(f32_to_bf16_bits(x32)).astype(np.float64))
+
+
+@pytest.mark.parametrize("ao,gs", [(False, 16), (True, 16), (True, -1)])
+def test_sequential_pass_second_hessian_is_the_quantized_sandwich(ao, gs):
+    """Kept in float64 between layers, X_2 = X_1 W_hat_1^T, so H_2 = W_hat_1 H_1 W_hat_1^T:
+    the quantized weights (not the original ones), in the original column order (act-order
+    undone) and the right orientation, carry the inputs onward."""
+    W1 = bf16_bits_to_f32(make_weight(48, 64, seed=4, layer=0)).astype(np.float64)
+    W2 = bf16_bits_to_f32(make_weight(32, 48, seed=4, layer=1)).astype(np.float64)
+    X = bf16_bits_to_f32(make_activations(ActSpec("heavy_tail", 600, 64, seed=4))).astype(np.float64)
+    res = orc.sequential_pass(X, [W1, W2], bits=3, group_size=gs, blocksize=16, act_order=ao, propagate=None)
+    H1, H2 = res["H"]
+    Wh = res["layers"][0]["W_hat"]
+    want = Wh @ H1 @ Wh.T
+    np.testing.assert_allclose(H2, want, rtol=1e-9, atol=1e-12 * np.abs(want).max())
+    assert not np.allclose(H2, W1 @ H1 @ W1.T, rtol=1e-3)
+    # the second layer is quantized against that Hessian
+    assert res["layers"][1]["codes"].shape == (32, 48)
+
+
+def _on_grid_weight(m, d, bits, g, rng):
+    """W = (code - zero) * scale with every row of every group holding the codes 0 and
+    2^b - 1 and a power-of-two scale: min/max give back exactly that scale and zero."""
+    q = rng.integers(0, 2 ** bits, size=(m, d))
+    q[:, 0::g] = 0
+    q[:, 1::g] = 2 ** bits - 1
+    z = rng.integers(0, 2 ** bits, size=(m, d // g)).astype(np.float64)
+    s = np.ldexp(1.0, -rng.integers(5, 9, size=(m, d // g)))
+    gi = np.arange(d) // g
+    return (q - z[:, gi]) * s[:, gi], q, s, z
+
+
+def test_sequential_pass_on_grid_weights_is_the_plain_product_chain():
+    """Weights already on their grid quantize to themselves with zero error, so nothing is
+    compensated and the pass reduces to X_0 W_1^T W_2^T W_3^T exactly; with bfloat16 between
+    layers every recorded input is a bfloat16 value within half an ulp of the float chain's."""
+    rng = np.random.default_rng(8)
+    X0 = bf16_bits_to_f32(make_activations(ActSpec("gauss_cov", 300, 64, seed=8))).astype(np.float64)
+    shapes = [(96, 64), (64, 96), (32, 64)]
+    Ws, Qs = [], []
+    for m, d in shapes:
+        W, q, s, z = _on_grid_weight(m, d, 4, 32, rng)
+        Ws.append(W)
+        Qs.append((q, s, z))
+    res = orc.sequential_pass(X0, Ws, bits=4, group_size=32, blocksize=32, propagate=None)
+    for lay, W, (q, s, z) in zip(res["layers"], Ws, Qs):
+        assert np.array_equal(lay["codes"], q)
+        assert np.array_equal(lay["scales"], s) and np.array_equal(lay["zeros"], z)
+        assert np.array_equal(lay["W_hat"], W)
+        assert np.all(lay["losses"] == 0)
+    assert np.array_equal(res["output"], X0 @ Ws[0].T @ Ws[1].T @ Ws[2].T)
+    rb = orc.sequential_pass(X0, Ws, bits=4, group_size=32, blocksize=32)
+    chain = X0 @ Ws[0].T
+    x1 = rb["inputs"][1]
+    assert np.array_equal(bf16_bits_to_f32(f32_to_bf16_bits(x1.astype(np.float32))).astype(np.float64), x1)
+    assert np.all(np.abs(x1 - chain) <= np.ldexp(np.abs(chain), -8))   # 8 significant bits
+
+
+def test_sequential_pass_layers_are_the_single_layer_path_on_their_inputs():
+    """Every layer of the pass is the single-layer path on H = 2 X_l^T X_l of the inputs it
+    records (bfloat16 values: the Hessian sees the rounded inputs, as a Hessian built from
+    stored bfloat16 activations does); a chain whose widths do not meet is refused."""
+    W, X = _layer(16, 64, 256, seed=30)
+    W2 = bf16_bits_to_f32(make_weight(24, 16, seed=30, layer=1)).astype(np.float64)
+    res = orc.sequential_pass(X, [W, W2], bits=4, group_size=16, blocksize=16)
+    for Wl, Xl, lay in zip((W, W2), res["inputs"], res["layers"]):
+        ref = orc.gptq_layer(Wl, 2.0 * (Xl.T @ Xl), 4, 16, 16)
+        for k in ("codes", "scales", "zeros", "W_hat", "losses"):
+            assert np.array_equal(lay[k], ref[k]), k
+    x1 = res["inputs"][1]
+    assert np.array_equal(bf16_bits_to_f32(f32_to_bf16_bits(x1.astype(np.float32))).astype(np.float64), x1)
+    with pytest.raises(ValueError):
+        orc.sequential_pass(X, [W, np.zeros((8, 15))], bits=4, group_size=-1, blocksize=16)
