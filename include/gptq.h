@@ -241,7 +241,8 @@ gptq_status gptq_quantize_layer(const void* W, int w_dtype, int64_t m, int64_t d
 /*
  * Helper for checks: unpack codes written by gptq_quantize_layer into one byte per
  * code. qweight as above (m x ceil(d*bits/32) words, device); codes device uint8
- * m x d row-major.
+ * m x d row-major. m <= 2^30, d <= 65536, m * d <= 2^36, else GPTQ_ERR_INVALID_ARG
+ * before any launch.
  */
 gptq_status gptq_unpack_codes(const uint32_t* qweight, int64_t m, int64_t d, int bits,
                               uint8_t* codes, gptq_stream_t stream);
@@ -261,7 +262,8 @@ gptq_status gptq_unpack_codes(const uint32_t* qweight, int64_t m, int64_t d, int
  *   m, d       rows and columns of W; d a multiple of 32.
  *   bits       2, 3, 4 or 8.  group_size  -1 or a multiple of 32 dividing d.
  *   X          device bf16 bits, T x d token-major, row stride ldx (ldx >= d,
- *              ldx % 8 == 0, 16-byte aligned). T >= 0 tokens (8 per launch inside).
+ *              ldx % 8 == 0, 16-byte aligned). 0 <= T < 2^31 tokens (8 per launch
+ *              inside).
  *   Y          device fp32, T x m, row stride ldy >= m.
  * Asynchronous on `stream`; argument errors return GPTQ_ERR_INVALID_ARG before any
  * launch. This is the use of the stored layer that the pages describe, not a step of

@@ -284,7 +284,8 @@ gptq_status gptq_unpack_codes(const uint32_t* qweight, int64_t m, int64_t d, int
                               gptq_stream_t stream) {
   g_last_error[0] = 0;
   if (!qweight || !codes) return set_error(GPTQ_ERR_INVALID_ARG, "NULL pointer");
-  if (m < 0 || d < 0) return set_error(GPTQ_ERR_INVALID_ARG, "negative size");
+  if (m < 0 || m > ((int64_t)1 << 30) || d < 0 || d > 65536 || m * d > ((int64_t)1 << 36))
+    return set_error(GPTQ_ERR_INVALID_ARG, "m in [0, 2^30], d in [0, 65536] and m * d <= 2^36 are required");
   if (bits != 2 && bits != 3 && bits != 4 && bits != 8) return set_error(GPTQ_ERR_INVALID_ARG, "bits must be 2, 3, 4 or 8");
   return unpack_launch(qweight, m, d, bits, codes, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -299,7 +300,8 @@ gptq_status gptq_dequant_gemv(const uint32_t* qweight, const float* scales, cons
   if (bits != 2 && bits != 3 && bits != 4 && bits != 8) return set_error(GPTQ_ERR_INVALID_ARG, "bits must be 2, 3, 4 or 8");
   if (group_size != -1 && (group_size < 32 || group_size % 32 || d % group_size))
     return set_error(GPTQ_ERR_INVALID_ARG, "group_size must be -1 or a multiple of 32 that divides d");
-  if (T < 0 || ldx < d || ldx % 8 || ldy < m) return set_error(GPTQ_ERR_INVALID_ARG, "bad T, ldx or ldy");
+  if (T < 0 || T > 0x7FFFFFFF || ldx < d || ldx % 8 || ldy < m)
+    return set_error(GPTQ_ERR_INVALID_ARG, "bad T, ldx or ldy");
   const size_t qa = (bits == 4 || bits == 8) ? 16 : (bits == 2 ? 8 : 4);
   if (!aligned(qweight, qa) || (T > 0 && !aligned(X, 16)) || !aligned(scales, 4) || !aligned(zeros, 4))
     return set_error(GPTQ_ERR_INVALID_ARG, "qweight (16 bytes for 4 and 8 bits, 8 for 2) or X (16 bytes) misaligned");

@@ -106,6 +106,50 @@ def _need_cuda(t: torch.Tensor, name: str, dtypes) -> None:
         raise TypeError(f"{name} must have dtype in {dtypes}, got {t.dtype}")
 
 
+def _need_buffer(t: torch.Tensor, name: str, shape, dtypes) -> None:
+    """A tensor the library reads or writes as a dense array: CUDA, one of `dtypes`, the
+    exact `shape`, contiguous."""
+    _need_cuda(t, name, dtypes)
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _need_rows(t: torch.Tensor, name: str, rows: int, cols: int, dtypes) -> None:
+    """A contiguous row-major array of `cols` columns with at least `rows` rows (the
+    library reads the first `rows`)."""
+    _need_cuda(t, name, dtypes)
+    if t.dim() != 2 or t.shape[1] != cols or t.shape[0] < rows:
+        raise ValueError(f"{name} must have shape (>= {rows}, {cols}), got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _one_device(*tensors) -> torch.device:
+    """The common device of the tensors, which must be the current CUDA device (the
+    library launches on the current device)."""
+    devs = {t.device for t in tensors if t is not None}
+    if len(devs) != 1:
+        raise ValueError(f"all tensors must be on one device, got {sorted(map(str, devs))}")
+    dev = devs.pop()
+    if dev.index is not None and dev.index != torch.cuda.current_device():
+        raise ValueError(f"tensors are on {dev} but the current device is cuda:{torch.cuda.current_device()}; "
+                         f"call under torch.cuda.device({dev.index})")
+    return dev
+
+
+def _need_workspace(ws: torch.Tensor, nbytes: int) -> int:
+    """Bytes of a caller workspace (any dtype), which must cover `nbytes`."""
+    _need_cuda(ws, "ws", (torch.uint8, torch.int8, torch.int32, torch.float32, torch.int64, torch.float64))
+    if not ws.is_contiguous():
+        raise ValueError("ws must be contiguous")
+    have = ws.numel() * ws.element_size()
+    if have < nbytes:
+        raise ValueError(f"ws holds {have} bytes, {nbytes} are needed")
+    return have
+
+
 # ----------------------------------------------------------------------------------
 def gptq_status_string(status: int) -> str:
     return _lib.gptq_status_string(status).decode()
@@ -151,6 +195,7 @@ def gptq_hessian_accumulate(X: torch.Tensor, H: torch.Tensor, alpha: float = 2.0
     n, d = X.shape
     if H.shape[0] != d or H.shape[1] != d:
         raise ValueError("H must be d x d")
+    _one_device(X, H)
     _check(_lib.gptq_hessian_accumulate(_ptr(X), n, d, X.stride(0), _ptr(H), H.stride(0), float(alpha),
                                         int(bool(zero_first)), _stream(stream)), "gptq_hessian_accumulate")
     return H
@@ -171,13 +216,19 @@ def gptq_factor(H: torch.Tensor, percdamp: float = 0.01, act_order: bool = False
     dev = H.device
     if Hinv1 is None:
         Hinv1 = torch.empty((d, d), dtype=torch.float32, device=dev)
-    if act_order and perm_out is None:
-        perm_out = torch.empty(d, dtype=torch.int32, device=dev)
+    _need_buffer(Hinv1, "Hinv1", (d, d), (torch.float32,))
+    if act_order:
+        if perm_out is None:
+            perm_out = torch.empty(d, dtype=torch.int32, device=dev)
+        _need_buffer(perm_out, "perm_out", (d,), (torch.int32,))
+    need = gptq_workspace_size(GPTQ_WS_FACTOR, 0, d)
     if ws is None:
-        ws = _workspace(gptq_workspace_size(GPTQ_WS_FACTOR, 0, d), dev)
+        ws = _workspace(need, dev)
+    ws_bytes = _need_workspace(ws, need)
+    _one_device(H, Hinv1, perm_out if act_order else None, ws)
     info = _c_i64(-1)
     st = _lib.gptq_factor(_ptr(H), d, float(percdamp), int(bool(act_order)), _ptr(perm_out) if act_order else None,
-                          _ptr(Hinv1), _ptr(ws), ws.numel(), ctypes.byref(info) if sync else None, _stream(stream))
+                          _ptr(Hinv1), _ptr(ws), ws_bytes, ctypes.byref(info) if sync else None, _stream(stream))
     _check(st, "gptq_factor")
     return Hinv1, (perm_out if act_order else None), (int(info.value) if sync else None)
 
@@ -192,7 +243,8 @@ def gptq_factor_static(H: torch.Tensor, Hinv1: torch.Tensor, percdamp: float = 0
     if not H.is_contiguous() or not Hinv1.is_contiguous() or Hinv1.shape != H.shape:
         raise ValueError("H and Hinv1 must be contiguous d x d tensors")
     if act_order:
-        _need_cuda(perm_out, "perm_out", (torch.int32,))
+        _need_buffer(perm_out, "perm_out", (d,), (torch.int32,))
+    _one_device(H, Hinv1, perm_out if act_order else None)
     info = _c_i64(-1)
     st = _lib.gptq_factor_static(_ptr(H), d, float(percdamp), int(bool(act_order)),
                                  _ptr(perm_out) if act_order else None, _ptr(Hinv1),
@@ -224,7 +276,7 @@ def gptq_quantize_layer(W: torch.Tensor, Hinv1: torch.Tensor, perm: Optional[tor
     if Hinv1.shape != (d, d) or not Hinv1.is_contiguous():
         raise ValueError("Hinv1 must be a contiguous d x d tensor")
     if perm is not None:
-        _need_cuda(perm, "perm", (torch.int32,))
+        _need_buffer(perm, "perm", (d,), (torch.int32,))
     dev = W.device
     G = 1 if group_size == -1 else (d // group_size if group_size > 0 else 1)
     if out is None:
@@ -234,19 +286,30 @@ def gptq_quantize_layer(W: torch.Tensor, Hinv1: torch.Tensor, perm: Optional[tor
             zeros=torch.empty((m, G), dtype=torch.float32, device=dev),
             col_losses=torch.empty(d, dtype=torch.float32, device=dev),
             bits=bits, group_size=group_size, d=d)
+    if (out.bits, out.group_size, out.d) != (bits, group_size, d):
+        raise ValueError(f"out describes bits={out.bits}, group_size={out.group_size}, d={out.d}; "
+                         f"the call has {bits}, {group_size}, {d}")
+    _need_buffer(out.qweight, "out.qweight", (m, (d * bits + 31) // 32), (torch.int32,))
+    _need_buffer(out.scales, "out.scales", (m, G), (torch.float32,))
+    _need_buffer(out.zeros, "out.zeros", (m, G), (torch.float32,))
+    _need_buffer(out.col_losses, "out.col_losses", (d,), (torch.float32,))
+    need = gptq_workspace_size(GPTQ_WS_QUANTIZE, m, d, bits, group_size, blocksize)
     if ws is None:
-        ws = _workspace(gptq_workspace_size(GPTQ_WS_QUANTIZE, m, d, bits, group_size, blocksize), dev)
+        ws = _workspace(need, dev)
+    ws_bytes = _need_workspace(ws, need)
+    _one_device(W, Hinv1, perm, out.qweight, out.scales, out.zeros, out.col_losses, ws)
     info = _c_i64(0)
     st = _lib.gptq_quantize_layer(_ptr(W), 0 if W.dtype == torch.float32 else 1, m, d, W.stride(0), _ptr(Hinv1),
                                   _ptr(perm), bits, group_size, blocksize, _ptr(out.qweight), _ptr(out.scales),
-                                  _ptr(out.zeros), _ptr(out.col_losses), _ptr(ws), ws.numel(),
+                                  _ptr(out.zeros), _ptr(out.col_losses), _ptr(ws), ws_bytes,
                                   ctypes.byref(info) if sync else None, _stream(stream))
     _check(st, "gptq_quantize_layer")
     return out
 
 
 def gptq_unpack_codes(qweight: torch.Tensor, m: int, d: int, bits: int, stream=None) -> torch.Tensor:
-    _need_cuda(qweight, "qweight", (torch.int32,))
+    _need_rows(qweight, "qweight", m, (d * bits + 31) // 32, (torch.int32,))
+    _one_device(qweight)
     codes = torch.empty((m, d), dtype=torch.uint8, device=qweight.device)
     _check(_lib.gptq_unpack_codes(_ptr(qweight), m, d, bits, _ptr(codes), _stream(stream)), "gptq_unpack_codes")
     return codes
@@ -258,11 +321,19 @@ def gptq_dequant_gemv(q: "QuantizedLayer", X: torch.Tensor, m: int, g_idx: Optio
     _need_cuda(X, "X", (torch.bfloat16, torch.int16))
     if X.dim() != 2 or X.stride(1) != 1 or X.shape[1] != q.d:
         raise ValueError("X must be T x d with unit column stride")
+    G = 1 if q.group_size == -1 else (q.d // q.group_size if q.group_size > 0 else 1)
+    _need_rows(q.qweight, "q.qweight", m, (q.d * q.bits + 31) // 32, (torch.int32,))
+    _need_rows(q.scales, "q.scales", m, G, (torch.float32,))
+    _need_rows(q.zeros, "q.zeros", m, G, (torch.float32,))
     if g_idx is not None:
-        _need_cuda(g_idx, "g_idx", (torch.int32,))
+        _need_buffer(g_idx, "g_idx", (q.d,), (torch.int32,))
     T = X.shape[0]
     if Y is None:
         Y = torch.empty((T, m), dtype=torch.float32, device=X.device)
+    _need_cuda(Y, "Y", (torch.float32,))
+    if Y.dim() != 2 or tuple(Y.shape) != (T, m) or Y.stride(1) != 1:
+        raise ValueError(f"Y must be ({T}, {m}) with unit column stride, got {tuple(Y.shape)}")
+    _one_device(q.qweight, q.scales, q.zeros, g_idx, X, Y)
     st = _lib.gptq_dequant_gemv(_ptr(q.qweight), _ptr(q.scales), _ptr(q.zeros), _ptr(g_idx), m, q.d, q.bits,
                                 q.group_size, _ptr(X), T, X.stride(0), _ptr(Y), Y.stride(0), _stream(stream))
     _check(st, "gptq_dequant_gemv")
@@ -282,6 +353,11 @@ def gptq_gemm_f32(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, a_kmajor: b
             raise ValueError(f"{nm} must be 2-D with unit column stride")
     M, N = C.shape
     K = A.shape[1] if a_kmajor else A.shape[0]
+    if (A.shape[0] if a_kmajor else A.shape[1]) != M:
+        raise ValueError(f"A must be ({M}, K) when a_kmajor, else (K, {M}); got {tuple(A.shape)}")
+    if tuple(B.shape) != ((N, K) if b_kmajor else (K, N)):
+        raise ValueError(f"B must be {(N, K) if b_kmajor else (K, N)}, got {tuple(B.shape)}")
+    _one_device(A, B, C)
     _check(_lib.gptq_gemm_f32(engine, int(a_kmajor), int(b_kmajor), M, N, K, _ptr(A), A.stride(0), _ptr(B),
                               B.stride(0), _ptr(C), C.stride(0), float(alpha), float(beta), int(lower_tiles),
                               _stream(stream)), "gptq_gemm_f32")

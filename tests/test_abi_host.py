@@ -157,6 +157,20 @@ def test_dequant_gemv_argument_checks(g):
     assert call(ldy=63) == g.GPTQ_ERR_INVALID_ARG
     assert call(q=P + 4) == g.GPTQ_ERR_INVALID_ARG                  # 4-bit words need 16-byte alignment
     assert call(T=0, X=None, Y=None) == g.GPTQ_OK                   # nothing to do
+    assert call(T=1 << 31) == g.GPTQ_ERR_INVALID_ARG                # token count beyond int32
+    assert call(T=-1) == g.GPTQ_ERR_INVALID_ARG
+    assert g.gptq_launch_count() == before
+
+
+def test_unpack_codes_argument_checks(g):
+    lib = g.library()
+    before = g.gptq_launch_count()
+    assert lib.gptq_unpack_codes(None, 4, 64, 4, P, None) == g.GPTQ_ERR_INVALID_ARG
+    assert lib.gptq_unpack_codes(P, 4, 64, 5, P, None) == g.GPTQ_ERR_INVALID_ARG
+    assert lib.gptq_unpack_codes(P, -1, 64, 4, P, None) == g.GPTQ_ERR_INVALID_ARG
+    assert lib.gptq_unpack_codes(P, 4, 65537, 4, P, None) == g.GPTQ_ERR_INVALID_ARG
+    assert lib.gptq_unpack_codes(P, (1 << 30) + 1, 64, 4, P, None) == g.GPTQ_ERR_INVALID_ARG
+    assert lib.gptq_unpack_codes(P, 1 << 30, 65536, 4, P, None) == g.GPTQ_ERR_INVALID_ARG    # m * d > 2^36
     assert g.gptq_launch_count() == before
 
 
