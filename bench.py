@@ -62,6 +62,55 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+# Nominal dense tensor-core ratio TF32 : bf16 on GB300 (1.1 : 2.25 PFLOP/s), applied to
+# the measured bf16 peak; FP32 FFMA peak from the unit counts and the maximum SM clock:
+# 152 SMs x 128 FP32 lanes x 2 flops per fused multiply-add.
+TF32_PER_BF16 = 1.1 / 2.25
+SM_COUNT, FP32_LANES_PER_SM = 152, 128
+
+
+def stage_rooflines(m, d, n, bits, group_size, blocksize, syrk_ms, quantize_ms, peaks):
+    """Both bars of the path, each stage against its own bound.
+
+    Hessian SYRK: n*d*(d+1) flops (upper triangle) against the measured bf16 peak.
+    Column loop + lazy update (the quantize call): T_roof = max(B / HBM,
+    F_lazy / P_tf32 + F_in / P_ffma) with B the algorithmic bytes (W in bf16, the upper
+    triangle of Hinv1, codes, scales and zeros, column losses), F_lazy the flops of the
+    lazy block updates Err1 @ Hinv1[block, rest] and F_in those of the rank-one updates
+    inside the blocks. The path computes every lazy product as three TF32 passes (fp32
+    accuracy), so the same bound with 3 F_lazy is given beside it.
+    """
+    G = 1 if group_size in (-1, 0) else d // group_size
+    f_lazy = f_in = 0.0
+    for i1 in range(0, d, blocksize):
+        nb = min(blocksize, d - i1)
+        f_lazy += 2.0 * m * nb * (d - i1 - nb)
+        f_in += 1.0 * m * nb * (nb - 1)
+    nbytes = 2.0 * m * d + 4.0 * d * (d + 1) / 2 + m * d * bits / 8 + 8.0 * m * G + 4.0 * d
+    hbm = peaks["hbm_gbs"] * 1e9
+    p_tf32 = peaks["bf16_tflops"] * 1e12 * TF32_PER_BF16
+    p_ffma = SM_COUNT * FP32_LANES_PER_SM * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6
+    t_mem = nbytes / hbm
+    t1 = max(t_mem, f_lazy / p_tf32 + f_in / p_ffma)
+    t3 = max(t_mem, 3 * f_lazy / p_tf32 + f_in / p_ffma)
+    syrk_flops = float(n) * d * (d + 1)
+    t_syrk = syrk_flops / (peaks["bf16_tflops"] * 1e12)
+    return {
+        "syrk": {"ms": round(syrk_ms, 4), "bound_ms": round(t_syrk * 1e3, 4),
+                 "frac": round(t_syrk * 1e3 / syrk_ms, 4), "bar": 0.60,
+                 "model": "n*d*(d+1) flops / measured bf16 peak"},
+        "column_loop_and_lazy_update": {
+            "ms": round(quantize_ms, 4), "bound_ms": round(t1 * 1e3, 4), "frac": round(t1 * 1e3 / quantize_ms, 4),
+            "bar": 0.50,
+            "bound_ms_three_pass": round(t3 * 1e3, 4), "frac_three_pass": round(t3 * 1e3 / quantize_ms, 4),
+            "model": "max(bytes / HBM, F_lazy / P_tf32 + F_in / P_ffma)",
+            "bytes": int(nbytes), "flops_lazy": f_lazy, "flops_in_block": f_in,
+            "p_tf32_tflops": round(p_tf32 / 1e12, 1), "p_ffma_tflops": round(p_ffma / 1e12, 2),
+            "peaks": "HBM and bf16 measured; TF32 = bf16 x 1.1/2.25 (nominal ratio); FFMA from unit counts "
+                     "and the maximum SM clock"},
+    }
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -419,6 +468,8 @@ def run_gpu(args):
                 "stages_ms": {k: round(statistics.mean(v), 4) for k, v in st_ms.items()},
                 "quantize_only_ms": round(statistics.mean(st_ms["factor"]) + statistics.mean(st_ms["quantize"]), 4),
                 "syrk_tflops": round(syrk_tflops, 2),
+                "stage_rooflines": stage_rooflines(m, d, n, wl.bits, wl.group_size, wl.blocksize, syrk_ms,
+                                                   statistics.mean(st_ms["quantize"]), peaks),
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
                 "clocks": clk, "wall_s_timed_region": round(t_wall, 4), "input_generation_s": round(t_gen, 2),
                 **line_note}
