@@ -19,6 +19,7 @@ namespace gptq {
 // host bookkeeping (defined in gptq_abi.cu)
 // ------------------------------------------------------------------------------
 gptq_status set_error(gptq_status st, const char* fmt, ...);
+void clear_error();   // empty this thread's last-error text (every entry point starts with it)
 void count_launch(int n = 1);
 
 // Opt-in launch timing (environment variable GPTQ_PROFILE=1): a ProfScope records a

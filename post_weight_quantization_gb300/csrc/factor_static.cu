@@ -63,6 +63,7 @@ using namespace gptq;
 
 extern "C" gptq_status gptq_factor_static(const float* H, int64_t d, float percdamp, int act_order,
                                           int32_t* perm_out, float* Hinv1, int64_t* info, gptq_stream_t stream) {
+  clear_error();
   if (!H || !Hinv1) return set_error(GPTQ_ERR_INVALID_ARG, "H and Hinv1 must not be NULL");
   if (d < 1) return set_error(GPTQ_ERR_INVALID_ARG, "d must be >= 1");
   if (d > kStaticMaxD)

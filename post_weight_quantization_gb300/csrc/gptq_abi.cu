@@ -60,6 +60,8 @@ gptq_status set_error(gptq_status st, const char* fmt, ...) {
   return st;
 }
 
+void clear_error() { g_last_error[0] = 0; }
+
 void count_launch(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
 
 gptq_status check_launch(const char* what) {

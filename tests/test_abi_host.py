@@ -162,6 +162,21 @@ def test_dequant_gemv_argument_checks(g):
     assert g.gptq_launch_count() == before
 
 
+def test_factor_static_argument_checks(g):
+    lib = g.library()
+    info = ctypes.c_int64(0)
+    call = lambda H, d, pd, ao, perm, U: lib.gptq_factor_static(H, d, pd, ao, perm, U, ctypes.byref(info), None)
+    before = g.gptq_launch_count()
+    assert call(None, 64, 0.01, 0, None, P) == g.GPTQ_ERR_INVALID_ARG
+    assert call(P, 0, 0.01, 0, None, P) == g.GPTQ_ERR_INVALID_ARG
+    assert call(P, 2049, 0.01, 0, None, P) == g.GPTQ_ERR_INVALID_ARG
+    assert "2048" in g.gptq_last_error()
+    assert call(P, 64, float("nan"), 0, None, P) == g.GPTQ_ERR_INVALID_ARG
+    assert call(P, 64, 0.01, 1, None, P) == g.GPTQ_ERR_INVALID_ARG       # act-order without perm_out
+    assert "perm_out" in g.gptq_last_error()
+    assert g.gptq_launch_count() == before
+
+
 def test_unpack_codes_argument_checks(g):
     lib = g.library()
     before = g.gptq_launch_count()
