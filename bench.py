@@ -69,8 +69,8 @@ TF32_PER_BF16 = 1.1 / 2.25
 SM_COUNT, FP32_LANES_PER_SM = 152, 128
 
 
-def stage_rooflines(m, d, n, bits, group_size, blocksize, syrk_ms, quantize_ms, peaks):
-    """Both bars of the path, each stage against its own bound.
+def stage_rooflines(m, d, n, bits, group_size, blocksize, syrk_ms, quantize_ms, peaks, factor_ms=None):
+    """Each stage against its own bound (bars for the SYRK and the column loop).
 
     Hessian SYRK: n*d*(d+1) flops (upper triangle) against the measured bf16 peak.
     Column loop + lazy update (the quantize call): T_roof = max(B / HBM,
@@ -79,6 +79,9 @@ def stage_rooflines(m, d, n, bits, group_size, blocksize, syrk_ms, quantize_ms, 
     lazy block updates Err1 @ Hinv1[block, rest] and F_in those of the rank-one updates
     inside the blocks. The path computes every lazy product as three TF32 passes (fp32
     accuracy), so the same bound with 3 F_lazy is given beside it.
+    Factor (reported, no bar): the Cholesky of the reversed damped Hessian and the
+    inverse of its triangular factor, d^3/3 flops each, against the TF32 peak, with one
+    and with three passes per product.
     """
     G = 1 if group_size in (-1, 0) else d // group_size
     f_lazy = f_in = 0.0
@@ -95,7 +98,7 @@ def stage_rooflines(m, d, n, bits, group_size, blocksize, syrk_ms, quantize_ms, 
     t3 = max(t_mem, 3 * f_lazy / p_tf32 + f_in / p_ffma)
     syrk_flops = float(n) * d * (d + 1)
     t_syrk = syrk_flops / (peaks["bf16_tflops"] * 1e12)
-    return {
+    out = {
         "syrk": {"ms": round(syrk_ms, 4), "bound_ms": round(t_syrk * 1e3, 4),
                  "frac": round(t_syrk * 1e3 / syrk_ms, 4), "bar": 0.60,
                  "model": "n*d*(d+1) flops / measured bf16 peak"},
@@ -109,6 +112,14 @@ def stage_rooflines(m, d, n, bits, group_size, blocksize, syrk_ms, quantize_ms, 
             "peaks": "HBM and bf16 measured; TF32 = bf16 x 1.1/2.25 (nominal ratio); FFMA from unit counts "
                      "and the maximum SM clock"},
     }
+    if factor_ms is not None:
+        f_fac = 2.0 * d ** 3 / 3
+        tf1, tf3 = f_fac / p_tf32, 3 * f_fac / p_tf32
+        out["factor"] = {"ms": round(factor_ms, 4), "flops": f_fac, "bound_ms": round(tf1 * 1e3, 4),
+                         "frac": round(tf1 * 1e3 / factor_ms, 4), "bound_ms_three_pass": round(tf3 * 1e3, 4),
+                         "frac_three_pass": round(tf3 * 1e3 / factor_ms, 4), "bar": None,
+                         "model": "(d^3/3 Cholesky + d^3/3 triangular inverse) flops / P_tf32"}
+    return out
 
 
 def host_cores() -> int:
@@ -469,7 +480,8 @@ def run_gpu(args):
                 "quantize_only_ms": round(statistics.mean(st_ms["factor"]) + statistics.mean(st_ms["quantize"]), 4),
                 "syrk_tflops": round(syrk_tflops, 2),
                 "stage_rooflines": stage_rooflines(m, d, n, wl.bits, wl.group_size, wl.blocksize, syrk_ms,
-                                                   statistics.mean(st_ms["quantize"]), peaks),
+                                                   statistics.mean(st_ms["quantize"]), peaks,
+                                                   factor_ms=statistics.mean(st_ms["factor"])),
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
                 "clocks": clk, "wall_s_timed_region": round(t_wall, 4), "input_generation_s": round(t_gen, 2),
                 **line_note}

@@ -30,6 +30,11 @@ def test_llama_4096_g128_bounds():
     s = r["syrk"]
     assert s["bound_ms"] == pytest.approx(262144 * 4096 * 4097 / 1917e12 * 1e3, abs=1e-4)
     assert s["frac"] == pytest.approx(s["bound_ms"] / 2.68, abs=1e-4)
+    assert "factor" not in r
+    f = bench.stage_rooflines(4096, 4096, 262144, 4, 128, 128, 2.68, 1.25, PEAKS, factor_ms=1.51)["factor"]
+    assert f["flops"] == pytest.approx(2 * 4096 ** 3 / 3)          # 4.58e10: the Cholesky and the inverse
+    assert f["bound_ms_three_pass"] == pytest.approx(3 * f["bound_ms"], abs=2e-4)
+    assert f["frac"] == pytest.approx(f["bound_ms"] / 1.51, abs=1e-4) and f["bar"] is None
 
 
 def test_memory_bound_and_ragged_shapes():
