@@ -7,9 +7,8 @@ Default workload: the Llama-style 4096 x 4096 projection, 4-bit, group 128, with
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gptq|reference]
 
-Prints one JSON line (rank 0). With N > 1 (torchrun) every rank quantizes its own
-replica of the layer (the path needs no exchange between GPUs); value is the total
-over ranks divided by the slowest rank's time.
+Prints one JSON line. The path runs on one GPU: with N > 1 (--gpus or a torchrun
+launch) rank 0 prints a line that says so and every rank exits before touching CUDA.
 """
 from __future__ import annotations
 
@@ -251,27 +250,27 @@ def kernel_traffic(kernel_file: str, key: str):
 
 
 # ----------------------------------------------------------------------------------
-def slowest_rank_seconds(t_local: float, world: int, device) -> float:
-    """The job's time over `world` replicas: the largest of the ranks' timed regions (the
-    job ends with its last replica). One all-reduce (max) when world > 1."""
-    if world <= 1:
-        return t_local
-    import torch
-    import torch.distributed as dist
-    tt = torch.tensor([t_local], dtype=torch.float64, device=device)
-    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-    return float(tt.item())
+def world_size(args) -> int:
+    """GPUs the run was asked for: the larger of --gpus and a torchrun WORLD_SIZE."""
+    return max(int(args.gpus), int(os.environ.get("WORLD_SIZE", "1")))
 
 
-def job_rate_mweights(world: int, steps: int, weights: int, t_max: float) -> float:
-    """Whole-job throughput: every replica quantizes `weights` per step."""
-    return world * steps * weights / t_max / 1e6
+def single_gpu_only_line(n: int) -> dict:
+    """The line printed for N > 1: the path and its kernels are built for one GPU (the
+    Hessian kernel's paired tiles share activation slabs by cluster multicast, which
+    only a one-GPU process may run), so no multi-GPU run is made."""
+    return {"metric": METRIC, "n_gpus": n,
+            "unavailable": "single-GPU path: the layer runs on one GPU; no multi-GPU or replica mode is built"}
+
+
+def rate_mweights(steps: int, weights: int, seconds: float) -> float:
+    """Throughput of `steps` layers of `weights` weights each in `seconds`."""
+    return steps * weights / seconds / 1e6
 
 
 # ----------------------------------------------------------------------------------
 def run_reference(args):
     """The oracle as it stands on the host cores, each step a bounded sample."""
-    import torch.distributed as dist  # noqa: F401  (only to honour torchrun env; rank 0 works)
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
@@ -291,18 +290,22 @@ def run_reference(args):
         if i >= args.warmup:
             times.append(r)
     t = statistics.mean(x["total_s"] for x in times)
+    wall = statistics.mean(x["sample_wall_s"] for x in times)
     weights = layer.m * layer.d
     value = weights / t / 1e6
     sample = (f"per step: oracle Hessian over {n_sample} of {spec.n} tokens (scaled x{spec.n / n_sample:g}), "
-              f"full d={layer.d} factor chain, column loop over {rows} of {layer.m} rows (scaled)")
+              f"full d={layer.d} factor chain, column loop over {rows} of {layer.m} rows (scaled); "
+              f"ms_per_step is the sample's wall time, value the layer rate scaled from it")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "Mweights/s",
-            "n_gpus": 0, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3),
+            "n_gpus": 0, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(wall * 1e3, 3),
+            "ms_per_layer_scaled": round(t * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded)",
             "config": {"workload": args.workload, "layer": layer.name, "m": layer.m, "d": layer.d,
                        "tokens": spec.n, "bits": wl.bits, "group_size": wl.group_size, "blocksize": wl.blocksize,
                        "act_order": wl.act_order},
             "cpu_baseline": {"value": round(value, 6), "unit": "Mweights/s", "cores": blas_threads(),
+                             "host_cores": host_cores(), "blas_threads": blas_threads(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 6), "unit": "Mweights/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "stages_s": {k: round(statistics.mean(x[k] for x in times), 4) for k in ("syrk_s", "factor_s", "loop_s")}}
@@ -311,14 +314,14 @@ def run_reference(args):
 
 # ----------------------------------------------------------------------------------
 def run_gpu(args):
+    n_req = world_size(args)
+    if n_req > 1:
+        if int(os.environ.get("RANK", "0")) == 0:
+            print(json.dumps(single_gpu_only_line(n_req)), flush=True)
+        return
     import torch
-    import torch.distributed as dist
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
@@ -380,10 +383,8 @@ def run_gpu(args):
     g.gptq_factor_status(ws_f) if hasattr(g, "gptq_factor_status") else None
 
     # ---- timed region
-    if world > 1:
-        dist.barrier()
     torch.cuda.synchronize()
-    clocks = Clocks(local, not args.no_clocks and rank == 0)
+    clocks = Clocks(local, not args.no_clocks)
     launches0 = g.gptq_launch_count()
     events = []
     t_wall = time.perf_counter()
@@ -396,8 +397,6 @@ def run_gpu(args):
     torch.cuda.synchronize()
     t_region1 = time.perf_counter()
     t_wall = t_region1 - t_wall
-    if world > 1:
-        dist.barrier()
     launches = g.gptq_launch_count() - launches0
     clk = clocks.stop(t_region0, t_region1)
     g.gptq_device_check()
@@ -408,9 +407,9 @@ def run_gpu(args):
         st_ms["factor"].append(ev[1].elapsed_time(ev[2]))
         st_ms["quantize"].append(ev[2].elapsed_time(ev[3]))
     step_ms = [a + b + c for a, b, c in zip(st_ms["syrk"], st_ms["factor"], st_ms["quantize"])]
-    t_max = slowest_rank_seconds(sum(step_ms) / 1e3, world, dev)
+    t_max = sum(step_ms) / 1e3
     weights = m * d
-    value = job_rate_mweights(world, args.steps, weights, t_max)
+    value = rate_mweights(args.steps, weights, t_max)
     ms_per_step = t_max / args.steps * 1e3
     syrk_ms = statistics.mean(st_ms["syrk"])
     syrk_flops = float(n) * d * (d + 1)
@@ -441,53 +440,50 @@ def run_gpu(args):
             b.record(stream)
             b.synchronize()
             e_ms.append(a.elapsed_time(b))
-        te = slowest_rank_seconds(sum(e_ms) / 1e3, world, dev)
+        te = sum(e_ms) / 1e3
         g.gptq_device_check()
-        e2e = {"value": round(job_rate_mweights(world, args.steps, weights, te), 4), "unit": "Mweights/s",
+        e2e = {"value": round(rate_mweights(args.steps, weights, te), 4), "unit": "Mweights/s",
                "ms_per_step": round(te / args.steps * 1e3, 4),
                "h2d_bytes_per_step": pipe.bytes_h2d(n), "d2h_bytes_per_step": pipe.bytes_d2h()}
 
-    # ---- CPU oracle baseline (rank 0, N = 1 only), bounded sample
+    # ---- CPU oracle baseline, bounded sample
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if not args.no_cpu_baseline:
         # about 10 s of host work: 1/2 of the tokens, the full factor, 1/8 of the rows
         n_s = min(n, max(2 * CHUNK, (n // 2) // CHUNK * CHUNK))
         rows = min(m, max(32, m // 8))
         r = oracle_sample(wl, layer, X_host.numpy().view(np.uint16)[:n_s], W_bits[:rows], n, m)
         cpu = {"value": round(weights / r["total_s"] / 1e6, 6), "unit": "Mweights/s", "cores": blas_threads(),
-               "kind": "oracle",
+               "host_cores": host_cores(), "blas_threads": blas_threads(), "kind": "oracle",
                "sample": (f"oracle Hessian over {n_s} of {n} tokens (scaled x{n / n_s:g}), full d={d} factor chain, "
                           f"column loop over {rows} of {m} rows (scaled x{m / rows:g}); "
                           f"sample wall {r['sample_wall_s']:.1f} s"),
                "stages_s": {k: round(r[k], 3) for k in ("syrk_s", "factor_s", "loop_s")}}
 
-    if rank == 0:
-        if args.tokens:
-            line_note = {"note": f"profiling case: {n} tokens instead of the workload's {wl.acts[layer.hessian].n}"}
-        else:
-            line_note = {}
-        line = {"metric": METRIC, "value": round(value, 4), "unit": "Mweights/s", "n_gpus": world,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16+f32",
-                "data": "synthetic (seeded generators; no dataset or trained weights available)",
-                "config": {"workload": args.workload, "layer": layer.name, "m": m, "d": d, "tokens": n,
-                           "bits": wl.bits, "group_size": wl.group_size, "blocksize": wl.blocksize,
-                           "percdamp": wl.percdamp, "act_order": wl.act_order,
-                           "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                           "l2": "inputs larger than L2 (X is %.2f GB per step) and a 256 MB L2 flush between "
-                                 "steps, outside the step's events" % (n * d * 2 / 1e9)},
-                "stages_ms": {k: round(statistics.mean(v), 4) for k, v in st_ms.items()},
-                "quantize_only_ms": round(statistics.mean(st_ms["factor"]) + statistics.mean(st_ms["quantize"]), 4),
-                "syrk_tflops": round(syrk_tflops, 2),
-                "stage_rooflines": stage_rooflines(m, d, n, wl.bits, wl.group_size, wl.blocksize, syrk_ms,
-                                                   statistics.mean(st_ms["quantize"]), peaks,
-                                                   factor_ms=statistics.mean(st_ms["factor"])),
-                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-                "clocks": clk, "wall_s_timed_region": round(t_wall, 4), "input_generation_s": round(t_gen, 2),
-                **line_note}
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
+    if args.tokens:
+        line_note = {"note": f"profiling case: {n} tokens instead of the workload's {wl.acts[layer.hessian].n}"}
+    else:
+        line_note = {}
+    line = {"metric": METRIC, "value": round(value, 4), "unit": "Mweights/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16+f32",
+            "data": "synthetic (seeded generators; no dataset or trained weights available)",
+            "config": {"workload": args.workload, "layer": layer.name, "m": m, "d": d, "tokens": n,
+                       "bits": wl.bits, "group_size": wl.group_size, "blocksize": wl.blocksize,
+                       "percdamp": wl.percdamp, "act_order": wl.act_order,
+                       "parallelism": "single GPU",
+                       "l2": "inputs larger than L2 (X is %.2f GB per step) and a 256 MB L2 flush between "
+                             "steps, outside the step's events" % (n * d * 2 / 1e9)},
+            "stages_ms": {k: round(statistics.mean(v), 4) for k, v in st_ms.items()},
+            "quantize_only_ms": round(statistics.mean(st_ms["factor"]) + statistics.mean(st_ms["quantize"]), 4),
+            "syrk_tflops": round(syrk_tflops, 2),
+            "stage_rooflines": stage_rooflines(m, d, n, wl.bits, wl.group_size, wl.blocksize, syrk_ms,
+                                               statistics.mean(st_ms["quantize"]), peaks,
+                                               factor_ms=statistics.mean(st_ms["factor"])),
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+            "clocks": clk, "wall_s_timed_region": round(t_wall, 4), "input_generation_s": round(t_gen, 2),
+            **line_note}
+    print(json.dumps(line), flush=True)
 
 
 def main():

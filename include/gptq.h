@@ -170,11 +170,14 @@ gptq_status gptq_factor_status(const void* ws, int64_t* info, gptq_stream_t stre
  * pool, or a pipeline that cannot take cudaMalloc's implicit device synchronization.
  * The pages have no counterpart of this call; it exists only for such callers.
  *
- * Same arguments, results and status codes as gptq_factor, minus ws / ws_bytes. The
- * scratch is a device array inside the library sized for d <= 2048 (17 MiB + 256
- * bytes), held on every GPU that loads the library until the process exits;
- * d > 2048 returns GPTQ_ERR_INVALID_ARG before anything is launched. The call
- * allocates nothing.
+ * Same arguments, results and status codes as gptq_factor, minus ws / ws_bytes, with
+ * one difference: `info` is required (NULL returns GPTQ_ERR_INVALID_ARG before
+ * anything is launched), because the outcome lives in the library's shared scratch,
+ * which no later call can read back and the next call overwrites; the call therefore
+ * always synchronizes `stream` once. The scratch is a device array inside the
+ * library sized for d <= 2048 (18 MiB + 256 bytes), held on every GPU that loads the
+ * library until the process exits; d > 2048 returns GPTQ_ERR_INVALID_ARG before
+ * anything is launched. The call allocates nothing.
  *
  * The first call on a device (with that device current) looks up the array's device
  * address and caches it; make that first call before any stream capture. All calls
@@ -287,6 +290,25 @@ gptq_status gptq_gemm_f32(int engine, int a_kmajor, int b_kmajor, int64_t M, int
                           const float* A, int64_t lda, const float* B, int64_t ldb, float* C,
                           int64_t ldc, float alpha, float beta, int lower_tiles,
                           gptq_stream_t stream);
+
+/*
+ * Self-test of the bounded on-device waits (for tests; not a step of the method, and
+ * the pages have no counterpart). Every spin-wait in the library gives up after a
+ * wall-clock limit, raises the device error word and returns, so a stuck producer
+ * cannot hang the GPU. This call runs one of those wait routines alone, on something nothing ever
+ * completes, with a short limit: which = 0 the counter wait of the Cholesky panels
+ * (acquire loads of a global counter that nothing publishes), which = 1 the mbarrier
+ * wait used by every copy and tensor-core hand-over (a barrier nothing arrives on).
+ * Nothing is in flight when the wait gives up.
+ *
+ *   limit_ns   the wait's limit in nanoseconds, 1e3 <= limit_ns <= 1e9.
+ *
+ * Synchronizes `stream`, then returns GPTQ_ERR_TIMEOUT (the expected outcome) when the
+ * wait gave up; the device error word is raised as well, so the next
+ * gptq_device_check() returns GPTQ_ERR_TIMEOUT once and clears it. Bad arguments
+ * return GPTQ_ERR_INVALID_ARG before any launch.
+ */
+gptq_status gptq_wait_selftest(int which, int64_t limit_ns, gptq_stream_t stream);
 
 #ifdef __cplusplus
 }

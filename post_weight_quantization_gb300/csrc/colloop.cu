@@ -430,7 +430,13 @@ __global__ void __launch_bounds__(cb_threads<LANES>(), 1) colblock_kernel(CBArgs
   for_phases<NS, SPP>(phase, std::make_integer_sequence<int, (KS + SPP - 1) / SPP>{});
 
   __syncthreads();
-  if (*abort_flag) return;
+  if (*abort_flag) {
+    // A wait gave up: copies armed on bars[0, nks) may still be landing in this CTA's
+    // shared memory. Warp 0 waits for each of them (bounded) before the CTA exits.
+    if (a.bulk && warp == 0 && lane < nks) mbar_wait_bounded(&bars[lane], 0, nullptr);
+    __syncwarp();
+    return;
+  }
 
   // ---- Err1 out (row-major, BS per row), loss partials, codes
   constexpr int ELD = SL::ELD, CLD = SL::CLD;

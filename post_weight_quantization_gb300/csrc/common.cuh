@@ -99,16 +99,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete. Gives up (returns false)
-// after kWaitLimitNs, or as soon as *abort becomes non-zero.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// after limit_ns (kWaitLimitNs unless a self-test asks for less), or as soon as
+// *abort becomes non-zero.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   unsigned long long t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (abort && *abort) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+      if (global_timer_ns() - t0 > limit_ns) return false;
     }
+  }
+}
+
+// Wait until *ctr >= target (wrapping compare), reading with acquire semantics at gpu
+// scope; gives up (returns false) after limit_ns.
+__device__ __forceinline__ bool wait_counter_bounded(const unsigned* ctr, unsigned target,
+                                                     unsigned long long limit_ns = kWaitLimitNs) {
+  const unsigned long long t0 = global_timer_ns();
+  for (;;) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if ((int)(v - target) >= 0) return true;
+    if (global_timer_ns() - t0 > limit_ns) return false;
+    __nanosleep(128);
   }
 }
 

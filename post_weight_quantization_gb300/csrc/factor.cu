@@ -510,19 +510,6 @@ constexpr size_t PANEL_SMEM = (size_t)((NB + RB) * SLD + SB * TLD + NB + 4) * si
 // latency-bound panel share an SM (the trailing update leaves it a few free SMs at a time).
 constexpr size_t PANEL_SMEM_RESERVED = PANEL_SMEM > 120 * 1024 ? PANEL_SMEM : 120 * 1024;
 
-// Wait until *ctr >= target (wrapping compare), reading with acquire semantics at gpu
-// scope; gives up after kWaitLimitNs.
-__device__ __forceinline__ bool wait_counter_bounded(const unsigned* ctr, unsigned target) {
-  const unsigned long long t0 = global_timer_ns();
-  for (;;) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
-    if ((int)(v - target) >= 0) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
-    __nanosleep(128);
-  }
-}
-
 // One 128-wide panel step. Without `ready` it waits for the kernel before it (the
 // previous trailing update) to complete. With it (look-ahead), that update is still
 // running: it publishes its tiles of this panel's column block by adding to *ready,

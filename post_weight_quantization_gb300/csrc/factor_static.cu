@@ -71,6 +71,9 @@ extern "C" gptq_status gptq_factor_static(const float* H, int64_t d, float percd
                      (long long)d, kStaticMaxD);
   if (!(percdamp >= 0.0f) || percdamp > 1e30f) return set_error(GPTQ_ERR_INVALID_ARG, "percdamp must be finite and >= 0");
   if (act_order && !perm_out) return set_error(GPTQ_ERR_INVALID_ARG, "act_order needs perm_out");
+  // The outcome (pivot failure, NaN/Inf, timeout) stays in the shared scratch's header,
+  // which the next call overwrites: it is read back here, so info is required.
+  if (!info) return set_error(GPTQ_ERR_INVALID_ARG, "gptq_factor_static needs info (its outcome is read back at once)");
   if (factor_workspace_bytes(d) > kStaticScratchBytes)
     return set_error(GPTQ_ERR_INVALID_ARG, "gptq_factor_static: scratch too small for d = %lld", (long long)d);
   void* scratch = nullptr;
@@ -80,7 +83,7 @@ extern "C" gptq_status gptq_factor_static(const float* H, int64_t d, float percd
   // the status header, and the matrix is fully written before it is read.
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   st = factor_launch(H, d, percdamp, act_order, perm_out, Hinv1, scratch, s);
-  if (st || !info) return st;
+  if (st) return st;
   long long inf = -1;
   st = factor_read_status(scratch, &inf, s);
   *info = inf;

@@ -145,11 +145,57 @@ int* device_error_word() {
   return g_err_addr[dev];
 }
 
+// ---- self-test of the bounded waits ----
+namespace {
+__device__ unsigned g_selftest_counter = 0;   // nothing ever publishes on it
+__device__ int g_selftest_gave_up = 0;
+
+// One thread runs one of the library's bounded waits on something that never
+// completes, with a short limit: which = 0 the counter wait the Cholesky panels use
+// (acquire loads of a counter in global memory), which = 1 the mbarrier wait every
+// copy and tensor-core hand-over uses (a barrier that nothing arrives on). Nothing is
+// in flight when it gives up; it reports the timeout like the real kernels do.
+__global__ void wait_selftest_kernel(int which, unsigned long long limit_ns, int* err_word) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  bool done;
+  if (which == 0) {
+    done = wait_counter_bounded(&g_selftest_counter, 1u, limit_ns);
+  } else {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    done = mbar_wait_bounded(&bar, 0, nullptr, limit_ns);
+  }
+  g_selftest_gave_up = done ? 0 : 1;
+  if (!done) report_device_error(err_word, DEVERR_TIMEOUT);
+}
+}  // namespace
+
 }  // namespace gptq
 
 using namespace gptq;
 
 extern "C" {
+
+gptq_status gptq_wait_selftest(int which, int64_t limit_ns, gptq_stream_t stream) {
+  g_last_error[0] = 0;
+  if (which != 0 && which != 1) return set_error(GPTQ_ERR_INVALID_ARG, "which must be 0 (counter) or 1 (mbarrier)");
+  if (limit_ns < 1000 || limit_ns > 1000000000)
+    return set_error(GPTQ_ERR_INVALID_ARG, "limit_ns must be in [1e3, 1e9]");
+  int* word = device_error_word();
+  if (!word) return set_error(GPTQ_ERR_CUDA, "device error word is not available");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  wait_selftest_kernel<<<1, 32, 0, s>>>(which, (unsigned long long)limit_ns, word);
+  count_launch();
+  if (gptq_status st = check_launch("wait_selftest_kernel")) return st;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return set_error(GPTQ_ERR_CUDA, "cudaStreamSynchronize failed");
+  int gave_up = 0;
+  if (cudaMemcpyFromSymbol(&gave_up, g_selftest_gave_up, sizeof(int)) != cudaSuccess)
+    return set_error(GPTQ_ERR_CUDA, "reading the self-test result failed");
+  if (gave_up) return set_error(GPTQ_ERR_TIMEOUT, "the %s wait gave up after %lld ns", which ? "mbarrier" : "counter",
+                                (long long)limit_ns);
+  return GPTQ_OK;
+}
 
 const char* gptq_status_string(int status) {
   switch (status) {

@@ -52,6 +52,7 @@ SIGNATURES = {
                                    _vp]),
     "gptq_gemm_f32": (_c_int, [_c_int, _c_int, _c_int, _c_i64, _c_i64, _c_i64, _vp, _c_i64, _vp, _c_i64, _vp, _c_i64,
                                _c_float, _c_float, _c_int, _vp]),
+    "gptq_wait_selftest": (_c_int, [_c_int, _c_i64, _vp]),
 }
 
 
@@ -171,6 +172,13 @@ def gptq_device_check(stream=None) -> None:
     _check(_lib.gptq_device_check(_stream(stream)), "gptq_device_check")
 
 
+def gptq_wait_selftest(which: int, limit_ns: int = 1_000_000, stream=None) -> int:
+    """Run one of the library's bounded waits alone on something that never completes
+    (which 0: the panels' counter wait, 1: the mbarrier wait) with a short limit; returns
+    the status (GPTQ_ERR_TIMEOUT is the expected outcome) without raising."""
+    return int(_lib.gptq_wait_selftest(int(which), int(limit_ns), _stream(stream)))
+
+
 def gptq_workspace_size(which: int, m: int, d: int, bits: int = 4, group_size: int = 128,
                         blocksize: int = 128) -> int:
     return int(_lib.gptq_workspace_size(which, m, d, bits, group_size, blocksize))
@@ -234,9 +242,11 @@ def gptq_factor(H: torch.Tensor, percdamp: float = 0.01, act_order: bool = False
 
 
 def gptq_factor_static(H: torch.Tensor, Hinv1: torch.Tensor, percdamp: float = 0.01, act_order: bool = False,
-                       perm_out: Optional[torch.Tensor] = None, sync: bool = True, stream=None):
+                       perm_out: Optional[torch.Tensor] = None, stream=None):
     """gptq_factor with the library's own device scratch (d <= 2048) instead of a workspace,
-    for callers that cannot allocate device memory. Outputs must be passed in."""
+    for callers that cannot allocate device memory. Outputs must be passed in. The call
+    always waits for the GPU (its outcome is read back from the shared scratch) and
+    raises GPTQError on a failed factorization."""
     _need_cuda(H, "H", (torch.float32,))
     _need_cuda(Hinv1, "Hinv1", (torch.float32,))
     d = H.shape[0]
@@ -247,10 +257,10 @@ def gptq_factor_static(H: torch.Tensor, Hinv1: torch.Tensor, percdamp: float = 0
     _one_device(H, Hinv1, perm_out if act_order else None)
     info = _c_i64(-1)
     st = _lib.gptq_factor_static(_ptr(H), d, float(percdamp), int(bool(act_order)),
-                                 _ptr(perm_out) if act_order else None, _ptr(Hinv1),
-                                 ctypes.byref(info) if sync else None, _stream(stream))
+                                 _ptr(perm_out) if act_order else None, _ptr(Hinv1), ctypes.byref(info),
+                                 _stream(stream))
     _check(st, "gptq_factor_static")
-    return Hinv1, (perm_out if act_order else None), (int(info.value) if sync else None)
+    return Hinv1, (perm_out if act_order else None), int(info.value)
 
 
 @dataclass

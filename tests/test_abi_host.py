@@ -174,6 +174,9 @@ def test_factor_static_argument_checks(g):
     assert call(P, 64, float("nan"), 0, None, P) == g.GPTQ_ERR_INVALID_ARG
     assert call(P, 64, 0.01, 1, None, P) == g.GPTQ_ERR_INVALID_ARG       # act-order without perm_out
     assert "perm_out" in g.gptq_last_error()
+    # without info the outcome could not be read back (the shared scratch holds it)
+    assert lib.gptq_factor_static(P, 64, 0.01, 0, None, P, None, None) == g.GPTQ_ERR_INVALID_ARG
+    assert "info" in g.gptq_last_error()
     assert g.gptq_launch_count() == before
 
 
@@ -206,3 +209,12 @@ def test_binding_signatures_match_the_header(g):
     for name, nargs in protos.items():
         assert name in g.SIGNATURES, f"{name} has no binding"
         assert len(g.SIGNATURES[name][1]) == nargs, (name, nargs, len(g.SIGNATURES[name][1]))
+
+
+def test_wait_selftest_argument_checks(g):
+    lib = g.library()
+    before = g.gptq_launch_count()
+    assert lib.gptq_wait_selftest(2, 1000000, None) == g.GPTQ_ERR_INVALID_ARG
+    assert lib.gptq_wait_selftest(0, 999, None) == g.GPTQ_ERR_INVALID_ARG
+    assert lib.gptq_wait_selftest(1, 1000000001, None) == g.GPTQ_ERR_INVALID_ARG
+    assert g.gptq_launch_count() == before

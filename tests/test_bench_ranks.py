@@ -1,56 +1,43 @@
-"""bench.py with N > 1 replicas (torchrun): the job's time is the slowest rank's and its
-rate counts every replica's weights; the reference arm does its work on rank 0 only.
-Two gloo ranks on the CPU."""
+"""bench.py asked for more than one GPU: the path is built for one GPU, so rank 0 prints
+one line that says the run is unavailable and every rank exits 0 before touching CUDA;
+the reference arm does its work on rank 0 only. Runs on the CPU."""
+import json
 import os
-import socket
+import subprocess
 import sys
-
-import torch.multiprocessing as mp
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def _free_port():
-    with socket.socket() as s:
-        s.bind(("127.0.0.1", 0))
-        return s.getsockname()[1]
+def _run(args, env_extra):
+    env = dict(os.environ)
+    env.update(env_extra)
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], capture_output=True, text=True,
+                          timeout=120, cwd=ROOT, env=env)
 
 
-def _rank(rank, world, port, q):
-    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
-    sys.path.insert(0, ROOT)
-    import torch.distributed as dist
-
-    import bench
-    dist.init_process_group("gloo", rank=rank, world_size=world)
-    t = bench.slowest_rank_seconds(1.0 + rank, world, "cpu")      # rank 1 is the slower one
-    rate = bench.job_rate_mweights(world, 10, 4096 * 4096, t)
-    dist.barrier()
-    dist.destroy_process_group()
-    q.put((rank, t, rate))
+def test_two_gpus_asked_prints_unavailable_line():
+    out = _run(["--gpus", "2", "--steps", "1", "--warmup", "3"], {})
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, out.stdout
+    r = json.loads(lines[0])
+    assert r["n_gpus"] == 2 and "single-GPU" in r["unavailable"]
+    assert "value" not in r
 
 
-def test_two_replicas_take_the_slowest_rank():
-    ctx = mp.get_context("spawn")
-    q = ctx.Queue()
-    port = _free_port()
-    procs = [ctx.Process(target=_rank, args=(r, 2, port, q)) for r in range(2)]
-    for p in procs:
-        p.start()
-    out = sorted(q.get(timeout=120) for _ in procs)
-    for p in procs:
-        p.join(timeout=60)
-        assert p.exitcode == 0
-    for rank, t, rate in out:
-        assert t == 2.0
-        assert abs(rate - 2 * 10 * 4096 * 4096 / 2.0 / 1e6) < 1e-9
+def test_torchrun_ranks_other_than_zero_print_nothing():
+    out = _run(["--gpus", "2"], {"WORLD_SIZE": "2", "RANK": "1", "LOCAL_RANK": "1"})
+    assert out.returncode == 0, out.stderr[-2000:]
+    assert out.stdout.strip() == ""
+    out0 = _run(["--gpus", "2"], {"WORLD_SIZE": "2", "RANK": "0", "LOCAL_RANK": "0"})
+    assert out0.returncode == 0 and "unavailable" in json.loads(out0.stdout.strip())
 
 
-def test_single_replica_needs_no_collective():
+def test_rate_counts_every_step():
     sys.path.insert(0, ROOT)
     import bench
-    assert bench.slowest_rank_seconds(1.25, 1, "cpu") == 1.25
-    assert bench.job_rate_mweights(1, 4, 1000, 2.0) == 4 * 1000 / 2.0 / 1e6
+    assert bench.rate_mweights(4, 1000, 2.0) == 4 * 1000 / 2.0 / 1e6
 
 
 def test_reference_arm_other_ranks_do_nothing(monkeypatch, capsys):

@@ -13,6 +13,7 @@ import pytest
 import torch
 
 from oracle import gptq_oracle as orc
+from parity_record import record
 from synth import bf16_bits_to_f32, gen_activations_into, workload
 
 pytestmark = pytest.mark.gpu
@@ -20,6 +21,12 @@ pytestmark = pytest.mark.gpu
 CODE_TOL = 0.005
 SCALE_RTOL = 1e-4
 ERR_RTOL = 0.02
+
+
+def far_fraction(What_p, res64, gi):
+    """Dequantized weights more than half of their group's float64 step away from the
+    float64 oracle's (rows and columns in processing order)."""
+    return float(np.mean(np.abs(What_p - res64["W_hat"]) > 0.5 * res64["scales"][:, gi]))
 
 
 @pytest.fixture(scope="module")
@@ -116,11 +123,17 @@ def test_end_to_end_full_size(g, layer_inputs, gpu_hessian, exact_hessian, bits,
     gsz = d if gs == -1 else gs
     gi = np.arange(d) // gsz
     What_p = (codes - zeros[:, gi]) * scales[:, gi]
+    far64 = far_fraction(What_p, res64, gi)
     Hp = H64[np.ix_(p, p)]
     e_gpu = orc.relative_output_error(Wp.astype(np.float64), What_p, Hp)
-    for res in (res64, res32):
-        e_orc = orc.relative_output_error(Wp.astype(np.float64), res["W_hat"].astype(np.float64), Hp)
-        assert abs(e_gpu - e_orc) <= ERR_RTOL * e_orc, (e_gpu, e_orc)
+    e_orc = [orc.relative_output_error(Wp.astype(np.float64), res["W_hat"].astype(np.float64), Hp)
+             for res in (res64, res32)]
+    record(f"4096x4096 n=262144 {bits}b g{gs}{' act-order' if act_order else ''}, whole path, 64 sampled rows",
+           mismatch_fp32=mism32, mismatch_fp64=np.mean(codes != res64["codes"]), what_far_fp64=far64,
+           err_gpu=e_gpu, err_oracle64=e_orc[0], err_oracle32=e_orc[1])
+    assert far64 <= CODE_TOL, far64
+    for e in e_orc:
+        assert abs(e_gpu - e) <= ERR_RTOL * e, (e_gpu, e)
 
 
 @pytest.mark.parametrize("bits,gs,act_order", [(4, 128, False), (3, -1, True), (4, 128, True)])
@@ -167,11 +180,17 @@ def test_layer_full_size(g, layer_inputs, gpu_hessian, bits, gs, act_order):
     assert np.max(np.abs(scales[:, 0] - res64["scales"][:, 0]) / res64["scales"][:, 0]) <= SCALE_RTOL
     gi = np.arange(d) // gsz
     What_p = (codes - zeros[:, gi]) * scales[:, gi]
+    far64 = far_fraction(What_p, res64, gi)
     Hp = Hfull[np.ix_(p, p)]
     e_gpu = orc.relative_output_error(Wp.astype(np.float64), What_p, Hp)
-    for res in (res64, res32):
-        e_orc = orc.relative_output_error(Wp.astype(np.float64), res["W_hat"].astype(np.float64), Hp)
-        assert abs(e_gpu - e_orc) <= ERR_RTOL * e_orc, (e_gpu, e_orc)
+    e_orc = [orc.relative_output_error(Wp.astype(np.float64), res["W_hat"].astype(np.float64), Hp)
+             for res in (res64, res32)]
+    record(f"4096x4096 n=262144 {bits}b g{gs}{' act-order' if act_order else ''}, column loop on the GPU Hinv1, "
+           f"64 sampled rows", mismatch_fp32=mism32, mismatch_fp64=np.mean(codes != res64["codes"]),
+           what_far_fp64=far64, err_gpu=e_gpu, err_oracle64=e_orc[0], err_oracle32=e_orc[1], hinv1_rel=rel)
+    assert far64 <= CODE_TOL, far64
+    for e in e_orc:
+        assert abs(e_gpu - e) <= ERR_RTOL * e, (e_gpu, e)
 
     # ---- properties at full size
     assert codes_all.min() >= 0 and codes_all.max() <= 2 ** bits - 1

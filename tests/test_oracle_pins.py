@@ -431,6 +431,29 @@ def test_gptq_beats_rtn_on_correlated_inputs(toy):
     assert e_gptq < 0.8 * e_rtn
 
 
+@pytest.mark.parametrize("n,ao", [(333, False), (333, True), (40, True)])
+def test_relative_output_error_is_the_direct_output_norm(n, ao):
+    """The output error through H equals ||(W - W_hat) X^T||_F / ||W X^T||_F computed from
+    the tokens themselves ("GPTQ: fixing errors as you go", Objective: the error of the
+    layer's outputs on the calibration inputs). Non-square W and X, more and fewer
+    tokens than channels (a singular H), and an act-order result in original column
+    order; a missing square root, the damped instead of the plain Hessian, or a
+    transposed product would each fail."""
+    m, d = 48, 96
+    W, X = _layer(m, d, n, seed=21 + n)
+    H = orc.hessian([X])                                  # 2 X^T X, undamped
+    res = orc.gptq_layer(W, H, 3, 32, 32, 0.01, act_order=ao)
+    direct = np.linalg.norm((W - res["W_hat"]) @ X.T) / np.linalg.norm(W @ X.T)
+    assert 1e-4 < direct < 1.0
+    got = orc.relative_output_error(W, res["W_hat"], H)
+    assert abs(got - direct) <= 1e-12 * direct, (got, direct)
+    # any positive multiple of X^T X gives the same ratio (H / n, as one listing keeps it)
+    assert abs(orc.relative_output_error(W, res["W_hat"], H / (7.0 * n)) - direct) <= 1e-12 * direct
+    # the damped Hessian gives a different (larger) number: the metric uses the plain one
+    Hd, _ = orc.damp(H, 0.01)
+    assert orc.relative_output_error(W, res["W_hat"], Hd) > direct * (1 + 1e-6)
+
+
 def test_codes_in_range_all_bits(toy):
     W, _, H = toy
     for bits, g in ((2, 64), (3, -1), (4, 128), (8, 128)):
