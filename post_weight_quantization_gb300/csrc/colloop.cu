@@ -494,6 +494,346 @@ __global__ void __launch_bounds__(cb_threads<LANES>(), 1) colblock_kernel(CBArgs
   }
 }
 
+// ---------------------------------------------------------------------------------
+// Column block with one chain warp per 32 rows: 128-column blocks whose groups start
+// on block boundaries (group_size a multiple of 128, or per-channel statistics).
+//
+// Lane r of warp 0 runs row r's dependent chain once: quantize, dequantize, error and
+// the update of the next column. Warps 1-3 and 5-7 (update warps, lane = row too) hold
+// the block's quads (4 columns) 4..31 in registers, quad q in update warp
+// (q - 4) % 6, and move them by the errors of every finished quad. Warp 4 issues the
+// copies and then only waits, so the chain warp has its scheduler to itself (warps w
+// and w + 4 share one).
+//
+// Hand-over: at the start of quad j the chain takes quad j + 1 from the W tile in
+// shared memory, where its update warp stored it as soon as it carried the errors of
+// quads 0 .. j - 3 (quads 1-3 come straight from the loaded tile); the chain applies
+// the errors of quads j - 2 and j - 1 to it (they are still in its registers) and,
+// while it works through quad j, each of quad j's errors. An update warp therefore has
+// two quads of the chain's time to deliver a quad. Every weight still receives every
+// earlier column's correction -- the product rounded, then subtracted -- in column
+// order, so a block rounds exactly like the blocked loop in float32.
+//
+// Errors and codes of a finished quad go to shared memory (one 16-byte and one 4-byte
+// store per lane) and an mbarrier per quad tells the update warps; another mbarrier per
+// quad hands the updated quad back. Every wait is bounded.
+namespace chain {
+constexpr int BS = 128;
+constexpr int NQ = BS / 4;                 // quads per block
+constexpr int THREADS = 256;
+constexpr int NUPD = 6;                    // update warps
+constexpr int FIRST_UPD = 4;               // first quad held by an update warp
+constexpr int NSLOT = (NQ - FIRST_UPD + NUPD - 1) / NUPD;
+constexpr int WLD = BS + 4;                // padded rows of the W, error and code tiles (floats)
+struct Smem {
+  static constexpr size_t us = 0;                                        // Hinv1[i1 + t][i1 + c]
+  static constexpr size_t ws = us + sizeof(float) * BS * BS;             // W block, 32 x WLD
+  static constexpr size_t es = ws + sizeof(float) * 32 * WLD;            // Err1, 32 x WLD
+  static constexpr size_t cs = es + sizeof(float) * 32 * WLD;            // codes (as floats), 32 x WLD
+  static constexpr size_t dinfo = cs + sizeof(float) * 32 * WLD;
+  static constexpr size_t bars = dinfo + sizeof(float4) * BS;           // W, U x 4, errors x NQ, hand-over x NQ
+  static constexpr int NBARS = 1 + 4 + 2 * NQ;
+  static constexpr size_t flag = bars + sizeof(uint64_t) * NBARS;
+  static constexpr size_t total = flag + 16;
+};
+static_assert(Smem::dinfo % 16 == 0 && Smem::bars % 8 == 0, "shared-memory layout alignment");
+
+__device__ __forceinline__ float upd(float w, float e, float u) { return __fsub_rn(w, __fmul_rn(e, u)); }
+
+// rint(v) (round half to even) for |v| < 2^22 by adding and removing 1.5 * 2^23: the
+// sum lies in [2^23, 2^24), where floats are the integers. Outside that range the value
+// differs from rint(v) but stays beyond the same end of [0, 2^b - 1] (b <= 8), so the
+// clamped code is the same; two additions instead of a rounding instruction on the
+// chain.
+__device__ __forceinline__ float rint_small(float v) {
+  constexpr float kShift = 12582912.0f;      // 1.5 * 2^23
+  return __fsub_rn(__fadd_rn(v, kShift), kShift);
+}
+
+// v[k] -= e_i * U[row_i][col + k] for the four rows i of quad `pq`, in row order
+__device__ __forceinline__ void apply_quad(float (&v)[4], const float (&e)[4], const float* __restrict__ Us, int pq,
+                                          int col) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 u = *reinterpret_cast<const float4*>(Us + (4 * pq + i) * BS + col);
+    v[0] = upd(v[0], e[i], u.x);
+    v[1] = upd(v[1], e[i], u.y);
+    v[2] = upd(v[2], e[i], u.z);
+    v[3] = upd(v[3], e[i], u.w);
+  }
+}
+}  // namespace chain
+
+__global__ void __launch_bounds__(chain::THREADS, 1) colchain_kernel(CBArgs a) {
+  using namespace chain;
+  using SM = chain::Smem;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  float* Us = reinterpret_cast<float*>(smem_raw + SM::us);
+  float* Ws = reinterpret_cast<float*>(smem_raw + SM::ws);
+  float* Es = reinterpret_cast<float*>(smem_raw + SM::es);
+  float* Qs = reinterpret_cast<float*>(smem_raw + SM::cs);
+  float4* dinfo = reinterpret_cast<float4*>(smem_raw + SM::dinfo);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + SM::bars);
+  uint64_t* wbar = bars;                      // the W block
+  uint64_t* ubar = bars + 1;                  // Hinv1 rows [32k, 32k + 32)
+  uint64_t* ebar = bars + 5;                  // errors of quad p are in Es
+  uint64_t* hbar = bars + 5 + NQ;             // quad q is back in Ws, ready for the chain
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + SM::flag);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r0 = blockIdx.x * 32, r = r0 + lane;
+  const bool active = r < a.m;
+  const int d = a.d, i1 = a.i1;
+  const int ncols = min(BS, d - i1);          // a multiple of 4 on this path
+  const int nq = ncols >> 2;
+  const int nrows = min(32, a.m - r0);
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    mbar_init(wbar, 1);
+    for (int k = 0; k < 4; ++k) mbar_init(&ubar[k], 1);
+    for (int q = 0; q < NQ; ++q) {
+      mbar_init(&ebar[q], 32);
+      mbar_init(&hbar[q], 32);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // Hinv1's diagonal block, final before this kernel's stream predecessor starts: row t
+  // from column t & ~3 on, 32 rows per barrier
+  if (warp == 4) {
+    if (lane < 4) {
+      uint32_t bytes = 0;
+      for (int t = 32 * lane; t < min(32 * lane + 32, ncols); ++t) bytes += (uint32_t)(ncols - (t & ~3)) * 4u;
+      mbar_arrive_expect_tx(&ubar[lane], bytes);
+    }
+    __syncwarp();
+    for (int t = lane; t < ncols; t += 32) {
+      const int c0 = t & ~3;
+      bulk_load(Us + t * BS + c0, a.U + (long long)(i1 + t) * d + i1 + c0, (uint32_t)(ncols - c0) * 4u,
+                &ubar[t >> 5]);
+    }
+  }
+  // W, dinfo and the statistics may come from the kernel just before (which still reads
+  // Err1, written below)
+  grid_dep_launch();
+  grid_dep_wait();
+  if (warp == 4) {
+    if (lane == 0) mbar_arrive_expect_tx(wbar, (uint32_t)(nrows * ncols) * 4u);
+    __syncwarp();
+    if (lane < nrows) bulk_load(Ws + lane * WLD, a.Wf + (long long)(r0 + lane) * d + i1, (uint32_t)ncols * 4u, wbar);
+    else
+      for (int c = 0; c < BS; c += 4) *reinterpret_cast<float4*>(Ws + lane * WLD + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int t = tid; t < BS; t += THREADS) dinfo[t] = (t < ncols) ? a.dinfo[i1 + t] : make_float4(1.f, 1.f, 0.f, 0.f);
+  __syncthreads();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ the chain warp
+    const float qmax = (float)((1 << a.bits) - 1);
+    const float inv_qmax = rcp_rn(qmax);
+    float s = 1.0f, inv_s = 1.0f, z = 0.0f;
+    bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(wbar, 0, abort_flag));
+    if (ok) {
+      if (a.stats_given || (i1 % a.g) != 0) {          // statistics from an earlier block or precomputed
+        if (active) {
+          s = a.scales[(long long)r * a.G + i1 / a.g];
+          z = a.zeros[(long long)r * a.G + i1 / a.g];
+        }
+        inv_s = rcp_rn(s);
+      } else {
+        // the group starts here: min and max of the row's current weights over the group
+        float mn = INFINITY, mx = -INFINITY;
+        for (int c = 0; c < ncols; c += 4) {
+          const float4 v = *reinterpret_cast<const float4*>(Ws + lane * WLD + c);
+          mn = fminf(fminf(mn, v.x), fminf(fminf(v.y, v.z), v.w));
+          mx = fmaxf(fmaxf(mx, v.x), fmaxf(fmaxf(v.y, v.z), v.w));
+        }
+        const float* wrow = a.Wf + (long long)(active ? r : 0) * d;
+        for (int c = i1 + ncols; c < i1 + a.g && c < d; c += 4) {   // a group wider than the block
+          const float4 v = *reinterpret_cast<const float4*>(wrow + c);
+          mn = fminf(fminf(mn, v.x), fminf(fminf(v.y, v.z), v.w));
+          mx = fmaxf(fmaxf(mx, v.x), fmaxf(fmaxf(v.y, v.z), v.w));
+        }
+        group_params(mn, mx, qmax, inv_qmax, s, inv_s, z);
+        if (active) {
+          a.scales[(long long)r * a.G + i1 / a.g] = s;
+          a.zeros[(long long)r * a.G + i1 / a.g] = z;
+        }
+      }
+      float cur[4], nxt[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f}, e2[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const float4 v = *reinterpret_cast<const float4*>(Ws + lane * WLD);
+        cur[0] = v.x; cur[1] = v.y; cur[2] = v.z; cur[3] = v.w;
+      }
+#pragma unroll 1
+      for (int j = 0; j < nq; ++j) {
+        // the waits first, so the quad's work below is one straight block of code the
+        // compiler can interleave: the chain of each column with the independent updates
+        if (j + 1 >= FIRST_UPD && j + 1 < nq) {
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&hbar[j + 1], 0, abort_flag));
+          if (!ok) break;
+        }
+        if ((j & 7) == 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&ubar[j >> 3], 0, abort_flag));
+          if (!ok) break;
+        }
+        // quad j + 1 (past the last quad it reads padding and is never used); the errors
+        // of quads j - 2 and j - 1 (zeros, against quad 0's rows, before there are any)
+        {
+          const float4 v = *reinterpret_cast<const float4*>(Ws + lane * WLD + 4 * (j + 1));
+          nxt[0] = v.x; nxt[1] = v.y; nxt[2] = v.z; nxt[3] = v.w;
+        }
+        apply_quad(nxt, e2, Us, max(j - 2, 0), 4 * (j + 1));
+        apply_quad(nxt, e1, Us, max(j - 1, 0), 4 * (j + 1));
+        float ec[4], qc[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int t = 4 * j + c;
+          const float4 di = dinfo[t];                          // U[t][t], 1 / U[t][t]
+          const float4 ua = *reinterpret_cast<const float4*>(Us + t * BS + 4 * j);       // this quad
+          const float4 ub = *reinterpret_cast<const float4*>(Us + t * BS + 4 * j + 4);   // the next one
+          const float x = cur[c];
+          const float qv = fminf(fmaxf(rint_small(__fadd_rn(div_mk(x, s, inv_s), z)), 0.0f), qmax);
+          const float wq = __fmul_rn(__fsub_rn(qv, z), s);
+          const float e = div_mk(__fsub_rn(x, wq), di.x, di.y);
+          ec[c] = e;
+          qc[c] = qv;
+          if (c < 1) cur[1] = upd(cur[1], e, ua.y);
+          if (c < 2) cur[2] = upd(cur[2], e, ua.z);
+          if (c < 3) cur[3] = upd(cur[3], e, ua.w);
+          nxt[0] = upd(nxt[0], e, ub.x);
+          nxt[1] = upd(nxt[1], e, ub.y);
+          nxt[2] = upd(nxt[2], e, ub.z);
+          nxt[3] = upd(nxt[3], e, ub.w);
+        }
+        *reinterpret_cast<float4*>(Es + lane * WLD + 4 * j) = make_float4(ec[0], ec[1], ec[2], ec[3]);
+        *reinterpret_cast<float4*>(Qs + lane * WLD + 4 * j) = make_float4(qc[0], qc[1], qc[2], qc[3]);
+        mbar_arrive(&ebar[j]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          e2[k] = e1[k];
+          e1[k] = ec[k];
+          cur[k] = nxt[k];
+        }
+      }
+    }
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      report_device_error(a.err_word, DEVERR_TIMEOUT);
+    }
+  } else if (warp != 4) {
+    // ------------------------------------------------------------ update warps
+    const int u = (warp < 4) ? warp - 1 : warp - 2;
+    const int nslot = (nq - 1 - FIRST_UPD - u >= 0) ? (nq - 1 - FIRST_UPD - u) / NUPD + 1 : 0;
+    const int qlast = FIRST_UPD + u + NUPD * (nslot - 1);
+    float w[NSLOT][4];
+    bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(wbar, 0, abort_flag));
+    if (ok && nslot > 0) {
+#pragma unroll
+      for (int k = 0; k < NSLOT; ++k) {
+        if (k < nslot) {
+          const float4 v = *reinterpret_cast<const float4*>(Ws + lane * WLD + 4 * (FIRST_UPD + u + NUPD * k));
+          w[k][0] = v.x; w[k][1] = v.y; w[k][2] = v.z; w[k][3] = v.w;
+        } else {
+          w[k][0] = w[k][1] = w[k][2] = w[k][3] = 0.0f;
+        }
+      }
+#pragma unroll 1
+      for (int p = 0; p + FIRST_UPD <= qlast; ++p) {
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&ebar[p], 0, abort_flag));
+        if (!ok) break;
+        if ((p & 7) == 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&ubar[p >> 3], 0, abort_flag));
+          if (!ok) break;
+        }
+        float ep[4];
+        {
+          const float4 v = *reinterpret_cast<const float4*>(Es + lane * WLD + 4 * p);
+          ep[0] = v.x; ep[1] = v.y; ep[2] = v.z; ep[3] = v.w;
+        }
+#pragma unroll
+        for (int k = 0; k < NSLOT; ++k) {
+          const int q = FIRST_UPD + u + NUPD * k;
+          if (k < nslot && q >= p + FIRST_UPD) {
+            apply_quad(w[k], ep, Us, p, 4 * q);
+            if (q == p + FIRST_UPD) {                        // quad q now carries quads 0..q-4: hand it over
+              *reinterpret_cast<float4*>(Ws + lane * WLD + 4 * q) = make_float4(w[k][0], w[k][1], w[k][2], w[k][3]);
+              mbar_arrive(&hbar[q]);
+            }
+          }
+        }
+      }
+    }
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      report_device_error(a.err_word, DEVERR_TIMEOUT);
+    }
+  }
+
+  __syncthreads();
+  if (*abort_flag) {
+    // A wait gave up: the copies armed on wbar and ubar[] may still be landing in this
+    // CTA's shared memory. Warp 4 waits for them (bounded) before the CTA exits.
+    if (warp == 4) {
+      if (lane == 0) mbar_wait_bounded(wbar, 0, nullptr);
+      if (lane < 4) mbar_wait_bounded(&ubar[lane], 0, nullptr);
+    }
+    __syncwarp();
+    return;
+  }
+
+  // ---- Err1 out (row-major), loss partials, codes
+  for (int idx = tid; idx < 32 * BS; idx += THREADS) {
+    const int rr = idx / BS, t = idx % BS;
+    if (t < ncols && rr < nrows) {
+      const float e = Es[rr * WLD + t];
+      const long long o = (long long)(r0 + rr) * a.eld + a.eoff + t;
+      a.err[o] = e;
+      a.err_lo[o] = e - __uint_as_float(__float_as_uint(e) & 0xFFFFE000u);
+    }
+  }
+  {
+    // column t = tid / 2: rows 16 h .. 16 h + 15 in order, then the pair's two sums
+    const int t = tid >> 1, h = tid & 1;
+    float lsum = 0.0f;
+    if (t < ncols)
+      for (int rr = 16 * h; rr < 16 * h + 16; ++rr) {
+        const float e = (rr < nrows) ? Es[rr * WLD + t] : 0.0f;
+        lsum = __fadd_rn(lsum, __fmul_rn(__fmul_rn(e, e), 0.5f));
+      }
+    lsum = __fadd_rn(lsum, __shfl_xor_sync(0xffffffffu, lsum, 1));
+    if (t < ncols && h == 0) a.part[(long long)blockIdx.x * d + i1 + t] = lsum;
+  }
+  auto code_at = [&](int rr, int t) -> uint32_t { return (uint32_t)(int)Qs[rr * WLD + t]; };
+  if (a.codes8) {
+    for (int idx = tid; idx < 32 * BS; idx += THREADS) {
+      const int rr = idx / BS, t = idx % BS;
+      if (t < ncols && rr < nrows) a.codes8[(long long)(r0 + rr) * d + i1 + t] = (uint8_t)code_at(rr, t);
+    }
+  } else {
+    // words [i1 b / 32, ceil((i1 + ncols) b / 32)) of each row; i1 b is a multiple of 32
+    const int bits = a.bits;
+    const int wb = (int)(((long long)i1 * bits) >> 5);
+    const int we = (int)(((long long)(i1 + ncols) * bits + 31) >> 5);
+    const int nw = we - wb;
+    for (int idx = tid; idx < 32 * nw; idx += THREADS) {
+      const int rr = idx / nw, wi = wb + idx % nw;
+      if (rr >= nrows) continue;
+      const long long b0 = (long long)wi * 32;
+      const int jf = (int)(b0 / bits);
+      const int jl = min(i1 + ncols - 1, (int)((b0 + 31) / bits));
+      uint64_t v = 0;
+      for (int j = jf; j <= jl; ++j) {
+        const uint64_t code = code_at(rr, j - i1);
+        const long long sh = (long long)j * bits - b0;
+        v |= (sh >= 0) ? (code << sh) : (code >> (-sh));
+      }
+      a.qweight[(long long)(r0 + rr) * a.wpr + wi] = (uint32_t)v;
+    }
+  }
+}
+
 // col_losses[j] = sum over the CTAs' partials: 32 columns per CTA, the 8 warps each sum
 // every 8th partial, then warp 0 adds the 8 sums (fixed order)
 __global__ void loss_finalize_kernel(const float* __restrict__ part, int nrg, int d, const int* __restrict__ perm,
@@ -638,12 +978,12 @@ Layout layout(long long m, long long d, int blocksize) {
   return L;
 }
 
-template <int BS, int LANES>
-gptq_status run_blocks(CBArgs a, const float* Ut, const float* Ut_lo, cudaStream_t s) {
-  using SL = CBSmem<BS, LANES>;
-  if (cudaFuncSetAttribute(colblock_kernel<BS, LANES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)SL::total) != cudaSuccess)
-    return set_error(GPTQ_ERR_CUDA, "cudaFuncSetAttribute(colblock_kernel) failed");
+// Every block of BS columns: the column-block kernel (`kernel`, `threads` threads and
+// `smem` bytes of dynamic shared memory per CTA of 32 rows), then the lazy updates.
+gptq_status run_blocks(void (*kernel)(CBArgs), int threads, size_t smem, int BS, CBArgs a, const float* Ut,
+                       const float* Ut_lo, cudaStream_t s) {
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return set_error(GPTQ_ERR_CUDA, "cudaFuncSetAttribute(column-block kernel) failed");
   const int m = a.m, d = a.d;
   const int nrg = (m + ROWS_PER_CTA - 1) / ROWS_PER_CTA;
   const int OB = outer_width(BS, a.g, a.stats_given);
@@ -672,9 +1012,8 @@ gptq_status run_blocks(CBArgs a, const float* Ut, const float* Ut_lo, cudaStream
       a.eoff = i1 - o1;
       {
         ProfScope ps("quantize.colblock", s);
-        if (launch_pdl(colblock_kernel<BS, LANES>, dim3(nrg), dim3(cb_threads<LANES>()), SL::total, s, a) !=
-            cudaSuccess)
-          return check_launch("colblock_kernel");
+        if (launch_pdl(kernel, dim3(nrg), dim3(threads), smem, s, a) != cudaSuccess)
+          return check_launch("column-block kernel");
         count_launch();
       }
       if (i2 < o2)   // the rest of this outer block
@@ -684,6 +1023,11 @@ gptq_status run_blocks(CBArgs a, const float* Ut, const float* Ut_lo, cudaStream
       if (gptq_status st = lazy(0, o1, o2 - o1, o2, d)) return st;
   }
   return check_launch("column-loop kernels");
+}
+
+template <int BS, int LANES>
+gptq_status run_blocks_lanes(CBArgs a, const float* Ut, const float* Ut_lo, cudaStream_t s) {
+  return run_blocks(colblock_kernel<BS, LANES>, cb_threads<LANES>(), CBSmem<BS, LANES>::total, BS, a, Ut, Ut_lo, s);
 }
 
 }  // namespace colloop
@@ -746,11 +1090,16 @@ gptq_status quantize_launch(const void* W, int w_dtype, long long m_, long long 
   a.err_word = device_error_word();
   gptq_status st;
   switch (blocksize) {
-    case 32: st = run_blocks<32, 8>(a, Ut, Ut_lo, s); break;
-    case 64: st = run_blocks<64, 8>(a, Ut, Ut_lo, s); break;
+    case 32: st = run_blocks_lanes<32, 8>(a, Ut, Ut_lo, s); break;
+    case 64: st = run_blocks_lanes<64, 8>(a, Ut, Ut_lo, s); break;
     default:
-      // 64-column steps need groups that start on them
-      st = (a.stats_given || g % 64 == 0) ? run_blocks<128, 16>(a, Ut, Ut_lo, s) : run_blocks<128, 8>(a, Ut, Ut_lo, s);
+      if ((a.stats_given || g % 128 == 0) && a.bulk && a.vecw)
+        // groups start on block boundaries: one chain warp per 32 rows
+        st = run_blocks(colchain_kernel, chain::THREADS, chain::Smem::total, 128, a, Ut, Ut_lo, s);
+      else if (a.stats_given || g % 64 == 0)   // 64-column steps need groups that start on them
+        st = run_blocks_lanes<128, 16>(a, Ut, Ut_lo, s);
+      else
+        st = run_blocks_lanes<128, 8>(a, Ut, Ut_lo, s);
       break;
   }
   if (st) return st;
