@@ -103,12 +103,12 @@ gptq_status gptq_hessian_accumulate(const uint16_t* X, int64_t n, int64_t d, int
                                     gptq_stream_t stream);
 
 /* Workspace kinds for gptq_workspace_size(). */
-enum { GPTQ_WS_FACTOR = 0, GPTQ_WS_QUANTIZE = 1 };
+enum { GPTQ_WS_FACTOR = 0, GPTQ_WS_QUANTIZE = 1, GPTQ_WS_DEQUANT_GEMM = 2 };
 
 /*
  * Bytes of device workspace a call needs (0 for an invalid request). `which` is
- * GPTQ_WS_FACTOR (uses d only) or GPTQ_WS_QUANTIZE (uses m, d, bits, group_size,
- * blocksize). The workspace must be 256-byte aligned; its contents on entry do not
+ * GPTQ_WS_FACTOR (uses d only), GPTQ_WS_QUANTIZE (uses m, d, bits, group_size,
+ * blocksize) or GPTQ_WS_DEQUANT_GEMM (uses m and d; d a multiple of 32). The workspace must be 256-byte aligned; its contents on entry do not
  * matter.
  */
 size_t gptq_workspace_size(int which, int64_t m, int64_t d, int bits, int group_size,
@@ -276,6 +276,41 @@ gptq_status gptq_dequant_gemv(const uint32_t* qweight, const float* scales, cons
                               const int32_t* g_idx, int64_t m, int64_t d, int bits, int group_size,
                               const uint16_t* X, int64_t T, int64_t ldx, float* Y, int64_t ldy,
                               gptq_stream_t stream);
+
+/*
+ * The quantized layer applied to many tokens on the tensor cores: Y = X W_hat^T straight
+ * from the packed form, with w_hat[r][j] = (code[r][j] - zero[r][g]) * scale[r][g] and
+ * g = j / group_size ("GPTQ: fixing errors as you go": the stored low-bit weights and
+ * per-group scales stand in for the layer's weights). This is also the propagation step
+ * when layers are quantized one after another ("The GPTQ Algorithm", procedure steps
+ * 1-4): with y_bf16 = 1 the outputs come out as bf16, ready to be the next layer's
+ * calibration inputs for gptq_hessian_accumulate.
+ *
+ * code - zero is an integer of at most 8 bits, exact in bf16, so every product with a
+ * bf16 token is exact; each group's partial sum is formed on the tensor cores with fp32
+ * accumulation and added, times the group's scale, in fp32. Groups are the natural
+ * consecutive column groups (act-order layers with several groups per row need the
+ * dequant GEMV, which takes g_idx; per-channel layers, group_size -1, work in any column
+ * order).
+ *
+ *   qweight, scales, zeros  as written by gptq_quantize_layer (device; m x
+ *              ceil(d*bits/32) words, m x G floats each).
+ *   m, d       rows and columns of W; d a multiple of 32, d <= 65536.
+ *   bits       2, 3, 4 or 8.  group_size  -1 or a multiple of 32 dividing d.
+ *   X          device bf16 bits, T x d token-major, row stride ldx (ldx >= d,
+ *              ldx % 8 == 0, 16-byte aligned).
+ *   T          tokens, 0 <= T < 2^31.
+ *   Y          device, T x m with row stride ldy >= m: fp32 (y_bf16 = 0) or bf16 bits
+ *              rounded to nearest even (y_bf16 = 1).
+ *   ws         device workspace of gptq_workspace_size(GPTQ_WS_DEQUANT_GEMM, m, d, ...)
+ *              bytes (the integer operand, m x d bf16), 256-byte aligned.
+ * Asynchronous on `stream`; argument errors return GPTQ_ERR_INVALID_ARG before any
+ * launch.
+ */
+gptq_status gptq_dequant_gemm(const uint32_t* qweight, const float* scales, const float* zeros,
+                              int64_t m, int64_t d, int bits, int group_size, const uint16_t* X,
+                              int64_t T, int64_t ldx, void* Y, int y_bf16, int64_t ldy, void* ws,
+                              size_t ws_bytes, gptq_stream_t stream);
 
 /*
  * Helper for checks: C = beta * C + alpha * A B (fp32, single batch) with the GEMM the

@@ -783,14 +783,19 @@ __global__ void __launch_bounds__(chain::THREADS, 1) colchain_kernel(CBArgs a) {
     return;
   }
 
-  // ---- Err1 out (row-major), loss partials, codes
-  for (int idx = tid; idx < 32 * BS; idx += THREADS) {
-    const int rr = idx / BS, t = idx % BS;
-    if (t < ncols && rr < nrows) {
-      const float e = Es[rr * WLD + t];
-      const long long o = (long long)(r0 + rr) * a.eld + a.eoff + t;
-      a.err[o] = e;
-      a.err_lo[o] = e - __uint_as_float(__float_as_uint(e) & 0xFFFFE000u);
+  // ---- Err1 out (row-major) with its low parts, 16 bytes at a time (the row stride and
+  // the block's offset in it are multiples of 4)
+  for (int idx = tid; idx < 32 * (BS / 4); idx += THREADS) {
+    const int rr = idx / (BS / 4), c = 4 * (idx % (BS / 4));
+    if (c < ncols && rr < nrows) {
+      const float4 e = *reinterpret_cast<const float4*>(Es + rr * WLD + c);
+      const long long o = (long long)(r0 + rr) * a.eld + a.eoff + c;
+      *reinterpret_cast<float4*>(a.err + o) = e;
+      *reinterpret_cast<float4*>(a.err_lo + o) =
+          make_float4(e.x - __uint_as_float(__float_as_uint(e.x) & 0xFFFFE000u),
+                      e.y - __uint_as_float(__float_as_uint(e.y) & 0xFFFFE000u),
+                      e.z - __uint_as_float(__float_as_uint(e.z) & 0xFFFFE000u),
+                      e.w - __uint_as_float(__float_as_uint(e.w) & 0xFFFFE000u));
     }
   }
   {
@@ -806,27 +811,39 @@ __global__ void __launch_bounds__(chain::THREADS, 1) colchain_kernel(CBArgs a) {
     if (t < ncols && h == 0) a.part[(long long)blockIdx.x * d + i1 + t] = lsum;
   }
   auto code_at = [&](int rr, int t) -> uint32_t { return (uint32_t)(int)Qs[rr * WLD + t]; };
+  const int bits = a.bits;
   if (a.codes8) {
     for (int idx = tid; idx < 32 * BS; idx += THREADS) {
       const int rr = idx / BS, t = idx % BS;
       if (t < ncols && rr < nrows) a.codes8[(long long)(r0 + rr) * d + i1 + t] = (uint8_t)code_at(rr, t);
     }
+  } else if (32 % bits == 0) {
+    // 2, 4 and 8 bits: word w of the block holds columns [w cpw, (w + 1) cpw); i1 bits is
+    // a multiple of 32 (i1 is a multiple of 128)
+    const int cpw = 32 / bits;
+    const int nwb = (ncols + cpw - 1) / cpw, wb = (i1 * bits) >> 5;
+    for (int idx = tid; idx < 32 * nwb; idx += THREADS) {
+      const int rr = idx / nwb, w = idx - rr * nwb;
+      if (rr >= nrows) continue;
+      uint32_t v = 0;
+      for (int k = 0, t = w * cpw; k < cpw && t < ncols; ++k, ++t) v |= code_at(rr, t) << (k * bits);
+      a.qweight[(long long)(r0 + rr) * a.wpr + wb + w] = v;
+    }
   } else {
-    // words [i1 b / 32, ceil((i1 + ncols) b / 32)) of each row; i1 b is a multiple of 32
-    const int bits = a.bits;
-    const int wb = (int)(((long long)i1 * bits) >> 5);
-    const int we = (int)(((long long)(i1 + ncols) * bits + 31) >> 5);
+    // words [i1 b / 32, ceil((i1 + ncols) b / 32)) of each row (d b < 2^20: int arithmetic)
+    const int wb = (i1 * bits) >> 5;
+    const int we = ((i1 + ncols) * bits + 31) >> 5;
     const int nw = we - wb;
     for (int idx = tid; idx < 32 * nw; idx += THREADS) {
       const int rr = idx / nw, wi = wb + idx % nw;
       if (rr >= nrows) continue;
-      const long long b0 = (long long)wi * 32;
-      const int jf = (int)(b0 / bits);
-      const int jl = min(i1 + ncols - 1, (int)((b0 + 31) / bits));
+      const int b0 = wi * 32;
+      const int jf = b0 / bits;
+      const int jl = min(i1 + ncols - 1, (b0 + 31) / bits);
       uint64_t v = 0;
       for (int j = jf; j <= jl; ++j) {
         const uint64_t code = code_at(rr, j - i1);
-        const long long sh = (long long)j * bits - b0;
+        const int sh = j * bits - b0;
         v |= (sh >= 0) ? (code << sh) : (code >> (-sh));
       }
       a.qweight[(long long)(r0 + rr) * a.wpr + wi] = (uint32_t)v;

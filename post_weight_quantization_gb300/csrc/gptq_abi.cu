@@ -32,6 +32,11 @@ gptq_status unpack_launch(const uint32_t* qweight, long long m, long long d, int
 gptq_status dequant_gemv_launch(const uint32_t* qweight, const float* scales, const float* zeros, const int32_t* g_idx,
                                 long long m, long long d, int bits, int group_size, const uint16_t* X, long long T,
                                 long long ldx, float* Y, long long ldy, cudaStream_t s);
+size_t dequant_gemm_workspace_bytes(long long m, long long d);
+bool tensor_maps_available();
+gptq_status dequant_gemm_launch(const uint32_t* qweight, const float* scales, const float* zeros, long long m,
+                                long long d, int bits, int group_size, const uint16_t* X, long long T, long long ldx,
+                                void* Y, int y_bf16, long long ldy, void* ws, cudaStream_t s);
 
 namespace {
 thread_local char g_last_error[512] = "";
@@ -261,6 +266,10 @@ size_t gptq_workspace_size(int which, int64_t m, int64_t d, int bits, int group_
     if (blocksize != 32 && blocksize != 64 && blocksize != 128) return 0;
     return quantize_workspace_bytes(m, d, blocksize);
   }
+  if (which == GPTQ_WS_DEQUANT_GEMM) {
+    if (m < 1 || m > (int64_t)1 << 30 || d % 32) return 0;
+    return dequant_gemm_workspace_bytes(m, d);
+  }
   return 0;
 }
 
@@ -355,6 +364,32 @@ gptq_status gptq_dequant_gemv(const uint32_t* qweight, const float* scales, cons
     return set_error(GPTQ_ERR_INVALID_ARG, "qweight (16 bytes for 4 and 8 bits, 8 for 2) or X (16 bytes) misaligned");
   if (T == 0) return GPTQ_OK;
   return dequant_gemv_launch(qweight, scales, zeros, g_idx, m, d, bits, group_size, X, T, ldx, Y, ldy,
+                             reinterpret_cast<cudaStream_t>(stream));
+}
+
+gptq_status gptq_dequant_gemm(const uint32_t* qweight, const float* scales, const float* zeros, int64_t m, int64_t d,
+                              int bits, int group_size, const uint16_t* X, int64_t T, int64_t ldx, void* Y, int y_bf16,
+                              int64_t ldy, void* ws, size_t ws_bytes, gptq_stream_t stream) {
+  g_last_error[0] = 0;
+  if (!qweight || !scales || !zeros || !ws || (T > 0 && (!X || !Y))) return set_error(GPTQ_ERR_INVALID_ARG, "NULL pointer");
+  if (m < 1 || m > ((int64_t)1 << 30) || d < 32 || d > 65536 || d % 32)
+    return set_error(GPTQ_ERR_INVALID_ARG, "m >= 1 and d a multiple of 32 in [32, 65536] are required");
+  if (bits != 2 && bits != 3 && bits != 4 && bits != 8) return set_error(GPTQ_ERR_INVALID_ARG, "bits must be 2, 3, 4 or 8");
+  if (group_size != -1 && (group_size < 32 || group_size % 32 || d % group_size))
+    return set_error(GPTQ_ERR_INVALID_ARG, "group_size must be -1 or a multiple of 32 that divides d");
+  if (y_bf16 != 0 && y_bf16 != 1) return set_error(GPTQ_ERR_INVALID_ARG, "y_bf16 must be 0 (fp32) or 1 (bf16)");
+  if (T < 0 || T > 0x7FFFFFFF || ldx < d || ldx % 8 || ldy < m)
+    return set_error(GPTQ_ERR_INVALID_ARG, "bad T, ldx or ldy");
+  if (((T + 127) / 128) * ((m + 127) / 128) > 0x7FFFFFFF) return set_error(GPTQ_ERR_INVALID_ARG, "too many output tiles");
+  if (!aligned(qweight, 4) || !aligned(scales, 4) || !aligned(zeros, 4) || (T > 0 && !aligned(X, 16)))
+    return set_error(GPTQ_ERR_INVALID_ARG, "X must be 16-byte aligned (qweight, scales, zeros 4-byte)");
+  if (!aligned(ws, 256)) return set_error(GPTQ_ERR_INVALID_ARG, "ws must be 256-byte aligned");
+  if (ws_bytes < dequant_gemm_workspace_bytes(m, d))
+    return set_error(GPTQ_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", ws_bytes,
+                     dequant_gemm_workspace_bytes(m, d));
+  if (T == 0) return GPTQ_OK;
+  if (!tensor_maps_available()) return set_error(GPTQ_ERR_UNSUPPORTED, "the tensor-map encoder is not available");
+  return dequant_gemm_launch(qweight, scales, zeros, m, d, bits, group_size, X, T, ldx, Y, y_bf16, ldy, ws,
                              reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -499,6 +499,9 @@ static bool force_ffma() {
 
 bool tc_gemm_available() { return !force_ffma() && tc::encode_fn() != nullptr; }
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() { return tc::encode_fn(); }
+bool tensor_maps_available() { return tc::encode_fn() != nullptr; }
+
 gptq_status tc_gemm(const simt::GemmArgs& g, int batches, bool a_kmaj, bool b_kmaj, cudaStream_t s) {
   using namespace tc;
   if (g.M <= 0 || g.N <= 0 || batches <= 0) return GPTQ_OK;

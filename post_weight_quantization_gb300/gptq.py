@@ -30,6 +30,7 @@ GPTQ_ERR_CUDA = 5
 GPTQ_ERR_TIMEOUT = 6
 GPTQ_WS_FACTOR = 0
 GPTQ_WS_QUANTIZE = 1
+GPTQ_WS_DEQUANT_GEMM = 2
 
 _c_int, _c_i64, _c_size, _c_float, _vp = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float, ctypes.c_void_p
 
@@ -53,6 +54,8 @@ SIGNATURES = {
     "gptq_gemm_f32": (_c_int, [_c_int, _c_int, _c_int, _c_i64, _c_i64, _c_i64, _vp, _c_i64, _vp, _c_i64, _vp, _c_i64,
                                _c_float, _c_float, _c_int, _vp]),
     "gptq_wait_selftest": (_c_int, [_c_int, _c_i64, _vp]),
+    "gptq_dequant_gemm": (_c_int, [_vp, _vp, _vp, _c_i64, _c_i64, _c_int, _c_int, _vp, _c_i64, _c_i64, _vp, _c_int,
+                                   _c_i64, _vp, _c_size, _vp]),
 }
 
 
@@ -347,6 +350,36 @@ def gptq_dequant_gemv(q: "QuantizedLayer", X: torch.Tensor, m: int, g_idx: Optio
     st = _lib.gptq_dequant_gemv(_ptr(q.qweight), _ptr(q.scales), _ptr(q.zeros), _ptr(g_idx), m, q.d, q.bits,
                                 q.group_size, _ptr(X), T, X.stride(0), _ptr(Y), Y.stride(0), _stream(stream))
     _check(st, "gptq_dequant_gemv")
+    return Y
+
+
+def gptq_dequant_gemm(q: "QuantizedLayer", X: torch.Tensor, m: int, Y: Optional[torch.Tensor] = None,
+                      out_bf16: bool = False, ws: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Y = X W_hat^T (T x m) on the tensor cores from the packed layer q and bf16 tokens X
+    (T x d); fp32 output, or bf16 with out_bf16 (the next layer's calibration inputs)."""
+    _need_cuda(X, "X", (torch.bfloat16, torch.int16))
+    if X.dim() != 2 or X.stride(1) != 1 or X.shape[1] != q.d:
+        raise ValueError("X must be T x d with unit column stride")
+    G = 1 if q.group_size == -1 else (q.d // q.group_size if q.group_size > 0 else 1)
+    _need_rows(q.qweight, "q.qweight", m, (q.d * q.bits + 31) // 32, (torch.int32,))
+    _need_rows(q.scales, "q.scales", m, G, (torch.float32,))
+    _need_rows(q.zeros, "q.zeros", m, G, (torch.float32,))
+    T = X.shape[0]
+    ydt = torch.bfloat16 if out_bf16 else torch.float32
+    if Y is None:
+        Y = torch.empty((T, m), dtype=ydt, device=X.device)
+    _need_cuda(Y, "Y", (ydt,))
+    if Y.dim() != 2 or tuple(Y.shape) != (T, m) or Y.stride(1) != 1:
+        raise ValueError(f"Y must be ({T}, {m}) with unit column stride, got {tuple(Y.shape)}")
+    need = gptq_workspace_size(GPTQ_WS_DEQUANT_GEMM, m, q.d)
+    if ws is None:
+        ws = _workspace(need, X.device)
+    ws_bytes = _need_workspace(ws, need)
+    _one_device(q.qweight, q.scales, q.zeros, X, Y, ws)
+    st = _lib.gptq_dequant_gemm(_ptr(q.qweight), _ptr(q.scales), _ptr(q.zeros), m, q.d, q.bits, q.group_size,
+                                _ptr(X), T, X.stride(0), _ptr(Y), int(bool(out_bf16)), Y.stride(0), _ptr(ws), ws_bytes,
+                                _stream(stream))
+    _check(st, "gptq_dequant_gemm")
     return Y
 
 

@@ -218,3 +218,27 @@ def test_wait_selftest_argument_checks(g):
     assert lib.gptq_wait_selftest(0, 999, None) == g.GPTQ_ERR_INVALID_ARG
     assert lib.gptq_wait_selftest(1, 1000000001, None) == g.GPTQ_ERR_INVALID_ARG
     assert g.gptq_launch_count() == before
+
+
+def test_dequant_gemm_argument_checks(g):
+    lib = g.library()
+    before = g.gptq_launch_count()
+    ws = 1 << 30
+    call = lambda q=P, s=P, z=P, m=64, d=256, bits=4, gs=128, X=P, T=16, ldx=256, Y=P, yb=0, ldy=64, w=P, wb=ws: \
+        lib.gptq_dequant_gemm(q, s, z, m, d, bits, gs, X, T, ldx, Y, yb, ldy, w, wb, None)
+    assert call(q=None) == g.GPTQ_ERR_INVALID_ARG
+    assert call(w=None) == g.GPTQ_ERR_INVALID_ARG
+    assert call(d=250, ldx=256) == g.GPTQ_ERR_INVALID_ARG           # d not a multiple of 32
+    assert call(bits=5) == g.GPTQ_ERR_INVALID_ARG
+    assert call(gs=96) == g.GPTQ_ERR_INVALID_ARG                    # does not divide d
+    assert call(yb=2) == g.GPTQ_ERR_INVALID_ARG
+    assert call(ldx=260) == g.GPTQ_ERR_INVALID_ARG                  # not a multiple of 8
+    assert call(ldy=63) == g.GPTQ_ERR_INVALID_ARG
+    assert call(X=P + 8) == g.GPTQ_ERR_INVALID_ARG                  # X must be 16-byte aligned
+    assert call(w=P + 128) == g.GPTQ_ERR_INVALID_ARG                # ws must be 256-byte aligned
+    assert call(wb=64 * 256 * 2 - 1) == g.GPTQ_ERR_INVALID_ARG      # workspace too small
+    assert call(T=0, X=None, Y=None) == g.GPTQ_OK                   # nothing to do
+    assert call(T=-1) == g.GPTQ_ERR_INVALID_ARG
+    assert g.gptq_launch_count() == before
+    assert g.gptq_workspace_size(g.GPTQ_WS_DEQUANT_GEMM, 64, 256) >= 64 * 256 * 2
+    assert g.gptq_workspace_size(g.GPTQ_WS_DEQUANT_GEMM, 64, 250) == 0

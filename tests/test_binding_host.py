@@ -174,3 +174,27 @@ def test_tensors_on_two_devices_are_refused(g, fake):
     H = torch.zeros((64, 64))
     with pytest.raises(ValueError):
         g.gptq_factor(H, Hinv1=torch.zeros((64, 64), device="meta"), sync=False)
+
+
+def test_dequant_gemm_marshalling(g, fake):
+    m, d, T = 96, 256, 300
+    q = _layer(g, m, d, 4, 128)
+    X = torch.zeros((T, d + 8), dtype=torch.int16)[:, :d]          # row stride d + 8
+    Y = g.gptq_dequant_gemm(q, X, m, out_bf16=True)
+    name, a = fake.calls[-1]
+    assert name == "gptq_dequant_gemm"
+    assert a[3:7] == (m, d, 4, 128) and a[8:10] == (T, d + 8) and a[11] == 1 and a[12] == m
+    assert a[14] == g.gptq_workspace_size(g.GPTQ_WS_DEQUANT_GEMM, m, d)
+    assert Y.dtype == torch.bfloat16 and tuple(Y.shape) == (T, m)
+    g.gptq_dequant_gemm(q, X, m, Y=torch.zeros((T, m)))
+    assert fake.calls[-1][1][11] == 0
+    n = len(fake.calls)
+    with pytest.raises(TypeError):
+        g.gptq_dequant_gemm(q, X, m, Y=torch.zeros((T, m)), out_bf16=True)       # dtype of Y
+    with pytest.raises(ValueError):
+        g.gptq_dequant_gemm(q, X, m, Y=torch.zeros((T - 1, m)))
+    with pytest.raises(ValueError):
+        g.gptq_dequant_gemm(q, X, m, ws=torch.zeros(16, dtype=torch.uint8))
+    with pytest.raises(ValueError):
+        g.gptq_dequant_gemm(q, torch.zeros((T, d - 32), dtype=torch.int16), m)
+    assert len(fake.calls) == n

@@ -1,12 +1,16 @@
-"""gptq_dequant_gemv: Y = X W_hat^T straight from the packed layer, against the oracle's
-dequantize-and-multiply in float64 on the GPU's own quantized output (codes, scales,
-zeros and, for act-order groups, g_idx)."""
+"""gptq_dequant_gemv: Y = X W_hat^T straight from a packed layer, against the oracle's
+dequantize-and-multiply in float64.
+
+The packed layers are built on the CPU from seeded random codes, zeros and scales (and,
+for act-order groups, a random column order giving g_idx) and packed by the oracle's
+bitstream packer, so both sides read the same bytes and nothing the oracle consumes
+comes from the GPU."""
 import numpy as np
 import pytest
 import torch
 
 from oracle import gptq_oracle as orc
-from synth import ActSpec, bf16_bits_to_f32, make_activations, make_weight
+from synth import ActSpec, bf16_bits_to_f32, make_activations
 
 pytestmark = pytest.mark.gpu
 
@@ -19,22 +23,30 @@ def g():
     return gptq
 
 
-def _g_idx(perm, d, gs):
-    gi = np.empty(d, dtype=np.int64)
-    gi[perm] = np.arange(d) // (d if gs == -1 else gs)
-    return gi
+def packed_layer(m, d, bits, gs, act_order, seed):
+    rng = np.random.default_rng(seed)
+    G = 1 if gs == -1 else d // gs
+    codes = rng.integers(0, 2 ** bits, size=(m, d))
+    zeros = rng.integers(0, 2 ** bits, size=(m, G)).astype(np.float32)
+    scales = (0.002 * (0.5 + rng.random((m, G)))).astype(np.float32)
+    gi = None
+    if act_order and G > 1:
+        perm = rng.permutation(d)
+        gi = np.empty(d, dtype=np.int64)
+        gi[perm] = np.arange(d) // gs           # groups formed in processing order
+    return orc.pack_codes(codes, bits), scales, zeros, gi
 
 
-def _check(g, q, m, d, bits, gs, perm, T, seed, rows=None):
-    gi = None if perm is None else _g_idx(perm.cpu().numpy().astype(np.int64), d, gs)
+def _check(g, m, d, bits, gs, act_order, T, seed, rows=None):
+    words, sc, ze, gi = packed_layer(m, d, bits, gs, act_order, seed)
+    q = g.QuantizedLayer(torch.from_numpy(words.view(np.int32)).cuda(), torch.from_numpy(sc).cuda(),
+                         torch.from_numpy(ze).cuda(), torch.zeros(d, device="cuda"), bits, gs, d)
     gi_dev = None if gi is None else torch.from_numpy(gi.astype(np.int32)).cuda()
-    Xb = make_activations(ActSpec("heavy_tail", T, d, seed=seed))
+    Xb = make_activations(ActSpec("heavy_tail", T, d, seed=seed + 1))
     Xd = torch.from_numpy(Xb.view(np.int16)).cuda()
     Y = g.gptq_dequant_gemv(q, Xd, m, g_idx=gi_dev)
     torch.cuda.synchronize()
     g.gptq_device_check()
-    words = q.qweight.cpu().numpy().view(np.uint32)
-    sc, ze = q.scales.cpu().numpy(), q.zeros.cpu().numpy()
     if rows is not None:
         words, sc, ze = words[rows], sc[rows], ze[rows]
     X = bf16_bits_to_f32(Xb).astype(np.float64)
@@ -52,22 +64,10 @@ def _check(g, q, m, d, bits, gs, perm, T, seed, rows=None):
                                         (4, 128, True)])
 @pytest.mark.parametrize("T", [1, 5, 11])
 def test_dequant_gemv_matches_oracle(g, bits, gs, ao, T):
-    m, d = 200, 768
-    W_bits = make_weight(m, d, 51)
-    X_bits = make_activations(ActSpec("heavy_tail", 4096, d, seed=51))
-    Wd = torch.from_numpy(W_bits.view(np.int16)).cuda().view(torch.bfloat16)
-    q, _, _, perm = g.quantize_layer(Wd, [torch.from_numpy(X_bits.view(np.int16)).cuda()], bits=bits, group_size=gs,
-                                     blocksize=32 if gs == 32 else 64, act_order=ao)
-    _check(g, q, m, d, bits, gs, perm, T, seed=100 + T)
+    _check(g, 200, 768, bits, gs, ao, T, seed=100 + T + bits)
 
 
 def test_dequant_gemv_full_size_layer(g):
-    """The 4096 x 4096 4-bit g128 layer (Hessian from 16384 tokens), eight tokens,
-    sampled rows against the oracle."""
-    m = d = 4096
-    W_bits = make_weight(m, d, 1)
-    X_bits = make_activations(ActSpec("heavy_tail", 16384, d, seed=1))
-    Wd = torch.from_numpy(W_bits.view(np.int16)).cuda().view(torch.bfloat16)
-    q, _, _, _ = g.quantize_layer(Wd, [torch.from_numpy(X_bits.view(np.int16)).cuda()], bits=4, group_size=128)
-    rows = np.sort(np.random.default_rng(3).choice(m, size=96, replace=False))
-    _check(g, q, m, d, 4, 128, None, 8, seed=7, rows=rows)
+    """A 4096 x 4096 4-bit g128 packed layer, eight tokens, sampled rows against the oracle."""
+    rows = np.sort(np.random.default_rng(3).choice(4096, size=96, replace=False))
+    _check(g, 4096, 4096, 4, 128, False, 8, seed=7, rows=rows)
