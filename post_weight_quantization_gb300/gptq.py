@@ -427,6 +427,30 @@ def quantize_layer(W: torch.Tensor, X_batches, bits: int = 4, group_size: int = 
     return q, H, Hinv1, perm
 
 
+def sequential_quantize(X0: torch.Tensor, weights, bits: int = 4, group_size: int = 128, blocksize: int = 128,
+                        percdamp: float = 0.01, act_order: bool = False, alpha: float = 2.0, stream=None):
+    """Layers quantized one after another ("The GPTQ Algorithm", procedure steps 1-4): each
+    layer of a chain of linear layers is calibrated on the bf16 outputs of the quantized
+    layers before it. X0 (n x d0, bf16) are the first layer's inputs; weights[l] is
+    (m_l x d_l) with d_{l+1} = m_l. Layer l is quantized from its inputs, then
+    gptq_dequant_gemm computes its outputs from the packed layer, rounded to bf16, which
+    become layer l+1's inputs.
+
+    Returns (layers, inputs, output): layers[l] = (QuantizedLayer, perm), inputs[l] the
+    bf16 tokens layer l was calibrated on, output the last layer's bf16 outputs."""
+    X = X0
+    layers, inputs = [], []
+    for W in weights:
+        if X.shape[1] != W.shape[1]:
+            raise ValueError(f"a layer of width {W.shape[1]} follows outputs of width {X.shape[1]}")
+        inputs.append(X)
+        q, _, _, perm = quantize_layer(W, [X], bits=bits, group_size=group_size, blocksize=blocksize,
+                                       percdamp=percdamp, act_order=act_order, alpha=alpha, stream=stream)
+        layers.append((q, perm))
+        X = gptq_dequant_gemm(q, X, W.shape[0], out_bf16=True, stream=stream)
+    return layers, inputs, X
+
+
 def token_pieces(n: int, chunk: int):
     """Token ranges for HostPipeline: chunks of `chunk` tokens, the last one cut in four
     (when it has at least 4096 tokens), so the Hessian of the final piece, the one step

@@ -198,3 +198,26 @@ def test_dequant_gemm_marshalling(g, fake):
     with pytest.raises(ValueError):
         g.gptq_dequant_gemm(q, torch.zeros((T, d - 32), dtype=torch.int16), m)
     assert len(fake.calls) == n
+
+
+def test_sequential_quantize_marshalling(g, fake):
+    """Each layer runs Hessian, factor, column loop, then the dequant GEMM whose bf16
+    output is the next layer's Hessian input; a width mismatch raises before any call."""
+    n = 512
+    X0 = torch.zeros((n, 256), dtype=torch.int16)
+    Ws = [torch.zeros((128, 256), dtype=torch.bfloat16), torch.zeros((64, 128), dtype=torch.bfloat16)]
+    layers, inputs, out = g.sequential_quantize(X0, Ws, bits=4, group_size=128)
+    names = [c[0] for c in fake.calls]
+    per_layer = ["gptq_hessian_accumulate", "gptq_factor", "gptq_quantize_layer", "gptq_dequant_gemm"]
+    assert names == per_layer * 2
+    h1, gemm1, h2, gemm2 = fake.calls[0][1], fake.calls[3][1], fake.calls[4][1], fake.calls[7][1]
+    assert h1[0] == X0.data_ptr() and h1[1:3] == (n, 256)
+    assert gemm1[3:5] == (128, 256) and gemm1[7] == X0.data_ptr() and gemm1[11] == 1
+    assert h2[0] == gemm1[10] and h2[1:3] == (n, 128)           # layer 2 sees layer 1's bf16 outputs
+    assert gemm2[3:5] == (64, 128) and gemm2[7] == gemm1[10] and gemm2[10] == out.data_ptr()
+    assert [x.data_ptr() for x in inputs] == [X0.data_ptr(), gemm1[10]]
+    assert out.dtype == torch.bfloat16 and tuple(out.shape) == (n, 64) and len(layers) == 2
+    k = len(fake.calls)
+    with pytest.raises(ValueError):
+        g.sequential_quantize(X0, [torch.zeros((64, 128), dtype=torch.bfloat16)])
+    assert len(fake.calls) == k

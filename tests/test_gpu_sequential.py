@@ -2,7 +2,7 @@
 1-4; "GPTQ: fixing errors as you go", the algorithm in words): each layer's Hessian is
 accumulated from the outputs of the layers already quantized, computed on the tensor
 cores from the packed layer and rounded to bf16 (gptq_dequant_gemm), then the layer is
-factored and quantized. Compared with the oracle's sequential pass in float64 on the
+factored and quantized (the binding's sequential_quantize). Compared with the oracle's sequential pass in float64 on the
 same seeded W and X0 (nothing the oracle consumes comes from the GPU).
 
 Weights already on their quantization grid make no rounding decision: every layer must
@@ -45,19 +45,12 @@ def g():
 
 
 def gpu_chain(g, X0_bits, W_bits_list, bits, gs, act_order):
-    X = torch.from_numpy(X0_bits.view(np.int16)).cuda()
-    layers, inputs = [], []
-    for W_bits in W_bits_list:
-        m = W_bits.shape[0]
-        Wd = torch.from_numpy(W_bits.view(np.int16)).cuda().view(torch.bfloat16)
-        inputs.append(X)
-        q, H, U, perm = g.quantize_layer(Wd, [X], bits=bits, group_size=gs, blocksize=128, act_order=act_order)
-        Y = g.gptq_dequant_gemm(q, X, m, out_bf16=True)
-        torch.cuda.synchronize()
-        g.gptq_device_check()
-        layers.append((q, perm))
-        X = Y.view(torch.int16)
-    return layers, inputs, X
+    X0 = torch.from_numpy(X0_bits.view(np.int16)).cuda()
+    Ws = [torch.from_numpy(w.view(np.int16)).cuda().view(torch.bfloat16) for w in W_bits_list]
+    layers, inputs, out = g.sequential_quantize(X0, Ws, bits=bits, group_size=gs, blocksize=128, act_order=act_order)
+    torch.cuda.synchronize()
+    g.gptq_device_check()
+    return layers, inputs, out
 
 
 def gpu_w_hat(g, q, perm, m, d, bits, gs):
@@ -72,7 +65,7 @@ def gpu_w_hat(g, q, perm, m, d, bits, gs):
 
 
 def bf16_values(t):
-    return bf16_bits_to_f32(t.cpu().numpy().view(np.uint16)).astype(np.float64)
+    return bf16_bits_to_f32(t.view(torch.int16).cpu().numpy().view(np.uint16)).astype(np.float64)
 
 
 @pytest.mark.parametrize("bits,gs,act_order,nlayers", [(4, 128, False, 3), (3, -1, True, 2), (2, 64, False, 2)])
