@@ -29,13 +29,20 @@
 //
 // The quantizer uses correctly rounded quotients (see div_mk) and no fused
 // multiply-add, so each step rounds exactly like the listing's float32 arithmetic.
+#include <cudaTypedefs.h>
+
 #include <algorithm>
+#include <cstdlib>
+#include <string>
 #include <utility>
 
 #include "common.cuh"
 #include "simt_gemm.cuh"
 
 namespace gptq {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();   // tc_gemm.cu
+
 namespace colloop {
 
 struct QHeader {
@@ -851,6 +858,612 @@ __global__ void __launch_bounds__(chain::THREADS, 1) colchain_kernel(CBArgs a) {
   }
 }
 
+// ---------------------------------------------------------------------------------
+// An outer block on one SM per 32 rows: the chain column block of every 128-column
+// block of the outer block, and the lazy updates inside the outer block on this SM's
+// own tensor core.
+//
+// The column loop of a row depends on no other row, so the CTA that owns 32 rows can
+// move its rows' later columns itself. After block b it computes, for every later
+// 128-column tile t of the outer block, D[c][r] = sum_k Hinv1[i1 + k][tile col c] *
+// Err1[r][k] as D = Ut_tile (M = 128 columns, K-major) x Err1^T (N = 32 rows,
+// K-major), three TF32 passes (hi lo, lo hi, hi hi) per 32-deep k chunk, two 64-deep
+// accumulators per tile added in registers, round to nearest, then W -= D: the same
+// products, sums and rounding as the tensor-core lazy update of the two-level scheme.
+// Tile b + 1 comes first and goes straight into the chain's shared-memory W tile, so
+// the next block starts ~2 us after the chain of this one ends; the other tiles run
+// while the next block's chain does (the tensor core is otherwise idle here).
+//
+// Warps: 0 the chain, 1-3 and 5-7 the update warps (as in colchain_kernel; after a
+// block they split Err1 into the hi and lo parts of the MMA's B operand); 4 copies
+// Hinv1's first diagonal block and the first W tile, then its lane 0 streams the Ut
+// tiles (TMA, 3-stage ring of 32-deep chunks); 8-11 the tensor-memory epilogue (lane
+// quadrant = warp % 4; thread = column of a tile); 12 allocates tensor memory and its
+// lane 0 issues the MMAs.
+//
+// Per block b: the W tile (the bulk copy for b = 0, else the epilogue's tile) -> the
+// chain, errors written over the consumed quads of the W tile, codes as bytes (two
+// buffers by block parity) -> the split into the B operand once the previous block's
+// operand is free -> the MMAs of tiles b + 1 .. -> epilogue: tile b + 1 into the W
+// tile (held in registers since tile b's turn), Err1, losses and codes of block b,
+// then the other tiles (tile b + 2 kept in registers, the rest read-modify-written in
+// the fp32 working copy). Every wait is bounded.
+namespace mchain {
+using chain::BS;
+using chain::FIRST_UPD;
+using chain::NQ;
+using chain::NSLOT;
+using chain::NUPD;
+using chain::WLD;
+constexpr int THREADS = 416;
+constexpr int COPY_WARP = 4;
+constexpr int EPI_WARP0 = 8;
+constexpr int MMA_WARP = 12;
+constexpr int NWG = 224;                          // threads of warps 0-3 and 5-7
+constexpr int STAGES = 3;
+constexpr int NBUF = 4;                           // tensor-memory accumulators, 32 columns each
+constexpr uint32_t TMEM_COLS = 128;
+constexpr int QLD = BS + 4;                       // padded row of the code tile (bytes)
+constexpr uint32_t A_BYTES = 128u * 32u * 4u;     // 128 tile columns x 32 k, one part
+constexpr uint32_t STAGE_BYTES = 2u * A_BYTES;    // hi and lo
+constexpr uint32_t BOP_BYTES = 32u * BS * 4u;     // 32 rows x 128 k, one part (four 4 KB k chunks)
+struct Smem {
+  static constexpr size_t us = 0;                                        // Hinv1[i1 + t][i1 + c]
+  static constexpr size_t ws = us + sizeof(float) * BS * BS;             // W tile / errors, 32 x WLD
+  static constexpr size_t qb = ws + sizeof(float) * 32 * WLD;            // codes, 2 x 32 x QLD bytes
+  static constexpr size_t dinfo = qb + 2 * 32 * QLD;
+  static constexpr size_t bop = (dinfo + sizeof(float4) * BS + 1023) & ~(size_t)1023;
+  static constexpr size_t ring = bop + 2 * BOP_BYTES;
+  static constexpr size_t bars = ring + STAGES * STAGE_BYTES;
+  // wbar, wready, ubar[4], ebar[NQ], hbar[NQ], bop_full, bop_free, afull/aempty[STAGES],
+  // tfull/tempty[NBUF], drain
+  static constexpr int NBARS = 2 + 4 + 2 * NQ + 2 + 2 * STAGES + 2 * NBUF + 1;
+  static constexpr size_t tslot = bars + sizeof(uint64_t) * NBARS;
+  static constexpr size_t flag = tslot + 8;
+  static constexpr size_t used = flag + 8;
+  static constexpr size_t total = used + 1024;                           // the base is aligned up to 1024
+};
+static_assert(Smem::dinfo % 16 == 0 && Smem::ring % 1024 == 0 && Smem::bars % 8 == 0, "shared-memory layout");
+static_assert(Smem::total <= 232448, "shared memory per CTA");
+
+// byte offset of element (row r, k t) in a 128-byte-swizzled K-major operand of 32 rows
+__device__ __forceinline__ uint32_t bop_off(int r, int t) {
+  return (uint32_t)((t >> 5) * 4096 + r * 128 + ((((t & 31) >> 2) ^ (r & 7)) << 4) + ((t & 3) << 2));
+}
+__device__ __forceinline__ uint64_t desc_k(uint32_t base, int kk) { return umma_sdesc_sw128(base + kk * 32, 16, 1024); }
+__device__ __forceinline__ void bar_wg() { asm volatile("bar.sync 1, %0;" ::"n"(NWG) : "memory"); }
+__device__ __forceinline__ float lo_part(float x) { return x - __uint_as_float(__float_as_uint(x) & 0xFFFFE000u); }
+
+struct Args {
+  CBArgs a;
+  int o1;                     // first column of the outer block
+  int nb;                     // 128-column blocks in it
+};
+}  // namespace mchain
+
+__global__ void __launch_bounds__(mchain::THREADS, 1)
+colmma_kernel(const __grid_constant__ CUtensorMap map_ut, const __grid_constant__ CUtensorMap map_utlo,
+              const mchain::Args p) {
+  using namespace mchain;
+  using chain::apply_quad;
+  using chain::rint_small;
+  using chain::upd;
+  const CBArgs& a = p.a;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  float* Us = reinterpret_cast<float*>(sm + Smem::us);
+  float* Ws = reinterpret_cast<float*>(sm + Smem::ws);
+  uint8_t* Qb = sm + Smem::qb;
+  float4* dinfo = reinterpret_cast<float4*>(sm + Smem::dinfo);
+  uint8_t* bop = sm + Smem::bop;
+  uint8_t* ring = sm + Smem::ring;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Smem::bars);
+  uint64_t* wbar = bars;                      // W tile of block 0 (bulk copy)
+  uint64_t* wready = bars + 1;                // W tile of block b >= 1 (epilogue), completion b - 1
+  uint64_t* ubar = bars + 2;                  // Hinv1 rows [32k, 32k + 32) (+ dinfo on 0), completion b
+  uint64_t* ebar = ubar + 4;                  // errors of quad p in the W tile, completion b
+  uint64_t* hbar = ebar + NQ;                 // quad q handed back to the chain, completion b
+  uint64_t* bop_full = hbar + NQ;             // B operand of block b written, completion b
+  uint64_t* bop_free = bop_full + 1;          // MMAs and epilogue done with block b's operand
+  uint64_t* afull = bop_free + 1;
+  uint64_t* aempty = afull + STAGES;
+  uint64_t* tfull = aempty + STAGES;
+  uint64_t* tempty = tfull + NBUF;
+  uint64_t* drain = tempty + NBUF;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + Smem::tslot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Smem::flag);
+  volatile int* last_diag = abort_flag + 1;   // last block whose diagonal block was armed
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r0 = blockIdx.x * 32;
+  const int d = a.d, o1 = p.o1, nb = p.nb;
+  const int nrows = min(32, a.m - r0);
+  auto ncols_of = [&](int b) { return min(BS, d - (o1 + BS * b)); };
+  auto fail = [&]() {
+    *abort_flag = 1;
+    report_device_error(a.err_word, DEVERR_TIMEOUT);
+  };
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    *last_diag = 0;
+    mbar_init(wbar, 1);
+    mbar_init(wready, 4);
+    for (int k = 0; k < 4; ++k) mbar_init(&ubar[k], 1);
+    for (int q = 0; q < NQ; ++q) {
+      mbar_init(&ebar[q], 32);
+      mbar_init(&hbar[q], 32);
+    }
+    mbar_init(bop_full, 1);
+    mbar_init(bop_free, 5);                   // the MMA thread and the four epilogue warps
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&afull[s], 1);
+      mbar_init(&aempty[s], 1);
+    }
+    for (int b = 0; b < NBUF; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+    }
+    mbar_init(drain, 1);
+    fence_mbar_init();
+    prefetch_tmap(&map_ut);
+    prefetch_tmap(&map_utlo);
+  }
+  if (warp == MMA_WARP) tmem_alloc(tslot, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tslot;
+
+  // Hinv1's diagonal block of block b (row t from column t & ~3 on) and its dinfo, by
+  // one warp; Hinv1 and dinfo are final before this kernel's stream predecessor starts
+  auto issue_diag = [&](int b) {
+    const int i1 = o1 + BS * b, ncols = ncols_of(b);
+    if (lane < 4) {
+      uint32_t bytes = (lane == 0) ? (uint32_t)ncols * 16u : 0u;
+      for (int t = 32 * lane; t < min(32 * lane + 32, ncols); ++t) bytes += (uint32_t)(ncols - (t & ~3)) * 4u;
+      mbar_arrive_expect_tx(&ubar[lane], bytes);
+    }
+    __syncwarp();
+    for (int t = lane; t < ncols; t += 32) {
+      const int c0 = t & ~3;
+      bulk_load(Us + t * BS + c0, a.U + (long long)(i1 + t) * d + i1 + c0, (uint32_t)(ncols - c0) * 4u,
+                &ubar[t >> 5]);
+    }
+    if (lane == 0) {
+      bulk_load(dinfo, a.dinfo + i1, (uint32_t)ncols * 16u, &ubar[0]);
+      *last_diag = b;
+    }
+  };
+  if (warp == COPY_WARP) issue_diag(0);
+  // W and the statistics come from earlier kernels (the outer update before this one)
+  grid_dep_launch();
+  grid_dep_wait();
+  if (warp == COPY_WARP) {
+    const int ncols = ncols_of(0);
+    if (lane >= nrows)                          // rows past m: zeros, stored before the barrier's arrival
+      for (int c = 0; c < BS; c += 4) *reinterpret_cast<float4*>(Ws + lane * WLD + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+    __syncwarp();
+    if (lane == 0) mbar_arrive_expect_tx(wbar, (uint32_t)(nrows * ncols) * 4u);
+    __syncwarp();
+    if (lane < nrows) bulk_load(Ws + lane * WLD, a.Wf + (long long)(r0 + lane) * d + o1, (uint32_t)ncols * 4u, wbar);
+  }
+
+  if (warp < EPI_WARP0 && warp != COPY_WARP) {
+    // ------------------------------------------------------------ chain and update warps
+    const int wtid = (warp < COPY_WARP) ? tid : tid - 32;     // 0 .. NWG - 1
+    const float qmax = (float)((1 << a.bits) - 1);
+    const float inv_qmax = rcp_rn(qmax);
+    const int r = r0 + lane;
+    const bool active = r < a.m;
+    for (int b = 0; b < nb; ++b) {
+      const int i1 = o1 + BS * b, ncols = ncols_of(b), nq = ncols >> 2;
+      const uint32_t par = (uint32_t)b & 1u;
+      uint8_t* Qc = Qb + (b & 1) * 32 * QLD;
+      bool ok = __all_sync(0xffffffffu, *abort_flag == 0);
+      if (ok) ok = __all_sync(0xffffffffu, b == 0 ? mbar_wait_bounded(wbar, 0, abort_flag)
+                                                  : mbar_wait_bounded(wready, (uint32_t)(b - 1) & 1u, abort_flag));
+      if (ok && warp == 0) {
+        // ---- the chain: row `lane`'s dependent sequence, once per column
+        float s = 1.0f, inv_s = 1.0f, z = 0.0f;
+        if (a.stats_given || (i1 % a.g) != 0) {
+          if (active) {
+            s = a.scales[(long long)r * a.G + i1 / a.g];
+            z = a.zeros[(long long)r * a.G + i1 / a.g];
+          }
+          inv_s = rcp_rn(s);
+        } else {
+          float mn = INFINITY, mx = -INFINITY;
+          for (int c = 0; c < ncols; c += 4) {
+            const float4 v = *reinterpret_cast<const float4*>(Ws + lane * WLD + c);
+            mn = fminf(fminf(mn, v.x), fminf(fminf(v.y, v.z), v.w));
+            mx = fmaxf(fmaxf(mx, v.x), fmaxf(fmaxf(v.y, v.z), v.w));
+          }
+          group_params(mn, mx, qmax, inv_qmax, s, inv_s, z);
+          if (active) {
+            a.scales[(long long)r * a.G + i1 / a.g] = s;
+            a.zeros[(long long)r * a.G + i1 / a.g] = z;
+          }
+        }
+        float cur[4], nxt[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f}, e2[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+          const float4 v = *reinterpret_cast<const float4*>(Ws + lane * WLD);
+          cur[0] = v.x; cur[1] = v.y; cur[2] = v.z; cur[3] = v.w;
+        }
+#pragma unroll 1
+        for (int j = 0; j < nq; ++j) {
+          if (j + 1 >= FIRST_UPD && j + 1 < nq) {
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(&hbar[j + 1], par, abort_flag));
+            if (!ok) break;
+          }
+          if ((j & 7) == 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(&ubar[j >> 3], par, abort_flag));
+            if (!ok) break;
+          }
+          {
+            const float4 v = *reinterpret_cast<const float4*>(Ws + lane * WLD + 4 * (j + 1));
+            nxt[0] = v.x; nxt[1] = v.y; nxt[2] = v.z; nxt[3] = v.w;
+          }
+          apply_quad(nxt, e2, Us, max(j - 2, 0), 4 * (j + 1));
+          apply_quad(nxt, e1, Us, max(j - 1, 0), 4 * (j + 1));
+          float ec[4], qc[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int t = 4 * j + c;
+            const float4 di = dinfo[t];
+            const float4 ua = *reinterpret_cast<const float4*>(Us + t * BS + 4 * j);
+            const float4 ub = *reinterpret_cast<const float4*>(Us + t * BS + 4 * j + 4);
+            const float x = cur[c];
+            const float qv = fminf(fmaxf(rint_small(__fadd_rn(div_mk(x, s, inv_s), z)), 0.0f), qmax);
+            const float wq = __fmul_rn(__fsub_rn(qv, z), s);
+            const float e = div_mk(__fsub_rn(x, wq), di.x, di.y);
+            ec[c] = e;
+            qc[c] = qv;
+            if (c < 1) cur[1] = upd(cur[1], e, ua.y);
+            if (c < 2) cur[2] = upd(cur[2], e, ua.z);
+            if (c < 3) cur[3] = upd(cur[3], e, ua.w);
+            nxt[0] = upd(nxt[0], e, ub.x);
+            nxt[1] = upd(nxt[1], e, ub.y);
+            nxt[2] = upd(nxt[2], e, ub.z);
+            nxt[3] = upd(nxt[3], e, ub.w);
+          }
+          // quad j of the W tile is consumed: its errors take its place
+          *reinterpret_cast<float4*>(Ws + lane * WLD + 4 * j) = make_float4(ec[0], ec[1], ec[2], ec[3]);
+          *reinterpret_cast<uchar4*>(Qc + lane * QLD + 4 * j) =
+              make_uchar4((unsigned char)qc[0], (unsigned char)qc[1], (unsigned char)qc[2], (unsigned char)qc[3]);
+          mbar_arrive(&ebar[j]);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            e2[k] = e1[k];
+            e1[k] = ec[k];
+            cur[k] = nxt[k];
+          }
+        }
+      } else if (ok) {
+        // ---- update warps: quads FIRST_UPD + u, + NUPD, ... of the row in registers
+        const int u = (warp < COPY_WARP) ? warp - 1 : warp - 2;
+        const int nslot = (nq - 1 - FIRST_UPD - u >= 0) ? (nq - 1 - FIRST_UPD - u) / NUPD + 1 : 0;
+        const int qlast = FIRST_UPD + u + NUPD * (nslot - 1);
+        float w[NSLOT][4];
+        if (nslot > 0) {
+#pragma unroll
+          for (int k = 0; k < NSLOT; ++k) {
+            if (k < nslot) {
+              const float4 v = *reinterpret_cast<const float4*>(Ws + lane * WLD + 4 * (FIRST_UPD + u + NUPD * k));
+              w[k][0] = v.x; w[k][1] = v.y; w[k][2] = v.z; w[k][3] = v.w;
+            } else {
+              w[k][0] = w[k][1] = w[k][2] = w[k][3] = 0.0f;
+            }
+          }
+#pragma unroll 1
+          for (int q0 = 0; q0 + FIRST_UPD <= qlast; ++q0) {
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(&ebar[q0], par, abort_flag));
+            if (!ok) break;
+            if ((q0 & 7) == 0) {
+              ok = __all_sync(0xffffffffu, mbar_wait_bounded(&ubar[q0 >> 3], par, abort_flag));
+              if (!ok) break;
+            }
+            float ep[4];
+            {
+              const float4 v = *reinterpret_cast<const float4*>(Ws + lane * WLD + 4 * q0);
+              ep[0] = v.x; ep[1] = v.y; ep[2] = v.z; ep[3] = v.w;
+            }
+#pragma unroll
+            for (int k = 0; k < NSLOT; ++k) {
+              const int q = FIRST_UPD + u + NUPD * k;
+              if (k < nslot && q >= q0 + FIRST_UPD) {
+                apply_quad(w[k], ep, Us, q0, 4 * q);
+                if (q == q0 + FIRST_UPD) {
+                  *reinterpret_cast<float4*>(Ws + lane * WLD + 4 * q) = make_float4(w[k][0], w[k][1], w[k][2], w[k][3]);
+                  mbar_arrive(&hbar[q]);
+                }
+              }
+            }
+          }
+        }
+      }
+      if (!ok && lane == 0 && !*abort_flag) fail();
+      bar_wg();                                              // block b done: errors, codes in place
+      if (b + 1 < nb && warp == 1 && __all_sync(0xffffffffu, *abort_flag == 0)) {
+        fence_proxy_async_smem();                            // the diagonal block's reads before the copies
+        issue_diag(b + 1);
+      }
+      // errors -> the MMA operand: hi (the fp32 value; the tensor core reads its tf32
+      // part) and lo, 128-byte swizzled, once the previous block's operand is free
+      bool okf = !*abort_flag;
+      if (okf && b >= 1) okf = mbar_wait_bounded(bop_free, (uint32_t)(b - 1) & 1u, abort_flag);
+      if (okf) {
+        for (int idx = wtid; idx < 32 * (BS / 4); idx += NWG) {
+          const int rr = idx >> 5, t = 4 * (idx & 31);
+          const float4 e = *reinterpret_cast<const float4*>(Ws + rr * WLD + t);
+          const uint32_t off = bop_off(rr, t);
+          *reinterpret_cast<float4*>(bop + off) = e;
+          *reinterpret_cast<float4*>(bop + BOP_BYTES + off) =
+              make_float4(lo_part(e.x), lo_part(e.y), lo_part(e.z), lo_part(e.w));
+        }
+        fence_proxy_async_smem();                            // generic writes -> tensor-core reads
+      } else if (!*abort_flag) {
+        fail();
+      }
+      bar_wg();
+      if (wtid == 0 && !*abort_flag) mbar_arrive(bop_full);
+    }
+  } else if (warp == COPY_WARP) {
+    // ------------------------------------------------------------ Ut tiles (TMA; the warp waits, lane 0 issues)
+    int stage = 0;
+    uint32_t phase = 0, armed = 0, last_phase = 0;
+    bool ok = true;
+    for (int b = 0; ok && b < nb; ++b) {
+      const int i1 = o1 + BS * b;
+      for (int t = b + 1; ok && t < nb; ++t)
+        for (int kc = 0; kc < 4; ++kc) {
+          if (!__all_sync(0xffffffffu, mbar_wait_bounded(&aempty[stage], phase ^ 1u, abort_flag))) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            uint8_t* dst = ring + stage * STAGE_BYTES;
+            mbar_arrive_expect_tx(&afull[stage], STAGE_BYTES);
+            tma_load_2d(dst, &map_ut, &afull[stage], i1 + 32 * kc, o1 + BS * t);
+            tma_load_2d(dst + A_BYTES, &map_utlo, &afull[stage], i1 + 32 * kc, o1 + BS * t);
+          }
+          __syncwarp();
+          armed |= 1u << stage;
+          last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+    }
+    if (!ok && lane == 0 && !*abort_flag) fail();
+    if (lane == 0)
+      for (int s = 0; s < STAGES; ++s)
+        if (armed & (1u << s)) mbar_wait_bounded(&afull[s], (last_phase >> s) & 1u, nullptr);
+  } else if (warp == MMA_WARP) {
+    // ------------------------------------------------------------ MMA issuer (lane 0; the warp waits)
+    constexpr uint32_t IDESC = umma_idesc(/*tf32*/ 2, false, false, 128, 32);
+    const uint32_t ring_u = smem_u32(ring), bop_u = smem_u32(bop);
+    int stage = 0;
+    uint32_t phase = 0, it = 0;
+    bool ok = true, issued_any = false;
+    for (int b = 0; ok && b < nb; ++b) {
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(bop_full, (uint32_t)b & 1u, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      bool issued = false;
+      for (int t = b + 1; ok && t < nb; ++t)
+        for (int ch = 0; ok && ch < 2; ++ch) {
+          const uint32_t buf = it % NBUF;
+          if (!__all_sync(0xffffffffu, mbar_wait_bounded(&tempty[buf], ((it / NBUF) & 1u) ^ 1u, abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t dt = tmem_base + buf * 32u;
+          for (int s2 = 0; s2 < 2; ++s2) {
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&afull[stage], phase, abort_flag))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            if (lane == 0) {
+              const uint32_t ah = ring_u + stage * STAGE_BYTES, al = ah + A_BYTES;
+              const uint32_t bh = bop_u + (uint32_t)(2 * ch + s2) * 4096u, bl = bh + BOP_BYTES;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                // Ut_lo Err1_hi, Ut_hi Err1_lo, Ut_hi Err1_hi: the order of the tensor-core
+                // lazy update's three passes (Err1_hi Ut_lo, Err1_lo Ut_hi, Err1_hi Ut_hi)
+                umma_tf32(dt, desc_k(al, kk), desc_k(bh, kk), IDESC, (s2 > 0 || kk > 0) ? 1u : 0u);
+                umma_tf32(dt, desc_k(ah, kk), desc_k(bl, kk), IDESC, 1u);
+                umma_tf32(dt, desc_k(ah, kk), desc_k(bh, kk), IDESC, 1u);
+              }
+              umma_commit(&aempty[stage]);
+            }
+            __syncwarp();
+            issued = true;
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          }
+          if (!ok) break;
+          if (lane == 0) umma_commit(&tfull[buf]);
+          __syncwarp();
+          ++it;
+        }
+      if (!ok) break;
+      if (lane == 0) {
+        if (issued) umma_commit(bop_free);        // arrives when this block's products are done
+        else mbar_arrive(bop_free);
+      }
+      __syncwarp();
+      issued_any |= issued;
+    }
+    if (!ok && lane == 0 && !*abort_flag) fail();
+    if (issued_any && lane == 0) {
+      umma_commit(drain);
+      mbar_wait_bounded(drain, 0, nullptr);
+    }
+  } else {
+    // ------------------------------------------------------------ tensor-memory epilogue
+    const int e = warp - EPI_WARP0;                        // lane quadrant (== warp % 4)
+    const int etid = tid - EPI_WARP0 * 32;                 // 0 .. 127
+    const int c = 32 * e + lane;                           // column within a tile
+    const uint32_t taddr = tmem_base + ((uint32_t)(32 * e) << 16);
+    uint32_t it = 0;
+    bool ok = true;
+    float rn[32];                                          // the next block's W tile column
+    if (nb > 1) {
+      const int col = o1 + BS + c;
+#pragma unroll
+      for (int rr = 0; rr < 32; ++rr)
+        rn[rr] = (rr < nrows && col < d) ? __ldcg(a.Wf + (long long)(r0 + rr) * d + col) : 0.0f;
+    }
+    // Err1 with its low parts, the loss partials and the codes of block b
+    auto block_out = [&](int b) {
+      const int i1 = o1 + BS * b, ncols = ncols_of(b);
+      if (ok && !__all_sync(0xffffffffu, mbar_wait_bounded(bop_full, (uint32_t)b & 1u, abort_flag))) {
+        ok = false;
+        if (!*abort_flag) fail();
+      }
+      if (!ok) return;
+      if (c < ncols) {
+        const long long o = (long long)r0 * a.eld + (i1 - o1) + c;
+        float l[2] = {0.0f, 0.0f};
+        // 16 rows at a time: all shared-memory reads before the global stores, which the
+        // compiler cannot move them across
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float hv[16], lv[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const uint32_t off = bop_off(16 * h + k, c);
+            hv[k] = *reinterpret_cast<const float*>(bop + off);
+            lv[k] = *reinterpret_cast<const float*>(bop + BOP_BYTES + off);
+          }
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int rr = 16 * h + k;
+            if (rr < nrows) {
+              a.err[o + (long long)rr * a.eld] = hv[k];
+              a.err_lo[o + (long long)rr * a.eld] = lv[k];
+              l[h] = __fadd_rn(l[h], __fmul_rn(__fmul_rn(hv[k], hv[k]), 0.5f));
+            }
+          }
+        }
+        a.part[(long long)blockIdx.x * d + i1 + c] = __fadd_rn(l[0], l[1]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bop_free);
+      const uint8_t* Qc = Qb + (b & 1) * 32 * QLD;
+      const int bits = a.bits;
+      if (a.codes8) {
+        for (int idx = etid; idx < 32 * BS; idx += 128) {
+          const int rr = idx / BS, t = idx % BS;
+          if (t < ncols && rr < nrows) a.codes8[(long long)(r0 + rr) * d + i1 + t] = Qc[rr * QLD + t];
+        }
+      } else if (32 % bits == 0) {
+        const int cpw = 32 / bits;
+        const int nwb = (ncols + cpw - 1) / cpw, wb = (i1 * bits) >> 5;
+        for (int idx = etid; idx < 32 * nwb; idx += 128) {
+          const int rr = idx / nwb, w = idx - rr * nwb;
+          if (rr >= nrows) continue;
+          uint32_t v = 0;
+          for (int k = 0, t = w * cpw; k < cpw && t < ncols; ++k, ++t) v |= (uint32_t)Qc[rr * QLD + t] << (k * bits);
+          a.qweight[(long long)(r0 + rr) * a.wpr + wb + w] = v;
+        }
+      } else {
+        const int wb = (i1 * bits) >> 5;
+        const int we = ((i1 + ncols) * bits + 31) >> 5;
+        const int nw = we - wb;
+        for (int idx = etid; idx < 32 * nw; idx += 128) {
+          const int rr = idx / nw, wi = wb + idx % nw;
+          if (rr >= nrows) continue;
+          const int b0 = wi * 32;
+          const int jf = b0 / bits;
+          const int jl = min(i1 + ncols - 1, (b0 + 31) / bits);
+          uint64_t v = 0;
+          for (int j = jf; j <= jl; ++j) {
+            const uint64_t code = Qc[rr * QLD + (j - i1)];
+            const int sh = j * bits - b0;
+            v |= (sh >= 0) ? (code << sh) : (code >> (-sh));
+          }
+          a.qweight[(long long)(r0 + rr) * a.wpr + wi] = (uint32_t)v;
+        }
+      }
+    };
+    for (int b = 0; ok && b < nb; ++b) {
+      for (int t = b + 1; ok && t < nb; ++t) {
+        float acc[32];
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          const uint32_t buf = it % NBUF;
+          if (!__all_sync(0xffffffffu, mbar_wait_bounded(&tfull[buf], (it / NBUF) & 1u, abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          float v[32];
+          tmem_ld_32x32b_x32(taddr + buf * 32u, v);
+#pragma unroll
+          for (int rr = 0; rr < 32; ++rr) acc[rr] = (ch == 0) ? v[rr] : __fadd_rn(acc[rr], v[rr]);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[buf]);
+          ++it;
+        }
+        if (!ok) {
+          if (!*abort_flag) fail();
+          break;
+        }
+        const int col = o1 + BS * t + c;
+        if (t == b + 1) {
+          // the next block's W tile: its column c, all 32 rows
+#pragma unroll
+          for (int rr = 0; rr < 32; ++rr) Ws[rr * WLD + c] = __fsub_rn(rn[rr], acc[rr]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(wready);
+          block_out(b);
+        } else {
+          // 16 rows at a time: all loads in flight before any store (a store between
+          // them would keep the compiler from moving the next load above it)
+          float* wcol = const_cast<float*>(a.Wf) + (long long)r0 * d + col;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float x[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const int rr = 16 * h + k;
+              x[k] = (rr < nrows && col < d) ? __ldcg(wcol + (long long)rr * d) : 0.0f;
+            }
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const int rr = 16 * h + k;
+              if (t == b + 2) {
+                rn[rr] = __fsub_rn(x[k], acc[rr]);                     // the next critical tile
+              } else if (rr < nrows && col < d) {
+                __stcg(wcol + (long long)rr * d, __fsub_rn(x[k], acc[rr]));
+              }
+            }
+          }
+        }
+      }
+      if (ok && b == nb - 1) block_out(b);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    // A wait gave up: wait (bounded) for the copies still landing in shared memory
+    if (warp == COPY_WARP && lane == 0) mbar_wait_bounded(wbar, 0, nullptr);
+    if (warp == 1 && lane < 4) mbar_wait_bounded(&ubar[lane], (uint32_t)*last_diag & 1u, nullptr);
+  }
+  if (warp == MMA_WARP) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
 // col_losses[j] = sum over the CTAs' partials: 32 columns per CTA, the 8 warps each sum
 // every 8th partial, then warp 0 adds the 8 sums (fixed order)
 __global__ void loss_finalize_kernel(const float* __restrict__ part, int nrg, int d, const int* __restrict__ perm,
@@ -995,32 +1608,36 @@ Layout layout(long long m, long long d, int blocksize) {
   return L;
 }
 
+// W[:, c0:c1] -= Err1[:, e0:e0+K] @ Hinv1[k0:k0+K, c0:c1] on the tensor cores (Err1
+// row-major with row stride a.eld; B(k, j) = Ut[c0 + j][k0 + k])
+gptq_status lazy_update(const CBArgs& a, const float* Ut, const float* Ut_lo, int e0, int k0, int K, int c0, int c1,
+                        cudaStream_t s) {
+  const int m = a.m, d = a.d;
+  simt::GemmArgs ga{};
+  ga.M = m; ga.N = c1 - c0; ga.K = K; ga.M_last = m; ga.K_last = K;
+  ga.A = a.err + e0; ga.lda = a.eld;
+  ga.B = Ut + (long long)c0 * d + k0; ga.ldb = d;
+  ga.A_lo = a.err_lo + e0; ga.lda_lo = a.eld;
+  ga.B_lo = Ut_lo + (long long)c0 * d + k0; ga.ldb_lo = d;
+  ga.C = const_cast<float*>(a.Wf) + c0; ga.ldc = d;
+  ga.alpha = -1.0f; ga.beta = 1.0f;
+  ga.vec = (d % 4 == 0) && simt::aligned16(a.Wf) && simt::aligned16(Ut) && simt::aligned16(a.err);
+  ga.b_final = 1;             // Ut is written once, before the first column block
+  ProfScope ps("quantize.lazy_gemm", s);
+  return tc_gemm(ga, 1, true, true, s);
+}
+
 // Every block of BS columns: the column-block kernel (`kernel`, `threads` threads and
 // `smem` bytes of dynamic shared memory per CTA of 32 rows), then the lazy updates.
 gptq_status run_blocks(void (*kernel)(CBArgs), int threads, size_t smem, int BS, CBArgs a, const float* Ut,
                        const float* Ut_lo, cudaStream_t s) {
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return set_error(GPTQ_ERR_CUDA, "cudaFuncSetAttribute(column-block kernel) failed");
-  const int m = a.m, d = a.d;
-  const int nrg = (m + ROWS_PER_CTA - 1) / ROWS_PER_CTA;
+  const int d = a.d;
+  const int nrg = (a.m + ROWS_PER_CTA - 1) / ROWS_PER_CTA;
   const int OB = outer_width(BS, a.g, a.stats_given);
-  const bool vec = (d % 4 == 0) && simt::aligned16(a.Wf) && simt::aligned16(Ut) && simt::aligned16(a.err);
   a.eld = OB;
-  // W[:, c0:c1] -= Err1[:, e0:e0+K] @ Hinv1[k0:k0+K, c0:c1];  B(k, j) = Ut[c0 + j][k0 + k]
-  auto lazy = [&](int e0, int k0, int K, int c0, int c1) -> gptq_status {
-    simt::GemmArgs ga{};
-    ga.M = m; ga.N = c1 - c0; ga.K = K; ga.M_last = m; ga.K_last = K;
-    ga.A = a.err + e0; ga.lda = OB;
-    ga.B = Ut + (long long)c0 * d + k0; ga.ldb = d;
-    ga.A_lo = a.err_lo + e0; ga.lda_lo = OB;
-    ga.B_lo = Ut_lo + (long long)c0 * d + k0; ga.ldb_lo = d;
-    ga.C = const_cast<float*>(a.Wf) + c0; ga.ldc = d;
-    ga.alpha = -1.0f; ga.beta = 1.0f;
-    ga.vec = vec;
-    ga.b_final = 1;             // Ut is written once, before the first column block
-    ProfScope ps2("quantize.lazy_gemm", s);
-    return tc_gemm(ga, 1, true, true, s);
-  };
+  auto lazy = [&](int e0, int k0, int K, int c0, int c1) { return lazy_update(a, Ut, Ut_lo, e0, k0, K, c0, c1, s); };
   for (int o1 = 0; o1 < d; o1 += OB) {
     const int o2 = std::min(o1 + OB, d);
     for (int i1 = o1; i1 < o2; i1 += BS) {
@@ -1045,6 +1662,60 @@ gptq_status run_blocks(void (*kernel)(CBArgs), int threads, size_t smem, int BS,
 template <int BS, int LANES>
 gptq_status run_blocks_lanes(CBArgs a, const float* Ut, const float* Ut_lo, cudaStream_t s) {
   return run_blocks(colblock_kernel<BS, LANES>, cb_threads<LANES>(), CBSmem<BS, LANES>::total, BS, a, Ut, Ut_lo, s);
+}
+
+// 2-D map over Ut (d x d fp32, row-major): boxes of 32 k x 128 rows, 128-byte swizzle,
+// rows past d read as zeros
+bool make_ut_map(CUtensorMap* map, const float* base, int d) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)d};
+  cuuint64_t strides[1] = {(cuuint64_t)d * 4};
+  cuuint32_t box[2] = {32, 128};
+  cuuint32_t es[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 128-column blocks, groups of 128 or per-channel: one colmma_kernel launch per outer
+// block (the blocks and the lazy updates inside it), then the update of everything
+// right of the outer block.
+gptq_status run_outer_blocks(CBArgs a, const float* Ut, const float* Ut_lo, cudaStream_t s) {
+  using namespace mchain;
+  if (cudaFuncSetAttribute(colmma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Smem::total) !=
+      cudaSuccess)
+    return set_error(GPTQ_ERR_CUDA, "cudaFuncSetAttribute(colmma_kernel) failed");
+  CUtensorMap mu, mul;
+  if (!make_ut_map(&mu, Ut, a.d) || !make_ut_map(&mul, Ut_lo, a.d))
+    return set_error(GPTQ_ERR_CUDA, "cuTensorMapEncodeTiled failed for Hinv1^T");
+  const int d = a.d;
+  const int nrg = (a.m + ROWS_PER_CTA - 1) / ROWS_PER_CTA;
+  const int OB = outer_width(BS, a.g, a.stats_given);
+  a.eld = OB;
+  for (int o1 = 0; o1 < d; o1 += OB) {
+    const int o2 = std::min(o1 + OB, d);
+    Args p{a, o1, (o2 - o1 + BS - 1) / BS};
+    {
+      ProfScope ps("quantize.colblock", s);
+      if (launch_pdl(colmma_kernel, dim3(nrg), dim3(THREADS), Smem::total, s, mu, mul, p) != cudaSuccess)
+        return check_launch("colmma_kernel");
+      count_launch();
+    }
+    if (o2 < d)
+      if (gptq_status st = lazy_update(a, Ut, Ut_lo, 0, o1, o2 - o1, o2, d, s)) return st;
+  }
+  return check_launch("column-loop kernels");
+}
+
+// GPTQ_COLUMN_KERNEL=chain selects the per-block chain kernel with the lazy updates as
+// separate tensor-core GEMMs for every configuration that kernel serves.
+static bool prefer_chain_kernel() {
+  static const bool f = [] {
+    const char* v = getenv("GPTQ_COLUMN_KERNEL");
+    return v && std::string(v) == "chain";
+  }();
+  return f;
 }
 
 }  // namespace colloop
@@ -1110,7 +1781,10 @@ gptq_status quantize_launch(const void* W, int w_dtype, long long m_, long long 
     case 32: st = run_blocks_lanes<32, 8>(a, Ut, Ut_lo, s); break;
     case 64: st = run_blocks_lanes<64, 8>(a, Ut, Ut_lo, s); break;
     default:
-      if ((a.stats_given || g % 128 == 0) && a.bulk && a.vecw)
+      if ((a.stats_given || g == 128) && a.bulk && a.vecw && tc_gemm_available() && !prefer_chain_kernel())
+        // one launch per outer block, its lazy updates on each SM's own tensor core
+        st = run_outer_blocks(a, Ut, Ut_lo, s);
+      else if ((a.stats_given || g % 128 == 0) && a.bulk && a.vecw)
         // groups start on block boundaries: one chain warp per 32 rows
         st = run_blocks(colchain_kernel, chain::THREADS, chain::Smem::total, 128, a, Ut, Ut_lo, s);
       else if (a.stats_given || g % 64 == 0)   // 64-column steps need groups that start on them
