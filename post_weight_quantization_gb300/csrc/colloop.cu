@@ -943,7 +943,7 @@ struct Args {
 
 __global__ void __launch_bounds__(mchain::THREADS, 1)
 colmma_kernel(const __grid_constant__ CUtensorMap map_ut, const __grid_constant__ CUtensorMap map_utlo,
-              const mchain::Args p) {
+              const __grid_constant__ CUtensorMap map_u, const mchain::Args p) {
   using namespace mchain;
   using chain::apply_quad;
   using chain::rint_small;
@@ -961,10 +961,10 @@ colmma_kernel(const __grid_constant__ CUtensorMap map_ut, const __grid_constant_
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Smem::bars);
   uint64_t* wbar = bars;                      // W tile of block 0 (bulk copy)
   uint64_t* wready = bars + 1;                // W tile of block b >= 1 (epilogue), completion b - 1
-  uint64_t* ubar = bars + 2;                  // Hinv1 rows [32k, 32k + 32) (+ dinfo on 0), completion b
+  uint64_t* ubar = bars + 2;                  // Hinv1's diagonal block and dinfo, completion b
   uint64_t* ebar = ubar + 4;                  // errors of quad p in the W tile, completion b
   uint64_t* hbar = ebar + NQ;                 // quad q handed back to the chain, completion b
-  uint64_t* bop_full = hbar + NQ;             // B operand of block b written, completion b
+  uint64_t* bop_full = hbar + NQ;             // B operand of block b written (NWG arrivals), completion b
   uint64_t* bop_free = bop_full + 1;          // MMAs and epilogue done with block b's operand
   uint64_t* afull = bop_free + 1;
   uint64_t* aempty = afull + STAGES;
@@ -990,12 +990,12 @@ colmma_kernel(const __grid_constant__ CUtensorMap map_ut, const __grid_constant_
     *last_diag = 0;
     mbar_init(wbar, 1);
     mbar_init(wready, 4);
-    for (int k = 0; k < 4; ++k) mbar_init(&ubar[k], 1);
+    mbar_init(ubar, 1);
     for (int q = 0; q < NQ; ++q) {
       mbar_init(&ebar[q], 32);
       mbar_init(&hbar[q], 32);
     }
-    mbar_init(bop_full, 1);
+    mbar_init(bop_full, NWG);                 // every converting thread, after its writes
     mbar_init(bop_free, 5);                   // the MMA thread and the four epilogue warps
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&afull[s], 1);
@@ -1009,6 +1009,7 @@ colmma_kernel(const __grid_constant__ CUtensorMap map_ut, const __grid_constant_
     fence_mbar_init();
     prefetch_tmap(&map_ut);
     prefetch_tmap(&map_utlo);
+    prefetch_tmap(&map_u);
   }
   if (warp == MMA_WARP) tmem_alloc(tslot, TMEM_COLS);
   tc_fence_before();
@@ -1016,27 +1017,18 @@ colmma_kernel(const __grid_constant__ CUtensorMap map_ut, const __grid_constant_
   tc_fence_after();
   const uint32_t tmem_base = *tslot;
 
-  // Hinv1's diagonal block of block b (row t from column t & ~3 on) and its dinfo, by
-  // one warp; Hinv1 and dinfo are final before this kernel's stream predecessor starts
+  // Hinv1's diagonal block of block b (one 128 x 128 TMA box, zeros past d) and its
+  // dinfo, by one thread: one request instead of a copy per row (128 row copies took
+  // the issuing warp ~4 us); Hinv1 and dinfo are final before this kernel's stream
+  // predecessor starts
   auto issue_diag = [&](int b) {
     const int i1 = o1 + BS * b, ncols = ncols_of(b);
-    if (lane < 4) {
-      uint32_t bytes = (lane == 0) ? (uint32_t)ncols * 16u : 0u;
-      for (int t = 32 * lane; t < min(32 * lane + 32, ncols); ++t) bytes += (uint32_t)(ncols - (t & ~3)) * 4u;
-      mbar_arrive_expect_tx(&ubar[lane], bytes);
-    }
-    __syncwarp();
-    for (int t = lane; t < ncols; t += 32) {
-      const int c0 = t & ~3;
-      bulk_load(Us + t * BS + c0, a.U + (long long)(i1 + t) * d + i1 + c0, (uint32_t)(ncols - c0) * 4u,
-                &ubar[t >> 5]);
-    }
-    if (lane == 0) {
-      bulk_load(dinfo, a.dinfo + i1, (uint32_t)ncols * 16u, &ubar[0]);
-      *last_diag = b;
-    }
+    mbar_arrive_expect_tx(ubar, (uint32_t)(BS * BS * 4) + (uint32_t)ncols * 16u);
+    tma_load_2d(Us, &map_u, ubar, i1, i1);
+    bulk_load(dinfo, a.dinfo + i1, (uint32_t)ncols * 16u, ubar);
+    *last_diag = b;
   };
-  if (warp == COPY_WARP) issue_diag(0);
+  if (warp == COPY_WARP && lane == 0) issue_diag(0);
   // W and the statistics come from earlier kernels (the outer update before this one)
   grid_dep_launch();
   grid_dep_wait();
@@ -1097,8 +1089,8 @@ colmma_kernel(const __grid_constant__ CUtensorMap map_ut, const __grid_constant_
             ok = __all_sync(0xffffffffu, mbar_wait_bounded(&hbar[j + 1], par, abort_flag));
             if (!ok) break;
           }
-          if ((j & 7) == 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(&ubar[j >> 3], par, abort_flag));
+          if (j == 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(ubar, par, abort_flag));
             if (!ok) break;
           }
           {
@@ -1160,8 +1152,8 @@ colmma_kernel(const __grid_constant__ CUtensorMap map_ut, const __grid_constant_
           for (int q0 = 0; q0 + FIRST_UPD <= qlast; ++q0) {
             ok = __all_sync(0xffffffffu, mbar_wait_bounded(&ebar[q0], par, abort_flag));
             if (!ok) break;
-            if ((q0 & 7) == 0) {
-              ok = __all_sync(0xffffffffu, mbar_wait_bounded(&ubar[q0 >> 3], par, abort_flag));
+            if (q0 == 0) {
+              ok = __all_sync(0xffffffffu, mbar_wait_bounded(ubar, par, abort_flag));
               if (!ok) break;
             }
             float ep[4];
@@ -1185,8 +1177,8 @@ colmma_kernel(const __grid_constant__ CUtensorMap map_ut, const __grid_constant_
       }
       if (!ok && lane == 0 && !*abort_flag) fail();
       bar_wg();                                              // block b done: errors, codes in place
-      if (b + 1 < nb && warp == 1 && __all_sync(0xffffffffu, *abort_flag == 0)) {
-        fence_proxy_async_smem();                            // the diagonal block's reads before the copies
+      if (b + 1 < nb && wtid == 32 && !*abort_flag) {
+        fence_proxy_async_smem();                            // the diagonal block's reads before the copy
         issue_diag(b + 1);
       }
       // errors -> the MMA operand: hi (the fp32 value; the tensor core reads its tf32
@@ -1206,101 +1198,101 @@ colmma_kernel(const __grid_constant__ CUtensorMap map_ut, const __grid_constant_
       } else if (!*abort_flag) {
         fail();
       }
-      bar_wg();
-      if (wtid == 0 && !*abort_flag) mbar_arrive(bop_full);
+      // each thread signals its own part (a single arrival after a group barrier reached
+      // the MMA warp about 4 us late); the next block's chain cannot overwrite the errors
+      // before every part is converted, since its W tile comes after these products
+      mbar_arrive(bop_full);
     }
   } else if (warp == COPY_WARP) {
-    // ------------------------------------------------------------ Ut tiles (TMA; the warp waits, lane 0 issues)
-    int stage = 0;
-    uint32_t phase = 0, armed = 0, last_phase = 0;
-    bool ok = true;
-    for (int b = 0; ok && b < nb; ++b) {
-      const int i1 = o1 + BS * b;
-      for (int t = b + 1; ok && t < nb; ++t)
-        for (int kc = 0; kc < 4; ++kc) {
-          if (!__all_sync(0xffffffffu, mbar_wait_bounded(&aempty[stage], phase ^ 1u, abort_flag))) {
-            ok = false;
-            break;
-          }
-          if (lane == 0) {
+    // ------------------------------------------------------------ Ut tiles (TMA), lane 0
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, armed = 0, last_phase = 0;
+      bool ok = true;
+      for (int b = 0; ok && b < nb; ++b) {
+        const int i1 = o1 + BS * b;
+        for (int t = b + 1; ok && t < nb; ++t)
+          for (int kc = 0; kc < 4; ++kc) {
+            if (!mbar_wait_bounded(&aempty[stage], phase ^ 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
             uint8_t* dst = ring + stage * STAGE_BYTES;
             mbar_arrive_expect_tx(&afull[stage], STAGE_BYTES);
             tma_load_2d(dst, &map_ut, &afull[stage], i1 + 32 * kc, o1 + BS * t);
             tma_load_2d(dst + A_BYTES, &map_utlo, &afull[stage], i1 + 32 * kc, o1 + BS * t);
+            armed |= 1u << stage;
+            last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           }
-          __syncwarp();
-          armed |= 1u << stage;
-          last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-        }
-    }
-    if (!ok && lane == 0 && !*abort_flag) fail();
-    if (lane == 0)
+      }
+      if (!ok && !*abort_flag) fail();
       for (int s = 0; s < STAGES; ++s)
         if (armed & (1u << s)) mbar_wait_bounded(&afull[s], (last_phase >> s) & 1u, nullptr);
+    }
   } else if (warp == MMA_WARP) {
-    // ------------------------------------------------------------ MMA issuer (lane 0; the warp waits)
-    constexpr uint32_t IDESC = umma_idesc(/*tf32*/ 2, false, false, 128, 32);
-    const uint32_t ring_u = smem_u32(ring), bop_u = smem_u32(bop);
-    int stage = 0;
-    uint32_t phase = 0, it = 0;
-    bool ok = true, issued_any = false;
-    for (int b = 0; ok && b < nb; ++b) {
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(bop_full, (uint32_t)b & 1u, abort_flag))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      bool issued = false;
-      for (int t = b + 1; ok && t < nb; ++t)
-        for (int ch = 0; ok && ch < 2; ++ch) {
-          const uint32_t buf = it % NBUF;
-          if (!__all_sync(0xffffffffu, mbar_wait_bounded(&tempty[buf], ((it / NBUF) & 1u) ^ 1u, abort_flag))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t dt = tmem_base + buf * 32u;
-          for (int s2 = 0; s2 < 2; ++s2) {
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&afull[stage], phase, abort_flag))) {
+    // ------------------------------------------------------------ MMA issuer, lane 0
+    // A lean loop: the tensor core holds only a few MMAs in flight, so every cycle the
+    // issuing thread spends between stages (warp-wide waits and votes cost ~550 cycles
+    // per 12-MMA stage here) is a cycle the tensor pipe idles. Descriptors advance by
+    // 32 bytes per k-step: +2 in the 16-byte address field.
+    if (lane == 0) {
+      constexpr uint32_t IDESC = umma_idesc(/*tf32*/ 2, false, false, 128, 32);
+      const uint32_t ring_u = smem_u32(ring), bop_u = smem_u32(bop);
+      int stage = 0;
+      uint32_t phase = 0, it = 0;
+      bool ok = true, issued_any = false;
+      for (int b = 0; ok && b < nb; ++b) {
+        if (!mbar_wait_poll(bop_full, (uint32_t)b & 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        bool issued = false;
+        for (int t = b + 1; ok && t < nb; ++t)
+          for (int ch = 0; ok && ch < 2; ++ch) {
+            const uint32_t buf = it & (NBUF - 1);
+            if (!mbar_wait_bounded(&tempty[buf], ((it / NBUF) & 1u) ^ 1u, abort_flag)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            if (lane == 0) {
-              const uint32_t ah = ring_u + stage * STAGE_BYTES, al = ah + A_BYTES;
-              const uint32_t bh = bop_u + (uint32_t)(2 * ch + s2) * 4096u, bl = bh + BOP_BYTES;
+            const uint32_t dt = tmem_base + buf * 32u;
+            for (int s2 = 0; s2 < 2; ++s2) {
+              if (!mbar_wait_bounded(&afull[stage], phase, abort_flag)) {
+                ok = false;
+                break;
+              }
+              const uint32_t ah = ring_u + stage * STAGE_BYTES;
+              const uint32_t bh = bop_u + (uint32_t)(2 * ch + s2) * 4096u;
+              const uint64_t dah = desc_k(ah, 0), dal = desc_k(ah + A_BYTES, 0);
+              const uint64_t dbh = desc_k(bh, 0), dbl = desc_k(bh + BOP_BYTES, 0);
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
                 // Ut_lo Err1_hi, Ut_hi Err1_lo, Ut_hi Err1_hi: the order of the tensor-core
                 // lazy update's three passes (Err1_hi Ut_lo, Err1_lo Ut_hi, Err1_hi Ut_hi)
-                umma_tf32(dt, desc_k(al, kk), desc_k(bh, kk), IDESC, (s2 > 0 || kk > 0) ? 1u : 0u);
-                umma_tf32(dt, desc_k(ah, kk), desc_k(bl, kk), IDESC, 1u);
-                umma_tf32(dt, desc_k(ah, kk), desc_k(bh, kk), IDESC, 1u);
+                umma_tf32(dt, dal + 2 * kk, dbh + 2 * kk, IDESC, (s2 > 0 || kk > 0) ? 1u : 0u);
+                umma_tf32(dt, dah + 2 * kk, dbl + 2 * kk, IDESC, 1u);
+                umma_tf32(dt, dah + 2 * kk, dbh + 2 * kk, IDESC, 1u);
               }
               umma_commit(&aempty[stage]);
+              issued = true;
+              if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
-            __syncwarp();
-            issued = true;
-            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            if (!ok) break;
+            umma_commit(&tfull[buf]);
+            ++it;
           }
-          if (!ok) break;
-          if (lane == 0) umma_commit(&tfull[buf]);
-          __syncwarp();
-          ++it;
-        }
-      if (!ok) break;
-      if (lane == 0) {
-        if (issued) umma_commit(bop_free);        // arrives when this block's products are done
+        if (!ok) break;
+        if (issued) umma_commit(bop_free);          // arrives when this block's products are done
         else mbar_arrive(bop_free);
+        issued_any |= issued;
       }
-      __syncwarp();
-      issued_any |= issued;
-    }
-    if (!ok && lane == 0 && !*abort_flag) fail();
-    if (issued_any && lane == 0) {
-      umma_commit(drain);
-      mbar_wait_bounded(drain, 0, nullptr);
+      if (!ok && !*abort_flag) fail();
+      if (issued_any) {
+        umma_commit(drain);
+        mbar_wait_bounded(drain, 0, nullptr);
+      }
     }
   } else {
     // ------------------------------------------------------------ tensor-memory epilogue
@@ -1455,7 +1447,7 @@ colmma_kernel(const __grid_constant__ CUtensorMap map_ut, const __grid_constant_
   if (*abort_flag) {
     // A wait gave up: wait (bounded) for the copies still landing in shared memory
     if (warp == COPY_WARP && lane == 0) mbar_wait_bounded(wbar, 0, nullptr);
-    if (warp == 1 && lane < 4) mbar_wait_bounded(&ubar[lane], (uint32_t)*last_diag & 1u, nullptr);
+    if (warp == 1 && lane == 0) mbar_wait_bounded(ubar, (uint32_t)*last_diag & 1u, nullptr);
   }
   if (warp == MMA_WARP) {
     __syncwarp();
@@ -1666,15 +1658,16 @@ gptq_status run_blocks_lanes(CBArgs a, const float* Ut, const float* Ut_lo, cuda
 
 // 2-D map over Ut (d x d fp32, row-major): boxes of 32 k x 128 rows, 128-byte swizzle,
 // rows past d read as zeros
-bool make_ut_map(CUtensorMap* map, const float* base, int d) {
+bool make_ut_map(CUtensorMap* map, const float* base, int d, uint32_t box_inner = 32,
+                 CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)d};
   cuuint64_t strides[1] = {(cuuint64_t)d * 4};
-  cuuint32_t box[2] = {32, 128};
+  cuuint32_t box[2] = {box_inner, 128};
   cuuint32_t es[2] = {1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1686,9 +1679,12 @@ gptq_status run_outer_blocks(CBArgs a, const float* Ut, const float* Ut_lo, cuda
   if (cudaFuncSetAttribute(colmma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Smem::total) !=
       cudaSuccess)
     return set_error(GPTQ_ERR_CUDA, "cudaFuncSetAttribute(colmma_kernel) failed");
-  CUtensorMap mu, mul;
-  if (!make_ut_map(&mu, Ut, a.d) || !make_ut_map(&mul, Ut_lo, a.d))
-    return set_error(GPTQ_ERR_CUDA, "cuTensorMapEncodeTiled failed for Hinv1^T");
+  CUtensorMap mu, mul, mh;
+  // Ut and its low parts: 32-deep k chunks of 128 rows, swizzled for the MMA; Hinv1:
+  // the 128 x 128 diagonal block as plain rows
+  if (!make_ut_map(&mu, Ut, a.d) || !make_ut_map(&mul, Ut_lo, a.d) ||
+      !make_ut_map(&mh, a.U, a.d, 128, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return set_error(GPTQ_ERR_CUDA, "cuTensorMapEncodeTiled failed for Hinv1");
   const int d = a.d;
   const int nrg = (a.m + ROWS_PER_CTA - 1) / ROWS_PER_CTA;
   const int OB = outer_width(BS, a.g, a.stats_given);
@@ -1698,7 +1694,7 @@ gptq_status run_outer_blocks(CBArgs a, const float* Ut, const float* Ut_lo, cuda
     Args p{a, o1, (o2 - o1 + BS - 1) / BS};
     {
       ProfScope ps("quantize.colblock", s);
-      if (launch_pdl(colmma_kernel, dim3(nrg), dim3(THREADS), Smem::total, s, mu, mul, p) != cudaSuccess)
+      if (launch_pdl(colmma_kernel, dim3(nrg), dim3(THREADS), Smem::total, s, mu, mul, mh, p) != cudaSuccess)
         return check_launch("colmma_kernel");
       count_launch();
     }

@@ -114,6 +114,35 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// Non-blocking test of a phase (mbarrier.test_wait never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_wait_bounded by polling with test_wait: for a lone waiting thread whose phase is
+// completed by other threads' plain arrivals (measured: try_wait noticed such a
+// completion microseconds late).
+__device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                               unsigned long long limit_ns = kWaitLimitNs) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((it & 1023u) == 0) {
+      if (abort && *abort) return false;
+      if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+  }
+}
+
 // Wait until *ctr >= target (wrapping compare), reading with acquire semantics at gpu
 // scope; gives up (returns false) after limit_ns.
 __device__ __forceinline__ bool wait_counter_bounded(const unsigned* ctr, unsigned target,
