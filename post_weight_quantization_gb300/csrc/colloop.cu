@@ -1517,6 +1517,7 @@ __global__ void transpose4_kernel(const float* __restrict__ U, float* __restrict
                                   int d) {
   __shared__ float tile[32][33];
   const int bx = blockIdx.x * 32, by = blockIdx.y * 32;
+  if (bx + 31 < by) return;     // Ut rows bx.., columns by..: above the diagonal, never read
   const int r = threadIdx.x >> 3, c4 = (threadIdx.x & 7) * 4;
   float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
   if (by + r < d && bx + c4 < d) v = *reinterpret_cast<const float4*>(U + (long long)(by + r) * d + bx + c4);
@@ -1536,11 +1537,14 @@ __global__ void transpose4_kernel(const float* __restrict__ U, float* __restrict
 }
 
 // Ut = Hinv1^T (the lazy update reads Hinv1's rows as K-major operand columns) and
-// its low parts Ut_lo = Ut - Ut with the 13 low mantissa bits cleared
+// its low parts Ut_lo = Ut - Ut with the 13 low mantissa bits cleared. Hinv1 is upper
+// triangular and every lazy update reads Ut[c][k] with c beyond the k block (the
+// columns right of it), so only the 32 x 32 tiles on and below the diagonal are written.
 __global__ void transpose_kernel(const float* __restrict__ U, float* __restrict__ Ut, float* __restrict__ Ut_lo,
                                  int d) {
   __shared__ float tile[32][33];
   const int bx = blockIdx.x * 32, by = blockIdx.y * 32;
+  if (bx + 31 < by) return;     // Ut rows bx.., columns by..: above the diagonal, never read
   for (int yy = threadIdx.y; yy < 32; yy += 8) {
     const int r = by + yy, c = bx + threadIdx.x;
     tile[yy][threadIdx.x] = (r < d && c < d) ? U[(long long)r * d + c] : 0.0f;

@@ -14,11 +14,16 @@ With ordinary weights the first layer meets the single-layer tolerances (dequant
 weights off the float64 oracle's by more than half a step: at most 0.5%; relative output
 error within 2%). Its few codes that float32 and float64 set differently change the next
 layer's inputs slightly, and GPTQ's code choices are chaotic in their inputs, so the two
-runs drift apart with depth (measured: about 1% of the inputs' norm after two 4-bit
-layers, more at 2 and 3 bits). Later layers are held to the output-error tolerance (within
-2% of the oracle's layer on the oracle's inputs) and the propagated inputs to a bounded
-drift, over three layers at 4 bits g128 and two layers at 3 and 2 bits; the figures are
-recorded.
+runs drift apart with depth: one code in three thousand set differently in a 2-bit layer
+was measured to move the next 2-bit layer's codes in 11% of places and the chain's
+output by 10% of its norm (the Hessian's split sums are added in a varying order, so
+which run meets such a flip varies too). Later layers are held to the output-error
+tolerance (within 2% of the oracle's layer on the oracle's inputs). The propagated
+inputs are held to the distance two valid quantizations of the chain can have: each
+chain's output before layer l is off the unquantized chain's by about the sum of the
+layers' relative output errors, so the two differ by at most twice the oracle's sum
+(DRIFT_SCALE) up to second-order terms. Three layers at 4 bits g128, two at 3 and 2 bits;
+the figures are recorded.
 """
 import numpy as np
 import pytest
@@ -33,7 +38,7 @@ pytestmark = pytest.mark.gpu
 
 CODE_TOL = 0.005
 ERR_RTOL = 0.02
-DRIFT_TOL = 0.05
+DRIFT_SCALE = 2.0
 
 
 @pytest.fixture(scope="module")
@@ -78,6 +83,7 @@ def test_chain_against_sequential_pass(g, bits, gs, act_order, nlayers):
     ref = orc.sequential_pass(bf16_bits_to_f32(X0_bits).astype(np.float64), Ws, bits=bits, group_size=gs,
                               blocksize=128, act_order=act_order)
     layers, inputs, out = gpu_chain(g, X0_bits, W_bits, bits, gs, act_order)
+    err_sum = 0.0                        # the oracle's relative output errors of the layers before
     for li, ((q, perm), res) in enumerate(zip(layers, ref["layers"])):
         m, d = dims[li]
         Xo = ref["inputs"][li]
@@ -89,15 +95,16 @@ def test_chain_against_sequential_pass(g, bits, gs, act_order, nlayers):
         record(f"sequential layer {li + 1} of {nlayers}, {m}x{d} n={n} {bits}b g{gs}{' act-order' if act_order else ''}",
                what_far_fp64=far, mismatch_fp64=np.mean(codes != res["codes"]), err_gpu=e_gpu, err_oracle64=e_orc,
                input_drift=drift)
-        assert drift < DRIFT_TOL, (li, drift)
+        assert drift <= DRIFT_SCALE * err_sum, (li, drift, err_sum)
         if li == 0:
             assert drift == 0.0                   # the same bf16 tokens
             assert far <= CODE_TOL, far
         assert abs(e_gpu - e_orc) <= ERR_RTOL * e_orc, (li, e_gpu, e_orc)
+        err_sum += e_orc
     yo = orc.round_to_bf16(ref["output"])
     drift_out = np.linalg.norm(bf16_values(out) - yo) / np.linalg.norm(yo)
     record(f"sequential chain output, {bits}b g{gs}{' act-order' if act_order else ''}", input_drift=drift_out)
-    assert drift_out < DRIFT_TOL
+    assert drift_out <= DRIFT_SCALE * err_sum, (drift_out, err_sum)
 
 
 def on_grid_weight(m, d, bits, gs, rng):
