@@ -133,7 +133,7 @@ __device__ __forceinline__ float rcp_rn(float s) {
 __device__ __forceinline__ void group_params(float mn, float mx, float qmax, float inv_qmax, float& s, float& inv_s,
                                              float& z) {
   s = fmaxf(div_mk(__fsub_rn(mx, mn), qmax, inv_qmax), 1e-8f);
-  inv_s = rcp_rn(s);
+  inv_s = __frcp_rn(s);        // the correctly rounded reciprocal, as rcp_rn, without fp64 steps
   z = fminf(fmaxf(rintf(div_mk(-mn, s, inv_s)), 0.0f), qmax);
 }
 
@@ -1049,6 +1049,13 @@ colmma_kernel(const __grid_constant__ CUtensorMap map_ut, const __grid_constant_
     const float inv_qmax = rcp_rn(qmax);
     const int r = r0 + lane;
     const bool active = r < a.m;
+    // per-channel statistics (precomputed, one group per row): read once, not per block
+    float s_row = 1.0f, z_row = 0.0f;
+    if (warp == 0 && a.stats_given && active) {
+      s_row = a.scales[(long long)r * a.G];
+      z_row = a.zeros[(long long)r * a.G];
+    }
+    const float inv_s_row = rcp_rn(s_row);
     for (int b = 0; b < nb; ++b) {
       const int i1 = o1 + BS * b, ncols = ncols_of(b), nq = ncols >> 2;
       const uint32_t par = (uint32_t)b & 1u;
@@ -1058,25 +1065,24 @@ colmma_kernel(const __grid_constant__ CUtensorMap map_ut, const __grid_constant_
                                                   : mbar_wait_bounded(wready, (uint32_t)(b - 1) & 1u, abort_flag));
       if (ok && warp == 0) {
         // ---- the chain: row `lane`'s dependent sequence, once per column
-        float s = 1.0f, inv_s = 1.0f, z = 0.0f;
-        if (a.stats_given || (i1 % a.g) != 0) {
-          if (active) {
-            s = a.scales[(long long)r * a.G + i1 / a.g];
-            z = a.zeros[(long long)r * a.G + i1 / a.g];
+        float s = s_row, inv_s = inv_s_row, z = z_row;
+        const bool group_start = !a.stats_given;         // groups of 128: every block starts one
+        if (group_start) {
+          // min and max of the row over the block, four independent running values
+          float mn4[4] = {INFINITY, INFINITY, INFINITY, INFINITY}, mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 2
+          for (int c = 0; c < ncols; c += 16) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              if (c + 4 * u < ncols) {
+                const float4 v = *reinterpret_cast<const float4*>(Ws + lane * WLD + c + 4 * u);
+                mn4[u] = fminf(mn4[u], fminf(fminf(v.x, v.y), fminf(v.z, v.w)));
+                mx4[u] = fmaxf(mx4[u], fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+              }
           }
-          inv_s = rcp_rn(s);
-        } else {
-          float mn = INFINITY, mx = -INFINITY;
-          for (int c = 0; c < ncols; c += 4) {
-            const float4 v = *reinterpret_cast<const float4*>(Ws + lane * WLD + c);
-            mn = fminf(fminf(mn, v.x), fminf(fminf(v.y, v.z), v.w));
-            mx = fmaxf(fmaxf(mx, v.x), fmaxf(fmaxf(v.y, v.z), v.w));
-          }
+          const float mn = fminf(fminf(mn4[0], mn4[1]), fminf(mn4[2], mn4[3]));
+          const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
           group_params(mn, mx, qmax, inv_qmax, s, inv_s, z);
-          if (active) {
-            a.scales[(long long)r * a.G + i1 / a.g] = s;
-            a.zeros[(long long)r * a.G + i1 / a.g] = z;
-          }
         }
         float cur[4], nxt[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f}, e2[4] = {0.f, 0.f, 0.f, 0.f};
         {
@@ -1131,6 +1137,13 @@ colmma_kernel(const __grid_constant__ CUtensorMap map_ut, const __grid_constant_
             e1[k] = ec[k];
             cur[k] = nxt[k];
           }
+        }
+        // the group's scale and zero leave after the block's chain: a global store issued
+        // before it stalled the chain's start while the epilogue warps' stores filled the
+        // memory pipeline
+        if (group_start && active) {
+          a.scales[(long long)r * a.G + i1 / BS] = s;
+          a.zeros[(long long)r * a.G + i1 / BS] = z;
         }
       } else if (ok) {
         // ---- update warps: quads FIRST_UPD + u, + NUPD, ... of the row in registers

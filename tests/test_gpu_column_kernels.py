@@ -40,8 +40,12 @@ for (m, d, n, bits, gs, ao, seed) in CASES:
 print(json.dumps(out))
 """
 
+# (m, d, tokens, bits, group, act-order, seed): ragged rows (300, 33, 1), a ragged last
+# block (d = 1000), an outer block of one block (d = 1408 = 640 + 640 + 128), one row,
+# per-channel and act-order, and the 4096-square layer
 CASES = [(544, 1024, 8192, 4, 128, False, 3), (520, 1280, 4096, 2, 128, False, 4), (300, 1000, 4096, 3, -1, False, 5),
-         (544, 1024, 8192, 4, 128, True, 6), (4096, 4096, 16384, 4, 128, False, 7)]
+         (544, 1024, 8192, 4, 128, True, 6), (4096, 4096, 16384, 4, 128, False, 7), (1, 256, 512, 4, 128, False, 8),
+         (33, 384, 1024, 8, 128, False, 9), (96, 1408, 2048, 4, 128, False, 10)]
 
 
 def run_child(env_extra):
