@@ -135,7 +135,8 @@ size_t gptq_workspace_size(int which, int64_t m, int64_t d, int bits, int group_
  *              NULL).
  *   Hinv1      device fp32, d x d, leading dimension d. Receives U with
  *              H_d^-1 = U^T U, U upper triangular with a positive diagonal; the
- *              strictly lower triangle is set to zero.
+ *              strictly lower triangle is set to zero. Its previous contents are
+ *              never read; after a failed factorization they are unspecified.
  *   ws         device workspace of gptq_workspace_size(GPTQ_WS_FACTOR, 0, d, ...)
  *              bytes.
  *   info       host pointer or NULL. When non-NULL the call synchronizes `stream`

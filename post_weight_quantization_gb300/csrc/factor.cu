@@ -542,6 +542,8 @@ __global__ void __launch_bounds__(PANEL_THREADS, 2) chol_panel_kernel(float* __r
 // P[k0 + i][k0 + c] = Lsave[k0 + i][k0 + c] for the lower triangle of every diagonal
 // block (blockIdx.y = block, 8 rows per CTA in x)
 __global__ void place_diag_kernel(float* __restrict__ P, const float* __restrict__ Lsave, int d, const Header* hdr) {
+  grid_dep_wait();              // launched behind the kernel that wrote its inputs
+  grid_dep_launch();
   if (hdr->failed) return;
   const int k0 = blockIdx.y * NB;
   const int nb = min(NB, d - k0);
@@ -571,6 +573,8 @@ __global__ void __launch_bounds__(64) diag_inverse_kernel(const float* __restric
                                                           const Header* hdr) {
   __shared__ float L[NBI][NBI + 1];
   __shared__ float invd[NBI];
+  grid_dep_wait();              // launched behind the kernel that wrote its inputs
+  grid_dep_launch();
   if (hdr->failed) return;
   const int k0 = blockIdx.x * NBI;
   const int nb = min(NBI, d - k0);
@@ -596,14 +600,11 @@ __global__ void __launch_bounds__(64) diag_inverse_kernel(const float* __restric
   }
 }
 
-__global__ void zero_kernel(float* __restrict__ M, long long n) {
-  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n; idx += (long long)gridDim.x * blockDim.x)
-    M[idx] = 0.0f;
-}
-
 // In place: M[a][b] <-> M[d-1-a][d-1-b], then the strict lower triangle cleared: turns
 // X = L^-1 (lower, with its transpose stored above) into J X J (upper, lower zero).
 __global__ void reverse_kernel(float* __restrict__ M, int d, const Header* hdr) {
+  grid_dep_wait();              // launched behind the kernel that wrote its inputs
+  grid_dep_launch();
   if (hdr->failed) return;
   const long long n = (long long)d * d;
   for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n / 2;
@@ -619,6 +620,8 @@ __global__ void reverse_kernel(float* __restrict__ M, int d, const Header* hdr) 
 // The same for d % 4 == 0 and a 16-byte aligned M: elements idx .. idx + 3 (one row) swap
 // with the 16-byte piece at n - 4 - idx, which holds their partners in reverse order.
 __global__ void reverse4_kernel(float* __restrict__ M, int d, const Header* hdr) {
+  grid_dep_wait();              // launched behind the kernel that wrote its inputs
+  grid_dep_launch();
   if (hdr->failed) return;
   const long long n = (long long)d * d;
   float4* M4 = reinterpret_cast<float4*>(M);
@@ -640,6 +643,8 @@ __global__ void reverse4_kernel(float* __restrict__ M, int d, const Header* hdr)
 __global__ void pair_transpose_kernel(float* __restrict__ M, int d, int sz, int np, int c_last,
                                       const Header* hdr) {
   __shared__ float tile[32][33];
+  grid_dep_wait();              // launched behind the product that wrote its input
+  grid_dep_launch();
   if (hdr->failed) return;
   const int z = blockIdx.z;
   const int a0 = 2 * z * sz, c0 = a0 + sz;
@@ -752,12 +757,20 @@ gptq_status factor_launch(const float* H, long long d_, float percdamp, int act_
   // ---- X = L^-1 in natural order inside Hinv1: diagonal blocks, then recursive doubling
   {
     ProfScope ps("factor.zero_diag_inverse", s);
-    place_diag_kernel<<<dim3(NB / 8, (unsigned)((d + NB - 1) / NB)), dim3(32, 8), 0, s>>>(P, Hinv1, d, hdr);
+    if (launch_pdl(place_diag_kernel, dim3(NB / 8, (unsigned)((d + NB - 1) / NB)), dim3(32, 8), 0, s, P,
+                   (const float*)Hinv1, d, (const Header*)hdr) != cudaSuccess)
+      return check_launch("place_diag_kernel");
     count_launch();
-    zero_kernel<<<std::max(1, std::min(4096, (int)(((long long)d * d + 255) / 256))), 256, 0, s>>>(Hinv1, (long long)d * d);
-    diag_inverse_kernel<<<(d + NBI - 1) / NBI, NBI, 0, s>>>(P, Hinv1, d, hdr);
+    // No clearing pass: every element of Hinv1 is written below before anything reads
+    // it (the diagonal blocks whole, then at every level each pair's X block below the
+    // diagonal and its transpose above), and the masked triangles of the products'
+    // operands are replaced by zeros, not multiplied, so what the buffer held is never
+    // used.
+    if (launch_pdl(diag_inverse_kernel, dim3((d + NBI - 1) / NBI), dim3(NBI), 0, s, (const float*)P, Hinv1, d,
+                   (const Header*)hdr) != cudaSuccess)
+      return check_launch("diag_inverse_kernel");
   }
-  count_launch(2);
+  count_launch();
   // Doubling over block pairs (A, C) = ([2p sz, 2p sz + sz), [2p sz + sz, ...)): with
   // X = L^-1 kept below the diagonal of Hinv1 and Y = X^T above it (shared diagonal),
   //   T = Y[A][A] L[C][A]^T           (= (L[C][A] X[A][A])^T, into P's unused upper part)
@@ -798,16 +811,20 @@ gptq_status factor_launch(const float* H, long long d_, float percdamp, int act_
     g2.skip = failed;
     if (gptq_status st = tc_gemm(g2, np, true, true, s)) return st;
     dim3 tg((unsigned)((sz + 31) / 32), (unsigned)((sz + 31) / 32), (unsigned)np);
-    pair_transpose_kernel<<<tg, dim3(32, 8), 0, s>>>(Hinv1, d, sz, np, c_last, hdr);
+    if (launch_pdl(pair_transpose_kernel, tg, dim3(32, 8), 0, s, Hinv1, d, sz, np, c_last, (const Header*)hdr) !=
+        cudaSuccess)
+      return check_launch("pair_transpose_kernel");
     count_launch();
   }
   ProfScope ps_rev("factor.reverse", s);
-  if (vec)
-    reverse4_kernel<<<std::max(1, std::min(4096, (int)(((long long)d * d / 8 + 255) / 256))), 256, 0, s>>>(Hinv1, d,
-                                                                                                         hdr);
-  else
-    reverse_kernel<<<std::max(1, std::min(4096, (int)(((long long)d * d / 2 + 255) / 256))), 256, 0, s>>>(Hinv1, d,
-                                                                                                        hdr);
+  {
+    const bool v4 = vec;
+    const long long work = v4 ? (long long)d * d / 8 : (long long)d * d / 2;
+    const dim3 grid((unsigned)std::max(1, std::min(4096, (int)((work + 255) / 256))));
+    if (launch_pdl(v4 ? reverse4_kernel : reverse_kernel, grid, dim3(256), 0, s, Hinv1, d, (const Header*)hdr) !=
+        cudaSuccess)
+      return check_launch("reverse_kernel");
+  }
   count_launch();
   return check_launch("triangular-inverse kernels");
 }

@@ -178,8 +178,11 @@ def _spd(d, n, seed):
 def test_factor_matches_three_step_chain(g, d, n):
     H = _spd(d, n, seed=d)
     Hg = torch.from_numpy(H.astype(np.float32)).cuda()
-    U, _, info = g.gptq_factor(Hg, percdamp=0.01)
+    # the output buffer starts as NaN: the factor must write every element it leaves
+    U0 = torch.full((d, d), float("nan"), dtype=torch.float32, device="cuda")
+    U, _, info = g.gptq_factor(Hg, percdamp=0.01, Hinv1=U0)
     assert info == -1
+    assert U.data_ptr() == U0.data_ptr() and bool(torch.isfinite(U).all())
     Ug = U.cpu().numpy().astype(np.float64)
     Hd, _ = orc.damp(H.astype(np.float32).astype(np.float64), 0.01)
     Uo = orc.hinv1(Hd)
