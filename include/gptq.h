@@ -16,7 +16,9 @@
  * Conventions shared by every call:
  *   - Pointers to matrices are DEVICE pointers owned by the caller. The library
  *     allocates no memory: scratch comes from a caller-provided device workspace
- *     whose size gptq_workspace_size() returns.
+ *     whose size gptq_workspace_size() returns. The one exception is the
+ *     host-buffer pipeline (gptq_pipeline_*), which takes HOST pointers and owns
+ *     the device buffers it copies into.
  *   - Matrices are row-major with an explicit leading dimension in elements.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL means the legacy default
  *     stream) and runs asynchronously, except where a call documents a
@@ -312,6 +314,72 @@ gptq_status gptq_dequant_gemm(const uint32_t* qweight, const float* scales, cons
                               int64_t m, int64_t d, int bits, int group_size, const uint16_t* X,
                               int64_t T, int64_t ldx, void* Y, int y_bf16, int64_t ldy, void* ws,
                               size_t ws_bytes, gptq_stream_t stream);
+
+/*
+ * One layer end to end from HOST memory ("The GPTQ Algorithm", procedure steps 2-4 for
+ * one layer: the Hessian over the calibration batches, then the factor and the column
+ * loop; "GPTQ-style round-to-nearest with Hessian weighting", section "Computing the
+ * Hessian": H accumulated batch by batch). The tokens are copied to the GPU in chunks
+ * on the pipeline's own copy stream while the Hessian of the previous chunk runs on
+ * the caller's stream (two device chunk buffers in turn); W follows the last chunk;
+ * then gptq_factor and gptq_quantize_layer run, and the outputs are copied back to
+ * the caller's host buffers. Results equal those of the three device calls in a row
+ * on the same data (H = 2 X^T X).
+ *
+ * Unlike the calls above, a pipeline OWNS device memory: gptq_pipeline_create makes,
+ * on the current device, one allocation holding the two chunk buffers, W, H, Hinv1,
+ * the permutation, both workspaces and the outputs, plus a copy stream and its
+ * events. gptq_pipeline_run allocates nothing; gptq_pipeline_destroy frees all of it.
+ *
+ *   m, d, w_dtype, bits, group_size, blocksize, percdamp, act_order
+ *                   as for gptq_factor and gptq_quantize_layer; d a multiple of 8.
+ *   chunk_tokens    tokens per device chunk buffer, 1 <= chunk_tokens <= 2^24 (each
+ *                   buffer holds chunk_tokens x d bf16 values).
+ *   out             receives the pipeline; *out = NULL on failure.
+ * Errors: GPTQ_ERR_INVALID_ARG / GPTQ_ERR_UNSUPPORTED for settings gptq_quantize_layer
+ * would refuse, GPTQ_ERR_CUDA when the allocation or a stream or event fails (nothing
+ * is kept then).
+ */
+typedef struct gptq_pipeline gptq_pipeline;
+
+gptq_status gptq_pipeline_create(int64_t m, int64_t d, int w_dtype, int bits, int group_size,
+                                 int blocksize, float percdamp, int act_order,
+                                 int64_t chunk_tokens, gptq_pipeline** out);
+
+/*
+ * Enqueues one layer on `stream` (and the pipeline's copy stream) and returns without
+ * waiting. All buffers here are HOST memory; page-locked buffers let the copies overlap
+ * the Hessian (pageable ones work, with copies that do not overlap).
+ *
+ *   W            host, m x d row-major, row stride ldw >= d, type of w_dtype.
+ *   X            host bf16 bits, n x d token-major, row stride ldx >= d; n >= 0.
+ *   qweight, scales, zeros, col_losses
+ *                host outputs laid out as gptq_quantize_layer's.
+ *   perm         host int32[d] receiving the column order when the pipeline was made
+ *                with act_order (may be NULL to skip it); ignored otherwise.
+ * Every buffer must stay valid, and the outputs unread, until `stream` has been
+ * synchronized. Runs on one pipeline are ordered: a run's copies wait for the previous
+ * run's work, whatever streams they were given. The pipeline must be used on the
+ * device it was made on (GPTQ_ERR_INVALID_ARG otherwise). The outcome of the factor
+ * and of the column loop (not positive definite, non-finite W) is read afterwards with
+ * gptq_pipeline_status; after a failed factor the outputs are unspecified.
+ */
+gptq_status gptq_pipeline_run(gptq_pipeline* p, const void* W, int64_t ldw, const uint16_t* X,
+                              int64_t n, int64_t ldx, uint32_t* qweight, float* scales,
+                              float* zeros, float* col_losses, int32_t* perm,
+                              gptq_stream_t stream);
+
+/*
+ * Outcome of the last gptq_pipeline_run: synchronizes `stream`, then returns the
+ * factor's status (with *info as gptq_factor sets it) or, when the factor succeeded,
+ * the column loop's (GPTQ_ERR_NONFINITE with *info = 1 for a NaN or Inf in W); *info = -1
+ * when both succeeded. info may be NULL.
+ */
+gptq_status gptq_pipeline_status(gptq_pipeline* p, int64_t* info, gptq_stream_t stream);
+
+/* Waits for the pipeline's work, then frees its device memory, streams and events.
+ * NULL is accepted. */
+gptq_status gptq_pipeline_destroy(gptq_pipeline* p);
 
 /*
  * Helper for checks: C = beta * C + alpha * A B (fp32, single batch) with the GEMM the

@@ -21,6 +21,8 @@ namespace gptq {
 gptq_status set_error(gptq_status st, const char* fmt, ...);
 void clear_error();   // empty this thread's last-error text (every entry point starts with it)
 void count_launch(int n = 1);
+// The settings gptq_quantize_layer accepts (sizes, dtype, bits, group and block widths).
+gptq_status check_quantize_settings(long long m, long long d, int w_dtype, int bits, int group_size, int blocksize);
 
 // Opt-in launch timing (environment variable GPTQ_PROFILE=1): a ProfScope records a
 // CUDA event pair around the launches it encloses, on their stream; per-name totals

@@ -150,6 +150,24 @@ int* device_error_word() {
   return g_err_addr[dev];
 }
 
+gptq_status check_quantize_settings(long long m, long long d, int w_dtype, int bits, int group_size, int blocksize) {
+  if (m < 1 || m > (1LL << 30) || d < 1 || d > 65536 || m * d > (1LL << 36))
+    return set_error(GPTQ_ERR_INVALID_ARG, "m or d out of range");
+  if (w_dtype != 0 && w_dtype != 1) return set_error(GPTQ_ERR_INVALID_ARG, "w_dtype must be 0 (fp32) or 1 (bf16)");
+  if (bits != 2 && bits != 3 && bits != 4 && bits != 8) return set_error(GPTQ_ERR_INVALID_ARG, "bits must be 2, 3, 4 or 8");
+  if (blocksize < 1 || blocksize > 256) return set_error(GPTQ_ERR_INVALID_ARG, "blocksize must be in [1, 256]");
+  if (group_size != -1) {
+    if (group_size < 1 || d % group_size) return set_error(GPTQ_ERR_INVALID_ARG, "d must be a multiple of group_size");
+    if (group_size % blocksize && blocksize % group_size)
+      return set_error(GPTQ_ERR_INVALID_ARG, "group_size and blocksize must divide one another");
+  }
+  if (blocksize != 32 && blocksize != 64 && blocksize != 128)
+    return set_error(GPTQ_ERR_UNSUPPORTED, "this build runs blocksize 32, 64 or 128");
+  if (group_size != -1 && group_size % 32)
+    return set_error(GPTQ_ERR_UNSUPPORTED, "this build runs group sizes that are multiples of 32 (or -1)");
+  return GPTQ_OK;
+}
+
 // ---- self-test of the bounded waits ----
 namespace {
 __device__ unsigned g_selftest_counter = 0;   // nothing ever publishes on it
@@ -309,21 +327,8 @@ gptq_status gptq_quantize_layer(const void* W, int w_dtype, int64_t m, int64_t d
   g_last_error[0] = 0;
   if (!W || !Hinv1 || !qweight || !scales || !zeros || !col_losses || !ws)
     return set_error(GPTQ_ERR_INVALID_ARG, "a required pointer is NULL");
-  if (m < 1 || m > (int64_t)1 << 30 || d < 1 || d > 65536 || m * d > ((int64_t)1 << 36))
-    return set_error(GPTQ_ERR_INVALID_ARG, "m or d out of range");
+  if (gptq_status st = check_quantize_settings(m, d, w_dtype, bits, group_size, blocksize)) return st;
   if (ldw < d) return set_error(GPTQ_ERR_INVALID_ARG, "ldw < d");
-  if (w_dtype != 0 && w_dtype != 1) return set_error(GPTQ_ERR_INVALID_ARG, "w_dtype must be 0 (fp32) or 1 (bf16)");
-  if (bits != 2 && bits != 3 && bits != 4 && bits != 8) return set_error(GPTQ_ERR_INVALID_ARG, "bits must be 2, 3, 4 or 8");
-  if (blocksize < 1 || blocksize > 256) return set_error(GPTQ_ERR_INVALID_ARG, "blocksize must be in [1, 256]");
-  if (group_size != -1) {
-    if (group_size < 1 || d % group_size) return set_error(GPTQ_ERR_INVALID_ARG, "d must be a multiple of group_size");
-    if (group_size % blocksize && blocksize % group_size)
-      return set_error(GPTQ_ERR_INVALID_ARG, "group_size and blocksize must divide one another");
-  }
-  if (blocksize != 32 && blocksize != 64 && blocksize != 128)
-    return set_error(GPTQ_ERR_UNSUPPORTED, "this build runs blocksize 32, 64 or 128");
-  if (group_size != -1 && group_size % 32)
-    return set_error(GPTQ_ERR_UNSUPPORTED, "this build runs group sizes that are multiples of 32 (or -1)");
   if (!aligned(ws, 256)) return set_error(GPTQ_ERR_INVALID_ARG, "ws must be 256-byte aligned");
   const size_t need = quantize_workspace_bytes(m, d, blocksize);
   if (ws_bytes < need) return set_error(GPTQ_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", ws_bytes, need);

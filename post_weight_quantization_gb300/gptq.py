@@ -56,6 +56,11 @@ SIGNATURES = {
     "gptq_wait_selftest": (_c_int, [_c_int, _c_i64, _vp]),
     "gptq_dequant_gemm": (_c_int, [_vp, _vp, _vp, _c_i64, _c_i64, _c_int, _c_int, _vp, _c_i64, _c_i64, _vp, _c_int,
                                    _c_i64, _vp, _c_size, _vp]),
+    "gptq_pipeline_create": (_c_int, [_c_i64, _c_i64, _c_int, _c_int, _c_int, _c_int, _c_float, _c_int, _c_i64,
+                                      ctypes.POINTER(_vp)]),
+    "gptq_pipeline_run": (_c_int, [_vp, _vp, _c_i64, _vp, _c_i64, _c_i64, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "gptq_pipeline_status": (_c_int, [_vp, ctypes.POINTER(_c_i64), _vp]),
+    "gptq_pipeline_destroy": (_c_int, [_vp]),
 }
 
 
@@ -451,99 +456,79 @@ def sequential_quantize(X0: torch.Tensor, weights, bits: int = 4, group_size: in
     return layers, inputs, X
 
 
-def token_pieces(n: int, chunk: int):
-    """Token ranges for HostPipeline: chunks of `chunk` tokens, the last one cut in four
-    (when it has at least 4096 tokens), so the Hessian of the final piece, the one step
-    that no copy overlaps, is short."""
-    out, t0 = [], 0
-    while t0 < n:
-        t1 = min(n, t0 + chunk)
-        if t1 == n and t1 - t0 >= 4096:
-            q = (t1 - t0) // 4
-            out += [(t0 + k * q, t0 + (k + 1) * q if k < 3 else t1) for k in range(4)]
-        else:
-            out.append((t0, t1))
-        t0 = t1
-    return out
-
-
 class HostPipeline:
-    """End-to-end quantization of one layer from host (pinned) buffers.
+    """End-to-end quantization of one layer from host buffers, over the library's native
+    pipeline (gptq_pipeline_create / _run / _status / _destroy).
 
-    The calibration tokens are copied to the GPU in chunks on a copy stream while the
-    Hessian accumulates the previous chunk on the compute stream (two device chunk
-    buffers, ping-pong), then W is copied, the factor and the column loop run, and
-    the packed codes, scales, zeros and per-column losses are copied back. Device
-    buffers are allocated once per shape and reused across calls.
+    The library streams the calibration tokens to the GPU in chunks on its own copy
+    stream while the Hessian accumulates the chunk before on the caller's stream (two
+    device chunk buffers in turn), copies W, runs the factor and the column loop, and
+    copies the packed codes, scales, zeros, per-column losses (and the act-order
+    permutation) back into the pinned host tensors held here. Its device memory is one
+    allocation made at construction and reused by every run.
     """
 
     def __init__(self, m: int, d: int, bits: int = 4, group_size: int = 128, blocksize: int = 128,
                  percdamp: float = 0.01, act_order: bool = False, chunk_tokens: int = 32768,
                  w_dtype=torch.bfloat16, device="cuda"):
+        if w_dtype not in (torch.float32, torch.bfloat16):
+            raise TypeError("w_dtype must be torch.float32 or torch.bfloat16")
         self.m, self.d, self.bits, self.group_size, self.blocksize = m, d, bits, group_size, blocksize
-        self.percdamp, self.act_order, self.chunk = percdamp, act_order, chunk_tokens
-        dev = torch.device(device)
-        self.xbuf = [torch.empty((chunk_tokens, d), dtype=torch.int16, device=dev) for _ in range(2)]
-        self.W = torch.empty((m, d), dtype=w_dtype, device=dev)
-        self.H = torch.empty((d, d), dtype=torch.float32, device=dev)
-        self.Hinv1 = torch.empty((d, d), dtype=torch.float32, device=dev)
-        self.perm = torch.empty(d, dtype=torch.int32, device=dev) if act_order else None
-        self.ws_f = _workspace(gptq_workspace_size(GPTQ_WS_FACTOR, 0, d), dev)
-        self.ws_q = _workspace(gptq_workspace_size(GPTQ_WS_QUANTIZE, m, d, bits, group_size, blocksize), dev)
+        self.percdamp, self.act_order, self.chunk, self.w_dtype = percdamp, act_order, chunk_tokens, w_dtype
+        self.device = torch.device(device)
+        self._h = None
+        h = _vp()
+        with torch.cuda.device(self.device):
+            _check(_lib.gptq_pipeline_create(m, d, 1 if w_dtype == torch.bfloat16 else 0, bits, group_size, blocksize,
+                                             float(percdamp), 1 if act_order else 0, chunk_tokens, ctypes.byref(h)),
+                   "gptq_pipeline_create")
+        self._h = h
         G = 1 if group_size == -1 else d // group_size
-        self.out = QuantizedLayer(
-            qweight=torch.empty((m, (d * bits + 31) // 32), dtype=torch.int32, device=dev),
-            scales=torch.empty((m, G), dtype=torch.float32, device=dev),
-            zeros=torch.empty((m, G), dtype=torch.float32, device=dev),
-            col_losses=torch.empty(d, dtype=torch.float32, device=dev),
-            bits=bits, group_size=group_size, d=d)
         self.host_out = QuantizedLayer(
-            qweight=torch.empty(self.out.qweight.shape, dtype=torch.int32, pin_memory=True),
-            scales=torch.empty(self.out.scales.shape, dtype=torch.float32, pin_memory=True),
-            zeros=torch.empty(self.out.zeros.shape, dtype=torch.float32, pin_memory=True),
+            qweight=torch.empty((m, (d * bits + 31) // 32), dtype=torch.int32, pin_memory=True),
+            scales=torch.empty((m, G), dtype=torch.float32, pin_memory=True),
+            zeros=torch.empty((m, G), dtype=torch.float32, pin_memory=True),
             col_losses=torch.empty(d, dtype=torch.float32, pin_memory=True),
             bits=bits, group_size=group_size, d=d)
-        self.copy_stream = torch.cuda.Stream(device=dev)
-        self.copied = [torch.cuda.Event() for _ in range(2)]
-        self.consumed = [torch.cuda.Event() for _ in range(2)]
-        self.w_copied = torch.cuda.Event()
+        self.perm = torch.empty(d, dtype=torch.int32, pin_memory=True) if act_order else None
+
+    def __del__(self):
+        if getattr(self, "_h", None) is not None:
+            _lib.gptq_pipeline_destroy(self._h)
+            self._h = None
 
     def bytes_h2d(self, n_tokens: int) -> int:
-        return n_tokens * self.d * 2 + self.W.numel() * self.W.element_size()
+        return n_tokens * self.d * 2 + self.m * self.d * (2 if self.w_dtype == torch.bfloat16 else 4)
 
     def bytes_d2h(self) -> int:
-        o = self.out
-        return sum(t.numel() * t.element_size() for t in (o.qweight, o.scales, o.zeros, o.col_losses))
+        o = self.host_out
+        n = sum(t.numel() * t.element_size() for t in (o.qweight, o.scales, o.zeros, o.col_losses))
+        return n + (self.d * 4 if self.act_order else 0)
 
     def run(self, W_host: torch.Tensor, X_host: torch.Tensor, stream=None) -> QuantizedLayer:
-        """W_host (m x d, pinned, dtype of the pipeline), X_host (n x d bf16 bits as int16,
-        pinned). Returns host tensors; synchronize the stream before reading them."""
-        comp = torch.cuda.current_stream() if stream is None else stream
-        n = X_host.shape[0]
-        first = True
-        self.copy_stream.wait_stream(comp)          # earlier work on the caller's stream first
-        for c, (t0, t1) in enumerate(token_pieces(n, self.chunk)):
-            b = c & 1
-            buf = self.xbuf[b][: t1 - t0]
-            with torch.cuda.stream(self.copy_stream):
-                if c >= 2:
-                    self.copy_stream.wait_event(self.consumed[b])
-                buf.copy_(X_host[t0:t1], non_blocking=True)
-                self.copied[b].record(self.copy_stream)
-            comp.wait_event(self.copied[b])
-            gptq_hessian_accumulate(buf, self.H, alpha=2.0, zero_first=first, stream=comp)
-            self.consumed[b].record(comp)
-            first = False
-        with torch.cuda.stream(self.copy_stream):       # W behind the last token chunk
-            self.W.copy_(W_host, non_blocking=True)
-            self.w_copied.record(self.copy_stream)
-        gptq_factor(self.H, percdamp=self.percdamp, act_order=self.act_order, Hinv1=self.Hinv1, perm_out=self.perm,
-                    ws=self.ws_f, sync=False, stream=comp)
-        comp.wait_event(self.w_copied)
-        gptq_quantize_layer(self.W, self.Hinv1, self.perm, bits=self.bits, group_size=self.group_size,
-                            blocksize=self.blocksize, out=self.out, ws=self.ws_q, stream=comp)
-        with torch.cuda.stream(comp):
-            for src, dst in ((self.out.qweight, self.host_out.qweight), (self.out.scales, self.host_out.scales),
-                             (self.out.zeros, self.host_out.zeros), (self.out.col_losses, self.host_out.col_losses)):
-                dst.copy_(src, non_blocking=True)
-        return self.host_out
+        """W_host (m x d host tensor of the pipeline's dtype), X_host (n x d bf16 bits as
+        int16, host); both row-major with unit column stride (any row stride), pinned
+        for the copies to overlap the Hessian. Returns the host output tensors; they
+        are complete once the stream has been synchronized (check() reads the outcome)."""
+        for t, name in ((W_host, "W_host"), (X_host, "X_host")):
+            if t.is_cuda or t.dim() != 2 or t.shape[1] != self.d or t.stride(1) != 1:
+                raise ValueError(f"{name} must be a host tensor (rows, {self.d}) with unit column stride")
+        if W_host.dtype != self.w_dtype or W_host.shape[0] != self.m:
+            raise ValueError(f"W_host must be ({self.m}, {self.d}) {self.w_dtype}")
+        if X_host.dtype not in (torch.int16, torch.bfloat16):
+            raise TypeError("X_host must hold bf16 bits (torch.int16 or torch.bfloat16)")
+        o = self.host_out
+        with torch.cuda.device(self.device):
+            _check(_lib.gptq_pipeline_run(self._h, W_host.data_ptr(), W_host.stride(0), X_host.data_ptr(),
+                                          X_host.shape[0], X_host.stride(0), o.qweight.data_ptr(),
+                                          o.scales.data_ptr(), o.zeros.data_ptr(), o.col_losses.data_ptr(),
+                                          _ptr(self.perm), _stream(stream)), "gptq_pipeline_run")
+        return o
+
+    def check(self, stream=None) -> int:
+        """Synchronize the stream and raise GPTQError if the last run's factor or column
+        loop failed; returns info (-1 on success)."""
+        info = _c_i64(0)
+        with torch.cuda.device(self.device):
+            _check(_lib.gptq_pipeline_status(self._h, ctypes.byref(info), _stream(stream)), "gptq_pipeline_status")
+        return int(info.value)

@@ -127,17 +127,32 @@ def test_unpack_argument_checks(g):
     assert lib.gptq_unpack_codes(P, 4, 4, 5, P, None) == g.GPTQ_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("n,chunk", [(262144, 32768), (100, 32768), (5000, 4096), (8192, 4096), (0, 64)])
-def test_host_pipeline_token_pieces(g, n, chunk):
-    pieces = g.token_pieces(n, chunk)
-    # contiguous cover of [0, n), no piece longer than a chunk
-    assert [a for a, _ in pieces[1:]] == [b for _, b in pieces[:-1]]
-    assert (pieces[0][0], pieces[-1][1]) == (0, n) if n else pieces == []
-    assert all(0 < b - a <= chunk for a, b in pieces)
-    # a last chunk of at least 4096 tokens is cut in four
-    last = n - ((n - 1) // chunk) * chunk if n else 0
-    if last >= 4096:
-        assert len(pieces) == (n - last) // chunk + 4
+def test_host_pipeline_argument_checks(g):
+    """gptq_pipeline_create refuses the settings gptq_quantize_layer refuses, and a bad
+    chunk size, before it allocates or launches anything; the other pipeline calls
+    refuse a NULL pipeline (destroy accepts it)."""
+    lib = g.library()
+    before = g.gptq_launch_count()
+    out = ctypes.c_void_p(P)
+
+    def create(m=64, d=256, dt=1, bits=4, gs=128, bs=128, damp=0.01, ao=0, chunk=1024, o=True):
+        return lib.gptq_pipeline_create(m, d, dt, bits, gs, bs, damp, ao, chunk, ctypes.byref(out) if o else None)
+
+    assert create(o=False) == g.GPTQ_ERR_INVALID_ARG
+    assert create(bits=5) == g.GPTQ_ERR_INVALID_ARG and out.value is None
+    assert create(dt=2) == g.GPTQ_ERR_INVALID_ARG
+    assert create(m=0) == g.GPTQ_ERR_INVALID_ARG
+    assert create(d=12, gs=-1) == g.GPTQ_ERR_INVALID_ARG        # d a multiple of 8
+    assert create(gs=100) == g.GPTQ_ERR_INVALID_ARG
+    assert create(damp=-1.0) == g.GPTQ_ERR_INVALID_ARG
+    assert create(damp=float("nan")) == g.GPTQ_ERR_INVALID_ARG
+    assert create(chunk=0) == g.GPTQ_ERR_INVALID_ARG
+    assert create(chunk=(1 << 24) + 1) == g.GPTQ_ERR_INVALID_ARG
+    assert create(bs=16, gs=128) == g.GPTQ_ERR_UNSUPPORTED
+    assert lib.gptq_pipeline_run(None, P, 256, P, 10, 256, P, P, P, P, None, None) == g.GPTQ_ERR_INVALID_ARG
+    assert lib.gptq_pipeline_status(None, None, None) == g.GPTQ_ERR_INVALID_ARG
+    assert lib.gptq_pipeline_destroy(None) == g.GPTQ_OK
+    assert g.gptq_launch_count() == before
 
 
 def test_dequant_gemv_argument_checks(g):

@@ -357,6 +357,61 @@ def test_end_to_end_mid(g, m, d, n, bits, gs, ao):
     _end_to_end(g, W_bits, X_bits, bits, gs, 128, ao)
 
 
+def test_host_pipeline_strided_pageable(g):
+    """The host-buffer pipeline from pageable memory with row strides wider than d (a
+    view into wider host arrays), fp32 W, a last chunk cut in four pieces, on the NULL
+    stream; then a second layer shape's worth of checks on the same object."""
+    m, d, n, bits, gs = 256, 512, 14000, 3, 128
+    W_bits = make_weight(m, d, 43)
+    X_bits = make_activations(ActSpec("heavy_tail", n, d, seed=43))
+    W = bf16_bits_to_f32(W_bits)
+    Xwide = np.zeros((n, d + 40), dtype=np.uint16)
+    Xwide[:, :d] = X_bits
+    Wwide = np.zeros((m, d + 8), dtype=np.float32)
+    Wwide[:, :d] = W
+    X_host = torch.from_numpy(Xwide.view(np.int16))[:, :d]
+    W_host = torch.from_numpy(Wwide)[:, :d]
+    assert X_host.stride(0) == d + 40 and W_host.stride(0) == d + 8 and not X_host.is_pinned()
+    pipe = g.HostPipeline(m, d, bits=bits, group_size=gs, blocksize=128, chunk_tokens=8192, w_dtype=torch.float32)
+    out = pipe.run(W_host, X_host, stream=0)
+    assert pipe.check(stream=0) == -1
+    H = orc.hessian([bf16_bits_to_f32(X_bits)])
+    res64 = orc.gptq_layer(W.astype(np.float64), H, bits, gs, 128, 0.01, False)
+    res32 = orc.gptq_layer(W, H.astype(np.float32), bits, gs, 128, 0.01, False, dtype=np.float32)
+    codes = orc.unpack_codes(out.qweight.numpy().view(np.uint32), bits, d).astype(np.int64)
+    check_layer(W.astype(np.float64), res64, res32, codes, out.scales.numpy().astype(np.float64),
+                out.zeros.numpy().astype(np.float64), H, bits, gs, None,
+                case=f"host pipeline pageable strided {m}x{d} n={n} {bits}b g{gs} fp32 W")
+
+
+def test_host_pipeline_reports_failures(g):
+    """The pipeline's outcome call: a NaN in W is reported by the column loop
+    (GPTQ_ERR_NONFINITE, info 1); a channel that every token leaves at zero makes H
+    singular, which without damping the factor reports (GPTQ_ERR_NOT_PD at that
+    column); with the pages' damping the same tokens factor; each run on the same
+    pipeline object."""
+    m, d, n = 64, 256, 2048
+    X_bits = make_activations(ActSpec("heavy_tail", n, d, seed=44))
+    X_bits[:, 100] = 0
+    W = bf16_bits_to_f32(make_weight(m, d, 44))
+    X_host = torch.from_numpy(X_bits.view(np.int16)).pin_memory()
+    bad = W.copy()
+    bad[5, 17] = np.nan
+    pipe0 = g.HostPipeline(m, d, bits=4, group_size=128, percdamp=0.0, chunk_tokens=1024, w_dtype=torch.float32)
+    pipe0.run(torch.from_numpy(W).pin_memory(), X_host)
+    with pytest.raises(g.GPTQError) as ei:
+        pipe0.check()
+    assert ei.value.status == g.GPTQ_ERR_NOT_PD
+    pipe = g.HostPipeline(m, d, bits=4, group_size=128, percdamp=0.01, chunk_tokens=1024, w_dtype=torch.float32)
+    pipe.run(torch.from_numpy(bad).pin_memory(), X_host)
+    with pytest.raises(g.GPTQError) as ei:
+        pipe.check()
+    assert ei.value.status == g.GPTQ_ERR_NONFINITE
+    pipe.run(torch.from_numpy(W).pin_memory(), X_host)
+    assert pipe.check() == -1
+    g.gptq_device_check()
+
+
 def test_launch_counter_moves(g):
     before = g.gptq_launch_count()
     H = torch.empty((64, 64), dtype=torch.float32, device="cuda")
@@ -385,10 +440,10 @@ def test_host_pipeline_matches_oracle(g, act_order):
     res32 = orc.gptq_layer(W, H.astype(np.float32), bits, gs, 128, 0.01, act_order, dtype=np.float32)
     for _ in range(2):
         out = pipe.run(W_host, X_host)
-        torch.cuda.synchronize()
+        assert pipe.check() == -1
         g.gptq_device_check()
         codes = orc.unpack_codes(out.qweight.numpy().view(np.uint32), bits, d).astype(np.int64)
-        p = pipe.perm.cpu().numpy().astype(np.int64) if act_order else None
+        p = pipe.perm.numpy().astype(np.int64) if act_order else None
         if act_order and not np.array_equal(p, res64["perm"]):
             hx = np.diag(H)
             assert np.all(np.abs(hx[p] - hx[res64["perm"]]) <= 1e-6 * hx.max())
