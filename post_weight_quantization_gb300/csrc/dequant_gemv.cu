@@ -15,6 +15,10 @@
 // fp32 (a template constant: a runtime count would leave predicated-off work); the
 // warp's partial sums meet by shuffles. X (bf16, token-major) is read through the
 // read-only cache; every row reuses it.
+#include <algorithm>
+#include <cstdlib>
+#include <string>
+
 #include "common.cuh"
 
 namespace gptq {
@@ -180,6 +184,221 @@ gptq_status launch(const uint32_t* qweight, const float* scales, const float* ze
   return check_launch("dequant_gemv_kernel");
 }
 
+// ---------------------------------------------------------------------------------
+// The same product with the dot products on the tensor cores: for 2- and 4-bit codes in
+// natural groups the FMA version above spends about six instructions per code (unpack,
+// dequantize, convert the token, FMA) and is bound by instruction issue at a quarter of
+// the HBM rate; here the unpacked codes go from registers straight into mma.sync
+// (m16n8k16, bf16 operands, fp32 accumulation), which takes eight tokens at the cost of
+// one, and a code costs about two instructions, below the HBM rate. (The tcgen05 MMA
+// reads its operands from shared memory; staging the dequantized codes there would add
+// four bytes of shared-memory traffic per code, more than the code's half byte from
+// HBM.)
+//
+// Per row, code - zero is an integer of at most 4 bits: a pair of codes is taken out of
+// a packed word with one mask and OR-ed into the mantissas of a bf16 pair of 128
+// (0x4300: bf16 holds 128 ... 255 exactly), and a bf16 subtraction of 128 + zero leaves
+// code - zero exactly. The product with a bf16 token is exact; each block of columns
+// that shares one (scale, zero) is summed by the tensor core in fp32 and then scaled
+// and added in fp32.
+//
+// Layout: a CTA takes 16 rows, its 8 warps split the row's column blocks. A block is
+// 4 x WPT consecutive words of the row; lane (g, t) of a warp (g = lane / 4, t =
+// lane % 4) holds words t*WPT ... t*WPT + WPT - 1 of the block for rows g and g + 8
+// (the A fragment's rows) and the same columns of token g (the B fragment's column).
+// Word pair p of a word is the codes p and p + CPW/2 (CPW codes per word), which the
+// A fragment's bf16 pair puts at two consecutive k; the B fragment pairs the token's
+// values of the same two columns with one byte permute. The order of k inside an MMA
+// is thereby a fixed permutation of the block's columns, applied to both operands.
+namespace tcv {
+
+// GPTQ_GEMV_KERNEL=fma selects the FMA kernel for every case (to compare the two).
+inline bool gemv_fma_forced() {
+  static const bool forced = [] {
+    const char* v = getenv("GPTQ_GEMV_KERNEL");
+    return v && std::string(v) == "fma";
+  }();
+  return forced;
+}
+
+constexpr int WARPS = 8, ROWS = 16;
+constexpr uint32_t kBf16Pair128 = 0x43004300u;
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// a - c for bf16 pairs as a * 1 + (-c), one fused instruction; exact here (integers
+// below 256).
+__device__ __forceinline__ uint32_t sub_bf16x2(uint32_t a, uint32_t neg_c) {
+  uint32_t d;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(0x3F803F80u), "r"(neg_c));
+  return d;
+}
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// WPT consecutive words (vector loads as wide as the alignment allows: 16 bytes for
+// 4-bit rows, 8 for 2-bit), or zeros for a row past the end.
+template <int BITS, int WPT>
+__device__ __forceinline__ void load_words(const uint32_t* __restrict__ p, uint32_t (&w)[WPT], bool valid) {
+  if (!valid) {
+#pragma unroll
+    for (int u = 0; u < WPT; ++u) w[u] = 0u;
+    return;
+  }
+  if constexpr (WPT == 4 && BITS == 4) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+  } else if constexpr (WPT >= 2) {
+#pragma unroll
+    for (int u = 0; u < WPT; u += 2) {
+      const uint2 v = __ldg(reinterpret_cast<const uint2*>(p + u));
+      w[u] = v.x; w[u + 1] = v.y;
+    }
+  } else {
+    w[0] = __ldg(p);
+  }
+}
+
+// bf16 pair (-(128 + zero), -(128 + zero)); zero is an integer in [0, 2^bits - 1], so
+// 128 + zero has at most 8 significant bits and its fp32 encoding's upper half is its
+// bf16.
+__device__ __forceinline__ uint32_t neg_zero_pair(float z) {
+  return ((__float_as_uint(128.0f + z) >> 16) * 0x00010001u) | 0x80008000u;
+}
+
+template <int BITS, int WPT>
+__global__ void __launch_bounds__(WARPS * 32) gemv_mma_kernel(const uint32_t* __restrict__ qweight, int wpr,
+                                                              const float* __restrict__ scales,
+                                                              const float* __restrict__ zeros, int G, int gsize, int m,
+                                                              int d, const uint16_t* __restrict__ X, long long ldx,
+                                                              int T, float* __restrict__ Y, long long ldy) {
+  constexpr int CPW = 32 / BITS;                 // codes per word
+  constexpr uint32_t MASK2 = ((1u << BITS) - 1u) * 0x00010001u;
+  constexpr int VBW = 4 * WPT;                   // words of a row in one block
+  constexpr int VBC = VBW * CPW;                 // columns of one block
+  constexpr int SPW = CPW / 4;                   // MMAs per word (two code pairs each)
+  constexpr int NB = 16 / WPT;                   // blocks loaded at once: 2 * WPT * NB = 32 words
+  __shared__ float red[WARPS][ROWS][8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const int r0 = blockIdx.x * ROWS, ra = r0 + g, rb = r0 + g + 8;
+  const bool va = ra < m, vb = rb < m, tok = g < T;
+  const uint32_t* rowa = qweight + (long long)(va ? ra : 0) * wpr + t * WPT;
+  const uint32_t* rowb = qweight + (long long)(vb ? rb : 0) * wpr + t * WPT;
+  const uint16_t* xrow = X + (long long)(tok ? g : 0) * ldx + t * WPT * CPW;
+  const float* sca = scales + (long long)(va ? ra : 0) * G;
+  const float* scb = scales + (long long)(vb ? rb : 0) * G;
+  const float* zra = zeros + (long long)(va ? ra : 0) * G;
+  const float* zrb = zeros + (long long)(vb ? rb : 0) * G;
+  const int nvb = d / VBC;
+  float tot[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  // This warp's blocks v = warp + 8 k, in batches of NB whose words are all requested
+  // before the first is multiplied.
+  for (int v0 = warp; v0 < nvb; v0 += WARPS * NB) {
+    uint32_t wa[NB][WPT], wb[NB][WPT];
+#pragma unroll
+    for (int i = 0; i < NB; ++i) {
+      const int v = v0 + WARPS * i;
+      load_words<BITS, WPT>(rowa + (long long)v * VBW, wa[i], va && v < nvb);
+      load_words<BITS, WPT>(rowb + (long long)v * VBW, wb[i], vb && v < nvb);
+    }
+#pragma unroll
+    for (int i = 0; i < NB; ++i) {
+      const int v = v0 + WARPS * i;
+      if (v >= nvb) continue;
+      const int grp = (v * VBC) / gsize;
+      const float sa = va ? __ldg(sca + grp) : 0.0f, sb = vb ? __ldg(scb + grp) : 0.0f;
+      const uint32_t za = neg_zero_pair(va ? __ldg(zra + grp) : 0.0f);
+      const uint32_t zb = neg_zero_pair(vb ? __ldg(zrb + grp) : 0.0f);
+      float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int u = 0; u < WPT; ++u) {
+        uint32_t xw[CPW / 2];                    // token g's CPW columns of word u, bf16 pairs
+#pragma unroll
+        for (int q = 0; q < CPW / 8; ++q) {
+          uint4 xv = make_uint4(0u, 0u, 0u, 0u);
+          if (tok) xv = __ldg(reinterpret_cast<const uint4*>(xrow + (long long)v * VBC + u * CPW + 8 * q));
+          xw[4 * q] = xv.x; xw[4 * q + 1] = xv.y; xw[4 * q + 2] = xv.z; xw[4 * q + 3] = xv.w;
+        }
+#pragma unroll
+        for (int j = 0; j < SPW; ++j) {
+          // code pairs 2j and 2j + 1: codes (2j, 2j + CPW/2) and (2j + 1, 2j + 1 + CPW/2)
+          const uint32_t a0 = sub_bf16x2(((wa[i][u] >> (BITS * 2 * j)) & MASK2) | kBf16Pair128, za);
+          const uint32_t a2 = sub_bf16x2(((wa[i][u] >> (BITS * (2 * j + 1))) & MASK2) | kBf16Pair128, za);
+          const uint32_t a1 = sub_bf16x2(((wb[i][u] >> (BITS * 2 * j)) & MASK2) | kBf16Pair128, zb);
+          const uint32_t a3 = sub_bf16x2(((wb[i][u] >> (BITS * (2 * j + 1))) & MASK2) | kBf16Pair128, zb);
+          const uint32_t b0 = prmt(xw[j], xw[j + CPW / 4], 0x5410u);
+          const uint32_t b1 = prmt(xw[j], xw[j + CPW / 4], 0x7632u);
+          mma_bf16(c, a0, a1, a2, a3, b0, b1);
+        }
+      }
+      tot[0] = fmaf(sa, c[0], tot[0]);
+      tot[1] = fmaf(sa, c[1], tot[1]);
+      tot[2] = fmaf(sb, c[2], tot[2]);
+      tot[3] = fmaf(sb, c[3], tot[3]);
+    }
+  }
+  // c[0], c[1]: row g, tokens 2t and 2t + 1; c[2], c[3]: row g + 8
+  red[warp][g][2 * t] = tot[0];
+  red[warp][g][2 * t + 1] = tot[1];
+  red[warp][g + 8][2 * t] = tot[2];
+  red[warp][g + 8][2 * t + 1] = tot[3];
+  __syncthreads();
+  if (threadIdx.x < ROWS * 8) {
+    const int i = threadIdx.x >> 3, tk = threadIdx.x & 7;
+    float sum = 0.0f;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) sum += red[w][i][tk];
+    if (tk < T && r0 + i < m) Y[(long long)tk * ldy + r0 + i] = sum;
+  }
+}
+
+// Words of a row per thread in one block (1, 2 or 4), or 0 when the tensor-core path
+// does not apply: 2- and 4-bit codes, natural groups whose width is a multiple of four
+// threads' words (a block never straddles two groups), and a width that blocks cover.
+inline int words_per_thread(int bits, int group_size, long long d) {
+  if (bits != 2 && bits != 4) return 0;
+  const long long cols4 = 4LL * (32 / bits);          // columns of four threads' single words
+  const long long span = group_size == -1 ? d : group_size;
+  if (span % cols4) return 0;
+  const long long q = span / cols4;
+  return (q % 4 == 0) ? 4 : (q % 2 == 0) ? 2 : 1;
+}
+
+template <int BITS, int WPT>
+gptq_status launch(const uint32_t* qweight, const float* scales, const float* zeros, int m, int d, int G, int gsize,
+                   const uint16_t* X, long long ldx, int T, float* Y, long long ldy, cudaStream_t s) {
+  const int wpr = d * BITS / 32;
+  const dim3 grid((unsigned)((m + ROWS - 1) / ROWS));
+  for (int t0 = 0; t0 < T; t0 += 8) {
+    gemv_mma_kernel<BITS, WPT><<<grid, WARPS * 32, 0, s>>>(qweight, wpr, scales, zeros, G, gsize, m, d,
+                                                          X + (long long)t0 * ldx, ldx, std::min(8, T - t0),
+                                                          Y + (long long)t0 * ldy, ldy);
+    count_launch();
+  }
+  return check_launch("gemv_mma_kernel");
+}
+
+template <int BITS>
+gptq_status launch_bits(int wpt, const uint32_t* qweight, const float* scales, const float* zeros, int m, int d, int G,
+                        int gsize, const uint16_t* X, long long ldx, int T, float* Y, long long ldy, cudaStream_t s) {
+  switch (wpt) {
+    case 4: return launch<BITS, 4>(qweight, scales, zeros, m, d, G, gsize, X, ldx, T, Y, ldy, s);
+    case 2: return launch<BITS, 2>(qweight, scales, zeros, m, d, G, gsize, X, ldx, T, Y, ldy, s);
+    default: return launch<BITS, 1>(qweight, scales, zeros, m, d, G, gsize, X, ldx, T, Y, ldy, s);
+  }
+}
+
+}  // namespace tcv
+
 }  // namespace dgemv
 
 gptq_status dequant_gemv_launch(const uint32_t* qweight, const float* scales, const float* zeros, const int32_t* g_idx,
@@ -188,6 +407,12 @@ gptq_status dequant_gemv_launch(const uint32_t* qweight, const float* scales, co
   using namespace dgemv;
   const int G = (group_size == -1) ? 1 : (int)(d / group_size);
   const int gsize = (group_size == -1) ? (int)d : group_size;
+  // act-order groups (g_idx) and 3- and 8-bit codes take the FMA kernel
+  const int wpt = (g_idx && G > 1) ? 0 : tcv::words_per_thread(bits, group_size, d);
+  if (wpt && !tcv::gemv_fma_forced()) {
+    if (bits == 4) return tcv::launch_bits<4>(wpt, qweight, scales, zeros, (int)m, (int)d, G, gsize, X, ldx, (int)T, Y, ldy, s);
+    return tcv::launch_bits<2>(wpt, qweight, scales, zeros, (int)m, (int)d, G, gsize, X, ldx, (int)T, Y, ldy, s);
+  }
   switch (bits) {
     case 2: return launch<2>(qweight, scales, zeros, g_idx, (int)m, (int)d, G, gsize, X, ldx, (int)T, Y, ldy, s);
     case 3: return launch<3>(qweight, scales, zeros, g_idx, (int)m, (int)d, G, gsize, X, ldx, (int)T, Y, ldy, s);
