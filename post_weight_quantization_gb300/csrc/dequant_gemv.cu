@@ -278,9 +278,10 @@ __device__ __forceinline__ uint32_t neg_zero_pair(float z) {
 template <int BITS, int WPT>
 __global__ void __launch_bounds__(WARPS * 32) gemv_mma_kernel(const uint32_t* __restrict__ qweight, int wpr,
                                                               const float* __restrict__ scales,
-                                                              const float* __restrict__ zeros, int G, int gsize, int m,
-                                                              int d, const uint16_t* __restrict__ X, long long ldx,
-                                                              int T, float* __restrict__ Y, long long ldy) {
+                                                              const float* __restrict__ zeros, int G, int bpg,
+                                                              uint32_t bpg_mul, int m, int d,
+                                                              const uint16_t* __restrict__ X, long long ldx, int T,
+                                                              float* __restrict__ Y, long long ldy) {
   constexpr int CPW = 32 / BITS;                 // codes per word
   constexpr uint32_t MASK2 = ((1u << BITS) - 1u) * 0x00010001u;
   constexpr int VBW = 4 * WPT;                   // words of a row in one block
@@ -307,14 +308,16 @@ __global__ void __launch_bounds__(WARPS * 32) gemv_mma_kernel(const uint32_t* __
 #pragma unroll
     for (int i = 0; i < NB; ++i) {
       const int v = v0 + WARPS * i;
-      load_words<BITS, WPT>(rowa + (long long)v * VBW, wa[i], va && v < nvb);
-      load_words<BITS, WPT>(rowb + (long long)v * VBW, wb[i], vb && v < nvb);
+      load_words<BITS, WPT>(rowa + v * VBW, wa[i], va && v < nvb);
+      load_words<BITS, WPT>(rowb + v * VBW, wb[i], vb && v < nvb);
     }
 #pragma unroll
     for (int i = 0; i < NB; ++i) {
       const int v = v0 + WARPS * i;
       if (v >= nvb) continue;
-      const int grp = (v * VBC) / gsize;
+      // group of block v: v / bpg (blocks per group) as a multiply-high by
+      // ceil(2^32 / bpg), exact since v * bpg < 2^32
+      const int grp = bpg == 1 ? v : (int)__umulhi((uint32_t)v, bpg_mul);
       const float sa = va ? __ldg(sca + grp) : 0.0f, sb = vb ? __ldg(scb + grp) : 0.0f;
       const uint32_t za = neg_zero_pair(va ? __ldg(zra + grp) : 0.0f);
       const uint32_t zb = neg_zero_pair(vb ? __ldg(zrb + grp) : 0.0f);
@@ -325,7 +328,7 @@ __global__ void __launch_bounds__(WARPS * 32) gemv_mma_kernel(const uint32_t* __
 #pragma unroll
         for (int q = 0; q < CPW / 8; ++q) {
           uint4 xv = make_uint4(0u, 0u, 0u, 0u);
-          if (tok) xv = __ldg(reinterpret_cast<const uint4*>(xrow + (long long)v * VBC + u * CPW + 8 * q));
+          if (tok) xv = __ldg(reinterpret_cast<const uint4*>(xrow + (v * VBC + u * CPW + 8 * q)));
           xw[4 * q] = xv.x; xw[4 * q + 1] = xv.y; xw[4 * q + 2] = xv.z; xw[4 * q + 3] = xv.w;
         }
 #pragma unroll
@@ -377,9 +380,11 @@ template <int BITS, int WPT>
 gptq_status launch(const uint32_t* qweight, const float* scales, const float* zeros, int m, int d, int G, int gsize,
                    const uint16_t* X, long long ldx, int T, float* Y, long long ldy, cudaStream_t s) {
   const int wpr = d * BITS / 32;
+  const int bpg = gsize / (4 * WPT * (32 / BITS));              // blocks per group (a block never straddles two)
+  const uint32_t bpg_mul = bpg == 1 ? 0u : (uint32_t)((0x100000000ULL + (unsigned long long)bpg - 1) / bpg);
   const dim3 grid((unsigned)((m + ROWS - 1) / ROWS));
   for (int t0 = 0; t0 < T; t0 += 8) {
-    gemv_mma_kernel<BITS, WPT><<<grid, WARPS * 32, 0, s>>>(qweight, wpr, scales, zeros, G, gsize, m, d,
+    gemv_mma_kernel<BITS, WPT><<<grid, WARPS * 32, 0, s>>>(qweight, wpr, scales, zeros, G, bpg, bpg_mul, m, d,
                                                           X + (long long)t0 * ldx, ldx, std::min(8, T - t0),
                                                           Y + (long long)t0 * ldy, ldy);
     count_launch();
