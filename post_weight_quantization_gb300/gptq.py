@@ -11,6 +11,7 @@ that says how to build it; there is no fallback.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 from dataclasses import dataclass
@@ -456,6 +457,16 @@ def sequential_quantize(X0: torch.Tensor, weights, bits: int = 4, group_size: in
     return layers, inputs, X
 
 
+def _host_empty(shape, dtype) -> torch.Tensor:
+    """A host buffer for the pipeline's copies: page-locked where CUDA is present (so the
+    copies run asynchronously), ordinary memory otherwise."""
+    return torch.empty(shape, dtype=dtype, pin_memory=torch.cuda.is_available())
+
+
+def _on_device(dev: torch.device):
+    return torch.cuda.device(dev) if torch.cuda.is_available() else contextlib.nullcontext()
+
+
 class HostPipeline:
     """End-to-end quantization of one layer from host buffers, over the library's native
     pipeline (gptq_pipeline_create / _run / _status / _destroy).
@@ -478,19 +489,17 @@ class HostPipeline:
         self.device = torch.device(device)
         self._h = None
         h = _vp()
-        with torch.cuda.device(self.device):
+        with _on_device(self.device):
             _check(_lib.gptq_pipeline_create(m, d, 1 if w_dtype == torch.bfloat16 else 0, bits, group_size, blocksize,
                                              float(percdamp), 1 if act_order else 0, chunk_tokens, ctypes.byref(h)),
                    "gptq_pipeline_create")
         self._h = h
         G = 1 if group_size == -1 else d // group_size
         self.host_out = QuantizedLayer(
-            qweight=torch.empty((m, (d * bits + 31) // 32), dtype=torch.int32, pin_memory=True),
-            scales=torch.empty((m, G), dtype=torch.float32, pin_memory=True),
-            zeros=torch.empty((m, G), dtype=torch.float32, pin_memory=True),
-            col_losses=torch.empty(d, dtype=torch.float32, pin_memory=True),
+            qweight=_host_empty((m, (d * bits + 31) // 32), torch.int32), scales=_host_empty((m, G), torch.float32),
+            zeros=_host_empty((m, G), torch.float32), col_losses=_host_empty((d,), torch.float32),
             bits=bits, group_size=group_size, d=d)
-        self.perm = torch.empty(d, dtype=torch.int32, pin_memory=True) if act_order else None
+        self.perm = _host_empty((d,), torch.int32) if act_order else None
 
     def __del__(self):
         if getattr(self, "_h", None) is not None:
@@ -518,7 +527,7 @@ class HostPipeline:
         if X_host.dtype not in (torch.int16, torch.bfloat16):
             raise TypeError("X_host must hold bf16 bits (torch.int16 or torch.bfloat16)")
         o = self.host_out
-        with torch.cuda.device(self.device):
+        with _on_device(self.device):
             _check(_lib.gptq_pipeline_run(self._h, W_host.data_ptr(), W_host.stride(0), X_host.data_ptr(),
                                           X_host.shape[0], X_host.stride(0), o.qweight.data_ptr(),
                                           o.scales.data_ptr(), o.zeros.data_ptr(), o.col_losses.data_ptr(),
@@ -529,6 +538,6 @@ class HostPipeline:
         """Synchronize the stream and raise GPTQError if the last run's factor or column
         loop failed; returns info (-1 on success)."""
         info = _c_i64(0)
-        with torch.cuda.device(self.device):
+        with _on_device(self.device):
             _check(_lib.gptq_pipeline_status(self._h, ctypes.byref(info), _stream(stream)), "gptq_pipeline_status")
         return int(info.value)

@@ -221,3 +221,40 @@ def test_sequential_quantize_marshalling(g, fake):
     with pytest.raises(ValueError):
         g.sequential_quantize(X0, [torch.zeros((64, 128), dtype=torch.bfloat16)])
     assert len(fake.calls) == k
+
+
+def test_host_pipeline_marshalling(g, fake):
+    """HostPipeline hands the library its settings at creation, then per run the host
+    pointers with their row strides (views into wider arrays keep their stride), the
+    token count and the output buffers (the permutation only with act-order); bad
+    shapes and dtypes raise before any call."""
+    m, d = 48, 256
+    pipe = g.HostPipeline(m, d, bits=3, group_size=-1, blocksize=64, percdamp=0.02, act_order=True,
+                          chunk_tokens=1000, w_dtype=torch.float32, device="cpu")
+    name, a = fake.calls[-1]
+    assert name == "gptq_pipeline_create"
+    assert a[:6] == (m, d, 0, 3, -1, 64) and abs(a[6] - 0.02) < 1e-7 and a[7:9] == (1, 1000)
+    Wwide = torch.zeros((m, d + 8))
+    Xwide = torch.zeros((700, d + 16), dtype=torch.int16)
+    out = pipe.run(Wwide[:, :d], Xwide[:, :d])
+    name, a = fake.calls[-1]
+    assert name == "gptq_pipeline_run"
+    assert a[1] == Wwide.data_ptr() and a[2] == d + 8
+    assert a[3] == Xwide.data_ptr() and a[4:6] == (700, d + 16)
+    assert a[6:10] == (out.qweight.data_ptr(), out.scales.data_ptr(), out.zeros.data_ptr(), out.col_losses.data_ptr())
+    assert a[10] == pipe.perm.data_ptr() and pipe.perm.shape == (d,)
+    assert out.qweight.shape == (m, (d * 3 + 31) // 32) and out.scales.shape == (m, 1)
+    assert pipe.bytes_h2d(700) == 700 * d * 2 + m * d * 4
+    assert pipe.bytes_d2h() == out.qweight.numel() * 4 + 2 * m * 4 + d * 4 + d * 4
+    n_calls = len(fake.calls)
+    with pytest.raises(ValueError):
+        pipe.run(torch.zeros((m, d), dtype=torch.bfloat16), Xwide[:, :d])     # W dtype
+    with pytest.raises(ValueError):
+        pipe.run(Wwide[:, :d], torch.zeros((10, d + 1), dtype=torch.int16))  # X width
+    with pytest.raises(TypeError):
+        pipe.run(Wwide[:, :d], torch.zeros((10, d), dtype=torch.float32))    # X dtype
+    assert len(fake.calls) == n_calls
+    pipe2 = g.HostPipeline(m, d, bits=4, group_size=128, device="cpu")
+    assert fake.calls[-1][1][2] == 1 and pipe2.perm is None                  # bf16 W by default
+    pipe2.run(torch.zeros((m, d), dtype=torch.bfloat16), torch.zeros((5, d), dtype=torch.int16))
+    assert fake.calls[-1][1][10] is None
