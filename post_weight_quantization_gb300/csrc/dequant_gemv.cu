@@ -6,6 +6,9 @@
 // G(j) = j / group_size, or g_idx[j] for act-order groups. For the few tokens of a
 // decoding step this product reads every code once and is bound by HBM bandwidth.
 //
+// Two kernels: gemv_mma_kernel (below) for 2- and 4-bit codes in natural groups, and
+// this FMA kernel for 3- and 8-bit codes and act-order groups.
+//
 // dequant_gemv_kernel<BITS, GIDX>: one warp per row r; lane L takes the 32-column
 // chunks L, L + 32, ... of the row (BITS words each, read as 16-byte vectors where the
 // width allows; several chunks in flight per lane), unpacks the codes with compile-time
