@@ -449,9 +449,9 @@ def run_gpu(args):
     # ---- CPU oracle baseline, bounded sample
     cpu = None
     if not args.no_cpu_baseline:
-        # about 10 s of host work: 1/2 of the tokens, the full factor, 1/8 of the rows
-        n_s = min(n, max(2 * CHUNK, (n // 2) // CHUNK * CHUNK))
-        rows = min(m, max(32, m // 8))
+        # about 12 s of host work on 16 cores: every token, the full factor, 1/4 of the rows
+        n_s = n
+        rows = min(m, max(32, m // 4))
         r = oracle_sample(wl, layer, X_host.numpy().view(np.uint16)[:n_s], W_bits[:rows], n, m)
         cpu = {"value": round(weights / r["total_s"] / 1e6, 6), "unit": "Mweights/s", "cores": blas_threads(),
                "host_cores": host_cores(), "blas_threads": blas_threads(), "kind": "oracle",
