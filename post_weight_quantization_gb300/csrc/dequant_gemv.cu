@@ -102,8 +102,9 @@ __device__ __forceinline__ void chunk_fma(const uint32_t (&wv)[BITS], const uint
 template <int BITS, bool GIDX, int NT>
 __global__ void __launch_bounds__(WARPS * 32) dequant_gemv_kernel(const uint32_t* __restrict__ qweight, int wpr,
                                                                   const float* __restrict__ scales,
-                                                                  const float* __restrict__ zeros, int G, int gsize,
-                                                                  const int* __restrict__ g_idx, int m, int d,
+                                                                  const float* __restrict__ zeros, int G, int cpg,
+                                                                  uint32_t cpg_mul, const int* __restrict__ g_idx, int m,
+                                                                  int d,
                                                                   const uint16_t* __restrict__ X, long long ldx,
                                                                   float* __restrict__ Y, long long ldy) {
   const int r = blockIdx.x * WARPS + (threadIdx.x >> 5), lane = threadIdx.x & 31;
@@ -129,7 +130,9 @@ __global__ void __launch_bounds__(WARPS * 32) dequant_gemv_kernel(const uint32_t
       const int c0 = ch << 5;
       float s = 0.0f, z = 0.0f;
       if constexpr (!GIDX) {
-        const int grp = c0 / gsize;
+        // group of chunk ch: ch / cpg (chunks per group) as a multiply-high by
+        // ceil(2^32 / cpg), exact since ch * cpg < 2^32
+        const int grp = cpg == 1 ? ch : (int)__umulhi((uint32_t)ch, cpg_mul);
         s = __ldg(srow + grp);
         z = __fadd_rn(kTwo23, __ldg(zrow + grp));
       }
@@ -151,12 +154,14 @@ template <int BITS, int NT>
 void launch_nt(const uint32_t* qweight, int wpr, const float* scales, const float* zeros, const int* g_idx, int m,
                int d, int G, int gsize, const uint16_t* X, long long ldx, float* Y, long long ldy, cudaStream_t s) {
   const dim3 grid((unsigned)((m + WARPS - 1) / WARPS));
+  const int cpg = gsize >> 5;                              // 32-column chunks per group
+  const uint32_t cpg_mul = cpg == 1 ? 0u : (uint32_t)((0x100000000ULL + (unsigned long long)cpg - 1) / cpg);
   if (g_idx)
-    dequant_gemv_kernel<BITS, true, NT><<<grid, WARPS * 32, 0, s>>>(qweight, wpr, scales, zeros, G, gsize, g_idx, m, d,
-                                                                    X, ldx, Y, ldy);
+    dequant_gemv_kernel<BITS, true, NT><<<grid, WARPS * 32, 0, s>>>(qweight, wpr, scales, zeros, G, cpg, cpg_mul, g_idx,
+                                                                    m, d, X, ldx, Y, ldy);
   else
-    dequant_gemv_kernel<BITS, false, NT><<<grid, WARPS * 32, 0, s>>>(qweight, wpr, scales, zeros, G, gsize, g_idx, m,
-                                                                     d, X, ldx, Y, ldy);
+    dequant_gemv_kernel<BITS, false, NT><<<grid, WARPS * 32, 0, s>>>(qweight, wpr, scales, zeros, G, cpg, cpg_mul,
+                                                                     g_idx, m, d, X, ldx, Y, ldy);
   count_launch();
 }
 
