@@ -6,8 +6,8 @@
 // G(j) = j / group_size, or g_idx[j] for act-order groups. For the few tokens of a
 // decoding step this product reads every code once and is bound by HBM bandwidth.
 //
-// Two kernels: gemv_mma_kernel (below) for 2- and 4-bit codes in natural groups, and
-// this FMA kernel for 3- and 8-bit codes and act-order groups.
+// Two kernels: gemv_mma_kernel (below) for 2-, 3- and 4-bit codes in natural groups,
+// and this FMA kernel for 8-bit codes, act-order groups and narrow groups.
 //
 // dequant_gemv_kernel<BITS, GIDX>: one warp per row r; lane L takes the 32-column
 // chunks L, L + 32, ... of the row (BITS words each, read as 16-byte vectors where the
@@ -193,31 +193,32 @@ gptq_status launch(const uint32_t* qweight, const float* scales, const float* ze
 }
 
 // ---------------------------------------------------------------------------------
-// The same product with the dot products on the tensor cores: for 2- and 4-bit codes in
-// natural groups the FMA version above spends about six instructions per code (unpack,
-// dequantize, convert the token, FMA) and is bound by instruction issue at a quarter of
-// the HBM rate; here the unpacked codes go from registers straight into mma.sync
-// (m16n8k16, bf16 operands, fp32 accumulation), which takes eight tokens at the cost of
-// one, and a code costs about two instructions, below the HBM rate. (The tcgen05 MMA
-// reads its operands from shared memory; staging the dequantized codes there would add
-// four bytes of shared-memory traffic per code, more than the code's half byte from
-// HBM.)
+// The same product with the dot products on the tensor cores: for 2-, 3- and 4-bit codes
+// in natural groups the FMA version above spends about six instructions per code
+// (unpack, dequantize, convert the token, FMA) and is bound by instruction issue at a
+// quarter of the HBM rate; here the unpacked codes go from registers straight into
+// mma.sync (m16n8k16, bf16 operands, fp32 accumulation), which takes eight tokens at the
+// cost of one. (The tcgen05 MMA reads its operands from shared memory; staging the
+// dequantized codes there would add four bytes of shared-memory traffic per code, more
+// than the code's half byte from HBM.)
 //
 // Per row, code - zero is an integer of at most 4 bits: a pair of codes is taken out of
-// a packed word with one mask and OR-ed into the mantissas of a bf16 pair of 128
-// (0x4300: bf16 holds 128 ... 255 exactly), and a bf16 subtraction of 128 + zero leaves
-// code - zero exactly. The product with a bf16 token is exact; each block of columns
-// that shares one (scale, zero) is summed by the tensor core in fp32 and then scaled
-// and added in fp32.
+// the packed words and OR-ed into the mantissas of a bf16 pair of 128 (0x4300: bf16
+// holds 128 ... 255 exactly), and a bf16 subtraction of 128 + zero leaves code - zero
+// exactly. The product with a bf16 token is exact; each block of columns that shares
+// one (scale, zero) is summed by the tensor core in fp32 and then scaled and added in
+// fp32.
 //
-// Layout: a CTA takes 16 rows, its 8 warps split the row's column blocks. A block is
-// 4 x WPT consecutive words of the row; lane (g, t) of a warp (g = lane / 4, t =
-// lane % 4) holds words t*WPT ... t*WPT + WPT - 1 of the block for rows g and g + 8
-// (the A fragment's rows) and the same columns of token g (the B fragment's column).
-// Word pair p of a word is the codes p and p + CPW/2 (CPW codes per word), which the
-// A fragment's bf16 pair puts at two consecutive k; the B fragment pairs the token's
-// values of the same two columns with one byte permute. The order of k inside an MMA
-// is thereby a fixed permutation of the block's columns, applied to both operands.
+// Layout: a CTA takes 16 rows, its 8 warps split the row's column blocks. The packed
+// row is read in units: one word (CPW = 32 / bits codes) at 2 and 4 bits, three words
+// (32 codes) at 3 bits, whose codes straddle words. A block is 4 x UPT units; lane
+// (g, t) of a warp (g = lane / 4, t = lane % 4) holds units t*UPT ... t*UPT + UPT - 1 of
+// the block for rows g and g + 8 (the A fragment's rows) and the same columns of token
+// g (the B fragment's column). Code pair p of a unit of UC codes is the codes p and
+// p + UC/2, which the A fragment's bf16 pair puts at two consecutive k; the B fragment
+// pairs the token's values of the same two columns with one byte permute. The order of
+// k inside an MMA is thereby a fixed permutation of the block's columns, applied to
+// both operands.
 namespace tcv {
 
 // GPTQ_GEMV_KERNEL=fma selects the FMA kernel for every case (to compare the two).
@@ -231,6 +232,9 @@ inline bool gemv_fma_forced() {
 
 constexpr int WARPS = 8, ROWS = 16;
 constexpr uint32_t kBf16Pair128 = 0x43004300u;
+
+template <int BITS> constexpr int unit_words() { return BITS == 3 ? 3 : 1; }
+template <int BITS> constexpr int unit_codes() { return BITS == 3 ? 32 : 32 / BITS; }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
@@ -253,26 +257,44 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// WPT consecutive words (vector loads as wide as the alignment allows: 16 bytes for
-// 4-bit rows, 8 for 2-bit), or zeros for a row past the end.
-template <int BITS, int WPT>
-__device__ __forceinline__ void load_words(const uint32_t* __restrict__ p, uint32_t (&w)[WPT], bool valid) {
+// Codes p and p + UC/2 of a unit as the bf16 pair (128 + code_p, 128 + code_{p+UC/2})
+// (p is a compile-time constant once the callers' loops are unrolled). At 2 and 4 bits
+// the two codes sit 16 bits apart in one word: one shift and one mask-and-OR. At 3 bits
+// code p starts at bit 3p of the unit's 96 bits and code p + 16 at bit 48 + 3p: a
+// funnel shift brings each to bit 0 and 16 of a word.
+template <int BITS>
+__device__ __forceinline__ uint32_t code_pair(const uint32_t* w, int p) {
+  if constexpr (BITS == 3) {
+    const uint32_t lo = (3 * p < 32) ? __funnelshift_r(w[0], w[1], 3 * p) : (w[1] >> (3 * p - 32));
+    const uint32_t hi = (3 * p < 32) ? __funnelshift_r(w[1], w[2], 3 * p) : (w[2] >> (3 * p - 32));
+    return (lo & 0x00000007u) | (hi & 0x00070000u) | kBf16Pair128;
+  } else {
+    constexpr uint32_t MASK2 = ((1u << BITS) - 1u) * 0x00010001u;
+    return ((w[0] >> (BITS * p)) & MASK2) | kBf16Pair128;
+  }
+}
+
+// N consecutive words (vector loads as wide as the alignment allows: 16 bytes for 4-bit
+// rows, 8 for 2-bit, single words for 3-bit), or zeros for a row past the end.
+template <int BITS, int N>
+__device__ __forceinline__ void load_words(const uint32_t* __restrict__ p, uint32_t (&w)[N], bool valid) {
   if (!valid) {
 #pragma unroll
-    for (int u = 0; u < WPT; ++u) w[u] = 0u;
+    for (int u = 0; u < N; ++u) w[u] = 0u;
     return;
   }
-  if constexpr (WPT == 4 && BITS == 4) {
+  if constexpr (BITS == 4 && N == 4) {
     const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
     w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-  } else if constexpr (WPT >= 2) {
+  } else if constexpr (BITS != 3 && N >= 2) {
 #pragma unroll
-    for (int u = 0; u < WPT; u += 2) {
+    for (int u = 0; u < N; u += 2) {
       const uint2 v = __ldg(reinterpret_cast<const uint2*>(p + u));
       w[u] = v.x; w[u + 1] = v.y;
     }
   } else {
-    w[0] = __ldg(p);
+#pragma unroll
+    for (int u = 0; u < N; ++u) w[u] = __ldg(p + u);
   }
 }
 
@@ -283,26 +305,27 @@ __device__ __forceinline__ uint32_t neg_zero_pair(float z) {
   return ((__float_as_uint(128.0f + z) >> 16) * 0x00010001u) | 0x80008000u;
 }
 
-template <int BITS, int WPT>
+template <int BITS, int UPT>
 __global__ void __launch_bounds__(WARPS * 32) gemv_mma_kernel(const uint32_t* __restrict__ qweight, int wpr,
                                                               const float* __restrict__ scales,
                                                               const float* __restrict__ zeros, int G, int bpg,
                                                               uint32_t bpg_mul, int m, int d,
                                                               const uint16_t* __restrict__ X, long long ldx, int T,
                                                               float* __restrict__ Y, long long ldy) {
-  constexpr int CPW = 32 / BITS;                 // codes per word
-  constexpr uint32_t MASK2 = ((1u << BITS) - 1u) * 0x00010001u;
-  constexpr int VBW = 4 * WPT;                   // words of a row in one block
-  constexpr int VBC = VBW * CPW;                 // columns of one block
-  constexpr int SPW = CPW / 4;                   // MMAs per word (two code pairs each)
-  constexpr int NB = 16 / WPT;                   // blocks loaded at once: 2 * WPT * NB = 32 words
+  constexpr int UW = unit_words<BITS>();          // words of a unit
+  constexpr int UC = unit_codes<BITS>();          // codes of a unit
+  constexpr int TW = UPT * UW;                    // words of a row per thread and block
+  constexpr int VBW = 4 * TW;                     // words of a row in one block
+  constexpr int VBC = 4 * UPT * UC;               // columns of one block
+  constexpr int SPU = UC / 4;                     // MMAs per unit (two code pairs each)
+  constexpr int NB = (16 / TW) > 0 ? 16 / TW : 1; // blocks loaded at once: 2 * TW * NB <= 32 words
   __shared__ float red[WARPS][ROWS][8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int r0 = blockIdx.x * ROWS, ra = r0 + g, rb = r0 + g + 8;
   const bool va = ra < m, vb = rb < m, tok = g < T;
-  const uint32_t* rowa = qweight + (long long)(va ? ra : 0) * wpr + t * WPT;
-  const uint32_t* rowb = qweight + (long long)(vb ? rb : 0) * wpr + t * WPT;
-  const uint16_t* xrow = X + (long long)(tok ? g : 0) * ldx + t * WPT * CPW;
+  const uint32_t* rowa = qweight + (long long)(va ? ra : 0) * wpr + t * TW;
+  const uint32_t* rowb = qweight + (long long)(vb ? rb : 0) * wpr + t * TW;
+  const uint16_t* xrow = X + (long long)(tok ? g : 0) * ldx + t * UPT * UC;
   const float* sca = scales + (long long)(va ? ra : 0) * G;
   const float* scb = scales + (long long)(vb ? rb : 0) * G;
   const float* zra = zeros + (long long)(va ? ra : 0) * G;
@@ -312,12 +335,12 @@ __global__ void __launch_bounds__(WARPS * 32) gemv_mma_kernel(const uint32_t* __
   // This warp's blocks v = warp + 8 k, in batches of NB whose words are all requested
   // before the first is multiplied.
   for (int v0 = warp; v0 < nvb; v0 += WARPS * NB) {
-    uint32_t wa[NB][WPT], wb[NB][WPT];
+    uint32_t wa[NB][TW], wb[NB][TW];
 #pragma unroll
     for (int i = 0; i < NB; ++i) {
       const int v = v0 + WARPS * i;
-      load_words<BITS, WPT>(rowa + v * VBW, wa[i], va && v < nvb);
-      load_words<BITS, WPT>(rowb + v * VBW, wb[i], vb && v < nvb);
+      load_words<BITS, TW>(rowa + v * VBW, wa[i], va && v < nvb);
+      load_words<BITS, TW>(rowb + v * VBW, wb[i], vb && v < nvb);
     }
 #pragma unroll
     for (int i = 0; i < NB; ++i) {
@@ -331,23 +354,25 @@ __global__ void __launch_bounds__(WARPS * 32) gemv_mma_kernel(const uint32_t* __
       const uint32_t zb = neg_zero_pair(vb ? __ldg(zrb + grp) : 0.0f);
       float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-      for (int u = 0; u < WPT; ++u) {
-        uint32_t xw[CPW / 2];                    // token g's CPW columns of word u, bf16 pairs
+      for (int u = 0; u < UPT; ++u) {
+        uint32_t xw[UC / 2];                     // token g's UC columns of unit u, bf16 pairs
 #pragma unroll
-        for (int q = 0; q < CPW / 8; ++q) {
+        for (int q = 0; q < UC / 8; ++q) {
           uint4 xv = make_uint4(0u, 0u, 0u, 0u);
-          if (tok) xv = __ldg(reinterpret_cast<const uint4*>(xrow + (v * VBC + u * CPW + 8 * q)));
+          if (tok) xv = __ldg(reinterpret_cast<const uint4*>(xrow + (v * VBC + u * UC + 8 * q)));
           xw[4 * q] = xv.x; xw[4 * q + 1] = xv.y; xw[4 * q + 2] = xv.z; xw[4 * q + 3] = xv.w;
         }
+        const uint32_t* ua = wa[i] + u * UW;
+        const uint32_t* ub = wb[i] + u * UW;
 #pragma unroll
-        for (int j = 0; j < SPW; ++j) {
-          // code pairs 2j and 2j + 1: codes (2j, 2j + CPW/2) and (2j + 1, 2j + 1 + CPW/2)
-          const uint32_t a0 = sub_bf16x2(((wa[i][u] >> (BITS * 2 * j)) & MASK2) | kBf16Pair128, za);
-          const uint32_t a2 = sub_bf16x2(((wa[i][u] >> (BITS * (2 * j + 1))) & MASK2) | kBf16Pair128, za);
-          const uint32_t a1 = sub_bf16x2(((wb[i][u] >> (BITS * 2 * j)) & MASK2) | kBf16Pair128, zb);
-          const uint32_t a3 = sub_bf16x2(((wb[i][u] >> (BITS * (2 * j + 1))) & MASK2) | kBf16Pair128, zb);
-          const uint32_t b0 = prmt(xw[j], xw[j + CPW / 4], 0x5410u);
-          const uint32_t b1 = prmt(xw[j], xw[j + CPW / 4], 0x7632u);
+        for (int j = 0; j < SPU; ++j) {
+          // code pairs 2j and 2j + 1: codes (2j, 2j + UC/2) and (2j + 1, 2j + 1 + UC/2)
+          const uint32_t a0 = sub_bf16x2(code_pair<BITS>(ua, 2 * j), za);
+          const uint32_t a2 = sub_bf16x2(code_pair<BITS>(ua, 2 * j + 1), za);
+          const uint32_t a1 = sub_bf16x2(code_pair<BITS>(ub, 2 * j), zb);
+          const uint32_t a3 = sub_bf16x2(code_pair<BITS>(ub, 2 * j + 1), zb);
+          const uint32_t b0 = prmt(xw[j], xw[j + UC / 4], 0x5410u);
+          const uint32_t b1 = prmt(xw[j], xw[j + UC / 4], 0x7632u);
           mma_bf16(c, a0, a1, a2, a3, b0, b1);
         }
       }
@@ -372,27 +397,29 @@ __global__ void __launch_bounds__(WARPS * 32) gemv_mma_kernel(const uint32_t* __
   }
 }
 
-// Words of a row per thread in one block (1, 2 or 4), or 0 when the tensor-core path
-// does not apply: 2- and 4-bit codes, natural groups whose width is a multiple of four
-// threads' words (a block never straddles two groups), and a width that blocks cover.
-inline int words_per_thread(int bits, int group_size, long long d) {
-  if (bits != 2 && bits != 4) return 0;
-  const long long cols4 = 4LL * (32 / bits);          // columns of four threads' single words
+// Units of a row per thread in one block (1, 2 or 4), or 0 when the tensor-core path
+// does not apply: 2-, 3- and 4-bit codes, natural groups whose width is a multiple of
+// four threads' units (a block never straddles two groups), and a width that blocks
+// cover. At 3 bits a thread takes one unit of three words.
+inline int units_per_thread(int bits, int group_size, long long d) {
+  if (bits != 2 && bits != 3 && bits != 4) return 0;
+  const long long cols4 = 4LL * (bits == 3 ? 32 : 32 / bits);   // columns of four threads' single units
   const long long span = group_size == -1 ? d : group_size;
   if (span % cols4) return 0;
+  if (bits == 3) return 1;
   const long long q = span / cols4;
   return (q % 4 == 0) ? 4 : (q % 2 == 0) ? 2 : 1;
 }
 
-template <int BITS, int WPT>
+template <int BITS, int UPT>
 gptq_status launch(const uint32_t* qweight, const float* scales, const float* zeros, int m, int d, int G, int gsize,
                    const uint16_t* X, long long ldx, int T, float* Y, long long ldy, cudaStream_t s) {
   const int wpr = d * BITS / 32;
-  const int bpg = gsize / (4 * WPT * (32 / BITS));              // blocks per group (a block never straddles two)
+  const int bpg = gsize / (4 * UPT * unit_codes<BITS>());          // blocks per group (a block never straddles two)
   const uint32_t bpg_mul = bpg == 1 ? 0u : (uint32_t)((0x100000000ULL + (unsigned long long)bpg - 1) / bpg);
   const dim3 grid((unsigned)((m + ROWS - 1) / ROWS));
   for (int t0 = 0; t0 < T; t0 += 8) {
-    gemv_mma_kernel<BITS, WPT><<<grid, WARPS * 32, 0, s>>>(qweight, wpr, scales, zeros, G, bpg, bpg_mul, m, d,
+    gemv_mma_kernel<BITS, UPT><<<grid, WARPS * 32, 0, s>>>(qweight, wpr, scales, zeros, G, bpg, bpg_mul, m, d,
                                                           X + (long long)t0 * ldx, ldx, std::min(8, T - t0),
                                                           Y + (long long)t0 * ldy, ldy);
     count_launch();
@@ -401,9 +428,9 @@ gptq_status launch(const uint32_t* qweight, const float* scales, const float* ze
 }
 
 template <int BITS>
-gptq_status launch_bits(int wpt, const uint32_t* qweight, const float* scales, const float* zeros, int m, int d, int G,
+gptq_status launch_bits(int upt, const uint32_t* qweight, const float* scales, const float* zeros, int m, int d, int G,
                         int gsize, const uint16_t* X, long long ldx, int T, float* Y, long long ldy, cudaStream_t s) {
-  switch (wpt) {
+  switch (upt) {
     case 4: return launch<BITS, 4>(qweight, scales, zeros, m, d, G, gsize, X, ldx, T, Y, ldy, s);
     case 2: return launch<BITS, 2>(qweight, scales, zeros, m, d, G, gsize, X, ldx, T, Y, ldy, s);
     default: return launch<BITS, 1>(qweight, scales, zeros, m, d, G, gsize, X, ldx, T, Y, ldy, s);
@@ -420,11 +447,12 @@ gptq_status dequant_gemv_launch(const uint32_t* qweight, const float* scales, co
   using namespace dgemv;
   const int G = (group_size == -1) ? 1 : (int)(d / group_size);
   const int gsize = (group_size == -1) ? (int)d : group_size;
-  // act-order groups (g_idx) and 3- and 8-bit codes take the FMA kernel
-  const int wpt = (g_idx && G > 1) ? 0 : tcv::words_per_thread(bits, group_size, d);
-  if (wpt && !tcv::gemv_fma_forced()) {
-    if (bits == 4) return tcv::launch_bits<4>(wpt, qweight, scales, zeros, (int)m, (int)d, G, gsize, X, ldx, (int)T, Y, ldy, s);
-    return tcv::launch_bits<2>(wpt, qweight, scales, zeros, (int)m, (int)d, G, gsize, X, ldx, (int)T, Y, ldy, s);
+  // act-order groups (g_idx), 8-bit codes and groups narrower than a block take the FMA kernel
+  const int upt = (g_idx && G > 1) ? 0 : tcv::units_per_thread(bits, group_size, d);
+  if (upt && !tcv::gemv_fma_forced()) {
+    if (bits == 4) return tcv::launch_bits<4>(upt, qweight, scales, zeros, (int)m, (int)d, G, gsize, X, ldx, (int)T, Y, ldy, s);
+    if (bits == 3) return tcv::launch<3, 1>(qweight, scales, zeros, (int)m, (int)d, G, gsize, X, ldx, (int)T, Y, ldy, s);
+    return tcv::launch_bits<2>(upt, qweight, scales, zeros, (int)m, (int)d, G, gsize, X, ldx, (int)T, Y, ldy, s);
   }
   switch (bits) {
     case 2: return launch<2>(qweight, scales, zeros, g_idx, (int)m, (int)d, G, gsize, X, ldx, (int)T, Y, ldy, s);
