@@ -258,12 +258,11 @@ gptq_status gptq_unpack_codes(const uint32_t* qweight, int64_t m, int64_t d, int
  * form, w_hat[r][j] = (code[r][j] - zero[r][g]) * scale[r][g] with g = g_idx[j], or
  * j / group_size when g_idx is NULL ("GPTQ: fixing errors as you go": once quantized,
  * the stored low-bit weights and per-group scales stand in for the layer's weights).
- * Every code is read once per 8 tokens. 2-, 3- and 4-bit codes in natural groups
- * (g_idx NULL or one group per row) are summed per group on the tensor cores (exact
- * bf16 products of code - zero and the token, fp32 accumulation), then scaled in fp32;
- * 8-bit codes, act-order groups and groups narrower than the kernel's column blocks
- * take an fp32 FMA kernel. zeros must hold integers (as gptq_quantize_layer writes
- * them).
+ * Every code is read once per 8 tokens. Codes in natural groups (g_idx NULL or one
+ * group per row) are summed per group on the tensor cores (exact bf16 products of
+ * code - zero and the token, fp32 accumulation), then scaled in fp32; act-order groups
+ * and groups narrower than the kernel's column blocks take an fp32 FMA kernel. zeros
+ * must hold integers (as gptq_quantize_layer writes them).
  *
  *   qweight, scales, zeros  as written by gptq_quantize_layer (device; m x
  *              ceil(d*bits/32) words, m x G floats each). qweight 16-byte aligned

@@ -104,7 +104,9 @@ def main():
             for T in (1, 8):
                 us, nbytes = time_gemv(m, d, args.bits, args.group_size, T, args.reps, flush)
                 gbs = nbytes / us / 1e3
-                tc = args.bits in (2, 3, 4) and os.environ.get("GPTQ_GEMV_KERNEL") != "fma"
+                span = d if args.group_size == -1 else args.group_size    # the library's choice of kernel
+                tc = (os.environ.get("GPTQ_GEMV_KERNEL") != "fma"
+                      and span % (4 * {2: 16, 3: 32, 4: 8, 8: 8}[args.bits]) == 0)
                 print(json.dumps({"kernel": "gemv_mma_kernel" if tc else "dequant_gemv_kernel", "layer": name, "m": m, "d": d, "bits": args.bits,
                                   "group_size": args.group_size, "tokens": T, "us": round(us, 2),
                                   "bytes": int(nbytes), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 3),

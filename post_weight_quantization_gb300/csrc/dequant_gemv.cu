@@ -6,8 +6,8 @@
 // G(j) = j / group_size, or g_idx[j] for act-order groups. For the few tokens of a
 // decoding step this product reads every code once and is bound by HBM bandwidth.
 //
-// Two kernels: gemv_mma_kernel (below) for 2-, 3- and 4-bit codes in natural groups,
-// and this FMA kernel for 8-bit codes, act-order groups and narrow groups.
+// Two kernels: gemv_mma_kernel (below) for codes in natural groups, and this FMA kernel
+// for act-order groups and groups narrower than that kernel's column blocks.
 //
 // dequant_gemv_kernel<BITS, GIDX>: one warp per row r; lane L takes the 32-column
 // chunks L, L + 32, ... of the row (BITS words each, read as 16-byte vectors where the
@@ -193,8 +193,8 @@ gptq_status launch(const uint32_t* qweight, const float* scales, const float* ze
 }
 
 // ---------------------------------------------------------------------------------
-// The same product with the dot products on the tensor cores: for 2-, 3- and 4-bit codes
-// in natural groups the FMA version above spends about six instructions per code
+// The same product with the dot products on the tensor cores: for codes in natural
+// groups the FMA version above spends about six instructions per code
 // (unpack, dequantize, convert the token, FMA) and is bound by instruction issue at a
 // quarter of the HBM rate; here the unpacked codes go from registers straight into
 // mma.sync (m16n8k16, bf16 operands, fp32 accumulation), which takes eight tokens at the
@@ -202,16 +202,17 @@ gptq_status launch(const uint32_t* qweight, const float* scales, const float* ze
 // dequantized codes there would add four bytes of shared-memory traffic per code, more
 // than the code's half byte from HBM.)
 //
-// Per row, code - zero is an integer of at most 4 bits: a pair of codes is taken out of
-// the packed words and OR-ed into the mantissas of a bf16 pair of 128 (0x4300: bf16
-// holds 128 ... 255 exactly), and a bf16 subtraction of 128 + zero leaves code - zero
-// exactly. The product with a bf16 token is exact; each block of columns that shares
+// Per row, code - zero is an integer with |code - zero| <= 255, exact in bf16. At 2, 3
+// and 4 bits a pair of codes is taken out of the packed words and OR-ed into the
+// mantissas of a bf16 pair of 128 (0x4300: bf16 holds 128 ... 255 exactly), and a bf16
+// subtraction of 128 + zero leaves code - zero exactly; 8-bit codes go through fp32
+// (see code_pair). The product with a bf16 token is exact; each block of columns that shares
 // one (scale, zero) is summed by the tensor core in fp32 and then scaled and added in
 // fp32.
 //
 // Layout: a CTA takes 16 rows, its 8 warps split the row's column blocks. The packed
 // row is read in units: one word (CPW = 32 / bits codes) at 2 and 4 bits, three words
-// (32 codes) at 3 bits, whose codes straddle words. A block is 4 x UPT units; lane
+// (32 codes) at 3 bits, whose codes straddle words, two words (8 codes) at 8 bits. A block is 4 x UPT units; lane
 // (g, t) of a warp (g = lane / 4, t = lane % 4) holds units t*UPT ... t*UPT + UPT - 1 of
 // the block for rows g and g + 8 (the A fragment's rows) and the same columns of token
 // g (the B fragment's column). Code pair p of a unit of UC codes is the codes p and
@@ -233,8 +234,8 @@ inline bool gemv_fma_forced() {
 constexpr int WARPS = 8, ROWS = 16;
 constexpr uint32_t kBf16Pair128 = 0x43004300u;
 
-template <int BITS> constexpr int unit_words() { return BITS == 3 ? 3 : 1; }
-template <int BITS> constexpr int unit_codes() { return BITS == 3 ? 32 : 32 / BITS; }
+template <int BITS> constexpr int unit_words() { return BITS == 3 ? 3 : BITS == 8 ? 2 : 1; }
+template <int BITS> constexpr int unit_codes() { return BITS == 3 ? 32 : BITS == 8 ? 8 : 32 / BITS; }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
@@ -257,25 +258,37 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Codes p and p + UC/2 of a unit as the bf16 pair (128 + code_p, 128 + code_{p+UC/2})
-// (p is a compile-time constant once the callers' loops are unrolled). At 2 and 4 bits
-// the two codes sit 16 bits apart in one word: one shift and one mask-and-OR. At 3 bits
-// code p starts at bit 3p of the unit's 96 bits and code p + 16 at bit 48 + 3p: a
-// funnel shift brings each to bit 0 and 16 of a word.
+// Codes p and p + UC/2 of a unit, minus the row's zero, as an exact bf16 pair (p is a
+// compile-time constant once the callers' loops are unrolled). neg_z is the bf16 pair
+// -(128 + zero) and zf the float 2^23 + zero.
+//   2 and 4 bits: the two codes sit 16 bits apart in one word: one shift and one
+//     mask-and-OR give the pair (128 + code, 128 + code'), one bf16 subtraction the rest.
+//   3 bits: code p starts at bit 3p of the unit's 96 bits and code p + 16 at bit
+//     48 + 3p; a funnel shift brings each to bit 0 and 16 of a word, then as above.
+//   8 bits (128 + code would need 9 significant bits): byte p of each of the unit's two
+//     words is permuted into the mantissa of 2^23, 2^23 + zero is subtracted in fp32
+//     (exact), and the two results |code - zero| <= 255 convert to bf16 exactly.
 template <int BITS>
-__device__ __forceinline__ uint32_t code_pair(const uint32_t* w, int p) {
-  if constexpr (BITS == 3) {
+__device__ __forceinline__ uint32_t code_pair(const uint32_t* w, int p, uint32_t neg_z, float zf) {
+  if constexpr (BITS == 8) {
+    const uint32_t sel = 0x7650u | (uint32_t)p;      // byte p, then the bytes 00 00 4B of 2^23
+    const float lo = __fsub_rn(__uint_as_float(prmt(w[0], 0x4B000000u, sel)), zf);
+    const float hi = __fsub_rn(__uint_as_float(prmt(w[1], 0x4B000000u, sel)), zf);
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+  } else if constexpr (BITS == 3) {
     const uint32_t lo = (3 * p < 32) ? __funnelshift_r(w[0], w[1], 3 * p) : (w[1] >> (3 * p - 32));
     const uint32_t hi = (3 * p < 32) ? __funnelshift_r(w[1], w[2], 3 * p) : (w[2] >> (3 * p - 32));
-    return (lo & 0x00000007u) | (hi & 0x00070000u) | kBf16Pair128;
+    return sub_bf16x2((lo & 0x00000007u) | (hi & 0x00070000u) | kBf16Pair128, neg_z);
   } else {
     constexpr uint32_t MASK2 = ((1u << BITS) - 1u) * 0x00010001u;
-    return ((w[0] >> (BITS * p)) & MASK2) | kBf16Pair128;
+    return sub_bf16x2(((w[0] >> (BITS * p)) & MASK2) | kBf16Pair128, neg_z);
   }
 }
 
-// N consecutive words (vector loads as wide as the alignment allows: 16 bytes for 4-bit
-// rows, 8 for 2-bit, single words for 3-bit), or zeros for a row past the end.
+// N consecutive words (vector loads as wide as the alignment allows: 16 bytes for 4- and
+// 8-bit rows, 8 for 2-bit, single words for 3-bit), or zeros for a row past the end.
 template <int BITS, int N>
 __device__ __forceinline__ void load_words(const uint32_t* __restrict__ p, uint32_t (&w)[N], bool valid) {
   if (!valid) {
@@ -283,9 +296,12 @@ __device__ __forceinline__ void load_words(const uint32_t* __restrict__ p, uint3
     for (int u = 0; u < N; ++u) w[u] = 0u;
     return;
   }
-  if constexpr (BITS == 4 && N == 4) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
-    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+  if constexpr ((BITS == 4 || BITS == 8) && N % 4 == 0) {
+#pragma unroll
+    for (int u = 0; u < N; u += 4) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(p + u));
+      w[u] = v.x; w[u + 1] = v.y; w[u + 2] = v.z; w[u + 3] = v.w;
+    }
   } else if constexpr (BITS != 3 && N >= 2) {
 #pragma unroll
     for (int u = 0; u < N; u += 2) {
@@ -299,8 +315,8 @@ __device__ __forceinline__ void load_words(const uint32_t* __restrict__ p, uint3
 }
 
 // bf16 pair (-(128 + zero), -(128 + zero)); zero is an integer in [0, 2^bits - 1], so
-// 128 + zero has at most 8 significant bits and its fp32 encoding's upper half is its
-// bf16.
+// for bits <= 4 128 + zero has at most 8 significant bits and its fp32 encoding's upper
+// half is its bf16 (the 8-bit path uses 2^23 + zero instead).
 __device__ __forceinline__ uint32_t neg_zero_pair(float z) {
   return ((__float_as_uint(128.0f + z) >> 16) * 0x00010001u) | 0x80008000u;
 }
@@ -350,8 +366,9 @@ __global__ void __launch_bounds__(WARPS * 32) gemv_mma_kernel(const uint32_t* __
       // ceil(2^32 / bpg), exact since v * bpg < 2^32
       const int grp = bpg == 1 ? v : (int)__umulhi((uint32_t)v, bpg_mul);
       const float sa = va ? __ldg(sca + grp) : 0.0f, sb = vb ? __ldg(scb + grp) : 0.0f;
-      const uint32_t za = neg_zero_pair(va ? __ldg(zra + grp) : 0.0f);
-      const uint32_t zb = neg_zero_pair(vb ? __ldg(zrb + grp) : 0.0f);
+      const float zfa = va ? __ldg(zra + grp) : 0.0f, zfb = vb ? __ldg(zrb + grp) : 0.0f;
+      const uint32_t za = neg_zero_pair(zfa), zb = neg_zero_pair(zfb);
+      const float z23a = __fadd_rn(8388608.0f, zfa), z23b = __fadd_rn(8388608.0f, zfb);
       float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int u = 0; u < UPT; ++u) {
@@ -367,10 +384,10 @@ __global__ void __launch_bounds__(WARPS * 32) gemv_mma_kernel(const uint32_t* __
 #pragma unroll
         for (int j = 0; j < SPU; ++j) {
           // code pairs 2j and 2j + 1: codes (2j, 2j + UC/2) and (2j + 1, 2j + 1 + UC/2)
-          const uint32_t a0 = sub_bf16x2(code_pair<BITS>(ua, 2 * j), za);
-          const uint32_t a2 = sub_bf16x2(code_pair<BITS>(ua, 2 * j + 1), za);
-          const uint32_t a1 = sub_bf16x2(code_pair<BITS>(ub, 2 * j), zb);
-          const uint32_t a3 = sub_bf16x2(code_pair<BITS>(ub, 2 * j + 1), zb);
+          const uint32_t a0 = code_pair<BITS>(ua, 2 * j, za, z23a);
+          const uint32_t a2 = code_pair<BITS>(ua, 2 * j + 1, za, z23a);
+          const uint32_t a1 = code_pair<BITS>(ub, 2 * j, zb, z23b);
+          const uint32_t a3 = code_pair<BITS>(ub, 2 * j + 1, zb, z23b);
           const uint32_t b0 = prmt(xw[j], xw[j + UC / 4], 0x5410u);
           const uint32_t b1 = prmt(xw[j], xw[j + UC / 4], 0x7632u);
           mma_bf16(c, a0, a1, a2, a3, b0, b1);
@@ -402,8 +419,8 @@ __global__ void __launch_bounds__(WARPS * 32) gemv_mma_kernel(const uint32_t* __
 // four threads' units (a block never straddles two groups), and a width that blocks
 // cover. At 3 bits a thread takes one unit of three words.
 inline int units_per_thread(int bits, int group_size, long long d) {
-  if (bits != 2 && bits != 3 && bits != 4) return 0;
-  const long long cols4 = 4LL * (bits == 3 ? 32 : 32 / bits);   // columns of four threads' single units
+  if (bits != 2 && bits != 3 && bits != 4 && bits != 8) return 0;
+  const long long cols4 = 4LL * (bits == 3 ? 32 : bits == 8 ? 8 : 32 / bits);   // four threads' single units
   const long long span = group_size == -1 ? d : group_size;
   if (span % cols4) return 0;
   if (bits == 3) return 1;
@@ -447,11 +464,12 @@ gptq_status dequant_gemv_launch(const uint32_t* qweight, const float* scales, co
   using namespace dgemv;
   const int G = (group_size == -1) ? 1 : (int)(d / group_size);
   const int gsize = (group_size == -1) ? (int)d : group_size;
-  // act-order groups (g_idx), 8-bit codes and groups narrower than a block take the FMA kernel
+  // act-order groups (g_idx) and groups narrower than a block take the FMA kernel
   const int upt = (g_idx && G > 1) ? 0 : tcv::units_per_thread(bits, group_size, d);
   if (upt && !tcv::gemv_fma_forced()) {
     if (bits == 4) return tcv::launch_bits<4>(upt, qweight, scales, zeros, (int)m, (int)d, G, gsize, X, ldx, (int)T, Y, ldy, s);
     if (bits == 3) return tcv::launch<3, 1>(qweight, scales, zeros, (int)m, (int)d, G, gsize, X, ldx, (int)T, Y, ldy, s);
+    if (bits == 8) return tcv::launch_bits<8>(upt, qweight, scales, zeros, (int)m, (int)d, G, gsize, X, ldx, (int)T, Y, ldy, s);
     return tcv::launch_bits<2>(upt, qweight, scales, zeros, (int)m, (int)d, G, gsize, X, ldx, (int)T, Y, ldy, s);
   }
   switch (bits) {

@@ -60,24 +60,25 @@ def _check(g, m, d, bits, gs, act_order, T, seed, rows=None):
     assert np.all(np.abs(got - ref) <= bound), float(np.max(np.abs(got - ref) / bound))
 
 
-# 2-, 3- and 4-bit codes in natural groups run on the tensor cores (one, two or four
-# words of a row per thread and block: g32, g64 and g128 at 4 bits, g64, g128 and
-# per-channel at 2 bits; three-word units at 3 bits, g128, g256 and per-channel); 8-bit
-# codes, act-order groups (g_idx) and groups narrower than a block (2-bit g32, 3-bit
-# g64) on the FMA kernel. m = 200 leaves a partial 16-row tile; T = 11 is a piece of
-# eight and one of three tokens.
+# Codes in natural groups run on the tensor cores (one, two or four units of a row per
+# thread and block: g32, g64 and g128 at 4 bits, g64, g128 and per-channel at 2 bits;
+# three-word units at 3 bits, g128, g256 and per-channel; two-word units at 8 bits,
+# g32, g128 and per-channel); act-order groups (g_idx) and groups narrower than a
+# block (2-bit g32, 3-bit g64) on the FMA kernel. m = 200 leaves a partial 16-row
+# tile; T = 11 is a piece of eight and one of three tokens.
 @pytest.mark.parametrize("bits,gs,ao", [(4, 128, False), (3, -1, True), (2, 64, True), (8, 32, False),
                                         (4, 128, True), (4, 64, False), (4, 32, False), (4, -1, False),
                                         (2, 64, False), (2, 128, False), (2, -1, True), (2, 32, False),
-                                        (3, 128, False), (3, 256, False), (3, 64, False), (3, 128, True)])
+                                        (3, 128, False), (3, 256, False), (3, 64, False), (3, 128, True),
+                                        (8, 128, False), (8, -1, False), (8, 64, True)])
 @pytest.mark.parametrize("T", [1, 5, 11])
 def test_dequant_gemv_matches_oracle(g, bits, gs, ao, T):
     _check(g, 200, 768, bits, gs, ao, T, seed=100 + T + bits)
 
 
-@pytest.mark.parametrize("bits,gs", [(4, 128), (2, 64), (3, -1)])
+@pytest.mark.parametrize("bits,gs", [(4, 128), (2, 64), (3, -1), (8, 128)])
 def test_dequant_gemv_full_size_layer(g, bits, gs):
-    """A 4096 x 4096 packed layer (4-bit g128, 2-bit g64, 3-bit per-channel), eight
-    tokens, sampled rows against the oracle."""
+    """A 4096 x 4096 packed layer (4-bit g128, 2-bit g64, 3-bit per-channel, 8-bit g128),
+    eight tokens, sampled rows against the oracle."""
     rows = np.sort(np.random.default_rng(3).choice(4096, size=96, replace=False))
     _check(g, 4096, 4096, bits, gs, False, 8, seed=7, rows=rows)
