@@ -206,16 +206,16 @@ gptq_status launch(const uint32_t* qweight, const float* scales, const float* ze
 // and 4 bits a pair of codes is taken out of the packed words and OR-ed into the
 // mantissas of a bf16 pair of 128 (0x4300: bf16 holds 128 ... 255 exactly), and a bf16
 // subtraction of 128 + zero leaves code - zero exactly; 8-bit codes go through fp32
-// (see code_pair). The product with a bf16 token is exact; each block of columns that shares
-// one (scale, zero) is summed by the tensor core in fp32 and then scaled and added in
-// fp32.
+// (see code_pair). The product with a bf16 token is exact; each block of columns that
+// shares one (scale, zero) is summed by the tensor core in fp32 and then scaled and
+// added in fp32.
 //
 // Layout: a CTA takes 16 rows, its 8 warps split the row's column blocks. The packed
 // row is read in units: one word (CPW = 32 / bits codes) at 2 and 4 bits, three words
-// (32 codes) at 3 bits, whose codes straddle words, two words (8 codes) at 8 bits. A block is 4 x UPT units; lane
-// (g, t) of a warp (g = lane / 4, t = lane % 4) holds units t*UPT ... t*UPT + UPT - 1 of
-// the block for rows g and g + 8 (the A fragment's rows) and the same columns of token
-// g (the B fragment's column). Code pair p of a unit of UC codes is the codes p and
+// (32 codes) at 3 bits, whose codes straddle words, and two words (8 codes) at 8 bits.
+// A block is 4 x UPT units; lane (g, t) of a warp (g = lane / 4, t = lane % 4) holds
+// units t*UPT ... t*UPT + UPT - 1 of the block for rows g and g + 8 (the A fragment's
+// rows) and the same columns of token g (the B fragment's column). Code pair p of a unit of UC codes is the codes p and
 // p + UC/2, which the A fragment's bf16 pair puts at two consecutive k; the B fragment
 // pairs the token's values of the same two columns with one byte permute. The order of
 // k inside an MMA is thereby a fixed permutation of the block's columns, applied to
