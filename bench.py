@@ -297,7 +297,8 @@ def run_reference(args):
               f"full d={layer.d} factor chain, column loop over {rows} of {layer.m} rows (scaled); "
               f"ms_per_step is the sample's wall time, value the layer rate scaled from it")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "Mweights/s",
-            "n_gpus": 0, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(wall * 1e3, 3),
+            "n_gpus": world_size(args), "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(wall * 1e3, 3),
             "ms_per_layer_scaled": round(t * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded)",
