@@ -19,7 +19,7 @@ def test_reference_arm_line():
     for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
               "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e", "impl"):
         assert k in r, k
-    assert r["impl"] == "reference" and r["steps"] == 2 and r["warmup"] == 1
+    assert r["impl"] == "reference" and r["steps"] == 2 and r["warmup"] == 1 and r["n_gpus"] == 1
     assert r["value"] > 0 and r["unit"] == "Mweights/s" and r["higher_is_better"] is True
     assert r["config"]["workload"] == "toy_256" and (r["config"]["m"], r["config"]["d"]) == (256, 256)
     cb = r["cpu_baseline"]
